@@ -1,0 +1,158 @@
+/*
+ * w8a8.h — C ABI of the GB300 (sm_103a) W8A8 group-scaled quantized linear layer.
+ *
+ * The operation ("Deploying Hunyuan 770B in INT8 on domestic accelerators
+ * (FlagOS Hy4 preview 5)", §3.1, quantization granularity):
+ *   - activations are quantized per token, dynamically, at every call:
+ *       s_m = amax_k |A[m,k]| / 127,  qa[m,k] = round(A[m,k] / s_m)
+ *     (round = nearest, ties to even; codes clamped to [-127, 127]);
+ *   - weights are INT8 with one FP32 scale per group of 128 consecutive K
+ *     elements of an output row n: sw[n, g], g = k / 128;
+ *   - each group is multiplied INT8 x INT8 and accumulated exactly in integers,
+ *       P[m,n,g] = sum_{k in group g} qa[m,k] * qw[n,k]
+ *     and the FP32 scales are applied only at the end:
+ *       Y[m,n] = sa[m] * sum_g sw[n,g] * P[m,n,g].
+ * MoE expert layers (same page §1.3 and §4.4: each token goes to the experts
+ * its router picked) run the same computation per expert over the rows that
+ * were routed to it.
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers owned by the caller. The library
+ *     never allocates device memory inside these calls.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream). They
+ *     never synchronise the host and never read device data on the host, so
+ *     they can be captured in a CUDA graph. The status returned covers only
+ *     what the host can check (arguments, device capability, launch errors);
+ *     a device-side fault shows up later through the CUDA runtime and a
+ *     device-side wait that timed out through w8a8_device_error().
+ *   - Matrices are row-major with unit stride in their last dimension.
+ *     Pointers to int8/bf16/fp16 matrices read with TMA must be 16-byte
+ *     aligned; float vectors 4-byte aligned.
+ *   - Sizes are int64_t; the product of a matrix's dimensions must stay below
+ *     2^31 elements per operand (checked).
+ *   - Requires a device of compute capability 10.3 (GB300); any other device
+ *     returns W8A8_ERR_UNSUPPORTED.
+ */
+#ifndef W8A8_H
+#define W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *w8a8_stream_t;
+
+typedef enum {
+    W8A8_OK = 0,
+    W8A8_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, K % 128 != 0 ... */
+    W8A8_ERR_UNSUPPORTED = 2,   /* device is not compute capability 10.3 */
+    W8A8_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+    W8A8_ERR_WORKSPACE = 4,     /* workspace pointer missing or smaller than required */
+    W8A8_ERR_DEVICE_TIMEOUT = 5 /* reported by w8a8_device_error(): a device wait gave up */
+} w8a8_status;
+
+typedef enum { W8A8_BF16 = 0, W8A8_FP32 = 1 } w8a8_dtype;
+
+#define W8A8_GROUP 128
+
+/*
+ * Per-token dynamic activation quantization (Hunyuan-770B page §3.1,
+ * "activations quantized per token, dynamically"; "round(x / scale)").
+ *   a_bf16 [M, lda] BF16 (only the first K columns are read);
+ *   qa     [M, ldq] int8 output, qa[m,k] = clamp(rne(a[m,k] / sa[m]), -127, 127);
+ *   sa     [M] float output, sa[m] = amax_k |a[m,k]| / 127 (IEEE FP32 division).
+ * A row whose amax is 0 gets sa = 0 and all-zero codes. Inputs must be finite.
+ * K >= 1, lda >= K, ldq >= K. M == 0 is a no-op. Results are bit-identical to
+ * the FP32 definition above (no fast-math, no reciprocal multiply).
+ */
+w8a8_status w8a8_quant_act(const void *a_bf16, int64_t M, int64_t K, int64_t lda,
+                           int8_t *qa, int64_t ldq, float *sa, w8a8_stream_t stream);
+
+/*
+ * Per-row, per-128-K-group weight quantization (Hunyuan-770B page §3.1,
+ * "weights in groups of 128 elements, one scale per group"): offline input
+ * preparation for the GEMMs below.
+ *   w  [N, K] float; qw [N, K] int8; sw [N, K/128] float.
+ *   sw[n,g] = amax over the group / 127; qw = clamp(rne(w / sw), -127, 127).
+ * K must be a positive multiple of 128. N == 0 is a no-op.
+ */
+w8a8_status w8a8_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
+                              w8a8_stream_t stream);
+
+/*
+ * Bytes of device workspace w8a8_gemm needs for an M x K activation operand
+ * (the tensor-core operand staging buffer). 0 when M == 0.
+ */
+size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Dense W8A8 GEMM with per-group weight scales (Hunyuan-770B page §3.1:
+ * INT8 multiply-accumulate into INT32 per group, FP32 scales "multiplied back
+ * only at the end").
+ *   qa [M, K] int8, sa [M] float   (from w8a8_quant_act, ldq == K)
+ *   qw [N, K] int8, sw [N, K/128] float
+ *   y  [M, N] BF16 (round to nearest even) or FP32, per y_dtype.
+ *   debug_partials: NULL, or int32 [M, N, K/128] receiving every exact group
+ *                   partial P[m,n,g] (debug/parity use; slow).
+ *   workspace: device buffer of at least w8a8_gemm_workspace_size(M, N, K)
+ *              bytes, 256-byte aligned; its contents are scratch.
+ * K must be a positive multiple of 128; N >= 1. M == 0 is a no-op.
+ * The group sums are exact integers; Y is accumulated in FP32:
+ *   acc = sum_g fma(P_g, sw[n,g], acc), Y = sa[m] * acc
+ * so |Y - Y*| <= (G + 2) * 2^-24 * sum_g |sa*sw*P_g| for the exact Y*.
+ */
+w8a8_status w8a8_gemm(const int8_t *qa, const float *sa, const int8_t *qw, const float *sw,
+                      void *y, w8a8_dtype y_dtype, int64_t M, int64_t N, int64_t K,
+                      int32_t *debug_partials, void *workspace, size_t workspace_bytes,
+                      w8a8_stream_t stream);
+
+/*
+ * Bytes of device workspace w8a8_grouped_gemm needs for R routed rows.
+ */
+size_t w8a8_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K);
+
+/*
+ * MoE expert-grouped W8A8 GEMM (Hunyuan-770B page §1.3/§4.4: tokens are
+ * processed by the experts the router chose; one routed row per
+ * (token, expert) pair, rows sorted by expert).
+ *   qa      [R, K] int8, sa [R] float: routed rows, sorted by expert
+ *   offsets [E+1] int32 DEVICE array: rows of expert e are [offsets[e], offsets[e+1]).
+ *           Precondition: 0 = offsets[0] <= ... <= offsets[E] <= R. Not read on the
+ *           host; the kernel clamps every offset into [0, R] so a violation cannot
+ *           make it access memory out of bounds. Empty segments produce no work.
+ *   qw      [E, N, K] int8, sw [E, N, K/128] float: per-expert weights and scales
+ *   y       [R, N] BF16 or FP32. Only rows covered by a segment are written.
+ *   debug_partials: NULL or int32 [R, N, K/128].
+ *   workspace: >= w8a8_grouped_gemm_workspace_size(R, E, N, K) bytes, 256-aligned.
+ * E >= 1, N >= 1, K a positive multiple of 128. R == 0 is a no-op.
+ */
+w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *offsets,
+                              const int8_t *qw, const float *sw, void *y, w8a8_dtype y_dtype,
+                              int64_t R, int64_t E, int64_t N, int64_t K,
+                              int32_t *debug_partials, void *workspace, size_t workspace_bytes,
+                              w8a8_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *w8a8_status_string(w8a8_status status);
+
+/*
+ * Reads (and, if clear != 0, resets) the current device's error word, which a
+ * kernel sets when one of its bounded waits gives up instead of hanging.
+ * Synchronises the device. *code_out = 0 means no device-side error; any other
+ * value encodes the kernel, role and wait site. Returns W8A8_ERR_DEVICE_TIMEOUT
+ * when the word was non-zero, W8A8_OK otherwise.
+ */
+w8a8_status w8a8_device_error(uint64_t *code_out, int clear);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int w8a8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_H */

@@ -1,0 +1,197 @@
+// C ABI of libw8a8 (declared in include/w8a8.h): argument validation,
+// device capability check, workspace sizing and dispatch to the kernels.
+// No call allocates device memory, synchronises the host or reads device data.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/w8a8.h"
+#include "internal.h"
+
+namespace w8a8 {
+
+cudaError_t current_device_info(DeviceInfo *out) {
+    static DeviceInfo cache[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].device != dev) {
+        DeviceInfo d;
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
+                cudaSuccess)
+            return e;
+        cache[dev] = d;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+}  // namespace w8a8
+
+namespace {
+
+constexpr int64_t kMaxElems = (int64_t(1) << 31) - 1;
+constexpr size_t kWsAlign = 256;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+w8a8_status check_device(w8a8::DeviceInfo *info) {
+    if (w8a8::current_device_info(info) != cudaSuccess) return W8A8_ERR_CUDA;
+    if (info->cc_major != 10 || info->cc_minor != 3) return W8A8_ERR_UNSUPPORTED;
+    return W8A8_OK;
+}
+
+w8a8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Workspace: fp16 staging copy of the int8 activation codes [rows, K].
+size_t staging_bytes(int64_t rows, int64_t K) {
+    if (rows <= 0 || K <= 0) return 0;
+    return round_up(static_cast<size_t>(rows) * static_cast<size_t>(K) * 2, kWsAlign);
+}
+
+// Shared validation of the GEMM operands; E == 1 with offsets == nullptr is dense.
+w8a8_status check_gemm(const int8_t *qa, const float *sa, const void *offsets, const int8_t *qw,
+                       const float *sw, const void *y, int64_t R, int64_t E, int64_t N,
+                       int64_t K, bool grouped, void *workspace, size_t workspace_bytes) {
+    if (R < 0 || N <= 0 || K <= 0 || E <= 0) return W8A8_ERR_INVALID_ARG;
+    if (K % W8A8_GROUP != 0) return W8A8_ERR_INVALID_ARG;
+    if (grouped && E > w8a8::kMaxExperts) return W8A8_ERR_INVALID_ARG;
+    if (R > kMaxElems / K || E * N > kMaxElems / K || R > kMaxElems / N) return W8A8_ERR_INVALID_ARG;
+    if (R == 0) return W8A8_OK;
+    if (!qa || !sa || !qw || !sw || !y || (grouped && !offsets)) return W8A8_ERR_INVALID_ARG;
+    if (!aligned(qa, 16) || !aligned(qw, 16) || !aligned(sa, 4) || !aligned(sw, 4) ||
+        !aligned(y, 4) || (offsets && !aligned(offsets, 4)))
+        return W8A8_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < staging_bytes(R, K) || !aligned(workspace, kWsAlign))
+        return W8A8_ERR_WORKSPACE;
+    return W8A8_OK;
+}
+
+w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, const int8_t *qw,
+                     const float *sw, void *y, w8a8_dtype y_dtype, int64_t R, int64_t E,
+                     int64_t N, int64_t K, int32_t *dbg, void *workspace, w8a8_stream_t stream) {
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s);
+    if (e != cudaSuccess) return W8A8_ERR_CUDA;
+    w8a8::GemmProblem p;
+    p.sa = sa;
+    p.sw = sw;
+    p.qw = qw;
+    p.x16 = workspace;
+    p.offsets = offsets;
+    p.y = y;
+    p.debug_partials = dbg;
+    p.R = R;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.out_fp32 = (y_dtype == W8A8_FP32);
+    return from_cuda(w8a8::launch_gemm(p, info.num_sms, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int w8a8_version(void) { return 100; }
+
+const char *w8a8_status_string(w8a8_status status) {
+    switch (status) {
+        case W8A8_OK: return "W8A8_OK";
+        case W8A8_ERR_INVALID_ARG: return "W8A8_ERR_INVALID_ARG";
+        case W8A8_ERR_UNSUPPORTED: return "W8A8_ERR_UNSUPPORTED";
+        case W8A8_ERR_CUDA: return "W8A8_ERR_CUDA";
+        case W8A8_ERR_WORKSPACE: return "W8A8_ERR_WORKSPACE";
+        case W8A8_ERR_DEVICE_TIMEOUT: return "W8A8_ERR_DEVICE_TIMEOUT";
+    }
+    return "W8A8_UNKNOWN_STATUS";
+}
+
+w8a8_status w8a8_quant_act(const void *a_bf16, int64_t M, int64_t K, int64_t lda, int8_t *qa,
+                           int64_t ldq, float *sa, w8a8_stream_t stream) {
+    if (M < 0 || K <= 0 || lda < K || ldq < K) return W8A8_ERR_INVALID_ARG;
+    if (M > kMaxElems / lda || M > kMaxElems / ldq || M > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
+    if (M == 0) return W8A8_OK;
+    if (!a_bf16 || !qa || !sa || !aligned(a_bf16, 2) || !aligned(sa, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_quant_act(static_cast<const uint16_t *>(a_bf16), M, K, lda, qa,
+                                            ldq, sa, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
+                              w8a8_stream_t stream) {
+    if (N < 0 || K <= 0 || K % W8A8_GROUP != 0 || N > kMaxElems / K) return W8A8_ERR_INVALID_ARG;
+    if (N == 0) return W8A8_OK;
+    if (!w || !qw || !sw || !aligned(w, 16) || !aligned(qw, 4) || !aligned(sw, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(
+        w8a8::launch_quant_weight(w, N, K, qw, sw, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    return staging_bytes(M, K);
+}
+
+size_t w8a8_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K) {
+    (void)E;
+    (void)N;
+    return staging_bytes(R, K);
+}
+
+w8a8_status w8a8_gemm(const int8_t *qa, const float *sa, const int8_t *qw, const float *sw,
+                      void *y, w8a8_dtype y_dtype, int64_t M, int64_t N, int64_t K,
+                      int32_t *debug_partials, void *workspace, size_t workspace_bytes,
+                      w8a8_stream_t stream) {
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    w8a8_status st = check_gemm(qa, sa, nullptr, qw, sw, y, M, 1, N, K, false, workspace,
+                                workspace_bytes);
+    if (st != W8A8_OK || M == 0) return st;
+    if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
+    return run_gemm(qa, sa, nullptr, qw, sw, y, y_dtype, M, 1, N, K, debug_partials, workspace,
+                    stream);
+}
+
+w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *offsets,
+                              const int8_t *qw, const float *sw, void *y, w8a8_dtype y_dtype,
+                              int64_t R, int64_t E, int64_t N, int64_t K,
+                              int32_t *debug_partials, void *workspace, size_t workspace_bytes,
+                              w8a8_stream_t stream) {
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    w8a8_status st = check_gemm(qa, sa, offsets, qw, sw, y, R, E, N, K, true, workspace,
+                                workspace_bytes);
+    if (st != W8A8_OK || R == 0) return st;
+    if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
+    return run_gemm(qa, sa, offsets, qw, sw, y, y_dtype, R, E, N, K, debug_partials, workspace,
+                    stream);
+}
+
+w8a8_status w8a8_device_error(uint64_t *code_out, int clear) {
+    if (!code_out) return W8A8_ERR_INVALID_ARG;
+    unsigned long long v = 0;
+    if (w8a8::read_device_error(&v, clear != 0) != cudaSuccess) return W8A8_ERR_CUDA;
+    *code_out = v;
+    return v ? W8A8_ERR_DEVICE_TIMEOUT : W8A8_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,575 @@
+// Group-scaled W8A8 GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes ("Deploying Hunyuan 770B in INT8 on domestic
+// accelerators", §3.1): for every output element, each 128-wide K group is
+// multiplied INT8 x INT8 and summed exactly, the group sum is scaled by that
+// group's FP32 weight scale into an FP32 accumulator, and the per-token FP32
+// scale is applied once at the end. MoE expert layers (§1.3, §4.4) run the
+// same tiles per expert over the rows routed to it.
+//
+// How, on GB300:
+//  * sm_103a has no integer tcgen05 MMA, so the exact integer group sum is
+//    formed by tcgen05.mma kind::f16 on fp16 copies of the int8 codes: every
+//    int8 is an exact fp16 integer, every product (<= 127^2) is exact, and a
+//    128-term group sum (|P| <= 2,064,512 < 2^24) is an exact FP32 integer.
+//    Each group gets a FRESH accumulator in tensor memory, so the tensor core
+//    never adds numbers that are not exactly representable.
+//  * Swap-AB: the MMA's M side (128 TMEM lanes) is 128 weight rows n, its N
+//    side is up to 128 token rows per MMA batch (two batches per 256-token
+//    tile). So the weight scale sw[n, g] is one register per epilogue thread.
+//  * Weights stay int8 in HBM. A converter warpgroup reads each TMA-landed
+//    int8 weight tile from shared memory, widens it in registers and writes
+//    the fp16 A operand straight into tensor memory (tcgen05.st); the MMA
+//    takes A from TMEM, which keeps the conversion off shared-memory
+//    bandwidth. Token codes arrive as fp16 via TMA (B operand, 128B swizzle).
+//  * Two 128-column partial buffers in TMEM alternate between MMA batches;
+//    two epilogue warpgroups drain them (tcgen05.ld), fma the partial with
+//    sw[n,g] into register accumulators, and at the end of the tile multiply
+//    by sa[m] and store BF16 (round to nearest even) or FP32.
+//  * Persistent CTAs walk a tile list built on the device from the expert
+//    offsets (no host read, graph-capture safe). Within an (expert, weight
+//    tile) the token tiles are consecutive so CTAs running together share the
+//    weight tile through L2.
+//  * Every mbarrier wait is bounded (%globaltimer); a wait that gives up sets
+//    the library error word and the CTA drains its copies, frees TMEM and
+//    returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w8a8 {
+
+__device__ unsigned long long g_device_error = 0;
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kStages = 4;          // weight tiles in flight (SMEM landing + TMEM operand slots)
+constexpr int kBStages = 4;         // token batches in flight
+constexpr int kTileN = 128;         // weight rows per tile = MMA M = TMEM lanes
+constexpr int kGroupK = 128;        // K elements per scale group = per pipeline stage
+constexpr int kTileTokens = 256;    // token rows per tile (two MMA batches)
+constexpr int kBatchRows = 128;     // token rows per MMA batch (MMA N <= 128)
+constexpr int kBoxRows = 32;        // token rows per TMA box
+constexpr int kAStageBytes = kTileN * kGroupK;                 // 16 KB int8
+constexpr int kBAtomBytes = kBatchRows * 128;                  // 128 rows x 64 fp16
+constexpr int kBStageBytes = 2 * kBAtomBytes;                  // 32 KB
+constexpr int kTmemCols = 512;
+constexpr int kTmemA0 = 256;        // A operand slot s at columns [256 + 64 s, +64)
+constexpr int kEpiRegs = 184;   // 256 threads x 184 + 256 x 72 = 512 x 128 at launch
+constexpr int kOtherRegs = 72;
+
+// Shared memory layout (offsets from a 1024-byte aligned base).
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kAStageBytes;
+constexpr int kOffBar = kOffB + kBStages * kBStageBytes;
+constexpr int kNumBars = 6 * kStages + 2 * 2 + 1;     // see BarIdx
+constexpr int kOffMisc = kOffBar + 8 * 32;
+constexpr int kOffTab = kOffMisc + 64;
+constexpr int kTabBytes = 3 * (kMaxExperts + 1) * 4;
+constexpr int kSmemBytes = kOffTab + kTabBytes + 1024;  // + alignment slack
+static_assert(kNumBars <= 32, "barrier area");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert((kThreads / 2) * (kEpiRegs + kOtherRegs) == 65536, "register split");
+
+struct BarIdx {
+    static constexpr int a_full = 0;                 // [kStages] TMA -> converters
+    static constexpr int a_empty = kStages;          // [kStages] converters -> TMA
+    static constexpr int ta_full = 2 * kStages;      // [kStages] converters -> MMA
+    static constexpr int ta_empty = 3 * kStages;     // [kStages] MMA -> converters
+    static constexpr int b_full = 4 * kStages;       // [kBStages] TMA -> MMA
+    static constexpr int b_empty = 4 * kStages + kBStages;  // [kBStages] MMA -> TMA
+    static constexpr int p_full = 4 * kStages + 2 * kBStages;   // [2] MMA -> epilogue
+    static constexpr int p_empty = p_full + 2;       // [2] epilogue -> MMA
+    static constexpr int drain = p_empty + 2;        // MMA completion at exit
+};
+static_assert(BarIdx::drain < 32, "barrier count");
+
+struct KParams {
+    const float *sa;
+    const float *sw;
+    const int32_t *offsets;
+    void *y;
+    int32_t *dbg;
+    int R, E, N, K, G;
+    int n_tiles;
+    int out_fp32;
+    unsigned long long *err;
+};
+
+struct TileInfo {
+    int e, n0, m0, rows;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const int *s_lo,
+                                                const int *s_cnt, int E, int n_tiles) {
+    int lo = 0, hi = E;  // s_base[lo] <= t < s_base[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_base[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int local = t - s_base[lo];
+    const int cnt = s_cnt[lo];
+    const int m_tiles = (cnt + kTileTokens - 1) / kTileTokens;
+    const int nt = local / m_tiles;
+    const int mt = local - nt * m_tiles;
+    TileInfo ti;
+    ti.e = lo;
+    ti.n0 = nt * kTileN;
+    ti.m0 = s_lo[lo] + mt * kTileTokens;
+    ti.rows = min(kTileTokens, cnt - mt * kTileTokens);
+    return ti;
+}
+
+// Token rows of MMA batch h of a tile with n_eff (multiple of 16) rows.
+__device__ __forceinline__ int batch_rows(int n_eff, int nb, int h) {
+    return nb == 2 ? (h == 0 ? kBatchRows : n_eff - kBatchRows) : n_eff;
+}
+
+// Bounded wait used only on the exit path, independent of the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                 const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw_addr);
+
+    const uint32_t sA = base + kOffA;
+    const uint32_t sB = base + kOffB;
+    const uint32_t sBar = base + kOffBar;
+    volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    int *s_base = reinterpret_cast<int *>(smem + kOffTab);
+    int *s_lo = s_base + (kMaxExperts + 1);
+    int *s_cnt = s_lo + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    // ------------------------------------------------------------ set-up
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar(BarIdx::a_full + i), 1);
+            mbar_init(bar(BarIdx::a_empty + i), 4);
+            mbar_init(bar(BarIdx::ta_full + i), 4);
+            mbar_init(bar(BarIdx::ta_empty + i), 1);
+        }
+        for (int i = 0; i < kBStages; ++i) {
+            mbar_init(bar(BarIdx::b_full + i), 1);
+            mbar_init(bar(BarIdx::b_empty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(BarIdx::p_full + i), 1);
+            mbar_init(bar(BarIdx::p_empty + i), 8);
+        }
+        mbar_init(bar(BarIdx::drain), 1);
+        *s_abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 2) {
+        // Tile table: expert e owns tiles [s_base[e], s_base[e+1]); its rows
+        // are [s_lo[e], s_lo[e] + s_cnt[e]) with offsets clamped into [0, R].
+        int carry = 0;
+        for (int e0 = 0; e0 < p.E; e0 += 32) {
+            const int e = e0 + lane;
+            int lo = 0, cnt = 0;
+            if (e < p.E) {
+                if (p.offsets != nullptr) {
+                    int a = p.offsets[e], b = p.offsets[e + 1];
+                    a = min(max(a, 0), p.R);
+                    b = min(max(b, 0), p.R);
+                    lo = a;
+                    cnt = max(b - a, 0);
+                } else {
+                    lo = 0;
+                    cnt = p.R;
+                }
+            }
+            const int tiles = (e < p.E) ? p.n_tiles * ((cnt + kTileTokens - 1) / kTileTokens) : 0;
+            int incl = tiles;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (e < p.E) {
+                s_base[e] = carry + incl - tiles;
+                s_lo[e] = lo;
+                s_cnt[e] = cnt;
+            }
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) {
+            s_base[p.E] = carry;
+            *s_total = carry;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *s_tmem_base;
+    const int total = *s_total;
+    const int G = p.G;
+    const int wg = warp >> 2;
+
+    // Register split: each setmaxnreg sits inside its role's branch so that
+    // the register allocator sees only that role's code in the region.
+    if (warp < 4) {
+        setmaxnreg_dec<kOtherRegs>();
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t a_iss = 0, b_iss = 0;   // loads issued so far
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const int nb = n_eff > kBatchRows ? 2 : 1;
+                const int wrow = ti.e * p.N + ti.n0;
+                for (int g = 0; ok && g < G; ++g) {
+                    const uint32_t slot = a_iss % kStages, ph = (a_iss / kStages) & 1;
+                    if (!mbar_wait(bar(BarIdx::a_empty + slot), ph ^ 1, s_abort, p.err,
+                                   ROLE_PRODUCER, 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bar(BarIdx::a_full + slot), kAStageBytes);
+                    tma_load_2d(sA + slot * kAStageBytes, &tmap_w, g * kGroupK, wrow,
+                                bar(BarIdx::a_full + slot));
+                    ++a_iss;
+                    for (int h = 0; h < nb; ++h) {
+                        const uint32_t bslot = b_iss % kBStages, bph = (b_iss / kBStages) & 1;
+                        const int rows_h = batch_rows(n_eff, nb, h);
+                        const int nbox = (rows_h + kBoxRows - 1) / kBoxRows;
+                        if (!mbar_wait(bar(BarIdx::b_empty + bslot), bph ^ 1, s_abort, p.err,
+                                       ROLE_PRODUCER, 2)) { ok = false; break; }
+                        mbar_arrive_expect_tx(bar(BarIdx::b_full + bslot),
+                                              2u * nbox * kBoxRows * 128u);
+                        for (int a = 0; a < 2; ++a)
+                            for (int i = 0; i < nbox; ++i)
+                                tma_load_2d(sB + bslot * kBStageBytes + a * kBAtomBytes +
+                                                i * kBoxRows * 128,
+                                            &tmap_x, g * kGroupK + a * 64,
+                                            ti.m0 + h * kBatchRows + i * kBoxRows,
+                                            bar(BarIdx::b_full + bslot));
+                        ++b_iss;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA exits: the
+                // last kStages issues cover the latest use of every slot.
+                for (uint32_t i = a_iss > kStages ? a_iss - kStages : 0; i < a_iss; ++i)
+                    drain_wait(bar(BarIdx::a_full + i % kStages), (i / kStages) & 1);
+                for (uint32_t i = b_iss > kBStages ? b_iss - kBStages : 0; i < b_iss; ++i)
+                    drain_wait(bar(BarIdx::b_full + i % kBStages), (i / kBStages) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t gs = 0, bs = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const int nb = n_eff > kBatchRows ? 2 : 1;
+                for (int g = 0; ok && g < G; ++g, ++gs) {
+                    const uint32_t slot = gs % kStages, ph = (gs / kStages) & 1;
+                    if (!mbar_wait(bar(BarIdx::ta_full + slot), ph, s_abort, p.err, ROLE_MMA, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int h = 0; h < nb; ++h, ++bs) {
+                        const uint32_t bslot = bs % kBStages, bph = (bs / kBStages) & 1;
+                        const uint32_t pbuf = bs & 1, pph = (bs >> 1) & 1;
+                        if (!mbar_wait(bar(BarIdx::b_full + bslot), bph, s_abort, p.err, ROLE_MMA,
+                                       2) ||
+                            !mbar_wait(bar(BarIdx::p_empty + pbuf), pph ^ 1, s_abort, p.err,
+                                       ROLE_MMA, 3)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t idesc =
+                            idesc_f16_f32(kTileN, static_cast<uint32_t>(batch_rows(n_eff, nb, h)));
+                        const uint32_t d_tmem = tmem_base + pbuf * 128u;
+                        const uint32_t a_tmem = tmem_base + kTmemA0 + slot * 64u;
+                        const uint32_t b0 = sB + bslot * kBStageBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bdesc =
+                                smem_desc_sw128(b0 + (kk >> 2) * kBAtomBytes + (kk & 3) * 32);
+                            mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(BarIdx::p_full + pbuf));
+                        mma_commit(bar(BarIdx::b_empty + bslot));
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(BarIdx::ta_empty + slot));
+                }
+            }
+            // All MMAs issued by this thread complete before TMEM is freed.
+            mma_commit(bar(BarIdx::drain));
+            drain_wait(bar(BarIdx::drain), 0);
+        }
+    }
+    } else if (wg == 1) {
+        // --------------------------------------- weight converter (A -> TMEM)
+        setmaxnreg_dec<kOtherRegs>();
+        const int row = threadIdx.x - 128;     // weight row within the tile = TMEM lane
+        const int q = warp & 3;                // TMEM lane quarter of this warp
+        uint32_t gs = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for (int g = 0; g < G; ++g, ++gs) {
+                const uint32_t slot = gs % kStages, ph = (gs / kStages) & 1;
+                if (!mbar_wait(bar(BarIdx::a_full + slot), ph, s_abort, p.err, ROLE_CONVERT, 1) ||
+                    !mbar_wait(bar(BarIdx::ta_empty + slot), ph ^ 1, s_abort, p.err, ROLE_CONVERT,
+                               2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *rowp = smem + kOffA + slot * kAStageBytes + row * 128;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kTmemA0 +
+                                       slot * 64u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r16[16];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * j + cc;  // 16-byte chunk = one MMA k-step
+                        const uint4 v =
+                            *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
+                        i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
+                        i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
+                        i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
+                        i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
+                    }
+                    tmem_st_16cols(taddr + j * 16, r16);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BarIdx::a_empty + slot));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BarIdx::ta_full + slot));
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        setmaxnreg_inc<kEpiRegs>();
+        const int ewg = wg - 2;                // 0 or 1
+        const int q = warp & 3;
+        const int lrow = q * 32 + lane;        // weight row within the tile = TMEM lane
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        float acc[4][32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[i][j] = 0.0f;
+        uint32_t bs = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+            const int n_eff = (ti.rows + 15) & ~15;
+            const int nb = n_eff > kBatchRows ? 2 : 1;
+            const int n_local = ti.n0 + lrow;
+            const bool n_ok = n_local < p.N;
+            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            for (int g = 0; ok && g < G; ++g) {
+                const float s = n_ok ? __ldg(swp + g) : 0.0f;
+                for (int h = 0; h < nb; ++h, ++bs) {
+                    const uint32_t pbuf = bs & 1, pph = (bs >> 1) & 1;
+                    if (!mbar_wait(bar(BarIdx::p_full + pbuf), pph, s_abort, p.err, ROLE_EPILOGUE,
+                                   1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = nb == 2 ? 4 * ewg + i : 2 * i + ewg;  // 32-column chunk
+                        const bool in_batch = nb == 2 ? ((c >> 2) == h) : true;
+                        if (in_batch && c * 32 < n_eff) {
+                            const int col_in_buf = nb == 2 ? (c & 3) * 32 : c * 32;
+                            uint32_t v[32];
+                            tmem_ld_32cols_sync(lane_base + pbuf * 128u + col_in_buf, v);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                acc[i][j] = fmaf(__uint_as_float(v[j]), s, acc[i][j]);
+                            if (p.dbg != nullptr && n_ok) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    const int col = c * 32 + j;
+                                    if (col < ti.rows)
+                                        p.dbg[(static_cast<size_t>(ti.m0 + col) * p.N + n_local) *
+                                                  G + g] = __float2int_rn(__uint_as_float(v[j]));
+                                }
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BarIdx::p_empty + pbuf));
+                }
+            }
+            if (!ok) break;
+            // Token scale and store: Y[m, n] = sa[m] * acc.
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = nb == 2 ? 4 * ewg + i : 2 * i + ewg;
+                if (c * 32 < n_eff && n_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = c * 32 + j;
+                        if (col < ti.rows) {
+                            const int m = ti.m0 + col;
+                            const float out = acc[i][j] * __ldg(p.sa + m);
+                            const size_t idx = static_cast<size_t>(m) * p.N + n_local;
+                            if (p.out_fp32)
+                                static_cast<float *>(p.y)[idx] = out;
+                            else
+                                static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[i][j] = 0.0f;
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_bytes, const void *ptr,
+               uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+    auto fn = get_encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * elem_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
+    CUtensorMap tw, tx;
+    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
+                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
+        !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x16, (uint64_t)pr.K,
+                   (uint64_t)pr.R, 64, kBoxRows))
+        return cudaErrorInvalidValue;
+
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        // setmaxnreg.inc can only take registers the CTA was launched with:
+        // refuse to launch unless the launch allocation covers the split.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs * kThreads < (kThreads / 2) * (kEpiRegs + kOtherRegs))
+            return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(w8a8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = 1;
+    }
+
+    KParams kp;
+    kp.sa = pr.sa;
+    kp.sw = pr.sw;
+    kp.offsets = pr.offsets;
+    kp.y = pr.y;
+    kp.dbg = pr.debug_partials;
+    kp.R = static_cast<int>(pr.R);
+    kp.E = static_cast<int>(pr.E);
+    kp.N = static_cast<int>(pr.N);
+    kp.K = static_cast<int>(pr.K);
+    kp.G = static_cast<int>(pr.K / kGroupK);
+    kp.n_tiles = static_cast<int>((pr.N + kTileN - 1) / kTileN);
+    kp.out_fp32 = pr.out_fp32 ? 1 : 0;
+    unsigned long long *err = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
+    if (e != cudaSuccess) return e;
+    kp.err = err;
+
+    // Upper bound on the number of tiles (exact for one dense segment).
+    const int64_t m_tiles_bound =
+        pr.offsets == nullptr ? (pr.R + kTileTokens - 1) / kTileTokens
+                              : (pr.R + kTileTokens - 1) / kTileTokens + pr.E;
+    const int64_t tiles_bound = m_tiles_bound * kp.n_tiles;
+    const int64_t grid = tiles_bound < num_sms ? tiles_bound : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    w8a8_gemm_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tw, tx, kp);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_error(unsigned long long *value, bool clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(unsigned long long));
+    if (e != cudaSuccess) return e;
+    if (clear && *value != 0) {
+        const unsigned long long zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    }
+    return e;
+}
+
+}  // namespace w8a8

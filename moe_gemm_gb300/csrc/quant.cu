@@ -1,0 +1,242 @@
+// Quantizer kernels for sm_103a:
+//  * per-token dynamic activation quantization ("Deploying Hunyuan 770B in
+//    INT8 on domestic accelerators", §3.1: activations quantized per token,
+//    dynamically; codes = round(x / scale));
+//  * per-row, per-128-K-group weight quantization (same section: weights in
+//    groups of 128 elements, one scale per group);
+//  * the fp16 staging copy of int8 activation codes that the tensor-core
+//    GEMM consumes as its B operand (exact: every int8 is an fp16 integer).
+//
+// All three are HBM-bound streaming kernels: 16-byte vector loads, one CTA
+// (activation) or one warp (weight group) per reduction, warp-shuffle amax.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w8a8 {
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) {
+    return __uint_as_float(h << 16);
+}
+
+// round(x / s) with IEEE division and round-half-even, clamped to [-127, 127].
+__device__ __forceinline__ int quantize_exact(float x, float s) {
+    const int q = __float2int_rn(__fdiv_rn(x, s));
+    return max(-127, min(127, q));
+}
+
+// Same result as quantize_exact(x, s) for a normal s > 0, computed with the
+// reciprocal r = fl(1/s): y = fl(x*r) differs from the quotient x/s by at most
+// 2^-23 * |x/s| <= 1.6e-5 (|x/s| <= 127.00001), and fl(x/s) differs from x/s
+// by at most 0.8e-5. Unless y lies within 3e-5 of a half-integer, y and
+// fl(x/s) round to the same integer; inside that window the exact division
+// decides. So the codes are identical to round(fl(x/s)) in every case.
+__device__ __forceinline__ int quantize_fast(float x, float s, float r) {
+    const float y = x * r;
+    const float yi = rintf(y);
+    int q;
+    if (fabsf(y - yi) >= 0.5f - 3.0e-5f)
+        q = __float2int_rn(__fdiv_rn(x, s));
+    else
+        q = static_cast<int>(yi);
+    return max(-127, min(127, q));
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+    return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
+           ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
+}
+
+// Block-wide max of non-negative 32-bit integers (all threads get the result).
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = lane < (kQuantThreads / 32) ? red[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Quantize 8 BF16 values (one 16-byte vector) into 8 int8 codes.
+__device__ __forceinline__ uint2 quantize8(const uint4 v, float s, float r, bool fast) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        const float hi = bf16_bits_to_f32(w[i] >> 16);
+        if (s == 0.0f) {
+            q[2 * i] = 0;
+            q[2 * i + 1] = 0;
+        } else if (fast) {
+            q[2 * i] = quantize_fast(lo, s, r);
+            q[2 * i + 1] = quantize_fast(hi, s, r);
+        } else {
+            q[2 * i] = quantize_exact(lo, s);
+            q[2 * i + 1] = quantize_exact(hi, s);
+        }
+    }
+    return make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
+}
+
+// Max of |bf16| over a 16-byte vector, as the BF16 magnitude bit pattern:
+// for finite values, ordering of |x| equals the unsigned ordering of (bits & 0x7FFF).
+__device__ __forceinline__ uint32_t amax_bits8(const uint4 v) {
+    uint32_t m = 0;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = max(m, w[i] & 0x7FFFu);
+        m = max(m, (w[i] >> 16) & 0x7FFFu);
+    }
+    return m;
+}
+
+// One CTA per token row; the row stays in registers between the amax pass and
+// the quantize pass (VPT 16-byte vectors per thread, K <= 256 * 8 * VPT).
+template <int VPT>
+__global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
+    const uint16_t *__restrict__ a, int K, int64_t lda, int8_t *__restrict__ qa, int64_t ldq,
+    float *__restrict__ sa) {
+    __shared__ uint32_t red[kQuantThreads / 32];
+    const int64_t row = blockIdx.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a + row * lda);
+    uint2 *dst = reinterpret_cast<uint2 *>(qa + row * ldq);
+    const int nvec = K >> 3;
+    uint4 v[VPT];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * kQuantThreads;
+        v[i] = idx < nvec ? __ldcs(src + idx) : make_uint4(0, 0, 0, 0);
+        m = max(m, amax_bits8(v[i]));
+    }
+    m = block_max_u32(m, red);
+    const float amax = bf16_bits_to_f32(m);
+    const float s = __fdiv_rn(amax, 127.0f);
+    const bool fast = s >= 1.17549435e-38f;  // normal scale: 1/s is finite
+    const float r = fast ? __frcp_rn(s) : 0.0f;
+    if (threadIdx.x == 0) sa[row] = s;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * kQuantThreads;
+        if (idx < nvec) __stcs(dst + idx, quantize8(v[i], s, r, fast));
+    }
+}
+
+// Any K / stride / alignment: scalar two-pass version (re-reads the row).
+__global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
+    const uint16_t *__restrict__ a, int K, int64_t lda, int8_t *__restrict__ qa, int64_t ldq,
+    float *__restrict__ sa) {
+    __shared__ uint32_t red[kQuantThreads / 32];
+    const int64_t row = blockIdx.x;
+    const uint16_t *src = a + row * lda;
+    uint32_t m = 0;
+    for (int k = threadIdx.x; k < K; k += kQuantThreads) m = max(m, (uint32_t)src[k] & 0x7FFFu);
+    m = block_max_u32(m, red);
+    const float s = __fdiv_rn(bf16_bits_to_f32(m), 127.0f);
+    if (threadIdx.x == 0) sa[row] = s;
+    for (int k = threadIdx.x; k < K; k += kQuantThreads)
+        qa[row * ldq + k] =
+            static_cast<int8_t>(s == 0.0f ? 0 : quantize_exact(bf16_bits_to_f32(src[k]), s));
+}
+
+// One warp per (row n, group g): 128 floats, 4 per lane.
+__global__ void __launch_bounds__(256) quant_weight_kernel(const float *__restrict__ w, int64_t N,
+                                                           int K, int8_t *__restrict__ qw,
+                                                           float *__restrict__ sw) {
+    const int G = K / 128;
+    const int64_t item = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (item >= N * G) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t n = item / G;
+    const int g = static_cast<int>(item % G);
+    const float4 x = *reinterpret_cast<const float4 *>(w + n * K + g * 128 + lane * 4);
+    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float s = __fdiv_rn(m, 127.0f);
+    if (lane == 0) sw[n * G + g] = s;
+    uint32_t packed = 0;
+    if (s != 0.0f)
+        packed = pack4(quantize_exact(x.x, s), quantize_exact(x.y, s), quantize_exact(x.z, s),
+                       quantize_exact(x.w, s));
+    *reinterpret_cast<uint32_t *>(qw + n * K + g * 128 + lane * 4) = packed;
+}
+
+// int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] (dense).
+__global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restrict__ q,
+                                                          int64_t rows, int K, int64_t ldq,
+                                                          __half *__restrict__ out) {
+    const int vec_per_row = K >> 4;  // 16 codes per vector
+    const int64_t total = rows * vec_per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / vec_per_row;
+        const int c = static_cast<int>(i % vec_per_row);
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(q + r * ldq) + c);
+        uint4 o0, o1;
+        i8x4_to_f16x4(v.x, o0.x, o0.y);
+        i8x4_to_f16x4(v.y, o0.z, o0.w);
+        i8x4_to_f16x4(v.z, o1.x, o1.y);
+        i8x4_to_f16x4(v.w, o1.z, o1.w);
+        uint4 *d = reinterpret_cast<uint4 *>(out + r * K) + 2 * c;
+        d[0] = o0;
+        d[1] = o1;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
+                             int64_t ldq, float *sa, cudaStream_t stream) {
+    const bool vec_ok = (K % 8 == 0) && (lda % 8 == 0) && (ldq % 8 == 0) &&
+                        (reinterpret_cast<uintptr_t>(a) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(qa) % 8 == 0);
+    const int k = static_cast<int>(K);
+    const dim3 grid(static_cast<unsigned>(M));
+    if (vec_ok && K <= 256 * 8 * 1)
+        quant_act_vec_kernel<1><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
+    else if (vec_ok && K <= 256 * 8 * 2)
+        quant_act_vec_kernel<2><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
+    else if (vec_ok && K <= 256 * 8 * 4)
+        quant_act_vec_kernel<4><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
+    else if (vec_ok && K <= 256 * 8 * 8)
+        quant_act_vec_kernel<8><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
+    else
+        quant_act_generic_kernel<<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
+                                cudaStream_t stream) {
+    const int64_t items = N * (K / 128);
+    const unsigned blocks = static_cast<unsigned>((items + 7) / 8);
+    quant_weight_kernel<<<blocks, 256, 0, stream>>>(w, N, static_cast<int>(K), qw, sw);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
+                               int num_sms, cudaStream_t stream) {
+    const int64_t total = rows * (K / 16);
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    widen_codes_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        q, rows, static_cast<int>(K), ldq, static_cast<__half *>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace w8a8

@@ -11,3 +11,16 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def pytest_sessionstart(session):
+    # On a GPU machine, make sure the CUDA library is built for this host
+    # before the GPU tests import it (compiled objects are never shared
+    # between machines).
+    try:
+        import torch
+    except ImportError:
+        return
+    if torch.cuda.is_available():
+        import __graft_entry__
+        __graft_entry__.build()

@@ -1,0 +1,116 @@
+"""CPU tests of the C ABI: the library loads, exports every function that
+include/w8a8.h declares, and rejects bad arguments on the host before any
+device work (no compute calls here: no GPU is needed or touched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w8a8.h")
+
+OK, INVALID, UNSUPPORTED, CUDA_ERR, WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
+    L = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.w8a8_quant_act.argtypes = [vp, i64, i64, i64, vp, i64, vp, vp]
+    L.w8a8_quant_weight.argtypes = [vp, i64, i64, vp, vp, vp]
+    L.w8a8_gemm.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, ctypes.c_size_t, vp]
+    L.w8a8_grouped_gemm.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, vp,
+                                    ctypes.c_size_t, vp]
+    L.w8a8_gemm_workspace_size.argtypes = [i64, i64, i64]
+    L.w8a8_gemm_workspace_size.restype = ctypes.c_size_t
+    L.w8a8_grouped_gemm_workspace_size.argtypes = [i64, i64, i64, i64]
+    L.w8a8_grouped_gemm_workspace_size.restype = ctypes.c_size_t
+    L.w8a8_status_string.argtypes = [i32]
+    L.w8a8_status_string.restype = ctypes.c_char_p
+    return L
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(w8a8_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert {"w8a8_quant_act", "w8a8_gemm", "w8a8_grouped_gemm"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in w8a8.h but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"W8A8_OK"), (1, b"W8A8_ERR_INVALID_ARG"), (4, b"W8A8_ERR_WORKSPACE"),
+                       (99, b"W8A8_UNKNOWN_STATUS")]:
+        assert lib.w8a8_status_string(code) == name
+
+
+def test_workspace_size(lib):
+    assert lib.w8a8_gemm_workspace_size(0, 128, 128) == 0
+    assert lib.w8a8_gemm_workspace_size(3, 128, 128) == 768
+    assert lib.w8a8_gemm_workspace_size(32, 28672, 8192) == 32 * 8192 * 2
+    assert lib.w8a8_grouped_gemm_workspace_size(4096, 64, 3072, 4096) == 4096 * 4096 * 2
+
+
+FAKE = 1 << 20      # a 16-byte aligned non-null value; never dereferenced here
+
+
+def gemm(lib, qa=FAKE, sa=FAKE, qw=FAKE, sw=FAKE, y=FAKE, dt=0, M=16, N=128, K=128, dbg=None,
+         ws=FAKE, wsb=1 << 30):
+    return lib.w8a8_gemm(qa, sa, qw, sw, y, dt, M, N, K, dbg, ws, wsb, None)
+
+
+def test_gemm_host_validation(lib):
+    assert gemm(lib, K=100) == INVALID                 # K % 128 != 0
+    assert gemm(lib, K=0) == INVALID
+    assert gemm(lib, N=0) == INVALID
+    assert gemm(lib, M=-1) == INVALID
+    assert gemm(lib, qa=None) == INVALID
+    assert gemm(lib, sw=None) == INVALID
+    assert gemm(lib, qa=FAKE + 8) == INVALID           # TMA operand not 16-byte aligned
+    assert gemm(lib, sa=FAKE + 2) == INVALID
+    assert gemm(lib, dt=7) == INVALID
+    assert gemm(lib, ws=None) == WORKSPACE
+    assert gemm(lib, wsb=16 * 128 * 2 - 1) == WORKSPACE
+    assert gemm(lib, ws=FAKE + 16) == WORKSPACE        # workspace must be 256-byte aligned
+    assert gemm(lib, M=1 << 24, K=1 << 10) == INVALID  # operand above 2^31 elements
+    assert gemm(lib, M=0) == OK                        # no-op, no device work
+
+
+def test_grouped_host_validation(lib):
+    def call(off=FAKE, E=4, R=64, N=128, K=256, wsb=1 << 30):
+        return lib.w8a8_grouped_gemm(FAKE, FAKE, off, FAKE, FAKE, FAKE, 0, R, E, N, K, None,
+                                     FAKE, wsb, None)
+    assert call(off=None) == INVALID
+    assert call(E=0) == INVALID
+    assert call(E=1025) == INVALID
+    assert call(K=129) == INVALID
+    assert call(off=FAKE + 2) == INVALID
+    assert call(wsb=10) == WORKSPACE
+    assert call(R=0) == OK
+
+
+def test_quant_host_validation(lib):
+    assert lib.w8a8_quant_act(FAKE, 4, 0, 0, FAKE, 0, FAKE, None) == INVALID
+    assert lib.w8a8_quant_act(FAKE, 4, 64, 32, FAKE, 64, FAKE, None) == INVALID   # lda < K
+    assert lib.w8a8_quant_act(None, 4, 64, 64, FAKE, 64, FAKE, None) == INVALID
+    assert lib.w8a8_quant_act(FAKE, 0, 64, 64, FAKE, 64, FAKE, None) == OK
+    assert lib.w8a8_quant_weight(FAKE, 4, 100, FAKE, FAKE, None) == INVALID
+    assert lib.w8a8_quant_weight(FAKE + 4, 4, 128, FAKE, FAKE, None) == INVALID
+    assert lib.w8a8_quant_weight(FAKE, 0, 128, FAKE, FAKE, None) == OK
+
+
+def test_no_device_gives_cuda_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful without a GPU")
+    # Valid arguments reach the device check, which fails without a GPU; the
+    # fake pointers are never used.
+    assert lib.w8a8_quant_act(FAKE, 4, 64, 64, FAKE, 64, FAKE, None) in (CUDA_ERR, UNSUPPORTED)
