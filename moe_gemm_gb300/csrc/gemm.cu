@@ -64,19 +64,19 @@ constexpr int kBAtomBytes = kBatchRows * 128;                  // 128 rows x 64 
 constexpr int kBStageBytes = 2 * kBAtomBytes;                  // 32 KB
 constexpr int kTmemCols = 512;
 constexpr int kTmemA0 = 256;        // A operand slot s at columns [256 + 64 s, +64)
-constexpr int kEpiRegs = 184;   // 256 threads x 184 + 256 x 72 = 512 x 128 at launch
-constexpr int kOtherRegs = 72;
+constexpr int kEpiRegs = 192;   // 256 threads x 192 + 256 x 64 = 512 x 128 at launch
+constexpr int kOtherRegs = 64;
 
 // Shared memory layout (offsets from a 1024-byte aligned base).
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kAStageBytes;
 constexpr int kOffBar = kOffB + kBStages * kBStageBytes;
-constexpr int kNumBars = 6 * kStages + 2 * 2 + 1;     // see BarIdx
-constexpr int kOffMisc = kOffBar + 8 * 32;
+constexpr int kNumBars = 6 * kStages + 2 * 2 + 1 + kBStages;     // see BarIdx
+constexpr int kOffMisc = kOffBar + 8 * 64;
 constexpr int kOffTab = kOffMisc + 64;
 constexpr int kTabBytes = 3 * (kMaxExperts + 1) * 4;
 constexpr int kSmemBytes = kOffTab + kTabBytes + 1024;  // + alignment slack
-static_assert(kNumBars <= 32, "barrier area");
+static_assert(kNumBars <= 64, "barrier area");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert((kThreads / 2) * (kEpiRegs + kOtherRegs) == 65536, "register split");
 
@@ -90,8 +90,9 @@ struct BarIdx {
     static constexpr int p_full = 4 * kStages + 2 * kBStages;   // [2] MMA -> epilogue
     static constexpr int p_empty = p_full + 2;       // [2] epilogue -> MMA
     static constexpr int drain = p_empty + 2;        // MMA completion at exit
+    static constexpr int b_ready = drain + 1;        // [kBStages] token converter -> MMA
 };
-static_assert(BarIdx::drain < 32, "barrier count");
+static_assert(BarIdx::b_ready + kBStages <= 64, "barrier count");
 
 struct KParams {
     const float *sa;
@@ -109,6 +110,7 @@ struct TileInfo {
     int e, n0, m0, rows;
 };
 
+template <int kTT>
 __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const int *s_lo,
                                                 const int *s_cnt, int E, int n_tiles) {
     int lo = 0, hi = E;  // s_base[lo] <= t < s_base[hi]
@@ -118,14 +120,14 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const 
     }
     const int local = t - s_base[lo];
     const int cnt = s_cnt[lo];
-    const int m_tiles = (cnt + kTileTokens - 1) / kTileTokens;
+    const int m_tiles = (cnt + kTT - 1) / kTT;
     const int nt = local / m_tiles;
     const int mt = local - nt * m_tiles;
     TileInfo ti;
     ti.e = lo;
     ti.n0 = nt * kTileN;
-    ti.m0 = s_lo[lo] + mt * kTileTokens;
-    ti.rows = min(kTileTokens, cnt - mt * kTileTokens);
+    ti.m0 = s_lo[lo] + mt * kTT;
+    ti.rows = min(kTT, cnt - mt * kTT);
     return ti;
 }
 
@@ -142,9 +144,16 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// kBInt8 = true: the token operand arrives as int8 codes (TMA box of 128
+// bytes x 32 rows landing in the upper half of a B stage) and warps 2-3 widen
+// it to fp16 in place; tiles hold at most 128 token rows. kBInt8 = false: the
+// token operand is an fp16 staging copy loaded directly by TMA; tiles hold up
+// to 256 token rows in two MMA batches.
+template <bool kBInt8>
 __global__ void __launch_bounds__(kThreads, 1)
 w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
+    constexpr int kTT = kBInt8 ? kBatchRows : kTileTokens;   // token rows per tile
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -181,6 +190,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(bar(BarIdx::p_empty + i), 8);
         }
         mbar_init(bar(BarIdx::drain), 1);
+        for (int i = 0; i < kBStages; ++i) mbar_init(bar(BarIdx::b_ready + i), 2);
         *s_abort = 0;
         fence_mbarrier_init();
     }
@@ -211,7 +221,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     cnt = p.R;
                 }
             }
-            const int tiles = (e < p.E) ? p.n_tiles * ((cnt + kTileTokens - 1) / kTileTokens) : 0;
+            const int tiles = (e < p.E) ? p.n_tiles * ((cnt + kTT - 1) / kTT) : 0;
             int incl = tiles;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -249,7 +259,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
             uint32_t a_iss = 0, b_iss = 0;   // loads issued so far
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+                const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
                 const int n_eff = (ti.rows + 15) & ~15;
                 const int nb = n_eff > kBatchRows ? 2 : 1;
                 const int wrow = ti.e * p.N + ti.n0;
@@ -267,15 +277,26 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const int nbox = (rows_h + kBoxRows - 1) / kBoxRows;
                         if (!mbar_wait(bar(BarIdx::b_empty + bslot), bph ^ 1, s_abort, p.err,
                                        ROLE_PRODUCER, 2)) { ok = false; break; }
-                        mbar_arrive_expect_tx(bar(BarIdx::b_full + bslot),
-                                              2u * nbox * kBoxRows * 128u);
-                        for (int a = 0; a < 2; ++a)
+                        if constexpr (kBInt8) {
+                            // int8 codes: one 128-byte box column, into the upper atom.
+                            mbar_arrive_expect_tx(bar(BarIdx::b_full + bslot),
+                                                  nbox * kBoxRows * 128u);
                             for (int i = 0; i < nbox; ++i)
-                                tma_load_2d(sB + bslot * kBStageBytes + a * kBAtomBytes +
+                                tma_load_2d(sB + bslot * kBStageBytes + kBAtomBytes +
                                                 i * kBoxRows * 128,
-                                            &tmap_x, g * kGroupK + a * 64,
-                                            ti.m0 + h * kBatchRows + i * kBoxRows,
+                                            &tmap_x, g * kGroupK, ti.m0 + i * kBoxRows,
                                             bar(BarIdx::b_full + bslot));
+                        } else {
+                            mbar_arrive_expect_tx(bar(BarIdx::b_full + bslot),
+                                                  2u * nbox * kBoxRows * 128u);
+                            for (int a = 0; a < 2; ++a)
+                                for (int i = 0; i < nbox; ++i)
+                                    tma_load_2d(sB + bslot * kBStageBytes + a * kBAtomBytes +
+                                                    i * kBoxRows * 128,
+                                                &tmap_x, g * kGroupK + a * 64,
+                                                ti.m0 + h * kBatchRows + i * kBoxRows,
+                                                bar(BarIdx::b_full + bslot));
+                        }
                         ++b_iss;
                     }
                 }
@@ -295,7 +316,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
             uint32_t gs = 0, bs = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+                const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
                 const int n_eff = (ti.rows + 15) & ~15;
                 const int nb = n_eff > kBatchRows ? 2 : 1;
                 for (int g = 0; ok && g < G; ++g, ++gs) {
@@ -308,8 +329,8 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     for (int h = 0; h < nb; ++h, ++bs) {
                         const uint32_t bslot = bs % kBStages, bph = (bs / kBStages) & 1;
                         const uint32_t pbuf = bs & 1, pph = (bs >> 1) & 1;
-                        if (!mbar_wait(bar(BarIdx::b_full + bslot), bph, s_abort, p.err, ROLE_MMA,
-                                       2) ||
+                        const int b_bar = kBInt8 ? BarIdx::b_ready : BarIdx::b_full;
+                        if (!mbar_wait(bar(b_bar + bslot), bph, s_abort, p.err, ROLE_MMA, 2) ||
                             !mbar_wait(bar(BarIdx::p_empty + pbuf), pph ^ 1, s_abort, p.err,
                                        ROLE_MMA, 3)) {
                             ok = false;
@@ -337,6 +358,56 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
             // All MMAs issued by this thread complete before TMEM is freed.
             mma_commit(bar(BarIdx::drain));
             drain_wait(bar(BarIdx::drain), 0);
+        }
+    } else if (kBInt8) {
+        // ------------------------------ token converter (int8 -> fp16 in place)
+        // Row r of the stage's upper atom holds 128 int8 codes (128B swizzle);
+        // one thread reads the whole row into registers, then writes its fp16
+        // codes K 0..63 to the lower atom and K 64..127 over the int8 row.
+        const int tid = threadIdx.x - 64;      // 0..63
+        uint32_t bseq = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+            const int n_eff = (ti.rows + 15) & ~15;
+            for (int g = 0; g < G; ++g, ++bseq) {
+                const uint32_t bslot = bseq % kBStages, bph = (bseq / kBStages) & 1;
+                if (!mbar_wait(bar(BarIdx::b_full + bslot), bph, s_abort, p.err, ROLE_CONVERT, 3)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *stage = smem + kOffB + bslot * kBStageBytes;
+                for (int r = tid; r < n_eff; r += 64) {
+                    const int sw = r & 7;
+                    uint8_t *row0 = stage + r * 128;
+                    uint8_t *row1 = stage + kBAtomBytes + r * 128;
+                    // Chunks 0-3 (K 0..63) go to the lower atom; chunks 4-7 are
+                    // read before the upper atom row (their own storage) is written.
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint4 src[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            src[c] = *reinterpret_cast<const uint4 *>(
+                                row1 + (((4 * half + c) ^ sw) << 4));
+                        uint8_t *dst = half == 0 ? row0 : row1;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 lo, hi;
+                            i8x4_to_f16x4(src[c].x, lo.x, lo.y);
+                            i8x4_to_f16x4(src[c].y, lo.z, lo.w);
+                            i8x4_to_f16x4(src[c].z, hi.x, hi.y);
+                            i8x4_to_f16x4(src[c].w, hi.z, hi.w);
+                            const int j = 2 * c;
+                            *reinterpret_cast<uint4 *>(dst + ((j ^ sw) << 4)) = lo;
+                            *reinterpret_cast<uint4 *>(dst + (((j + 1) ^ sw) << 4)) = hi;
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BarIdx::b_ready + bslot));
+            }
         }
     }
     } else if (wg == 1) {
@@ -397,14 +468,23 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
         uint32_t bs = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+            const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
             const int n_eff = (ti.rows + 15) & ~15;
             const int nb = n_eff > kBatchRows ? 2 : 1;
             const int n_local = ti.n0 + lrow;
             const bool n_ok = n_local < p.N;
             const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            // Weight scales of this row, prefetched four groups ahead so the
+            // global-memory latency never sits between an MMA batch and its drain.
+            auto load_sw = [&](int g) -> float { return (n_ok && g < G) ? __ldg(swp + g) : 0.0f; };
+            float s_ring0 = load_sw(0), s_ring1 = load_sw(1), s_ring2 = load_sw(2),
+                  s_ring3 = load_sw(3);
             for (int g = 0; ok && g < G; ++g) {
-                const float s = n_ok ? __ldg(swp + g) : 0.0f;
+                const float s = s_ring0;
+                s_ring0 = s_ring1;
+                s_ring1 = s_ring2;
+                s_ring2 = s_ring3;
+                s_ring3 = load_sw(g + 4);
                 for (int h = 0; h < nb; ++h, ++bs) {
                     const uint32_t pbuf = bs & 1, pph = (bs >> 1) & 1;
                     if (!mbar_wait(bar(BarIdx::p_full + pbuf), pph, s_abort, p.err, ROLE_EPILOGUE,
@@ -504,15 +584,19 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_bytes, c
     return r == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
+template <bool kBInt8>
+cudaError_t launch_gemm_impl(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
+    constexpr int kTT = kBInt8 ? kBatchRows : kTileTokens;
     CUtensorMap tw, tx;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
-                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
-        !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x16, (uint64_t)pr.K,
-                   (uint64_t)pr.R, 64, kBoxRows))
+                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN))
         return cudaErrorInvalidValue;
+    const bool ok_x =
+        kBInt8 ? encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.x, (uint64_t)pr.K,
+                           (uint64_t)pr.R, 128, kBoxRows)
+               : encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x, (uint64_t)pr.K,
+                           (uint64_t)pr.R, 64, kBoxRows);
+    if (!ok_x) return cudaErrorInvalidValue;
 
     static int attr_done[64] = {0};
     int dev = 0;
@@ -521,12 +605,12 @@ cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream)
         // setmaxnreg.inc can only take registers the CTA was launched with:
         // refuse to launch unless the launch allocation covers the split.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel);
+        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel<kBInt8>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs * kThreads < (kThreads / 2) * (kEpiRegs + kOtherRegs))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(w8a8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+        e = cudaFuncSetAttribute(w8a8_gemm_kernel<kBInt8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
@@ -550,14 +634,21 @@ cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     kp.err = err;
 
     // Upper bound on the number of tiles (exact for one dense segment).
-    const int64_t m_tiles_bound =
-        pr.offsets == nullptr ? (pr.R + kTileTokens - 1) / kTileTokens
-                              : (pr.R + kTileTokens - 1) / kTileTokens + pr.E;
+    const int64_t m_tiles_bound = pr.offsets == nullptr ? (pr.R + kTT - 1) / kTT
+                                                        : (pr.R + kTT - 1) / kTT + pr.E;
     const int64_t tiles_bound = m_tiles_bound * kp.n_tiles;
     const int64_t grid = tiles_bound < num_sms ? tiles_bound : num_sms;
     if (grid <= 0) return cudaSuccess;
-    w8a8_gemm_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tw, tx, kp);
+    w8a8_gemm_kernel<kBInt8>
+        <<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tw, tx, kp);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
+    return pr.x_int8 ? launch_gemm_impl<true>(pr, num_sms, stream)
+                     : launch_gemm_impl<false>(pr, num_sms, stream);
 }
 
 cudaError_t read_device_error(unsigned long long *value, bool clear) {

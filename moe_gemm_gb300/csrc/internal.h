@@ -22,7 +22,8 @@ struct GemmProblem {
     const float *sa;          // [R]
     const float *sw;          // [E*N, G]
     const int8_t *qw;         // [E*N, K]
-    const void *x16;          // [R, K] fp16 codes (staged activations)
+    const void *x;            // [R, K] activation codes: int8 (x_int8) or an fp16 staging copy
+    bool x_int8;              // true: tiles of <= 128 token rows widened in shared memory
     const int32_t *offsets;   // [E+1] device, or nullptr for one dense segment [0, R)
     void *y;                  // [R, N]
     int32_t *debug_partials;  // nullable [R, N, G]
@@ -32,6 +33,10 @@ struct GemmProblem {
 
 // Maximum number of experts a grouped call may have.
 constexpr int kMaxExperts = 1024;
+
+// Dense calls with at most this many token rows read the int8 codes directly
+// (no staging copy); larger ones use 256-row tiles over an fp16 staging copy.
+constexpr int64_t kDirectMaxRows = 128;
 
 cudaError_t launch_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
 
