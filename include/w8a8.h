@@ -84,8 +84,9 @@ w8a8_status w8a8_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, 
                               w8a8_stream_t stream);
 
 /*
- * Bytes of device workspace w8a8_gemm needs for an M x K activation operand
- * (the tensor-core operand staging buffer). 0 when M == 0.
+ * Bytes of device workspace w8a8_gemm needs: an fp16 copy of the M x K int8
+ * activation codes (the tensor-core operand), rounded up to 256 bytes.
+ * 0 when M == 0.
  */
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -111,7 +112,8 @@ w8a8_status w8a8_gemm(const int8_t *qa, const float *sa, const int8_t *qw, const
                       w8a8_stream_t stream);
 
 /*
- * Bytes of device workspace w8a8_grouped_gemm needs for R routed rows.
+ * Bytes of device workspace w8a8_grouped_gemm needs for R routed rows (an
+ * fp16 copy of the R x K activation codes, rounded up to 256 bytes).
  */
 size_t w8a8_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K);
 

@@ -54,10 +54,10 @@ w8a8_status from_cuda(cudaError_t e) { return e == cudaSuccess ? W8A8_OK : W8A8_
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace: fp16 staging copy of the int8 activation codes [rows, K], used
-// only by dense calls with more than kDirectMaxRows rows.
+// Workspace: fp16 staging copy of the int8 activation codes [rows, K] (the
+// tensor-core operand), rounded up to 256 bytes.
 size_t staging_bytes(int64_t rows, int64_t K) {
-    if (rows <= w8a8::kDirectMaxRows || K <= 0) return 0;
+    if (rows <= 0 || K <= 0) return 0;
     return round_up(static_cast<size_t>(rows) * static_cast<size_t>(K) * 2, kWsAlign);
 }
 
@@ -74,8 +74,7 @@ w8a8_status check_gemm(const int8_t *qa, const float *sa, const void *offsets, c
     if (!aligned(qa, 16) || !aligned(qw, 16) || !aligned(sa, 4) || !aligned(sw, 4) ||
         !aligned(y, 4) || (offsets && !aligned(offsets, 4)))
         return W8A8_ERR_INVALID_ARG;
-    const size_t need = grouped ? 0 : staging_bytes(R, K);
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, kWsAlign)))
+    if (!workspace || workspace_bytes < staging_bytes(R, K) || !aligned(workspace, kWsAlign))
         return W8A8_ERR_WORKSPACE;
     return W8A8_OK;
 }
@@ -87,17 +86,13 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
     w8a8_status st = check_device(&info);
     if (st != W8A8_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool direct = offsets != nullptr || R <= w8a8::kDirectMaxRows;
-    if (!direct) {
-        cudaError_t e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s);
-        if (e != cudaSuccess) return W8A8_ERR_CUDA;
-    }
+    cudaError_t e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s);
+    if (e != cudaSuccess) return W8A8_ERR_CUDA;
     w8a8::GemmProblem p;
     p.sa = sa;
     p.sw = sw;
     p.qw = qw;
-    p.x = direct ? static_cast<const void *>(qa) : workspace;
-    p.x_int8 = direct;
+    p.x16 = workspace;
     p.offsets = offsets;
     p.y = y;
     p.debug_partials = dbg;
@@ -160,11 +155,9 @@ size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
 }
 
 size_t w8a8_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K) {
-    (void)R;
     (void)E;
     (void)N;
-    (void)K;
-    return 0;
+    return staging_bytes(R, K);
 }
 
 w8a8_status w8a8_gemm(const int8_t *qa, const float *sa, const int8_t *qw, const float *sw,

@@ -15,17 +15,25 @@
 //    Each group gets a FRESH accumulator in tensor memory, so the tensor core
 //    never adds numbers that are not exactly representable.
 //  * Swap-AB: the MMA's M side (128 TMEM lanes) is 128 weight rows n, its N
-//    side is up to 128 token rows per MMA batch (two batches per 256-token
-//    tile). So the weight scale sw[n, g] is one register per epilogue thread.
-//  * Weights stay int8 in HBM. A converter warpgroup reads each TMA-landed
-//    int8 weight tile from shared memory, widens it in registers and writes
-//    the fp16 A operand straight into tensor memory (tcgen05.st); the MMA
-//    takes A from TMEM, which keeps the conversion off shared-memory
-//    bandwidth. Token codes arrive as fp16 via TMA (B operand, 128B swizzle).
-//  * Two 128-column partial buffers in TMEM alternate between MMA batches;
-//    two epilogue warpgroups drain them (tcgen05.ld), fma the partial with
-//    sw[n,g] into register accumulators, and at the end of the tile multiply
-//    by sa[m] and store BF16 (round to nearest even) or FP32.
+//    side is a batch of up to 128 token rows. So the weight scale sw[n, g] is
+//    one register per epilogue thread.
+//  * Weights stay int8 in HBM. TMA lands each 128 x 128 int8 weight tile in
+//    shared memory; a converter warpgroup widens it in registers and writes
+//    the fp16 A operand straight into tensor memory (tcgen05.st), so the
+//    widening costs no shared-memory bandwidth beyond one read.
+//  * Token operand: an fp16 copy of the int8 codes (written by a staging
+//    kernel just before this one) is loaded by TMA with the 128-byte swizzle.
+//    This kernel is launched as a programmatic dependent of the staging
+//    kernel: only the token producer waits for it (griddepcontrol.wait); the
+//    weight stream, the conversion and all set-up start at once.
+//  * Weight tiles and token tiles have separate producers and pipelines whose
+//    depths are chosen per call; narrow token batches (decode) leave room for
+//    ~11 weight tiles in flight per SM.
+//  * Up to 8 partial buffers in TMEM (as many batches as fit in 256 columns)
+//    rotate between the MMA issuer and two epilogue warpgroups, which drain
+//    them (tcgen05.ld), fma the partial with sw[n,g] into register
+//    accumulators, and at the end of the tile multiply by sa[m] and store
+//    BF16 (round to nearest even) or FP32.
 //  * Persistent CTAs walk a tile list built on the device from the expert
 //    offsets (no host read, graph-capture safe). Within an (expert, weight
 //    tile) the token tiles are consecutive so CTAs running together share the
@@ -52,47 +60,43 @@ __device__ unsigned long long g_device_error = 0;
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 4;          // weight tiles in flight (SMEM landing + TMEM operand slots)
-constexpr int kBStages = 4;         // token batches in flight
+constexpr int kMaxAStages = 12;     // weight tiles in flight (shared memory)
+constexpr int kMaxBStages = 8;      // token batches in flight
+constexpr int kTmemSlots = 4;       // fp16 weight operands resident in TMEM
+constexpr int kMaxPBufs = 8;        // fp32 group-partial buffers in TMEM columns [0, 256)
 constexpr int kTileN = 128;         // weight rows per tile = MMA M = TMEM lanes
 constexpr int kGroupK = 128;        // K elements per scale group = per pipeline stage
-constexpr int kTileTokens = 256;    // token rows per tile (two MMA batches)
-constexpr int kBatchRows = 128;     // token rows per MMA batch (MMA N <= 128)
+constexpr int kMaxBatchRows = 128;  // token rows per MMA batch (MMA N <= 128)
 constexpr int kBoxRows = 32;        // token rows per TMA box
-constexpr int kAStageBytes = kTileN * kGroupK;                 // 16 KB int8
-constexpr int kBAtomBytes = kBatchRows * 128;                  // 128 rows x 64 fp16
-constexpr int kBStageBytes = 2 * kBAtomBytes;                  // 32 KB
+constexpr int kAStageBytes = kTileN * kGroupK;   // 16 KB int8
 constexpr int kTmemCols = 512;
-constexpr int kTmemA0 = 256;        // A operand slot s at columns [256 + 64 s, +64)
-constexpr int kEpiRegs = 192;   // 256 threads x 192 + 256 x 64 = 512 x 128 at launch
-constexpr int kOtherRegs = 64;
+constexpr int kTmemA0 = 256;        // TMEM weight slot s at columns [256 + 64 s, +64)
+constexpr int kEpiRegs = 200;       // 256 threads x 200 + 256 x 56 = 512 x 128 at launch
+constexpr int kOtherRegs = 56;
+constexpr int kSmemLimit = 232448;
 
-// Shared memory layout (offsets from a 1024-byte aligned base).
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kAStageBytes;
-constexpr int kOffBar = kOffB + kBStages * kBStageBytes;
-constexpr int kNumBars = 6 * kStages + 2 * 2 + 1 + kBStages;     // see BarIdx
-constexpr int kOffMisc = kOffBar + 8 * 64;
+// Shared memory: a fixed area (barriers, flags, tile table), then the weight
+// stages, then the token stages (offsets from a 1024-byte aligned base).
+constexpr int kOffBar = 0;
+constexpr int kOffMisc = 8 * 128;
 constexpr int kOffTab = kOffMisc + 64;
 constexpr int kTabBytes = 3 * (kMaxExperts + 1) * 4;
-constexpr int kSmemBytes = kOffTab + kTabBytes + 1024;  // + alignment slack
-static_assert(kNumBars <= 64, "barrier area");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kOffStages = ((kOffTab + kTabBytes + 1023) / 1024) * 1024;
 static_assert((kThreads / 2) * (kEpiRegs + kOtherRegs) == 65536, "register split");
 
 struct BarIdx {
-    static constexpr int a_full = 0;                 // [kStages] TMA -> converters
-    static constexpr int a_empty = kStages;          // [kStages] converters -> TMA
-    static constexpr int ta_full = 2 * kStages;      // [kStages] converters -> MMA
-    static constexpr int ta_empty = 3 * kStages;     // [kStages] MMA -> converters
-    static constexpr int b_full = 4 * kStages;       // [kBStages] TMA -> MMA
-    static constexpr int b_empty = 4 * kStages + kBStages;  // [kBStages] MMA -> TMA
-    static constexpr int p_full = 4 * kStages + 2 * kBStages;   // [2] MMA -> epilogue
-    static constexpr int p_empty = p_full + 2;       // [2] epilogue -> MMA
-    static constexpr int drain = p_empty + 2;        // MMA completion at exit
-    static constexpr int b_ready = drain + 1;        // [kBStages] token converter -> MMA
+    static constexpr int a_full = 0;                              // TMA -> weight converter
+    static constexpr int a_empty = a_full + kMaxAStages;          // weight converter -> TMA
+    static constexpr int ta_full = a_empty + kMaxAStages;         // weight converter -> MMA
+    static constexpr int ta_empty = ta_full + kTmemSlots;         // MMA -> weight converter
+    static constexpr int b_full = ta_empty + kTmemSlots;          // TMA -> MMA
+    static constexpr int b_empty = b_full + kMaxBStages;          // MMA -> TMA
+    static constexpr int p_full = b_empty + kMaxBStages;          // MMA -> epilogue
+    static constexpr int p_empty = p_full + kMaxPBufs;            // epilogue -> MMA
+    static constexpr int drain = p_empty + kMaxPBufs;             // MMA completion at exit
+    static constexpr int count = drain + 1;
 };
-static_assert(BarIdx::b_ready + kBStages <= 64, "barrier count");
+static_assert(BarIdx::count <= 128, "barrier area");
 
 struct KParams {
     const float *sa;
@@ -103,6 +107,11 @@ struct KParams {
     int R, E, N, K, G;
     int n_tiles;
     int out_fp32;
+    int a_stages;       // weight pipeline depth (<= kMaxAStages)
+    int b_stages;       // token pipeline depth (<= kMaxBStages)
+    int b_rows;         // token rows per MMA batch and per token stage (32, 64, 96 or 128)
+    int tile_tokens;    // token rows per tile (b_rows or 2 * b_rows)
+    int p_bufs;         // partial buffers in TMEM (p_bufs * b_rows <= 256)
     unsigned long long *err;
 };
 
@@ -110,9 +119,19 @@ struct TileInfo {
     int e, n0, m0, rows;
 };
 
-template <int kTT>
+// Ring position of a pipeline with n slots: slot index and phase parity.
+struct Ring {
+    uint32_t idx = 0, phase = 0;
+    __device__ __forceinline__ void advance(uint32_t n) {
+        if (++idx == n) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const int *s_lo,
-                                                const int *s_cnt, int E, int n_tiles) {
+                                                const int *s_cnt, int E, int tt) {
     int lo = 0, hi = E;  // s_base[lo] <= t < s_base[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -120,20 +139,20 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const 
     }
     const int local = t - s_base[lo];
     const int cnt = s_cnt[lo];
-    const int m_tiles = (cnt + kTT - 1) / kTT;
+    const int m_tiles = (cnt + tt - 1) / tt;
     const int nt = local / m_tiles;
     const int mt = local - nt * m_tiles;
     TileInfo ti;
     ti.e = lo;
     ti.n0 = nt * kTileN;
-    ti.m0 = s_lo[lo] + mt * kTT;
-    ti.rows = min(kTT, cnt - mt * kTT);
+    ti.m0 = s_lo[lo] + mt * tt;
+    ti.rows = min(tt, cnt - mt * tt);
     return ti;
 }
 
 // Token rows of MMA batch h of a tile with n_eff (multiple of 16) rows.
-__device__ __forceinline__ int batch_rows(int n_eff, int nb, int h) {
-    return nb == 2 ? (h == 0 ? kBatchRows : n_eff - kBatchRows) : n_eff;
+__device__ __forceinline__ int batch_rows(int n_eff, int nb, int h, int b_rows) {
+    return nb == 2 ? (h == 0 ? b_rows : n_eff - b_rows) : n_eff;
 }
 
 // Bounded wait used only on the exit path, independent of the abort flag.
@@ -144,54 +163,84 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// kBInt8 = true: the token operand arrives as int8 codes (TMA box of 128
-// bytes x 32 rows landing in the upper half of a B stage) and warps 2-3 widen
-// it to fp16 in place; tiles hold at most 128 token rows. kBInt8 = false: the
-// token operand is an fp16 staging copy loaded directly by TMA; tiles hold up
-// to 256 token rows in two MMA batches.
-template <bool kBInt8>
+// Bounded wait until the MMA issue turn counter reaches `want`.
+__device__ __forceinline__ bool turn_wait(volatile int *turn, uint32_t want, volatile int *abort,
+                                          unsigned long long *err) {
+    if (*turn == static_cast<int>(want)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (*turn != static_cast<int>(want)) {
+        __nanosleep(32);
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            record_device_error(err, KID_GEMM, ROLE_MMA, 4);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Waits for the copies of the last min(issued, slots) issues of a ring.
+__device__ __forceinline__ void drain_ring(uint32_t bar0, uint32_t issued, uint32_t slots) {
+    for (uint32_t i = issued > slots ? issued - slots : 0; i < issued; ++i)
+        drain_wait(bar0 + 8u * (i % slots), (i / slots) & 1u);
+}
+
+// Warp roles: 0 weight TMA producer, 1 and 3 MMA issuers (alternate groups;
+// warp 1 also allocates TMEM), 2 token TMA producer, 4-7 weight converter,
+// 8-15 epilogue (two warpgroups).
+// kDebug additionally writes every exact group partial.
+template <bool kDebug>
 __global__ void __launch_bounds__(kThreads, 1)
 w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
-    constexpr int kTT = kBInt8 ? kBatchRows : kTileTokens;   // token rows per tile
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw_addr);
 
-    const uint32_t sA = base + kOffA;
-    const uint32_t sB = base + kOffB;
+    const uint32_t SA = static_cast<uint32_t>(p.a_stages);
+    const uint32_t SB = static_cast<uint32_t>(p.b_stages);
+    const int b_rows = p.b_rows;
+    const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
+    const uint32_t b_stage_bytes = 2u * b_atom_bytes;
+    const uint32_t sA = base + kOffStages;
+    const uint32_t sB = sA + SA * kAStageBytes;
     const uint32_t sBar = base + kOffBar;
     volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    volatile int *s_turn = reinterpret_cast<volatile int *>(smem + kOffMisc + 12);
     int *s_base = reinterpret_cast<int *>(smem + kOffTab);
     int *s_lo = s_base + (kMaxExperts + 1);
     int *s_cnt = s_lo + (kMaxExperts + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int tt = p.tile_tokens;
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kMaxAStages; ++i) {
             mbar_init(bar(BarIdx::a_full + i), 1);
             mbar_init(bar(BarIdx::a_empty + i), 4);
+        }
+        for (int i = 0; i < kTmemSlots; ++i) {
             mbar_init(bar(BarIdx::ta_full + i), 4);
             mbar_init(bar(BarIdx::ta_empty + i), 1);
         }
-        for (int i = 0; i < kBStages; ++i) {
+        for (int i = 0; i < kMaxBStages; ++i) {
             mbar_init(bar(BarIdx::b_full + i), 1);
             mbar_init(bar(BarIdx::b_empty + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kMaxPBufs; ++i) {
             mbar_init(bar(BarIdx::p_full + i), 1);
             mbar_init(bar(BarIdx::p_empty + i), 8);
         }
-        mbar_init(bar(BarIdx::drain), 1);
-        for (int i = 0; i < kBStages; ++i) mbar_init(bar(BarIdx::b_ready + i), 2);
+        mbar_init(bar(BarIdx::drain), 2);
         *s_abort = 0;
+        *s_turn = 0;
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -221,7 +270,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     cnt = p.R;
                 }
             }
-            const int tiles = (e < p.E) ? p.n_tiles * ((cnt + kTT - 1) / kTT) : 0;
+            const int tiles = (e < p.E) ? p.n_tiles * ((cnt + tt - 1) / tt) : 0;
             int incl = tiles;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -253,183 +302,158 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
     // the register allocator sees only that role's code in the region.
     if (warp < 4) {
         setmaxnreg_dec<kOtherRegs>();
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            uint32_t a_iss = 0, b_iss = 0;   // loads issued so far
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------- weight TMA producer
+            Ring a;
+            uint32_t issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const int nb = n_eff > kBatchRows ? 2 : 1;
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int wrow = ti.e * p.N + ti.n0;
-                for (int g = 0; ok && g < G; ++g) {
-                    const uint32_t slot = a_iss % kStages, ph = (a_iss / kStages) & 1;
-                    if (!mbar_wait(bar(BarIdx::a_empty + slot), ph ^ 1, s_abort, p.err,
-                                   ROLE_PRODUCER, 1)) { ok = false; break; }
-                    mbar_arrive_expect_tx(bar(BarIdx::a_full + slot), kAStageBytes);
-                    tma_load_2d(sA + slot * kAStageBytes, &tmap_w, g * kGroupK, wrow,
-                                bar(BarIdx::a_full + slot));
-                    ++a_iss;
-                    for (int h = 0; h < nb; ++h) {
-                        const uint32_t bslot = b_iss % kBStages, bph = (b_iss / kBStages) & 1;
-                        const int rows_h = batch_rows(n_eff, nb, h);
-                        const int nbox = (rows_h + kBoxRows - 1) / kBoxRows;
-                        if (!mbar_wait(bar(BarIdx::b_empty + bslot), bph ^ 1, s_abort, p.err,
-                                       ROLE_PRODUCER, 2)) { ok = false; break; }
-                        if constexpr (kBInt8) {
-                            // int8 codes: one 128-byte box column, into the upper atom.
-                            mbar_arrive_expect_tx(bar(BarIdx::b_full + bslot),
-                                                  nbox * kBoxRows * 128u);
-                            for (int i = 0; i < nbox; ++i)
-                                tma_load_2d(sB + bslot * kBStageBytes + kBAtomBytes +
-                                                i * kBoxRows * 128,
-                                            &tmap_x, g * kGroupK, ti.m0 + i * kBoxRows,
-                                            bar(BarIdx::b_full + bslot));
-                        } else {
-                            mbar_arrive_expect_tx(bar(BarIdx::b_full + bslot),
-                                                  2u * nbox * kBoxRows * 128u);
-                            for (int a = 0; a < 2; ++a)
-                                for (int i = 0; i < nbox; ++i)
-                                    tma_load_2d(sB + bslot * kBStageBytes + a * kBAtomBytes +
-                                                    i * kBoxRows * 128,
-                                                &tmap_x, g * kGroupK + a * 64,
-                                                ti.m0 + h * kBatchRows + i * kBoxRows,
-                                                bar(BarIdx::b_full + bslot));
-                        }
-                        ++b_iss;
-                    }
-                }
-            }
-            if (!ok) {
-                // Let every copy already issued land before the CTA exits: the
-                // last kStages issues cover the latest use of every slot.
-                for (uint32_t i = a_iss > kStages ? a_iss - kStages : 0; i < a_iss; ++i)
-                    drain_wait(bar(BarIdx::a_full + i % kStages), (i / kStages) & 1);
-                for (uint32_t i = b_iss > kBStages ? b_iss - kBStages : 0; i < b_iss; ++i)
-                    drain_wait(bar(BarIdx::b_full + i % kBStages), (i / kBStages) & 1);
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t gs = 0, bs = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const int nb = n_eff > kBatchRows ? 2 : 1;
-                for (int g = 0; ok && g < G; ++g, ++gs) {
-                    const uint32_t slot = gs % kStages, ph = (gs / kStages) & 1;
-                    if (!mbar_wait(bar(BarIdx::ta_full + slot), ph, s_abort, p.err, ROLE_MMA, 1)) {
+                for (int g = 0; g < G; ++g) {
+                    if (!mbar_wait(bar(BarIdx::a_empty + a.idx), a.phase ^ 1u, s_abort, p.err,
+                                   ROLE_PRODUCER, 1)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    for (int h = 0; h < nb; ++h, ++bs) {
-                        const uint32_t bslot = bs % kBStages, bph = (bs / kBStages) & 1;
-                        const uint32_t pbuf = bs & 1, pph = (bs >> 1) & 1;
-                        const int b_bar = kBInt8 ? BarIdx::b_ready : BarIdx::b_full;
-                        if (!mbar_wait(bar(b_bar + bslot), bph, s_abort, p.err, ROLE_MMA, 2) ||
-                            !mbar_wait(bar(BarIdx::p_empty + pbuf), pph ^ 1, s_abort, p.err,
-                                       ROLE_MMA, 3)) {
-                            ok = false;
-                            break;
+                    mbar_arrive_expect_tx(bar(BarIdx::a_full + a.idx), kAStageBytes);
+                    tma_load_2d(sA + a.idx * kAStageBytes, &tmap_w, g * kGroupK, wrow,
+                                bar(BarIdx::a_full + a.idx));
+                    a.advance(SA);
+                    ++issued;
+                }
+            }
+            if (!ok) drain_ring(bar(BarIdx::a_full), issued, SA);
+        } else if ((warp == 1 || warp == 3) && lane == 0) {
+            // ------------------------------------------------ MMA issuers
+            // Two issuing threads take alternate groups, which doubles the rate
+            // at which MMAs and commits are issued. Their barrier waits are
+            // taken in turn (the issuer of group g waits only after the other
+            // has passed the waits of group g-1), i.e. in the same order as a
+            // single issuer: a parity wait can then never run two phases ahead
+            // of a barrier that the other issuer's groups also use.
+            const uint32_t me = warp == 1 ? 0u : 1u;
+            Ring ts, b, pr;
+            const uint32_t PB = static_cast<uint32_t>(p.p_bufs);
+            uint32_t gseq = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const int nb = n_eff > b_rows ? 2 : 1;
+                for (int g = 0; ok && g < G; ++g, ++gseq) {
+                    if ((gseq & 1u) != me) {
+                        for (int h = 0; h < nb; ++h) {
+                            b.advance(SB);
+                            pr.advance(PB);
                         }
-                        tc_fence_after();
-                        const uint32_t idesc =
-                            idesc_f16_f32(kTileN, static_cast<uint32_t>(batch_rows(n_eff, nb, h)));
-                        const uint32_t d_tmem = tmem_base + pbuf * 128u;
-                        const uint32_t a_tmem = tmem_base + kTmemA0 + slot * 64u;
-                        const uint32_t b0 = sB + bslot * kBStageBytes;
+                        ts.advance(kTmemSlots);
+                        continue;
+                    }
+                    // ---- waits, in turn
+                    if (!turn_wait(s_turn, gseq, s_abort, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    Ring bw = b, pw = pr;
+                    ok = mbar_wait(bar(BarIdx::ta_full + ts.idx), ts.phase, s_abort, p.err,
+                                   ROLE_MMA, 1);
+                    for (int h = 0; ok && h < nb; ++h) {
+                        ok = mbar_wait(bar(BarIdx::b_full + bw.idx), bw.phase, s_abort, p.err,
+                                       ROLE_MMA, 2) &&
+                             mbar_wait(bar(BarIdx::p_empty + pw.idx), pw.phase ^ 1u, s_abort,
+                                       p.err, ROLE_MMA, 3);
+                        bw.advance(SB);
+                        pw.advance(PB);
+                    }
+                    if (!ok) break;
+                    *s_turn = static_cast<int>(gseq + 1);
+                    tc_fence_after();
+                    // ---- issue (overlaps the other issuer's waits and MMAs)
+                    const uint32_t a_tmem = tmem_base + kTmemA0 + ts.idx * 64u;
+                    for (int h = 0; h < nb; ++h) {
+                        const uint32_t idesc = idesc_f16_f32(
+                            kTileN, static_cast<uint32_t>(batch_rows(n_eff, nb, h, b_rows)));
+                        const uint32_t d_tmem = tmem_base + pr.idx * static_cast<uint32_t>(b_rows);
+                        // Descriptors of the 8 k-steps differ only in the start-address
+                        // field (address >> 4, no carry out of its 14 bits below 256 KB).
+                        const uint64_t bdesc0 = smem_desc_sw128(sB + b.idx * b_stage_bytes);
+                        const uint64_t atom_step = b_atom_bytes >> 4;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t bdesc =
-                                smem_desc_sw128(b0 + (kk >> 2) * kBAtomBytes + (kk & 3) * 32);
+                                bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
                             mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar(BarIdx::p_full + pbuf));
-                        mma_commit(bar(BarIdx::b_empty + bslot));
+                        mma_commit(bar(BarIdx::p_full + pr.idx));
+                        mma_commit(bar(BarIdx::b_empty + b.idx));
+                        b.advance(SB);
+                        pr.advance(PB);
                     }
-                    if (!ok) break;
-                    mma_commit(bar(BarIdx::ta_empty + slot));
+                    mma_commit(bar(BarIdx::ta_empty + ts.idx));
+                    ts.advance(kTmemSlots);
                 }
             }
-            // All MMAs issued by this thread complete before TMEM is freed.
+            // All MMAs issued by this thread complete before TMEM is freed
+            // (the drain barrier expects one commit from each issuer).
             mma_commit(bar(BarIdx::drain));
             drain_wait(bar(BarIdx::drain), 0);
-        }
-    } else if (kBInt8) {
-        // ------------------------------ token converter (int8 -> fp16 in place)
-        // Row r of the stage's upper atom holds 128 int8 codes (128B swizzle);
-        // one thread reads the whole row into registers, then writes its fp16
-        // codes K 0..63 to the lower atom and K 64..127 over the int8 row.
-        const int tid = threadIdx.x - 64;      // 0..63
-        uint32_t bseq = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
-            const int n_eff = (ti.rows + 15) & ~15;
-            for (int g = 0; g < G; ++g, ++bseq) {
-                const uint32_t bslot = bseq % kBStages, bph = (bseq / kBStages) & 1;
-                if (!mbar_wait(bar(BarIdx::b_full + bslot), bph, s_abort, p.err, ROLE_CONVERT, 3)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *stage = smem + kOffB + bslot * kBStageBytes;
-                for (int r = tid; r < n_eff; r += 64) {
-                    const int sw = r & 7;
-                    uint8_t *row0 = stage + r * 128;
-                    uint8_t *row1 = stage + kBAtomBytes + r * 128;
-                    // Chunks 0-3 (K 0..63) go to the lower atom; chunks 4-7 are
-                    // read before the upper atom row (their own storage) is written.
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint4 src[4];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            src[c] = *reinterpret_cast<const uint4 *>(
-                                row1 + (((4 * half + c) ^ sw) << 4));
-                        uint8_t *dst = half == 0 ? row0 : row1;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint4 lo, hi;
-                            i8x4_to_f16x4(src[c].x, lo.x, lo.y);
-                            i8x4_to_f16x4(src[c].y, lo.z, lo.w);
-                            i8x4_to_f16x4(src[c].z, hi.x, hi.y);
-                            i8x4_to_f16x4(src[c].w, hi.z, hi.w);
-                            const int j = 2 * c;
-                            *reinterpret_cast<uint4 *>(dst + ((j ^ sw) << 4)) = lo;
-                            *reinterpret_cast<uint4 *>(dst + (((j + 1) ^ sw) << 4)) = hi;
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------- token TMA producer
+            // The fp16 token codes are written by the kernel launched just
+            // before this one: wait for it (and only here) before loading them.
+            griddep_wait();
+            Ring b;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const int nb = n_eff > b_rows ? 2 : 1;
+                for (int g = 0; ok && g < G; ++g) {
+                    for (int h = 0; h < nb; ++h) {
+                        const int rows_h = batch_rows(n_eff, nb, h, b_rows);
+                        const int nbox = (rows_h + kBoxRows - 1) / kBoxRows;
+                        if (!mbar_wait(bar(BarIdx::b_empty + b.idx), b.phase ^ 1u, s_abort, p.err,
+                                       ROLE_PRODUCER, 2)) {
+                            ok = false;
+                            break;
                         }
+                        const uint32_t stage = sB + b.idx * b_stage_bytes;
+                        mbar_arrive_expect_tx(bar(BarIdx::b_full + b.idx),
+                                              2u * nbox * kBoxRows * 128u);
+                        for (int a = 0; a < 2; ++a)
+                            for (int i = 0; i < nbox; ++i)
+                                tma_load_2d(stage + a * b_atom_bytes + i * kBoxRows * 128, &tmap_x,
+                                            g * kGroupK + a * 64, ti.m0 + h * b_rows + i * kBoxRows,
+                                            bar(BarIdx::b_full + b.idx));
+                        b.advance(SB);
+                        ++issued;
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BarIdx::b_ready + bslot));
             }
+            if (!ok) drain_ring(bar(BarIdx::b_full), issued, SB);
         }
-    }
     } else if (wg == 1) {
         // --------------------------------------- weight converter (A -> TMEM)
         setmaxnreg_dec<kOtherRegs>();
         const int row = threadIdx.x - 128;     // weight row within the tile = TMEM lane
         const int q = warp & 3;                // TMEM lane quarter of this warp
-        uint32_t gs = 0;
+        Ring a, ts;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            for (int g = 0; g < G; ++g, ++gs) {
-                const uint32_t slot = gs % kStages, ph = (gs / kStages) & 1;
-                if (!mbar_wait(bar(BarIdx::a_full + slot), ph, s_abort, p.err, ROLE_CONVERT, 1) ||
-                    !mbar_wait(bar(BarIdx::ta_empty + slot), ph ^ 1, s_abort, p.err, ROLE_CONVERT,
-                               2)) {
+            for (int g = 0; g < G; ++g) {
+                if (!mbar_wait(bar(BarIdx::a_full + a.idx), a.phase, s_abort, p.err, ROLE_CONVERT,
+                               1) ||
+                    !mbar_wait(bar(BarIdx::ta_empty + ts.idx), ts.phase ^ 1u, s_abort, p.err,
+                               ROLE_CONVERT, 2)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint8_t *rowp = smem + kOffA + slot * kAStageBytes + row * 128;
+                const uint8_t *rowp = smem + kOffStages + a.idx * kAStageBytes + row * 128;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kTmemA0 +
-                                       slot * 64u;
+                                       ts.idx * 64u;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint32_t r16[16];
@@ -446,11 +470,13 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     tmem_st_16cols(taddr + j * 16, r16);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BarIdx::a_empty + slot));
+                if (lane == 0) mbar_arrive(bar(BarIdx::a_empty + a.idx));
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BarIdx::ta_full + slot));
+                if (lane == 0) mbar_arrive(bar(BarIdx::ta_full + ts.idx));
+                a.advance(SA);
+                ts.advance(kTmemSlots);
             }
         }
     } else {
@@ -460,75 +486,94 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int q = warp & 3;
         const int lrow = q * 32 + lane;        // weight row within the tile = TMEM lane
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t PB = static_cast<uint32_t>(p.p_bufs);
+        const int cpb = b_rows / 32;           // 32-column chunks per batch
         float acc[4][32];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[i][j] = 0.0f;
-        uint32_t bs = 0;
+        Ring pr;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile<kTT>(t, s_base, s_lo, s_cnt, p.E, p.n_tiles);
+            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
             const int n_eff = (ti.rows + 15) & ~15;
-            const int nb = n_eff > kBatchRows ? 2 : 1;
+            const int nb = n_eff > b_rows ? 2 : 1;
             const int n_local = ti.n0 + lrow;
             const bool n_ok = n_local < p.N;
+            // Column ownership: with two batches, warpgroup w takes batch w;
+            // with one, the 32-column chunks alternate between the warpgroups.
+            // Slot i of acc[] holds tile columns [32 chunk(i), +32).
+            auto chunk_of = [&](int i) { return nb == 2 ? ewg * cpb + i : 2 * i + ewg; };
+            auto owned = [&](int i) {
+                return (nb == 2 ? i < cpb : true) && chunk_of(i) * 32 < n_eff;
+            };
             const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
-            // Weight scales of this row, prefetched four groups ahead so the
-            // global-memory latency never sits between an MMA batch and its drain.
+            // Weight scales of this row: the current quad of groups in cur*,
+            // the next quad in nxt*, loaded a whole quad ahead and only copied
+            // at a quad boundary, so no load latency sits in the drain loop.
             auto load_sw = [&](int g) -> float { return (n_ok && g < G) ? __ldg(swp + g) : 0.0f; };
-            float s_ring0 = load_sw(0), s_ring1 = load_sw(1), s_ring2 = load_sw(2),
-                  s_ring3 = load_sw(3);
+            float cur0 = load_sw(0), cur1 = load_sw(1), cur2 = load_sw(2), cur3 = load_sw(3);
+            float nxt0 = load_sw(4), nxt1 = load_sw(5), nxt2 = load_sw(6), nxt3 = load_sw(7);
             for (int g = 0; ok && g < G; ++g) {
-                const float s = s_ring0;
-                s_ring0 = s_ring1;
-                s_ring1 = s_ring2;
-                s_ring2 = s_ring3;
-                s_ring3 = load_sw(g + 4);
-                for (int h = 0; h < nb; ++h, ++bs) {
-                    const uint32_t pbuf = bs & 1, pph = (bs >> 1) & 1;
-                    if (!mbar_wait(bar(BarIdx::p_full + pbuf), pph, s_abort, p.err, ROLE_EPILOGUE,
-                                   1)) {
+                const int jq = g & 3;
+                if (jq == 0 && g > 0) {
+                    cur0 = nxt0;
+                    cur1 = nxt1;
+                    cur2 = nxt2;
+                    cur3 = nxt3;
+                    nxt0 = load_sw(g + 4);
+                    nxt1 = load_sw(g + 5);
+                    nxt2 = load_sw(g + 6);
+                    nxt3 = load_sw(g + 7);
+                }
+                const float s = jq == 0 ? cur0 : (jq == 1 ? cur1 : (jq == 2 ? cur2 : cur3));
+                for (int h = 0; h < nb; ++h) {
+                    if (!mbar_wait(bar(BarIdx::p_full + pr.idx), pr.phase, s_abort, p.err,
+                                   ROLE_EPILOGUE, 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    if (nb == 1 || h == ewg) {
+                        const uint32_t buf = lane_base + pr.idx * static_cast<uint32_t>(b_rows);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int c = nb == 2 ? 4 * ewg + i : 2 * i + ewg;  // 32-column chunk
-                        const bool in_batch = nb == 2 ? ((c >> 2) == h) : true;
-                        if (in_batch && c * 32 < n_eff) {
-                            const int col_in_buf = nb == 2 ? (c & 3) * 32 : c * 32;
-                            uint32_t v[32];
-                            tmem_ld_32cols_sync(lane_base + pbuf * 128u + col_in_buf, v);
+                        for (int i = 0; i < 4; ++i) {
+                            if (owned(i)) {
+                                const int col = nb == 2 ? i * 32 : chunk_of(i) * 32;
+                                uint32_t v[32];
+                                tmem_ld_32cols_sync(buf + col, v);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                acc[i][j] = fmaf(__uint_as_float(v[j]), s, acc[i][j]);
-                            if (p.dbg != nullptr && n_ok) {
+                                for (int j = 0; j < 32; ++j)
+                                    acc[i][j] = fmaf(__uint_as_float(v[j]), s, acc[i][j]);
+                                if (kDebug && n_ok) {
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) {
-                                    const int col = c * 32 + j;
-                                    if (col < ti.rows)
-                                        p.dbg[(static_cast<size_t>(ti.m0 + col) * p.N + n_local) *
-                                                  G + g] = __float2int_rn(__uint_as_float(v[j]));
+                                    for (int j = 0; j < 32; ++j) {
+                                        const int tcol = chunk_of(i) * 32 + j;
+                                        if (tcol < ti.rows)
+                                            p.dbg[(static_cast<size_t>(ti.m0 + tcol) * p.N +
+                                                   n_local) * G + g] =
+                                                __float2int_rn(__uint_as_float(v[j]));
+                                    }
                                 }
                             }
                         }
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(BarIdx::p_empty + pbuf));
+                    if (lane == 0) mbar_arrive_relaxed(bar(BarIdx::p_empty + pr.idx));
+                    pr.advance(PB);
                 }
             }
             if (!ok) break;
             // Token scale and store: Y[m, n] = sa[m] * acc.
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int c = nb == 2 ? 4 * ewg + i : 2 * i + ewg;
-                if (c * 32 < n_eff && n_ok) {
+                if (owned(i) && n_ok) {
+                    const int c0 = chunk_of(i) * 32;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const int col = c * 32 + j;
+                        const int col = c0 + j;
                         if (col < ti.rows) {
                             const int m = ti.m0 + col;
                             const float out = acc[i][j] * __ldg(p.sa + m);
@@ -584,33 +629,61 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_bytes, c
     return r == CUDA_SUCCESS;
 }
 
-template <bool kBInt8>
+// Pipeline shape of one call: batch width, tile rows, partial buffers and
+// stage counts, filling shared memory with weight stages after the token stages.
+struct PipeShape {
+    int b_rows, tile_tokens, b_stages, a_stages, p_bufs, smem_bytes;
+};
+
+PipeShape choose_pipe(const GemmProblem &pr) {
+    PipeShape s;
+    if (pr.offsets == nullptr && pr.R <= kMaxBatchRows) {
+        s.b_rows = static_cast<int>((pr.R + kBoxRows - 1) / kBoxRows * kBoxRows);
+        s.tile_tokens = s.b_rows;
+    } else if (pr.offsets == nullptr) {
+        s.b_rows = kMaxBatchRows;
+        s.tile_tokens = 2 * kMaxBatchRows;
+    } else {
+        s.b_rows = pr.grouped_batch_rows;
+        s.tile_tokens = 2 * pr.grouped_batch_rows;
+    }
+    s.p_bufs = 256 / s.b_rows;
+    if (s.p_bufs > kMaxPBufs) s.p_bufs = kMaxPBufs;
+    s.b_stages = 4;
+    const int b_stage_bytes = s.b_rows * 256;
+    const int avail = kSmemLimit - 1024 - kOffStages - s.b_stages * b_stage_bytes;
+    s.a_stages = avail / kAStageBytes;
+    if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
+    s.smem_bytes = kOffStages + s.a_stages * kAStageBytes + s.b_stages * b_stage_bytes + 1024;
+    return s;
+}
+
+template <bool kDebug>
 cudaError_t launch_gemm_impl(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
-    constexpr int kTT = kBInt8 ? kBatchRows : kTileTokens;
+    const PipeShape ps = choose_pipe(pr);
+    if (ps.a_stages < 2 || ps.b_rows % kBoxRows != 0 || ps.b_rows > kMaxBatchRows ||
+        ps.smem_bytes > kSmemLimit)
+        return cudaErrorInvalidConfiguration;
     CUtensorMap tw, tx;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
-                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN))
+                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
+        !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x16, (uint64_t)pr.K,
+                   (uint64_t)pr.R, 64, kBoxRows))
         return cudaErrorInvalidValue;
-    const bool ok_x =
-        kBInt8 ? encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.x, (uint64_t)pr.K,
-                           (uint64_t)pr.R, 128, kBoxRows)
-               : encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x, (uint64_t)pr.K,
-                           (uint64_t)pr.R, 64, kBoxRows);
-    if (!ok_x) return cudaErrorInvalidValue;
 
-    static int attr_done[64] = {0};
+    static int attr_done[64] = {0};   // per device, per instance
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         // setmaxnreg.inc can only take registers the CTA was launched with:
         // refuse to launch unless the launch allocation covers the split.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel<kBInt8>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel<kDebug>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs * kThreads < (kThreads / 2) * (kEpiRegs + kOtherRegs))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(w8a8_gemm_kernel<kBInt8>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(w8a8_gemm_kernel<kDebug>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
@@ -628,27 +701,47 @@ cudaError_t launch_gemm_impl(const GemmProblem &pr, int num_sms, cudaStream_t st
     kp.G = static_cast<int>(pr.K / kGroupK);
     kp.n_tiles = static_cast<int>((pr.N + kTileN - 1) / kTileN);
     kp.out_fp32 = pr.out_fp32 ? 1 : 0;
+    kp.a_stages = ps.a_stages;
+    kp.b_stages = ps.b_stages;
+    kp.b_rows = ps.b_rows;
+    kp.tile_tokens = ps.tile_tokens;
+    kp.p_bufs = ps.p_bufs;
     unsigned long long *err = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
     if (e != cudaSuccess) return e;
     kp.err = err;
 
     // Upper bound on the number of tiles (exact for one dense segment).
-    const int64_t m_tiles_bound = pr.offsets == nullptr ? (pr.R + kTT - 1) / kTT
-                                                        : (pr.R + kTT - 1) / kTT + pr.E;
+    const int64_t tt = ps.tile_tokens;
+    const int64_t m_tiles_bound = pr.offsets == nullptr ? (pr.R + tt - 1) / tt
+                                                        : (pr.R + tt - 1) / tt + pr.E;
     const int64_t tiles_bound = m_tiles_bound * kp.n_tiles;
     const int64_t grid = tiles_bound < num_sms ? tiles_bound : num_sms;
     if (grid <= 0) return cudaSuccess;
-    w8a8_gemm_kernel<kBInt8>
-        <<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tw, tx, kp);
+
+    // Programmatic dependent launch: the kernel may start while the staging
+    // kernel before it in the stream is still running; only its token
+    // producer waits for that kernel (griddepcontrol.wait).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(ps.smem_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel<kDebug>, tw, tx, kp);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
-    return pr.x_int8 ? launch_gemm_impl<true>(pr, num_sms, stream)
-                     : launch_gemm_impl<false>(pr, num_sms, stream);
+    return pr.debug_partials != nullptr ? launch_gemm_impl<true>(pr, num_sms, stream)
+                                        : launch_gemm_impl<false>(pr, num_sms, stream);
 }
 
 cudaError_t read_device_error(unsigned long long *value, bool clear) {

@@ -22,21 +22,17 @@ struct GemmProblem {
     const float *sa;          // [R]
     const float *sw;          // [E*N, G]
     const int8_t *qw;         // [E*N, K]
-    const void *x;            // [R, K] activation codes: int8 (x_int8) or an fp16 staging copy
-    bool x_int8;              // true: tiles of <= 128 token rows widened in shared memory
+    const void *x16;          // [R, K] fp16 copy of the int8 activation codes (staging)
     const int32_t *offsets;   // [E+1] device, or nullptr for one dense segment [0, R)
     void *y;                  // [R, N]
     int32_t *debug_partials;  // nullable [R, N, G]
     int64_t R, E, N, K;
     bool out_fp32;
+    int grouped_batch_rows = 64;  // token rows per MMA batch for grouped calls (32..128)
 };
 
 // Maximum number of experts a grouped call may have.
 constexpr int kMaxExperts = 1024;
-
-// Dense calls with at most this many token rows read the int8 codes directly
-// (no staging copy); larger ones use 256-row tiles over an fp16 staging copy.
-constexpr int64_t kDirectMaxRows = 128;
 
 cudaError_t launch_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
 

@@ -179,6 +179,9 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float *__restri
 __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restrict__ q,
                                                           int64_t rows, int K, int64_t ldq,
                                                           __half *__restrict__ out) {
+    // The GEMM that consumes this copy is launched as a programmatic
+    // dependent: let it start its set-up and weight stream right away.
+    griddep_launch_dependents();
     const int vec_per_row = K >> 4;  // 16 codes per vector
     const int64_t total = rows * vec_per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;

@@ -53,15 +53,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # Up to 128 token rows the GEMM reads the int8 codes directly: no workspace.
+    # fp16 staging copy of the activation codes, rounded up to 256 bytes.
     assert lib.w8a8_gemm_workspace_size(0, 128, 128) == 0
-    assert lib.w8a8_gemm_workspace_size(3, 128, 128) == 0
-    assert lib.w8a8_gemm_workspace_size(128, 28672, 8192) == 0
-    # Beyond that, an fp16 staging copy of the codes, rounded to 256 bytes.
-    assert lib.w8a8_gemm_workspace_size(129, 128, 128) == 129 * 128 * 2
+    assert lib.w8a8_gemm_workspace_size(3, 128, 128) == 768
+    assert lib.w8a8_gemm_workspace_size(1, 128, 128) == 256
     assert lib.w8a8_gemm_workspace_size(129, 128, 384) == (129 * 384 * 2 + 255) // 256 * 256
-    assert lib.w8a8_gemm_workspace_size(4096, 8192, 8192) == 4096 * 8192 * 2
-    assert lib.w8a8_grouped_gemm_workspace_size(4096, 64, 3072, 4096) == 0
+    assert lib.w8a8_gemm_workspace_size(32, 28672, 8192) == 32 * 8192 * 2
+    assert lib.w8a8_grouped_gemm_workspace_size(4096, 64, 3072, 4096) == 4096 * 4096 * 2
 
 
 FAKE = 1 << 20      # a 16-byte aligned non-null value; never dereferenced here
@@ -82,9 +80,9 @@ def test_gemm_host_validation(lib):
     assert gemm(lib, qa=FAKE + 8) == INVALID           # TMA operand not 16-byte aligned
     assert gemm(lib, sa=FAKE + 2) == INVALID
     assert gemm(lib, dt=7) == INVALID
-    assert gemm(lib, M=256, ws=None) == WORKSPACE
-    assert gemm(lib, M=256, wsb=256 * 128 * 2 - 1) == WORKSPACE
-    assert gemm(lib, M=256, ws=FAKE + 16) == WORKSPACE  # workspace must be 256-byte aligned
+    assert gemm(lib, ws=None) == WORKSPACE
+    assert gemm(lib, wsb=16 * 128 * 2 - 1) == WORKSPACE
+    assert gemm(lib, ws=FAKE + 16) == WORKSPACE        # workspace must be 256-byte aligned
     assert gemm(lib, M=1 << 24, K=1 << 10) == INVALID  # operand above 2^31 elements
     assert gemm(lib, M=0) == OK                        # no-op, no device work
 
@@ -98,6 +96,7 @@ def test_grouped_host_validation(lib):
     assert call(E=1025) == INVALID
     assert call(K=129) == INVALID
     assert call(off=FAKE + 2) == INVALID
+    assert call(wsb=10) == WORKSPACE
     assert call(R=0) == OK
 
 
