@@ -261,6 +261,23 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Loads issued exactly where they are written (volatile asm is not moved past
+// other volatile asm such as barrier waits), so a prefetch stays a prefetch:
+// the compiler may otherwise sink a load down to its first use.
+__device__ __forceinline__ float ldg_nc_f32_now(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ldg_nc_f32x4_now(const float *p) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // Programmatic dependent launch: wait until the kernels this one depends on
 // have completed and their writes are visible (a no-op without the launch
 // attribute), and let the next kernel in the stream start launching early.

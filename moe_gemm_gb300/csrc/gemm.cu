@@ -87,8 +87,8 @@ static_assert((kThreads / 2) * (kEpiRegs + kOtherRegs) == 65536, "register split
 struct BarIdx {
     static constexpr int a_full = 0;                              // TMA -> weight converter
     static constexpr int a_empty = a_full + kMaxAStages;          // weight converter -> TMA
-    static constexpr int ta_full = a_empty + kMaxAStages;         // weight converter -> MMA
-    static constexpr int ta_empty = ta_full + kTmemSlots;         // MMA -> weight converter
+    static constexpr int ready = a_empty + kMaxAStages;           // converter + admission -> MMA
+    static constexpr int ta_empty = ready + kTmemSlots;           // MMA -> weight converter
     static constexpr int b_full = ta_empty + kTmemSlots;          // TMA -> MMA
     static constexpr int b_empty = b_full + kMaxBStages;          // MMA -> TMA
     static constexpr int p_full = b_empty + kMaxBStages;          // MMA -> epilogue
@@ -163,34 +163,23 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Bounded wait until the MMA issue turn counter reaches `want`.
-__device__ __forceinline__ bool turn_wait(volatile int *turn, uint32_t want, volatile int *abort,
-                                          unsigned long long *err) {
-    if (*turn == static_cast<int>(want)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    while (*turn != static_cast<int>(want)) {
-        __nanosleep(32);
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            record_device_error(err, KID_GEMM, ROLE_MMA, 4);
-            return false;
-        }
-    }
-    return true;
-}
-
 // Waits for the copies of the last min(issued, slots) issues of a ring.
 __device__ __forceinline__ void drain_ring(uint32_t bar0, uint32_t issued, uint32_t slots) {
     for (uint32_t i = issued > slots ? issued - slots : 0; i < issued; ++i)
         drain_wait(bar0 + 8u * (i % slots), (i / slots) & 1u);
 }
 
-// Warp roles: 0 weight TMA producer, 1 and 3 MMA issuers (alternate groups;
-// warp 1 also allocates TMEM), 2 token TMA producer, 4-7 weight converter,
-// 8-15 epilogue (two warpgroups).
+// Warp roles: 0 weight TMA producer, 1 MMA issuer (+ TMEM allocation), 2 token
+// TMA producer, 3 admission (token tiles landed, partial buffers free), 4-7
+// weight converter, 8-15 epilogue (two warpgroups).
 // kDebug additionally writes every exact group partial.
-template <bool kDebug>
+// kSingle: every tile is one MMA batch of at most 64 token rows, so the TMEM
+// operand slot, token stage and partial buffer of a group share one 4-deep
+// ring and a single commit per group ("done", the ta_empty barrier) tells the
+// epilogue, the converter and the token producer that the group's MMAs are
+// complete. Otherwise each batch commits its partial buffer and token stage
+// separately.
+template <bool kDebug, bool kSingle>
 __global__ void __launch_bounds__(kThreads, 1)
 w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
@@ -210,7 +199,6 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
     volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
-    volatile int *s_turn = reinterpret_cast<volatile int *>(smem + kOffMisc + 12);
     int *s_base = reinterpret_cast<int *>(smem + kOffTab);
     int *s_lo = s_base + (kMaxExperts + 1);
     int *s_cnt = s_lo + (kMaxExperts + 1);
@@ -227,7 +215,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(bar(BarIdx::a_empty + i), 4);
         }
         for (int i = 0; i < kTmemSlots; ++i) {
-            mbar_init(bar(BarIdx::ta_full + i), 4);
+            mbar_init(bar(BarIdx::ready + i), 5);
             mbar_init(bar(BarIdx::ta_empty + i), 1);
         }
         for (int i = 0; i < kMaxBStages; ++i) {
@@ -238,9 +226,8 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(bar(BarIdx::p_full + i), 1);
             mbar_init(bar(BarIdx::p_empty + i), 8);
         }
-        mbar_init(bar(BarIdx::drain), 2);
+        mbar_init(bar(BarIdx::drain), 1);
         *s_abort = 0;
-        *s_turn = 0;
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -324,52 +311,24 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
             }
             if (!ok) drain_ring(bar(BarIdx::a_full), issued, SA);
-        } else if ((warp == 1 || warp == 3) && lane == 0) {
-            // ------------------------------------------------ MMA issuers
-            // Two issuing threads take alternate groups, which doubles the rate
-            // at which MMAs and commits are issued. Their barrier waits are
-            // taken in turn (the issuer of group g waits only after the other
-            // has passed the waits of group g-1), i.e. in the same order as a
-            // single issuer: a parity wait can then never run two phases ahead
-            // of a barrier that the other issuer's groups also use.
-            const uint32_t me = warp == 1 ? 0u : 1u;
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            // One wait per group (operand ready: weights in TMEM, token tiles
+            // landed, partial buffers free), then the group's MMAs and commits.
             Ring ts, b, pr;
             const uint32_t PB = static_cast<uint32_t>(p.p_bufs);
-            uint32_t gseq = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int n_eff = (ti.rows + 15) & ~15;
                 const int nb = n_eff > b_rows ? 2 : 1;
-                for (int g = 0; ok && g < G; ++g, ++gseq) {
-                    if ((gseq & 1u) != me) {
-                        for (int h = 0; h < nb; ++h) {
-                            b.advance(SB);
-                            pr.advance(PB);
-                        }
-                        ts.advance(kTmemSlots);
-                        continue;
-                    }
-                    // ---- waits, in turn
-                    if (!turn_wait(s_turn, gseq, s_abort, p.err)) {
+                for (int g = 0; g < G; ++g) {
+                    if (!mbar_wait(bar(BarIdx::ready + ts.idx), ts.phase, s_abort, p.err, ROLE_MMA,
+                                   1)) {
                         ok = false;
                         break;
                     }
-                    Ring bw = b, pw = pr;
-                    ok = mbar_wait(bar(BarIdx::ta_full + ts.idx), ts.phase, s_abort, p.err,
-                                   ROLE_MMA, 1);
-                    for (int h = 0; ok && h < nb; ++h) {
-                        ok = mbar_wait(bar(BarIdx::b_full + bw.idx), bw.phase, s_abort, p.err,
-                                       ROLE_MMA, 2) &&
-                             mbar_wait(bar(BarIdx::p_empty + pw.idx), pw.phase ^ 1u, s_abort,
-                                       p.err, ROLE_MMA, 3);
-                        bw.advance(SB);
-                        pw.advance(PB);
-                    }
-                    if (!ok) break;
-                    *s_turn = static_cast<int>(gseq + 1);
                     tc_fence_after();
-                    // ---- issue (overlaps the other issuer's waits and MMAs)
                     const uint32_t a_tmem = tmem_base + kTmemA0 + ts.idx * 64u;
                     for (int h = 0; h < nb; ++h) {
                         const uint32_t idesc = idesc_f16_f32(
@@ -385,8 +344,10 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                 bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
                             mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar(BarIdx::p_full + pr.idx));
-                        mma_commit(bar(BarIdx::b_empty + b.idx));
+                        if constexpr (!kSingle) {
+                            mma_commit(bar(BarIdx::p_full + pr.idx));
+                            mma_commit(bar(BarIdx::b_empty + b.idx));
+                        }
                         b.advance(SB);
                         pr.advance(PB);
                     }
@@ -394,10 +355,39 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     ts.advance(kTmemSlots);
                 }
             }
-            // All MMAs issued by this thread complete before TMEM is freed
-            // (the drain barrier expects one commit from each issuer).
+            // All MMAs issued by this thread complete before TMEM is freed.
             mma_commit(bar(BarIdx::drain));
             drain_wait(bar(BarIdx::drain), 0);
+        } else if (warp == 3 && lane == 0) {
+            // --------------------------------------------------- admission
+            // Waits, in group order, for the group's token tiles and for the
+            // partial buffers its batches will overwrite (drained by the
+            // epilogue), then adds its arrival to the group's operand-ready
+            // barrier, which the four converter warps complete.
+            Ring ts, b, pr;
+            const uint32_t PB = static_cast<uint32_t>(p.p_bufs);
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const int nb = n_eff > b_rows ? 2 : 1;
+                for (int g = 0; ok && g < G; ++g) {
+                    for (int h = 0; h < nb; ++h) {
+                        if (!mbar_wait(bar(BarIdx::b_full + b.idx), b.phase, s_abort, p.err,
+                                       ROLE_MMA, 2) ||
+                            !mbar_wait(bar(BarIdx::p_empty + pr.idx), pr.phase ^ 1u, s_abort,
+                                       p.err, ROLE_MMA, 3)) {
+                            ok = false;
+                            break;
+                        }
+                        b.advance(SB);
+                        pr.advance(PB);
+                    }
+                    if (!ok) break;
+                    mbar_arrive(bar(BarIdx::ready + ts.idx));
+                    ts.advance(kTmemSlots);
+                }
+            }
         } else if (warp == 2 && lane == 0) {
             // -------------------------------------------- token TMA producer
             // The fp16 token codes are written by the kernel launched just
@@ -414,7 +404,8 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     for (int h = 0; h < nb; ++h) {
                         const int rows_h = batch_rows(n_eff, nb, h, b_rows);
                         const int nbox = (rows_h + kBoxRows - 1) / kBoxRows;
-                        if (!mbar_wait(bar(BarIdx::b_empty + b.idx), b.phase ^ 1u, s_abort, p.err,
+                        const int b_free = kSingle ? BarIdx::ta_empty : BarIdx::b_empty;
+                        if (!mbar_wait(bar(b_free + b.idx), b.phase ^ 1u, s_abort, p.err,
                                        ROLE_PRODUCER, 2)) {
                             ok = false;
                             break;
@@ -474,7 +465,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BarIdx::ta_full + ts.idx));
+                if (lane == 0) mbar_arrive(bar(BarIdx::ready + ts.idx));
                 a.advance(SA);
                 ts.advance(kTmemSlots);
             }
@@ -509,27 +500,36 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 return (nb == 2 ? i < cpb : true) && chunk_of(i) * 32 < n_eff;
             };
             const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
-            // Weight scales of this row: the current quad of groups in cur*,
-            // the next quad in nxt*, loaded a whole quad ahead and only copied
-            // at a quad boundary, so no load latency sits in the drain loop.
-            auto load_sw = [&](int g) -> float { return (n_ok && g < G) ? __ldg(swp + g) : 0.0f; };
-            float cur0 = load_sw(0), cur1 = load_sw(1), cur2 = load_sw(2), cur3 = load_sw(3);
-            float nxt0 = load_sw(4), nxt1 = load_sw(5), nxt2 = load_sw(6), nxt3 = load_sw(7);
+            // Weight scales of this row: the current quad of groups in cur,
+            // the next quad in nxt, loaded a whole quad ahead (one 16-byte load
+            // when the row is 16-byte aligned) and only copied at a quad
+            // boundary, so no load latency sits in the drain loop.
+            const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
+            auto load_quad = [&](int g) -> float4 {
+                float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (!n_ok) return v;
+                if (vec_sw) {
+                    if (g < G) v = ldg_nc_f32x4_now(swp + g);
+                } else {
+                    if (g < G) v.x = ldg_nc_f32_now(swp + g);
+                    if (g + 1 < G) v.y = ldg_nc_f32_now(swp + g + 1);
+                    if (g + 2 < G) v.z = ldg_nc_f32_now(swp + g + 2);
+                    if (g + 3 < G) v.w = ldg_nc_f32_now(swp + g + 3);
+                }
+                return v;
+            };
+            float4 cur = load_quad(0);
+            float4 nxt = load_quad(4);
             for (int g = 0; ok && g < G; ++g) {
                 const int jq = g & 3;
                 if (jq == 0 && g > 0) {
-                    cur0 = nxt0;
-                    cur1 = nxt1;
-                    cur2 = nxt2;
-                    cur3 = nxt3;
-                    nxt0 = load_sw(g + 4);
-                    nxt1 = load_sw(g + 5);
-                    nxt2 = load_sw(g + 6);
-                    nxt3 = load_sw(g + 7);
+                    cur = nxt;
+                    nxt = load_quad(g + 4);
                 }
-                const float s = jq == 0 ? cur0 : (jq == 1 ? cur1 : (jq == 2 ? cur2 : cur3));
+                const float s = jq == 0 ? cur.x : (jq == 1 ? cur.y : (jq == 2 ? cur.z : cur.w));
                 for (int h = 0; h < nb; ++h) {
-                    if (!mbar_wait(bar(BarIdx::p_full + pr.idx), pr.phase, s_abort, p.err,
+                    const int p_ready = kSingle ? BarIdx::ta_empty : BarIdx::p_full;
+                    if (!mbar_wait(bar(p_ready + pr.idx), pr.phase, s_abort, p.err,
                                    ROLE_EPILOGUE, 1)) {
                         ok = false;
                         break;
@@ -633,6 +633,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_bytes, c
 // stage counts, filling shared memory with weight stages after the token stages.
 struct PipeShape {
     int b_rows, tile_tokens, b_stages, a_stages, p_bufs, smem_bytes;
+    bool single;    // one batch per tile, group rings tied (see the kernel's kSingle)
 };
 
 PipeShape choose_pipe(const GemmProblem &pr) {
@@ -645,11 +646,17 @@ PipeShape choose_pipe(const GemmProblem &pr) {
         s.tile_tokens = 2 * kMaxBatchRows;
     } else {
         s.b_rows = pr.grouped_batch_rows;
-        s.tile_tokens = 2 * pr.grouped_batch_rows;
+        s.tile_tokens = pr.grouped_batch_rows;
     }
-    s.p_bufs = 256 / s.b_rows;
-    if (s.p_bufs > kMaxPBufs) s.p_bufs = kMaxPBufs;
-    s.b_stages = 4;
+    s.single = s.tile_tokens == s.b_rows && s.b_rows <= 64;
+    if (s.single) {
+        s.p_bufs = kTmemSlots;           // rings tied to the TMEM operand slots
+        s.b_stages = kTmemSlots;
+    } else {
+        s.p_bufs = 256 / s.b_rows;
+        if (s.p_bufs > kMaxPBufs) s.p_bufs = kMaxPBufs;
+        s.b_stages = 4;
+    }
     const int b_stage_bytes = s.b_rows * 256;
     const int avail = kSmemLimit - 1024 - kOffStages - s.b_stages * b_stage_bytes;
     s.a_stages = avail / kAStageBytes;
@@ -658,9 +665,9 @@ PipeShape choose_pipe(const GemmProblem &pr) {
     return s;
 }
 
-template <bool kDebug>
-cudaError_t launch_gemm_impl(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
-    const PipeShape ps = choose_pipe(pr);
+template <bool kDebug, bool kSingle>
+cudaError_t launch_gemm_impl(const GemmProblem &pr, const PipeShape &ps, int num_sms,
+                             cudaStream_t stream) {
     if (ps.a_stages < 2 || ps.b_rows % kBoxRows != 0 || ps.b_rows > kMaxBatchRows ||
         ps.smem_bytes > kSmemLimit)
         return cudaErrorInvalidConfiguration;
@@ -678,11 +685,11 @@ cudaError_t launch_gemm_impl(const GemmProblem &pr, int num_sms, cudaStream_t st
         // setmaxnreg.inc can only take registers the CTA was launched with:
         // refuse to launch unless the launch allocation covers the split.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel<kDebug>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel<kDebug, kSingle>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs * kThreads < (kThreads / 2) * (kEpiRegs + kOtherRegs))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(w8a8_gemm_kernel<kDebug>,
+        e = cudaFuncSetAttribute(w8a8_gemm_kernel<kDebug, kSingle>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
@@ -732,7 +739,7 @@ cudaError_t launch_gemm_impl(const GemmProblem &pr, int num_sms, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel<kDebug>, tw, tx, kp);
+    e = cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel<kDebug, kSingle>, tw, tx, kp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -740,8 +747,13 @@ cudaError_t launch_gemm_impl(const GemmProblem &pr, int num_sms, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
-    return pr.debug_partials != nullptr ? launch_gemm_impl<true>(pr, num_sms, stream)
-                                        : launch_gemm_impl<false>(pr, num_sms, stream);
+    const PipeShape ps = choose_pipe(pr);
+    const bool dbg = pr.debug_partials != nullptr;
+    if (ps.single)
+        return dbg ? launch_gemm_impl<true, true>(pr, ps, num_sms, stream)
+                   : launch_gemm_impl<false, true>(pr, ps, num_sms, stream);
+    return dbg ? launch_gemm_impl<true, false>(pr, ps, num_sms, stream)
+               : launch_gemm_impl<false, false>(pr, ps, num_sms, stream);
 }
 
 cudaError_t read_device_error(unsigned long long *value, bool clear) {
