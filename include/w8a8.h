@@ -138,6 +138,39 @@ w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *
                               int32_t *debug_partials, void *workspace, size_t workspace_bytes,
                               w8a8_stream_t stream);
 
+/*
+ * Size of the scratch array built into the library for w8a8_gemm_noalloc:
+ * 8 MiB, enough for M * K <= 4,194,304 activation codes (e.g. M <= 512 at
+ * K = 8192, M <= 256 at K = 16384).
+ */
+#define W8A8_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * w8a8_gemm without a caller workspace, for callers that cannot allocate
+ * device memory at the point where they run the layer: for example an
+ * inference engine that hands a plug-in only a stream and buffers it planned
+ * ahead of time, a runtime whose memory pool forbids allocation on its hot
+ * path, or code running where a cudaMalloc would synchronise the device. It
+ * computes exactly what w8a8_gemm computes (same kernels, same results), but
+ * stages the fp16 copy of the activation codes in a fixed 8 MiB array that is
+ * part of the library (W8A8_NOALLOC_SCRATCH_BYTES), so it allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ * There is no counterpart of this call on the source pages; it is a
+ * deployment convenience.
+ *   Arguments: as w8a8_gemm, without debug_partials and workspace.
+ *   Returns W8A8_ERR_WORKSPACE when M * K * 2 bytes (rounded up to 256) do not
+ *   fit in the built-in scratch.
+ *   The first call on a device looks up the scratch's device address (once,
+ *   with that device current); make that first call before any stream
+ *   capture. All calls on a device share the one scratch array and it keeps
+ *   the last call's contents: calls that can overlap on the GPU (different
+ *   streams without ordering between them) race on it and must be ordered by
+ *   the caller.
+ */
+w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *qw,
+                              const float *sw, void *y, w8a8_dtype y_dtype, int64_t M, int64_t N,
+                              int64_t K, w8a8_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *w8a8_status_string(w8a8_status status);
 

@@ -49,12 +49,13 @@ def _load() -> ctypes.CDLL:
     lib.w8a8_gemm.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, ctypes.c_size_t, vp]
     lib.w8a8_grouped_gemm.argtypes = [vp, vp, vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, vp,
                                       ctypes.c_size_t, vp]
+    lib.w8a8_gemm_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, i64, vp]
     lib.w8a8_status_string.argtypes = [i32]
     lib.w8a8_status_string.restype = ctypes.c_char_p
     lib.w8a8_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint64), i32]
     lib.w8a8_version.restype = i32
     for name in ("w8a8_quant_act", "w8a8_quant_weight", "w8a8_gemm", "w8a8_grouped_gemm",
-                 "w8a8_device_error"):
+                 "w8a8_gemm_noalloc", "w8a8_device_error"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -155,6 +156,30 @@ def gemm(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
                           M, N, K, _ptr(P), _ptr(workspace), workspace.numel(), _stream(stream)),
            "w8a8_gemm")
     return (y, P) if debug_partials else y
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def gemm_noalloc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
+                 out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Same result as gemm(), for callers that cannot allocate device memory
+    when the layer runs: the library stages the activation codes in its own
+    fixed 8 MiB scratch array instead of a workspace (M*K*2 bytes must fit).
+    Calls that may overlap on the GPU share that array and must be ordered."""
+    _require(qa, torch.int8, "qa", 2)
+    _require(qw, torch.int8, "qw", 2)
+    _require(sa, torch.float32, "sa", 1)
+    _require(sw, torch.float32, "sw", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    if out is None:
+        raise ValueError("gemm_noalloc writes into a caller-provided `out` tensor")
+    _check(_lib.w8a8_gemm_noalloc(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(out),
+                                  _dtype_code(out_dtype), M, N, K, _stream(stream)),
+           "w8a8_gemm_noalloc")
+    return out
 
 
 def grouped_gemm(qa: torch.Tensor, sa: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor,

@@ -104,6 +104,35 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
     return from_cuda(w8a8::launch_gemm(p, info.num_sms, s));
 }
 
+// ---------------------------------------------------------------------------
+// Built-in scratch for w8a8_gemm_noalloc: the fp16 staging copy of the
+// activation codes lives in this fixed device array instead of a caller
+// workspace. Every GPU that loads the library keeps it until the process
+// exits; all calls on a device share it.
+constexpr size_t kNoallocScratchBytes = W8A8_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached. In host code the symbol
+// name is only a host-side handle, never a device address.
+cudaError_t noalloc_scratch_ptr(void **out) {
+    static void *ptrs[64] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        ptrs[dev] = p;
+    }
+    *out = ptrs[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -185,6 +214,24 @@ w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *
     if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
     return run_gemm(qa, sa, offsets, qw, sw, y, y_dtype, R, E, N, K, debug_partials, workspace,
                     stream);
+}
+
+w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *qw,
+                              const float *sw, void *y, w8a8_dtype y_dtype, int64_t M, int64_t N,
+                              int64_t K, w8a8_stream_t stream) {
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    if (M < 0 || N <= 0 || K <= 0 || K % W8A8_GROUP != 0) return W8A8_ERR_INVALID_ARG;
+    if (M == 0) return W8A8_OK;
+    // The staging copy needs M*K*2 bytes; larger problems do not fit the
+    // built-in scratch and are refused (use w8a8_gemm with a workspace).
+    if (M > kMaxElems / K || staging_bytes(M, K) > kNoallocScratchBytes) return W8A8_ERR_WORKSPACE;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    void *scratch = nullptr;
+    if (noalloc_scratch_ptr(&scratch) != cudaSuccess) return W8A8_ERR_CUDA;
+    return w8a8_gemm(qa, sa, qw, sw, y, y_dtype, M, N, K, nullptr, scratch, kNoallocScratchBytes,
+                     stream);
 }
 
 w8a8_status w8a8_device_error(uint64_t *code_out, int clear) {
