@@ -29,6 +29,8 @@
 //  * Weight tiles and token tiles have separate producers and pipelines whose
 //    depths are chosen per call; narrow token batches (decode) leave room for
 //    ~11 weight tiles in flight per SM.
+//  * Narrow token tiles (<= 64 rows: decode, MoE experts) run a kernel that
+//    moves two K groups per pipeline step, halving the per-group hand-offs.
 //  * Up to 8 partial buffers in TMEM (as many batches as fit in 256 columns)
 //    rotate between the MMA issuer and two epilogue warpgroups, which drain
 //    them (tcgen05.ld), fma the partial with sw[n,g] into register
@@ -150,6 +152,47 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const 
     return ti;
 }
 
+// Tile table (one warp): expert e owns tiles [s_base[e], s_base[e+1]); its
+// rows are [s_lo[e], s_lo[e] + s_cnt[e]) with the offsets clamped into [0, R]
+// (a dense problem is one segment [0, R)). tt = token rows per tile.
+__device__ __forceinline__ void build_tile_table(const KParams &p, int tt, int lane, int *s_base,
+                                                 int *s_lo, int *s_cnt, volatile int *s_total) {
+    int carry = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        int lo = 0, cnt = 0;
+        if (e < p.E) {
+            if (p.offsets != nullptr) {
+                int a = p.offsets[e], b = p.offsets[e + 1];
+                a = min(max(a, 0), p.R);
+                b = min(max(b, 0), p.R);
+                lo = a;
+                cnt = max(b - a, 0);
+            } else {
+                lo = 0;
+                cnt = p.R;
+            }
+        }
+        const int tiles = (e < p.E) ? p.n_tiles * ((cnt + tt - 1) / tt) : 0;
+        int incl = tiles;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (e < p.E) {
+            s_base[e] = carry + incl - tiles;
+            s_lo[e] = lo;
+            s_cnt[e] = cnt;
+        }
+        carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) {
+        s_base[p.E] = carry;
+        *s_total = carry;
+    }
+}
+
 // Token rows of MMA batch h of a tile with n_eff (multiple of 16) rows.
 __device__ __forceinline__ int batch_rows(int n_eff, int nb, int h, int b_rows) {
     return nb == 2 ? (h == 0 ? b_rows : n_eff - b_rows) : n_eff;
@@ -173,13 +216,9 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, uint32_t issued, uint3
 // TMA producer, 3 admission (token tiles landed, partial buffers free), 4-7
 // weight converter, 8-15 epilogue (two warpgroups).
 // kDebug additionally writes every exact group partial.
-// kSingle: every tile is one MMA batch of at most 64 token rows, so the TMEM
-// operand slot, token stage and partial buffer of a group share one 4-deep
-// ring and a single commit per group ("done", the ta_empty barrier) tells the
-// epilogue, the converter and the token producer that the group's MMAs are
-// complete. Otherwise each batch commits its partial buffer and token stage
-// separately.
-template <bool kDebug, bool kSingle>
+// Used for tiles of more than 64 token rows; narrow tiles take
+// w8a8_gemm_narrow_kernel below.
+template <bool kDebug>
 __global__ void __launch_bounds__(kThreads, 1)
 w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
@@ -238,44 +277,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 2) {
-        // Tile table: expert e owns tiles [s_base[e], s_base[e+1]); its rows
-        // are [s_lo[e], s_lo[e] + s_cnt[e]) with offsets clamped into [0, R].
-        int carry = 0;
-        for (int e0 = 0; e0 < p.E; e0 += 32) {
-            const int e = e0 + lane;
-            int lo = 0, cnt = 0;
-            if (e < p.E) {
-                if (p.offsets != nullptr) {
-                    int a = p.offsets[e], b = p.offsets[e + 1];
-                    a = min(max(a, 0), p.R);
-                    b = min(max(b, 0), p.R);
-                    lo = a;
-                    cnt = max(b - a, 0);
-                } else {
-                    lo = 0;
-                    cnt = p.R;
-                }
-            }
-            const int tiles = (e < p.E) ? p.n_tiles * ((cnt + tt - 1) / tt) : 0;
-            int incl = tiles;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (e < p.E) {
-                s_base[e] = carry + incl - tiles;
-                s_lo[e] = lo;
-                s_cnt[e] = cnt;
-            }
-            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-        if (lane == 0) {
-            s_base[p.E] = carry;
-            *s_total = carry;
-        }
-    }
+    if (warp == 2) build_tile_table(p, tt, lane, s_base, s_lo, s_cnt, s_total);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -344,10 +346,8 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                 bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
                             mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
                         }
-                        if constexpr (!kSingle) {
-                            mma_commit(bar(BarIdx::p_full + pr.idx));
-                            mma_commit(bar(BarIdx::b_empty + b.idx));
-                        }
+                        mma_commit(bar(BarIdx::p_full + pr.idx));
+                        mma_commit(bar(BarIdx::b_empty + b.idx));
                         b.advance(SB);
                         pr.advance(PB);
                     }
@@ -404,8 +404,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     for (int h = 0; h < nb; ++h) {
                         const int rows_h = batch_rows(n_eff, nb, h, b_rows);
                         const int nbox = (rows_h + kBoxRows - 1) / kBoxRows;
-                        const int b_free = kSingle ? BarIdx::ta_empty : BarIdx::b_empty;
-                        if (!mbar_wait(bar(b_free + b.idx), b.phase ^ 1u, s_abort, p.err,
+                        if (!mbar_wait(bar(BarIdx::b_empty + b.idx), b.phase ^ 1u, s_abort, p.err,
                                        ROLE_PRODUCER, 2)) {
                             ok = false;
                             break;
@@ -528,8 +527,7 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
                 const float s = jq == 0 ? cur.x : (jq == 1 ? cur.y : (jq == 2 ? cur.z : cur.w));
                 for (int h = 0; h < nb; ++h) {
-                    const int p_ready = kSingle ? BarIdx::ta_empty : BarIdx::p_full;
-                    if (!mbar_wait(bar(p_ready + pr.idx), pr.phase, s_abort, p.err,
+                    if (!mbar_wait(bar(BarIdx::p_full + pr.idx), pr.phase, s_abort, p.err,
                                    ROLE_EPILOGUE, 1)) {
                         ok = false;
                         break;
@@ -600,6 +598,376 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
 }
 
+
+// =============================================================================
+// Narrow tiles (every tile is one MMA batch of at most 64 token rows: decode
+// shapes and MoE experts). Two K groups move through the pipeline per step, so
+// every hand-off (barrier wait, arrive, commit) is paid once per 32 KB of
+// weights instead of once per 16 KB:
+//  * a weight stage is 128 rows x 256 K int8 (two TMA boxes, 256 contiguous
+//    bytes per weight row);
+//  * a step slot (2 of them) holds the fp16 A operands of both groups in TMEM
+//    (128 columns), their two partial buffers (2 x b_rows columns) and the
+//    step's token tiles in shared memory; one commit per step ("done") frees
+//    all of it and tells the epilogue the step's partials are ready;
+//  * each epilogue warpgroup owns one 32-column chunk of the token tile and
+//    drains both groups of a step with two loads and a single wait.
+// Warp roles as in w8a8_gemm_kernel.
+// =============================================================================
+constexpr int kNarrowSlots = 2;
+constexpr int kNarrowAStageBytes = 2 * kAStageBytes;   // 32 KB
+
+struct NBar {
+    static constexpr int a_full = 0;                     // [kMaxAStages] TMA -> converter
+    static constexpr int a_empty = a_full + kMaxAStages; // [kMaxAStages] converter -> TMA
+    static constexpr int ready = a_empty + kMaxAStages;  // [2] converter (4) + admission (1) -> MMA
+    static constexpr int done = ready + kNarrowSlots;    // [2] MMA commit -> epilogue, converter, TMA
+    static constexpr int b_full = done + kNarrowSlots;   // [2] TMA -> admission
+    static constexpr int p_empty = b_full + kNarrowSlots;// [2] epilogue -> admission
+    static constexpr int drain = p_empty + kNarrowSlots;
+    static constexpr int count = drain + 1;
+};
+static_assert(NBar::count <= 128, "barrier area");
+
+template <bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1)
+w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw_addr);
+
+    const uint32_t SA = static_cast<uint32_t>(p.a_stages);
+    const int b_rows = p.b_rows;                          // 32 or 64
+    const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
+    const uint32_t b_stage_bytes = 4u * b_atom_bytes;     // 2 groups x 2 atoms
+    const uint32_t sA = base + kOffStages;
+    const uint32_t sB = sA + SA * kNarrowAStageBytes;
+    const uint32_t sBar = base + kOffBar;
+    volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    int *s_base = reinterpret_cast<int *>(smem + kOffTab);
+    int *s_lo = s_base + (kMaxExperts + 1);
+    int *s_cnt = s_lo + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tt = p.tile_tokens;                         // == b_rows
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kMaxAStages; ++i) {
+            mbar_init(bar(NBar::a_full + i), 1);
+            mbar_init(bar(NBar::a_empty + i), 4);
+        }
+        for (int i = 0; i < kNarrowSlots; ++i) {
+            mbar_init(bar(NBar::ready + i), 5);
+            mbar_init(bar(NBar::done + i), 1);
+            mbar_init(bar(NBar::b_full + i), 1);
+            mbar_init(bar(NBar::p_empty + i), 8);
+        }
+        mbar_init(bar(NBar::drain), 1);
+        *s_abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 2) build_tile_table(p, tt, lane, s_base, s_lo, s_cnt, s_total);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *s_tmem_base;
+    const int total = *s_total;
+    const int G = p.G;
+    const int wg = warp >> 2;
+    // TMEM: partial buffer of (slot s, group j) at column (2 s + j) * b_rows;
+    // fp16 A operand of (slot s, group j) at column 256 + 128 s + 64 j.
+    auto pbuf_col = [&](uint32_t s, int j) -> uint32_t {
+        return (2u * s + static_cast<uint32_t>(j)) * static_cast<uint32_t>(b_rows);
+    };
+
+    if (warp < 4) {
+        setmaxnreg_dec<kOtherRegs>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------- weight TMA producer
+            Ring a;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int wrow = ti.e * p.N + ti.n0;
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    const int ng = min(2, G - g0);
+                    if (!mbar_wait(bar(NBar::a_empty + a.idx), a.phase ^ 1u, s_abort, p.err,
+                                   ROLE_PRODUCER, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(NBar::a_full + a.idx), ng * kAStageBytes);
+                    for (int j = 0; j < ng; ++j)
+                        tma_load_2d(sA + a.idx * kNarrowAStageBytes + j * kAStageBytes, &tmap_w,
+                                    (g0 + j) * kGroupK, wrow, bar(NBar::a_full + a.idx));
+                    a.advance(SA);
+                    ++issued;
+                }
+            }
+            if (!ok) drain_ring(bar(NBar::a_full), issued, SA);
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            Ring st;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(n_eff));
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    const int ng = min(2, G - g0);
+                    if (!mbar_wait(bar(NBar::ready + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
+                                   1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int j = 0; j < ng; ++j) {
+                        const uint32_t d_tmem = tmem_base + pbuf_col(st.idx, j);
+                        const uint32_t a_tmem = tmem_base + kTmemA0 + st.idx * 128u + j * 64u;
+                        const uint64_t bdesc0 = smem_desc_sw128(sB + st.idx * b_stage_bytes +
+                                                                j * 2u * b_atom_bytes);
+                        const uint64_t atom_step = b_atom_bytes >> 4;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bdesc =
+                                bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
+                            mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(bar(NBar::done + st.idx));
+                    st.advance(kNarrowSlots);
+                }
+            }
+            mma_commit(bar(NBar::drain));
+            drain_wait(bar(NBar::drain), 0);
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------- token TMA producer
+            griddep_wait();   // the fp16 token codes come from the kernel launched before
+            Ring st;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const int nbox = (n_eff + kBoxRows - 1) / kBoxRows;
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    const int ng = min(2, G - g0);
+                    if (!mbar_wait(bar(NBar::done + st.idx), st.phase ^ 1u, s_abort, p.err,
+                                   ROLE_PRODUCER, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t stage = sB + st.idx * b_stage_bytes;
+                    mbar_arrive_expect_tx(bar(NBar::b_full + st.idx),
+                                          static_cast<uint32_t>(ng * 2 * nbox * kBoxRows * 128));
+                    for (int j = 0; j < ng; ++j)
+                        for (int a = 0; a < 2; ++a)
+                            for (int i = 0; i < nbox; ++i)
+                                tma_load_2d(stage + (2 * j + a) * b_atom_bytes + i * kBoxRows * 128,
+                                            &tmap_x, (g0 + j) * kGroupK + a * 64,
+                                            ti.m0 + i * kBoxRows, bar(NBar::b_full + st.idx));
+                    st.advance(kNarrowSlots);
+                    ++issued;
+                }
+            }
+            if (!ok) drain_ring(bar(NBar::b_full), issued, kNarrowSlots);
+        } else if (warp == 3 && lane == 0) {
+            // --------------------------------------------------- admission
+            Ring st;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    if (!mbar_wait(bar(NBar::b_full + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
+                                   2) ||
+                        !mbar_wait(bar(NBar::p_empty + st.idx), st.phase ^ 1u, s_abort, p.err,
+                                   ROLE_MMA, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(bar(NBar::ready + st.idx));
+                    st.advance(kNarrowSlots);
+                }
+            }
+        }
+    } else if (wg == 1) {
+        // --------------------------------------- weight converter (A -> TMEM)
+        setmaxnreg_dec<kOtherRegs>();
+        const int row = threadIdx.x - 128;
+        const int q = warp & 3;
+        Ring a, st;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for (int g0 = 0; g0 < G; g0 += 2) {
+                const int ng = min(2, G - g0);
+                if (!mbar_wait(bar(NBar::a_full + a.idx), a.phase, s_abort, p.err, ROLE_CONVERT,
+                               1) ||
+                    !mbar_wait(bar(NBar::done + st.idx), st.phase ^ 1u, s_abort, p.err,
+                               ROLE_CONVERT, 2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int j = 0; j < ng; ++j) {
+                    const uint8_t *rowp =
+                        smem + kOffStages + a.idx * kNarrowAStageBytes + j * kAStageBytes + row * 128;
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                           kTmemA0 + st.idx * 128u + j * 64u;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        uint32_t r16[16];
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int c = 2 * jj + cc;
+                            const uint4 v =
+                                *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
+                            i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
+                            i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
+                            i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
+                            i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
+                        }
+                        tmem_st_16cols(taddr + jj * 16, r16);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(NBar::a_empty + a.idx));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(NBar::ready + st.idx));
+                a.advance(SA);
+                st.advance(kNarrowSlots);
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        setmaxnreg_inc<kEpiRegs>();
+        const int ewg = wg - 2;                // owns token columns [32 ewg, 32 ewg + 32)
+        const int q = warp & 3;
+        const int lrow = q * 32 + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+        Ring st;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+            const int n_eff = (ti.rows + 15) & ~15;
+            const bool owned = 32 * ewg < n_eff;   // warp-uniform
+            const int n_local = ti.n0 + lrow;
+            const bool n_ok = n_local < p.N;
+            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            // Scales of this row a quad of groups (two steps) ahead; loads are
+            // issued in place and only read after the next quad boundary.
+            auto load_quad = [&](int g) -> float4 {
+                float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (!n_ok || !owned) return v;
+                if (vec_sw) {
+                    if (g < G) v = ldg_nc_f32x4_now(swp + g);
+                } else {
+                    if (g < G) v.x = ldg_nc_f32_now(swp + g);
+                    if (g + 1 < G) v.y = ldg_nc_f32_now(swp + g + 1);
+                    if (g + 2 < G) v.z = ldg_nc_f32_now(swp + g + 2);
+                    if (g + 3 < G) v.w = ldg_nc_f32_now(swp + g + 3);
+                }
+                return v;
+            };
+            float4 cur = load_quad(0);
+            float4 nxt = load_quad(4);
+            for (int g0 = 0; ok && g0 < G; g0 += 2) {
+                const int ng = min(2, G - g0);
+                if ((g0 & 3) == 0 && g0 > 0) {
+                    cur = nxt;
+                    nxt = load_quad(g0 + 4);
+                }
+                const float s0 = (g0 & 3) == 0 ? cur.x : cur.z;
+                const float s1 = (g0 & 3) == 0 ? cur.y : cur.w;
+                if (!mbar_wait(bar(NBar::done + st.idx), st.phase, s_abort, p.err, ROLE_EPILOGUE,
+                               1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (owned) {
+                    const uint32_t c0 = lane_base + pbuf_col(st.idx, 0) + 32u * ewg;
+                    const uint32_t c1 = lane_base + pbuf_col(st.idx, 1) + 32u * ewg;
+                    uint32_t v0[32], v1[32];
+                    if (ng == 2) {
+                        tmem_ld_2x32cols_sync(c0, c1, v0, v1);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[j] = fmaf(__uint_as_float(v1[j]), s1,
+                                          fmaf(__uint_as_float(v0[j]), s0, acc[j]));
+                    } else {
+                        tmem_ld_32cols_sync(c0, v0);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(v0[j]), s0, acc[j]);
+                    }
+                    if (kDebug && n_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = 32 * ewg + j;
+                            if (col < ti.rows) {
+                                const size_t o =
+                                    (static_cast<size_t>(ti.m0 + col) * p.N + n_local) * G + g0;
+                                p.dbg[o] = __float2int_rn(__uint_as_float(v0[j]));
+                                if (ng == 2) p.dbg[o + 1] = __float2int_rn(__uint_as_float(v1[j]));
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + st.idx));
+                st.advance(kNarrowSlots);
+            }
+            if (!ok) break;
+            if (owned && n_ok) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int col = 32 * ewg + j;
+                    if (col < ti.rows) {
+                        const int m = ti.m0 + col;
+                        const float out = acc[j] * __ldg(p.sa + m);
+                        const size_t idx = static_cast<size_t>(m) * p.N + n_local;
+                        if (p.out_fp32)
+                            static_cast<float *>(p.y)[idx] = out;
+                        else
+                            static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
 // ------------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -633,7 +1001,7 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_bytes, c
 // stage counts, filling shared memory with weight stages after the token stages.
 struct PipeShape {
     int b_rows, tile_tokens, b_stages, a_stages, p_bufs, smem_bytes;
-    bool single;    // one batch per tile, group rings tied (see the kernel's kSingle)
+    bool narrow;    // one batch of <= 64 rows per tile: w8a8_gemm_narrow_kernel
 };
 
 PipeShape choose_pipe(const GemmProblem &pr) {
@@ -648,15 +1016,22 @@ PipeShape choose_pipe(const GemmProblem &pr) {
         s.b_rows = pr.grouped_batch_rows;
         s.tile_tokens = pr.grouped_batch_rows;
     }
-    s.single = s.tile_tokens == s.b_rows && s.b_rows <= 64;
-    if (s.single) {
-        s.p_bufs = kTmemSlots;           // rings tied to the TMEM operand slots
-        s.b_stages = kTmemSlots;
-    } else {
-        s.p_bufs = 256 / s.b_rows;
-        if (s.p_bufs > kMaxPBufs) s.p_bufs = kMaxPBufs;
-        s.b_stages = 4;
+    s.narrow = s.tile_tokens == s.b_rows && s.b_rows <= 64;
+    if (s.narrow) {
+        // Two step slots, each holding the token tiles of two K groups.
+        s.p_bufs = 2 * kNarrowSlots;
+        s.b_stages = kNarrowSlots;
+        const int b_slot_bytes = 4 * s.b_rows * 128;
+        const int avail = kSmemLimit - 1024 - kOffStages - kNarrowSlots * b_slot_bytes;
+        s.a_stages = avail / kNarrowAStageBytes;
+        if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
+        s.smem_bytes = kOffStages + s.a_stages * kNarrowAStageBytes +
+                       kNarrowSlots * b_slot_bytes + 1024;
+        return s;
     }
+    s.p_bufs = 256 / s.b_rows;
+    if (s.p_bufs > kMaxPBufs) s.p_bufs = kMaxPBufs;
+    s.b_stages = 4;
     const int b_stage_bytes = s.b_rows * 256;
     const int avail = kSmemLimit - 1024 - kOffStages - s.b_stages * b_stage_bytes;
     s.a_stages = avail / kAStageBytes;
@@ -665,9 +1040,9 @@ PipeShape choose_pipe(const GemmProblem &pr) {
     return s;
 }
 
-template <bool kDebug, bool kSingle>
-cudaError_t launch_gemm_impl(const GemmProblem &pr, const PipeShape &ps, int num_sms,
-                             cudaStream_t stream) {
+template <auto kernel>
+cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sms,
+                          cudaStream_t stream) {
     if (ps.a_stages < 2 || ps.b_rows % kBoxRows != 0 || ps.b_rows > kMaxBatchRows ||
         ps.smem_bytes > kSmemLimit)
         return cudaErrorInvalidConfiguration;
@@ -678,19 +1053,18 @@ cudaError_t launch_gemm_impl(const GemmProblem &pr, const PipeShape &ps, int num
                    (uint64_t)pr.R, 64, kBoxRows))
         return cudaErrorInvalidValue;
 
-    static int attr_done[64] = {0};   // per device, per instance
+    static int attr_done[64] = {0};   // per device, per kernel instance
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         // setmaxnreg.inc can only take registers the CTA was launched with:
         // refuse to launch unless the launch allocation covers the split.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, w8a8_gemm_kernel<kDebug, kSingle>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return e;
         if (fa.numRegs * kThreads < (kThreads / 2) * (kEpiRegs + kOtherRegs))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(w8a8_gemm_kernel<kDebug, kSingle>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         attr_done[dev] = 1;
     }
@@ -739,7 +1113,7 @@ cudaError_t launch_gemm_impl(const GemmProblem &pr, const PipeShape &ps, int num
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, w8a8_gemm_kernel<kDebug, kSingle>, tw, tx, kp);
+    e = cudaLaunchKernelEx(&cfg, kernel, tw, tx, kp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -749,11 +1123,11 @@ cudaError_t launch_gemm_impl(const GemmProblem &pr, const PipeShape &ps, int num
 cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     const PipeShape ps = choose_pipe(pr);
     const bool dbg = pr.debug_partials != nullptr;
-    if (ps.single)
-        return dbg ? launch_gemm_impl<true, true>(pr, ps, num_sms, stream)
-                   : launch_gemm_impl<false, true>(pr, ps, num_sms, stream);
-    return dbg ? launch_gemm_impl<true, false>(pr, ps, num_sms, stream)
-               : launch_gemm_impl<false, false>(pr, ps, num_sms, stream);
+    if (ps.narrow)
+        return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true>>(pr, ps, num_sms, stream)
+                   : launch_kernel<w8a8_gemm_narrow_kernel<false>>(pr, ps, num_sms, stream);
+    return dbg ? launch_kernel<w8a8_gemm_kernel<true>>(pr, ps, num_sms, stream)
+               : launch_kernel<w8a8_gemm_kernel<false>>(pr, ps, num_sms, stream);
 }
 
 cudaError_t read_device_error(unsigned long long *value, bool clear) {
