@@ -79,16 +79,45 @@ w8a8_status check_gemm(const int8_t *qa, const float *sa, const void *offsets, c
     return W8A8_OK;
 }
 
+// Full workspace: the staging copy, then (narrow-tile calls) the stream-K
+// split area at the next 256-byte boundary.
+size_t workspace_bytes_for(int64_t R, int64_t K, bool grouped) {
+    if (R <= 0) return 0;
+    return staging_bytes(R, K) + round_up(w8a8::sk_area_bytes(R, grouped), kWsAlign);
+}
+
 w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, const int8_t *qw,
                      const float *sw, void *y, w8a8_dtype y_dtype, int64_t R, int64_t E,
-                     int64_t N, int64_t K, int32_t *dbg, void *workspace, w8a8_stream_t stream) {
+                     int64_t N, int64_t K, int32_t *dbg, void *workspace, size_t workspace_bytes,
+                     w8a8_stream_t stream) {
     w8a8::DeviceInfo info;
     w8a8_status st = check_device(&info);
     if (st != W8A8_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s);
-    if (e != cudaSuccess) return W8A8_ERR_CUDA;
+    const bool grouped = offsets != nullptr;
     w8a8::GemmProblem p;
+    // The split area is optional: with a workspace that only holds the
+    // staging copy, tiles are never split across CTAs.
+    const size_t stage = staging_bytes(R, K);
+    if (w8a8::sk_area_bytes(R, grouped) > 0 &&
+        workspace_bytes >= workspace_bytes_for(R, K, grouped)) {
+        unsigned char *area = static_cast<unsigned char *>(workspace) + stage;
+        p.sk_cnt = reinterpret_cast<int *>(area);
+        p.sk_part = reinterpret_cast<float *>(area + w8a8::sk_counter_bytes());
+        p.sk_ld = static_cast<int>(w8a8::sk_slot_cols(R, grouped));
+    }
+    cudaError_t e = cudaSuccess;
+    if (w8a8::uses_gemv(R, grouped)) {
+        // The CUDA-core path reads the int8 codes directly; only the split
+        // counters need zeroing.
+        if (p.sk_cnt != nullptr)
+            e = cudaMemsetAsync(p.sk_cnt, 0, w8a8::sk_counter_bytes(), s);
+    } else {
+        e = w8a8::launch_widen_codes(qa, R, K, K, workspace, p.sk_cnt, 2 * w8a8::kSkMaxCtas,
+                                     info.num_sms, s);
+    }
+    if (e != cudaSuccess) return W8A8_ERR_CUDA;
+    p.qa = qa;
     p.sa = sa;
     p.sw = sw;
     p.qw = qw;
@@ -180,13 +209,15 @@ w8a8_status w8a8_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, 
 
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
     (void)N;
-    return staging_bytes(M, K);
+    if (K <= 0) return 0;
+    return workspace_bytes_for(M, K, false);
 }
 
 size_t w8a8_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K) {
     (void)E;
     (void)N;
-    return staging_bytes(R, K);
+    if (K <= 0) return 0;
+    return workspace_bytes_for(R, K, true);
 }
 
 w8a8_status w8a8_gemm(const int8_t *qa, const float *sa, const int8_t *qw, const float *sw,
@@ -199,7 +230,7 @@ w8a8_status w8a8_gemm(const int8_t *qa, const float *sa, const int8_t *qw, const
     if (st != W8A8_OK || M == 0) return st;
     if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
     return run_gemm(qa, sa, nullptr, qw, sw, y, y_dtype, M, 1, N, K, debug_partials, workspace,
-                    stream);
+                    workspace_bytes, stream);
 }
 
 w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *offsets,
@@ -213,7 +244,7 @@ w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *
     if (st != W8A8_OK || R == 0) return st;
     if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
     return run_gemm(qa, sa, offsets, qw, sw, y, y_dtype, R, E, N, K, debug_partials, workspace,
-                    stream);
+                    workspace_bytes, stream);
 }
 
 w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *qw,

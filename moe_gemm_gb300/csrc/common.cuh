@@ -78,6 +78,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // try_wait with a suspend-time hint: a thread whose phase is not complete is
 // suspended (it takes no issue slots from the warps doing work) until the
 // phase completes or about `hint_ns` elapse.
@@ -108,6 +120,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             *abort = 1;
             record_device_error(err, KID_GEMM, role, site);
             return false;
+        }
+    }
+}
+
+// Same contract as mbar_wait, but polls with the non-blocking test_wait
+// instead of suspending: for hand-offs on a pipeline's critical path, where
+// the wake-up latency of a suspended thread (hundreds of cycles) would be
+// paid on every step. Costs issue slots while it waits.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               unsigned long long *err, unsigned role,
+                                               unsigned site) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                record_device_error(err, KID_GEMM, role, site);
+                return false;
+            }
         }
     }
 }

@@ -3,7 +3,8 @@
 Bars (stated by the method's contract):
   * quantizer codes and scales, weight codes and scales, and the INT32 group
     partials (debug mode): bit-exact;
-  * FP32 output: |y - y*| <= 1e-5 * T and <= (G+2) 2^-24 T, T = sum_g |sa sw P|;
+  * FP32 output: |y - y*| <= 1e-5 * T and <= (G + ceil(G/2) + 1) 2^-24 T,
+    T = sum_g |sa sw P| (G group fmas, additions of K-split pieces, sa);
   * BF16 output: within 1 BF16 ulp of the correctly rounded y*, or
     |y - y*| <= 1e-5 T + ulp/2 (cancellation rows where T >> |y*|).
 Outputs are poisoned with NaN first so unwritten elements are caught.
@@ -35,11 +36,18 @@ def bf16_bits_of(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def check_fp32(y: np.ndarray, y_ref: np.ndarray, T: np.ndarray, K: int):
+def fp32_bound(K: int) -> float:
+    """Relative FP32 bound on |Y - Y*| / T: G group fmas, at most ceil(G/2) - 1
+    additions of K-split pieces, the token-scale multiply and one ulp of slack,
+    capped by the 1e-5 * sum|terms| accuracy the FP32 output must meet."""
     Gn = K // G
+    return min(1e-5, (Gn + (Gn + 1) // 2 + 1) * 2.0 ** -24)
+
+
+def check_fp32(y: np.ndarray, y_ref: np.ndarray, T: np.ndarray, K: int):
     err = np.abs(y.astype(np.float64) - y_ref)
     assert not np.isnan(y).any(), "unwritten (NaN) outputs"
-    bad = err > np.minimum(1e-5, (Gn + 2) * 2.0 ** -24) * T
+    bad = err > fp32_bound(K) * T
     assert not bad.any(), f"{bad.sum()} outputs out of tolerance; worst err/T {np.max(err / np.maximum(T, 1e-300)):.3e}"
 
 
@@ -281,4 +289,55 @@ def test_moe_t16_many_empty_segments():
 
 
 def test_no_device_error_recorded():
+    assert w8.device_error(clear=True) == 0
+
+
+# ------------------------------------------------------- K-split (stream-K)
+def _staging_only(rows, K):
+    """A workspace holding only the fp16 staging copy: tiles are never split."""
+    return torch.empty((rows * K * 2 + 255) // 256 * 256, dtype=torch.uint8, device=DEV)
+
+
+@pytest.mark.parametrize("M,N,K,out", [
+    (1, 4096, 8192, "fp32"),     # 32 tiles of 32 steps over all SMs: ~5 pieces per tile
+    (33, 1000, 1152, "bf16"),    # odd group count, one step per CTA, ragged N
+    (64, 28672, 1024, "fp32"),   # 224 tiles, ranges cross tile boundaries
+])
+def test_dense_k_split_matches_oracle_and_unsplit(M, N, K, out):
+    rng = np.random.default_rng(M + N + K)
+    a_bits = workloads.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    (qa, sa, qw, sw), (qa_o, sa_o, qw_o, sw_o) = quantize_pair(a_bits, w)
+    dt = torch.float32 if out == "fp32" else torch.bfloat16
+    y_ref, T = oracle.gemm(qa_o, sa_o, qw_o, sw_o)
+    ys = []
+    for ws in (None, None, _staging_only(M, K)):     # split twice, then unsplit
+        y = torch.full((M, N), float("nan"), dtype=dt, device=DEV)
+        w8.gemm(qa, sa, qw, sw, out_dtype=dt, out=y, workspace=ws)
+        torch.cuda.synchronize()
+        ys.append(y)
+        if out == "fp32":
+            check_fp32(y.cpu().numpy(), y_ref, T, K)
+        else:
+            check_bf16(bf16_bits_of(y), y_ref, T)
+    # the split result does not depend on which CTA finishes a tile last
+    assert torch.equal(ys[0], ys[1])
+    _, P = w8.gemm(qa, sa, qw, sw, out_dtype=dt, debug_partials=True)
+    np.testing.assert_array_equal(P.cpu().numpy(), oracle.group_partials(qa_o, qw_o))
+    assert w8.device_error(clear=True) == 0
+
+
+def test_grouped_k_split_matches_oracle_and_unsplit():
+    rng = np.random.default_rng(77)
+    R, E, N, K = 300, 6, 256, 1280
+    off = workloads.random_offsets(rng, R, E, empty_frac=0.2)
+    (qa, sa, qw, sw), (qa_o, sa_o, qw_o, sw_o) = make_grouped(rng, R, E, N, K, off)
+    offs = torch.from_numpy(off).to(DEV)
+    y_ref, T = oracle.grouped_gemm(qa_o, sa_o, off, qw_o, sw_o)
+    covered = slice(int(off[0]), int(off[E]))
+    for ws in (None, _staging_only(R, K)):
+        y = torch.full((R, N), float("nan"), dtype=torch.float32, device=DEV)
+        w8.grouped_gemm(qa, sa, offs, qw, sw, out_dtype=torch.float32, out=y, workspace=ws)
+        torch.cuda.synchronize()
+        check_fp32(y.cpu().numpy()[covered], y_ref[covered], T[covered], K)
     assert w8.device_error(clear=True) == 0
