@@ -86,13 +86,14 @@ w8a8_status w8a8_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, 
 /*
  * Bytes of device workspace w8a8_gemm asks for: an fp16 copy of the M x K
  * int8 activation codes (the tensor-core operand), rounded up to 256 bytes,
- * then, when M <= 64, a split area of 1280 + 160 * 2 * M * 128 * 4 bytes
- * (rounded up to 256) in which up to 160 CTAs exchange FP32 partial sums of
- * weight tiles whose K range they share. 0 when M == 0.
+ * then, when 5 <= M <= 8, a split area of 1280 + 160 * 2 * M * 128 * 4
+ * bytes (rounded up to 256) in which up to 160 CTAs exchange FP32 partial
+ * sums of weight tiles whose K range they share. 0 when M == 0.
  * The split area is optional: a workspace that holds only the staging copy
  * (M * K * 2 bytes rounded up to 256) is accepted, and the GEMM then never
  * splits a tile's K range across CTAs (slower when the weight tiles do not
  * divide evenly among the SMs; results agree within the stated bound).
+ * Calls with M <= 8 run on the CUDA cores and do not use the staging copy.
  */
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -111,9 +112,9 @@ size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * K must be a positive multiple of 128; N >= 1. M == 0 is a no-op.
  * The group sums are exact integers; Y is accumulated in FP32 over the
  * groups in K order, acc = fma(P_g, sw[n,g], acc), and Y = sa[m] * acc. When
- * a tile's K range is split into n pieces (n <= ceil(G/2), n = 1 without the
- * split area), each piece accumulates its groups from zero and the pieces are
- * added in K order, so
+ * a tile's K range is split into n pieces (only for 5 <= M <= 8 with the
+ * split area; n <= ceil(G/2), otherwise n = 1), each piece accumulates its
+ * groups from zero and the pieces are added in K order, so
  *   |Y - Y*| <= (G + n + 1) * 2^-24 * sum_g |sa*sw*P_g|  for the exact Y*,
  * and the result does not depend on the order in which CTAs finish.
  */
@@ -123,10 +124,8 @@ w8a8_status w8a8_gemm(const int8_t *qa, const float *sa, const int8_t *qw, const
                       w8a8_stream_t stream);
 
 /*
- * Bytes of device workspace w8a8_grouped_gemm asks for with R routed rows: an
- * fp16 copy of the R x K activation codes rounded up to 256 bytes, then a
- * split area of 1280 + 160 * 2 * 64 * 128 * 4 bytes (rounded up to 256), as
- * for w8a8_gemm. The split area is optional in the same way.
+ * Bytes of device workspace w8a8_grouped_gemm needs for R routed rows: an
+ * fp16 copy of the R x K activation codes, rounded up to 256 bytes.
  */
 size_t w8a8_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K);
 
@@ -142,8 +141,8 @@ size_t w8a8_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t N, int64_t
  *   qw      [E, N, K] int8, sw [E, N, K/128] float: per-expert weights and scales
  *   y       [R, N] BF16 or FP32. Only rows covered by a segment are written.
  *   debug_partials: NULL or int32 [R, N, K/128].
- *   workspace: w8a8_grouped_gemm_workspace_size(R, E, N, K) bytes (at least the
- *              staging part), 256-aligned. Error bound as for w8a8_gemm.
+ *   workspace: >= w8a8_grouped_gemm_workspace_size(R, E, N, K) bytes, 256-aligned.
+ * Y is accumulated as in w8a8_gemm (no K split): the error bound there with n = 1.
  * E >= 1, N >= 1, K a positive multiple of 128. R == 0 is a no-op.
  */
 w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *offsets,

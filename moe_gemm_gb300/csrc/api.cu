@@ -79,8 +79,8 @@ w8a8_status check_gemm(const int8_t *qa, const float *sa, const void *offsets, c
     return W8A8_OK;
 }
 
-// Full workspace: the staging copy, then (narrow-tile calls) the stream-K
-// split area at the next 256-byte boundary.
+// Full workspace: the staging copy, then (GEMV calls of 5..8 token rows) the
+// stream-K split area at the next 256-byte boundary.
 size_t workspace_bytes_for(int64_t R, int64_t K, bool grouped) {
     if (R <= 0) return 0;
     return staging_bytes(R, K) + round_up(w8a8::sk_area_bytes(R, grouped), kWsAlign);
@@ -104,7 +104,7 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
         unsigned char *area = static_cast<unsigned char *>(workspace) + stage;
         p.sk_cnt = reinterpret_cast<int *>(area);
         p.sk_part = reinterpret_cast<float *>(area + w8a8::sk_counter_bytes());
-        p.sk_ld = static_cast<int>(w8a8::sk_slot_cols(R, grouped));
+        p.sk_ld = static_cast<int>(R);
     }
     cudaError_t e = cudaSuccess;
     if (w8a8::uses_gemv(R, grouped)) {
@@ -113,8 +113,7 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
         if (p.sk_cnt != nullptr)
             e = cudaMemsetAsync(p.sk_cnt, 0, w8a8::sk_counter_bytes(), s);
     } else {
-        e = w8a8::launch_widen_codes(qa, R, K, K, workspace, p.sk_cnt, 2 * w8a8::kSkMaxCtas,
-                                     info.num_sms, s);
+        e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s);
     }
     if (e != cudaSuccess) return W8A8_ERR_CUDA;
     p.qa = qa;

@@ -114,10 +114,9 @@ struct KParams {
     int b_rows;         // token rows per MMA batch and per token stage (32, 64, 96 or 128)
     int tile_tokens;    // token rows per tile (b_rows or 2 * b_rows)
     int p_bufs;         // partial buffers in TMEM (p_bufs * b_rows <= 256)
-    int tab_off;        // narrow kernel: byte offset of the tile table in shared memory
-    int a_slots;        // narrow kernel: fp16 weight operand slots in TMEM (2 or 3)
+    int tab_off;        // byte offset of the tile table in shared memory
     unsigned long long *err;
-    // Stream-K split of the narrow kernel (null sk_cnt: whole tiles only).
+    // Stream-K split of the CUDA-core GEMV (null sk_cnt: whole tiles only).
     int *sk_cnt;        // [2 * grid] arrival counters of split tiles, zero at launch
     float *sk_part;     // [grid][2][sk_ld][128] FP32 piece partials
     int sk_ld;          // token columns per partial slot
@@ -612,57 +611,369 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
 // weights instead of once per 16 KB:
 //  * a weight stage is 128 rows x 256 K int8 (two TMA boxes, 256 contiguous
 //    bytes per weight row);
-//  * a step's fp16 A operands (both groups, 128 TMEM columns) sit in one of
-//    2 or 3 operand slots, its two partial buffers (2 x b_rows columns) in
-//    one of 2 partial slots; two commits per step free the operand slot for
-//    the converter ("a_free") and tell the epilogue the partials are ready
-//    ("done"). With 3 operand slots (token tiles of <= 32 rows) the
-//    converter works two steps ahead of the MMAs, off their critical path;
-//  * the step's token tiles sit in their own, deeper ring in shared memory
-//    (they come from L2, about a microsecond away under the weight stream),
-//    so they are requested several steps ahead; the epilogue, which waits
-//    for every step's completion anyway, hands their stages back;
+//  * a step slot (2 of them) holds the fp16 A operands of both groups in TMEM
+//    (128 columns), their two partial buffers (2 x b_rows columns) and the
+//    step's token tiles in shared memory; one commit per step ("done") frees
+//    all of it and tells the epilogue the step's partials are ready;
 //  * each epilogue warpgroup owns one 32-column chunk of the token tile and
 //    drains both groups of a step with two loads and a single wait.
-// Warp roles as in w8a8_gemm_kernel. The MMA issuer, whose waits are on the
-// step's critical path, polls instead of suspending.
-//
-// Work split (when the caller's workspace has room for it): the tiles that
-// fill whole waves go round-robin to the CTAs; the steps of the tiles left
-// over are divided into equal contiguous ranges, one per CTA (stream-K), so
-// every SM streams the same number of weight bytes. Each CTA works on its
-// stream-K range first and on its whole tiles after it, so that the combining
-// of split tiles overlaps the whole tiles instead of trailing the kernel. A
-// tile whose steps fall into several ranges is finished by the CTA that
-// completes its piece last: each piece stores its FP32 partial sum (before
-// the token scale), bumps the tile's arrival counter, and the last arrival
-// adds the pieces in K order (so the result does not depend on arrival
-// order), applies sa and stores y. No CTA waits for another.
+// Warp roles as in w8a8_gemm_kernel.
 // =============================================================================
-constexpr int kNarrowSlots = 2;        // partial-buffer slots
-constexpr int kNarrowMaxASlots = 3;    // fp16 operand slots in TMEM
+constexpr int kNarrowSlots = 2;
 constexpr int kNarrowAStageBytes = 2 * kAStageBytes;   // 32 KB
-constexpr int kNarrowOffStages = 2048;    // barriers, flags; the tile table follows the stages
-// One 32-column accumulator per epilogue thread leaves room for the other
-// roles' stream-K bookkeeping.
-constexpr int kNarrowEpiRegs = 184;
-constexpr int kNarrowOtherRegs = 72;
-static_assert((kThreads / 2) * (kNarrowEpiRegs + kNarrowOtherRegs) == 65536, "register split");
 
 struct NBar {
     static constexpr int a_full = 0;                     // [kMaxAStages] TMA -> converter
     static constexpr int a_empty = a_full + kMaxAStages; // [kMaxAStages] converter -> TMA
-    static constexpr int ready = a_empty + kMaxAStages;  // [a_slots] converter (4) + admission (1) -> MMA
-    static constexpr int a_free = ready + kNarrowMaxASlots; // [a_slots] MMA commit -> converter
-    static constexpr int done = a_free + kNarrowMaxASlots;  // [2] MMA commit -> epilogue
-    static constexpr int b_full = done + kNarrowSlots;   // [kMaxBStages] TMA -> admission
-    static constexpr int b_empty = b_full + kMaxBStages; // [kMaxBStages] epilogue -> token TMA
-    static constexpr int p_empty = b_empty + kMaxBStages;// [2] epilogue -> admission
+    static constexpr int ready = a_empty + kMaxAStages;  // [2] converter (4) + admission (1) -> MMA
+    static constexpr int done = ready + kNarrowSlots;    // [2] MMA commit -> epilogue, converter, TMA
+    static constexpr int b_full = done + kNarrowSlots;   // [2] TMA -> admission
+    static constexpr int p_empty = b_full + kNarrowSlots;// [2] epilogue -> admission
     static constexpr int drain = p_empty + kNarrowSlots;
     static constexpr int count = drain + 1;
 };
 static_assert(NBar::count <= 128, "barrier area");
 
+template <bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1)
+w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw_addr);
+
+    const uint32_t SA = static_cast<uint32_t>(p.a_stages);
+    const int b_rows = p.b_rows;                          // 32 or 64
+    const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
+    const uint32_t b_stage_bytes = 4u * b_atom_bytes;     // 2 groups x 2 atoms
+    const uint32_t sA = base + kOffStages;
+    const uint32_t sB = sA + SA * kNarrowAStageBytes;
+    const uint32_t sBar = base + kOffBar;
+    volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    int *s_base = reinterpret_cast<int *>(smem + kOffTab);
+    int *s_lo = s_base + (kMaxExperts + 1);
+    int *s_cnt = s_lo + (kMaxExperts + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tt = p.tile_tokens;                         // == b_rows
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kMaxAStages; ++i) {
+            mbar_init(bar(NBar::a_full + i), 1);
+            mbar_init(bar(NBar::a_empty + i), 4);
+        }
+        for (int i = 0; i < kNarrowSlots; ++i) {
+            mbar_init(bar(NBar::ready + i), 5);
+            mbar_init(bar(NBar::done + i), 1);
+            mbar_init(bar(NBar::b_full + i), 1);
+            mbar_init(bar(NBar::p_empty + i), 8);
+        }
+        mbar_init(bar(NBar::drain), 1);
+        *s_abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 2) build_tile_table(p, tt, lane, s_base, s_lo, s_cnt, s_total);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *s_tmem_base;
+    const int total = *s_total;
+    const int G = p.G;
+    const int wg = warp >> 2;
+    // TMEM: partial buffer of (slot s, group j) at column (2 s + j) * b_rows;
+    // fp16 A operand of (slot s, group j) at column 256 + 128 s + 64 j.
+    auto pbuf_col = [&](uint32_t s, int j) -> uint32_t {
+        return (2u * s + static_cast<uint32_t>(j)) * static_cast<uint32_t>(b_rows);
+    };
+
+    if (warp < 4) {
+        setmaxnreg_dec<kOtherRegs>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------- weight TMA producer
+            Ring a;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int wrow = ti.e * p.N + ti.n0;
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    const int ng = min(2, G - g0);
+                    if (!mbar_wait(bar(NBar::a_empty + a.idx), a.phase ^ 1u, s_abort, p.err,
+                                   ROLE_PRODUCER, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(NBar::a_full + a.idx), ng * kAStageBytes);
+                    for (int j = 0; j < ng; ++j)
+                        tma_load_2d(sA + a.idx * kNarrowAStageBytes + j * kAStageBytes, &tmap_w,
+                                    (g0 + j) * kGroupK, wrow, bar(NBar::a_full + a.idx));
+                    a.advance(SA);
+                    ++issued;
+                }
+            }
+            if (!ok) drain_ring(bar(NBar::a_full), issued, SA);
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            Ring st;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(n_eff));
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    const int ng = min(2, G - g0);
+                    if (!mbar_wait(bar(NBar::ready + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
+                                   1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int j = 0; j < ng; ++j) {
+                        const uint32_t d_tmem = tmem_base + pbuf_col(st.idx, j);
+                        const uint32_t a_tmem = tmem_base + kTmemA0 + st.idx * 128u + j * 64u;
+                        const uint64_t bdesc0 = smem_desc_sw128(sB + st.idx * b_stage_bytes +
+                                                                j * 2u * b_atom_bytes);
+                        const uint64_t atom_step = b_atom_bytes >> 4;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bdesc =
+                                bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
+                            mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(bar(NBar::done + st.idx));
+                    st.advance(kNarrowSlots);
+                }
+            }
+            mma_commit(bar(NBar::drain));
+            drain_wait(bar(NBar::drain), 0);
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------- token TMA producer
+            griddep_wait();   // the fp16 token codes come from the kernel launched before
+            Ring st;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const int n_eff = (ti.rows + 15) & ~15;
+                const int nbox = (n_eff + kBoxRows - 1) / kBoxRows;
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    const int ng = min(2, G - g0);
+                    if (!mbar_wait(bar(NBar::done + st.idx), st.phase ^ 1u, s_abort, p.err,
+                                   ROLE_PRODUCER, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t stage = sB + st.idx * b_stage_bytes;
+                    mbar_arrive_expect_tx(bar(NBar::b_full + st.idx),
+                                          static_cast<uint32_t>(ng * 2 * nbox * kBoxRows * 128));
+                    for (int j = 0; j < ng; ++j)
+                        for (int a = 0; a < 2; ++a)
+                            for (int i = 0; i < nbox; ++i)
+                                tma_load_2d(stage + (2 * j + a) * b_atom_bytes + i * kBoxRows * 128,
+                                            &tmap_x, (g0 + j) * kGroupK + a * 64,
+                                            ti.m0 + i * kBoxRows, bar(NBar::b_full + st.idx));
+                    st.advance(kNarrowSlots);
+                    ++issued;
+                }
+            }
+            if (!ok) drain_ring(bar(NBar::b_full), issued, kNarrowSlots);
+        } else if (warp == 3 && lane == 0) {
+            // --------------------------------------------------- admission
+            Ring st;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                for (int g0 = 0; g0 < G; g0 += 2) {
+                    if (!mbar_wait(bar(NBar::b_full + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
+                                   2) ||
+                        !mbar_wait(bar(NBar::p_empty + st.idx), st.phase ^ 1u, s_abort, p.err,
+                                   ROLE_MMA, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(bar(NBar::ready + st.idx));
+                    st.advance(kNarrowSlots);
+                }
+            }
+        }
+    } else if (wg == 1) {
+        // --------------------------------------- weight converter (A -> TMEM)
+        setmaxnreg_dec<kOtherRegs>();
+        const int row = threadIdx.x - 128;
+        const int q = warp & 3;
+        Ring a, st;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for (int g0 = 0; g0 < G; g0 += 2) {
+                const int ng = min(2, G - g0);
+                if (!mbar_wait(bar(NBar::a_full + a.idx), a.phase, s_abort, p.err, ROLE_CONVERT,
+                               1) ||
+                    !mbar_wait(bar(NBar::done + st.idx), st.phase ^ 1u, s_abort, p.err,
+                               ROLE_CONVERT, 2)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int j = 0; j < ng; ++j) {
+                    const uint8_t *rowp =
+                        smem + kOffStages + a.idx * kNarrowAStageBytes + j * kAStageBytes + row * 128;
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                           kTmemA0 + st.idx * 128u + j * 64u;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        uint32_t r16[16];
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int c = 2 * jj + cc;
+                            const uint4 v =
+                                *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
+                            i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
+                            i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
+                            i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
+                            i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
+                        }
+                        tmem_st_16cols(taddr + jj * 16, r16);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(NBar::a_empty + a.idx));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(NBar::ready + st.idx));
+                a.advance(SA);
+                st.advance(kNarrowSlots);
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        setmaxnreg_inc<kEpiRegs>();
+        const int ewg = wg - 2;                // owns token columns [32 ewg, 32 ewg + 32)
+        const int q = warp & 3;
+        const int lrow = q * 32 + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+        Ring st;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+            const int n_eff = (ti.rows + 15) & ~15;
+            const bool owned = 32 * ewg < n_eff;   // warp-uniform
+            const int n_local = ti.n0 + lrow;
+            const bool n_ok = n_local < p.N;
+            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            // Scales of this row a quad of groups (two steps) ahead; loads are
+            // issued in place and only read after the next quad boundary.
+            auto load_quad = [&](int g) -> float4 {
+                float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (!n_ok || !owned) return v;
+                if (vec_sw) {
+                    if (g < G) v = ldg_nc_f32x4_now(swp + g);
+                } else {
+                    if (g < G) v.x = ldg_nc_f32_now(swp + g);
+                    if (g + 1 < G) v.y = ldg_nc_f32_now(swp + g + 1);
+                    if (g + 2 < G) v.z = ldg_nc_f32_now(swp + g + 2);
+                    if (g + 3 < G) v.w = ldg_nc_f32_now(swp + g + 3);
+                }
+                return v;
+            };
+            float4 cur = load_quad(0);
+            float4 nxt = load_quad(4);
+            for (int g0 = 0; ok && g0 < G; g0 += 2) {
+                const int ng = min(2, G - g0);
+                if ((g0 & 3) == 0 && g0 > 0) {
+                    cur = nxt;
+                    nxt = load_quad(g0 + 4);
+                }
+                const float s0 = (g0 & 3) == 0 ? cur.x : cur.z;
+                const float s1 = (g0 & 3) == 0 ? cur.y : cur.w;
+                if (!mbar_wait(bar(NBar::done + st.idx), st.phase, s_abort, p.err, ROLE_EPILOGUE,
+                               1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (owned) {
+                    const uint32_t c0 = lane_base + pbuf_col(st.idx, 0) + 32u * ewg;
+                    const uint32_t c1 = lane_base + pbuf_col(st.idx, 1) + 32u * ewg;
+                    uint32_t v0[32], v1[32];
+                    if (ng == 2) {
+                        tmem_ld_2x32cols_sync(c0, c1, v0, v1);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[j] = fmaf(__uint_as_float(v1[j]), s1,
+                                          fmaf(__uint_as_float(v0[j]), s0, acc[j]));
+                    } else {
+                        tmem_ld_32cols_sync(c0, v0);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(v0[j]), s0, acc[j]);
+                    }
+                    if (kDebug && n_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = 32 * ewg + j;
+                            if (col < ti.rows) {
+                                const size_t o =
+                                    (static_cast<size_t>(ti.m0 + col) * p.N + n_local) * G + g0;
+                                p.dbg[o] = __float2int_rn(__uint_as_float(v0[j]));
+                                if (ng == 2) p.dbg[o + 1] = __float2int_rn(__uint_as_float(v1[j]));
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + st.idx));
+                st.advance(kNarrowSlots);
+            }
+            if (!ok) break;
+            if (owned && n_ok) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int col = 32 * ewg + j;
+                    if (col < ti.rows) {
+                        const int m = ti.m0 + col;
+                        const float out = acc[j] * __ldg(p.sa + m);
+                        const size_t idx = static_cast<size_t>(m) * p.N + n_local;
+                        if (p.out_fp32)
+                            static_cast<float *>(p.y)[idx] = out;
+                        else
+                            static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// Stream-K work split (used by the CUDA-core GEMV below).
 // This CTA's share of the work: the step range [u0, u1) of the stream-K part
 // (steps of tiles [dp, total), S per tile, numbered from 0 at tile dp, split
 // over g_sk CTAs), then round-robin whole tiles of [0, dp).
@@ -716,476 +1027,6 @@ __device__ __forceinline__ void for_each_piece(const WorkPlan &w, F &&f) {
         if (!f(t, 0, w.S)) return;
 }
 
-template <bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1)
-w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    uint8_t *smem = smem_raw + (base - raw_addr);
-
-    const uint32_t SA = static_cast<uint32_t>(p.a_stages);
-    const uint32_t NB = static_cast<uint32_t>(p.b_stages);
-    const int b_rows = p.b_rows;                          // 32 or 64
-    const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
-    const uint32_t b_stage_bytes = 4u * b_atom_bytes;     // 2 groups x 2 atoms
-    const uint32_t sA = base + kNarrowOffStages;
-    const uint32_t sB = sA + SA * kNarrowAStageBytes;
-    const uint32_t sBar = base + kOffBar;
-    volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
-    volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
-    volatile int *s_last = reinterpret_cast<volatile int *>(smem + kOffMisc + 12);
-    int *s_base = reinterpret_cast<int *>(smem + p.tab_off);
-    int *s_lo = s_base + (p.E + 1);
-    int *s_cnt = s_lo + (p.E + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int tt = p.tile_tokens;                         // == b_rows
-    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kMaxAStages; ++i) {
-            mbar_init(bar(NBar::a_full + i), 1);
-            mbar_init(bar(NBar::a_empty + i), 4);
-        }
-        for (int i = 0; i < kNarrowMaxASlots; ++i) {
-            mbar_init(bar(NBar::ready + i), 5);
-            mbar_init(bar(NBar::a_free + i), 1);
-        }
-        for (int i = 0; i < kNarrowSlots; ++i) {
-            mbar_init(bar(NBar::done + i), 1);
-            mbar_init(bar(NBar::p_empty + i), 8);
-        }
-        for (int i = 0; i < kMaxBStages; ++i) {
-            mbar_init(bar(NBar::b_full + i), 1);
-            mbar_init(bar(NBar::b_empty + i), 1);
-        }
-        mbar_init(bar(NBar::drain), 1);
-        *s_abort = 0;
-        fence_mbarrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmap_w);
-        tma_prefetch_desc(&tmap_x);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == 2) build_tile_table(p, tt, lane, s_base, s_lo, s_cnt, s_total);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    const uint32_t tmem_base = *s_tmem_base;
-    const int total = *s_total;
-    const int G = p.G;
-    const int wg = warp >> 2;
-    const WorkPlan plan = make_plan(total, G, p.sk_cnt != nullptr);
-    // TMEM: partial buffer of (slot s, group j) at column (2 s + j) * b_rows;
-    // fp16 A operand of (operand slot s, group j) at column a_col0 + 128 s +
-    // 64 j, the operand slots filling the columns above the partial buffers.
-    const uint32_t NSA = static_cast<uint32_t>(p.a_slots);
-    const uint32_t a_col0 = kTmemCols - 128u * NSA;
-    auto pbuf_col = [&](uint32_t s, int j) -> uint32_t {
-        return (2u * s + static_cast<uint32_t>(j)) * static_cast<uint32_t>(b_rows);
-    };
-
-    if (warp < 4) {
-        setmaxnreg_dec<kNarrowOtherRegs>();
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------- weight TMA producer
-            Ring a;
-            uint32_t issued = 0;
-            bool ok = true;
-            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int wrow = ti.e * p.N + ti.n0;
-                for (int st = s0; st < s1; ++st) {
-                    const int g0 = 2 * st;
-                    const int ng = min(2, G - g0);
-                    if (!mbar_wait(bar(NBar::a_empty + a.idx), a.phase ^ 1u, s_abort, p.err,
-                                   ROLE_PRODUCER, 1)) {
-                        ok = false;
-                        return false;
-                    }
-                    mbar_arrive_expect_tx(bar(NBar::a_full + a.idx), ng * kAStageBytes);
-                    for (int j = 0; j < ng; ++j)
-                        tma_load_2d(sA + a.idx * kNarrowAStageBytes + j * kAStageBytes, &tmap_w,
-                                    (g0 + j) * kGroupK, wrow, bar(NBar::a_full + a.idx));
-                    a.advance(SA);
-                    ++issued;
-                }
-                return true;
-            });
-            if (!ok) drain_ring(bar(NBar::a_full), issued, SA);
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------- MMA issuer
-            Ring ts, pr, bs;
-            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(n_eff));
-                for (int sg = s0; sg < s1; ++sg) {
-                    const int ng = min(2, G - 2 * sg);
-                    if (!mbar_wait_spin(bar(NBar::ready + ts.idx), ts.phase, s_abort, p.err,
-                                        ROLE_MMA, 1))
-                        return false;
-                    tc_fence_after();
-                    for (int j = 0; j < ng; ++j) {
-                        const uint32_t d_tmem = tmem_base + pbuf_col(pr.idx, j);
-                        const uint32_t a_tmem = tmem_base + a_col0 + ts.idx * 128u + j * 64u;
-                        const uint64_t bdesc0 = smem_desc_sw128(sB + bs.idx * b_stage_bytes +
-                                                                j * 2u * b_atom_bytes);
-                        const uint64_t atom_step = b_atom_bytes >> 4;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t bdesc =
-                                bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
-                            mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(bar(NBar::done + pr.idx));
-                    mma_commit(bar(NBar::a_free + ts.idx));
-                    ts.advance(NSA);
-                    pr.advance(kNarrowSlots);
-                    bs.advance(NB);
-                }
-                return true;
-            });
-            mma_commit(bar(NBar::drain));
-            drain_wait(bar(NBar::drain), 0);
-        } else if (warp == 2 && lane == 0) {
-            // -------------------------------------------- token TMA producer
-            griddep_wait();   // the fp16 token codes come from the kernel launched before
-            Ring bs;
-            uint32_t issued = 0;
-            bool ok = true;
-            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const int nbox = (n_eff + kBoxRows - 1) / kBoxRows;
-                for (int sg = s0; sg < s1; ++sg) {
-                    const int g0 = 2 * sg;
-                    const int ng = min(2, G - g0);
-                    if (!mbar_wait(bar(NBar::b_empty + bs.idx), bs.phase ^ 1u, s_abort, p.err,
-                                   ROLE_PRODUCER, 2)) {
-                        ok = false;
-                        return false;
-                    }
-                    const uint32_t stage = sB + bs.idx * b_stage_bytes;
-                    mbar_arrive_expect_tx(bar(NBar::b_full + bs.idx),
-                                          static_cast<uint32_t>(ng * 2 * nbox * kBoxRows * 128));
-                    for (int j = 0; j < ng; ++j)
-                        for (int a = 0; a < 2; ++a)
-                            for (int i = 0; i < nbox; ++i)
-                                tma_load_2d(stage + (2 * j + a) * b_atom_bytes + i * kBoxRows * 128,
-                                            &tmap_x, (g0 + j) * kGroupK + a * 64,
-                                            ti.m0 + i * kBoxRows, bar(NBar::b_full + bs.idx));
-                    bs.advance(NB);
-                    ++issued;
-                }
-                return true;
-            });
-            if (!ok) drain_ring(bar(NBar::b_full), issued, NB);
-        } else if (warp == 3 && lane == 0) {
-            // --------------------------------------------------- admission
-            Ring ts, pr, bs;
-            for_each_piece(plan, [&](int, int s0, int s1) -> bool {
-                for (int sg = s0; sg < s1; ++sg) {
-                    if (!mbar_wait(bar(NBar::b_full + bs.idx), bs.phase, s_abort, p.err, ROLE_MMA,
-                                   2) ||
-                        !mbar_wait(bar(NBar::p_empty + pr.idx), pr.phase ^ 1u, s_abort, p.err,
-                                   ROLE_MMA, 3))
-                        return false;
-                    mbar_arrive(bar(NBar::ready + ts.idx));
-                    ts.advance(NSA);
-                    pr.advance(kNarrowSlots);
-                    bs.advance(NB);
-                }
-                return true;
-            });
-        }
-    } else if (wg == 1) {
-        // --------------------------------------- weight converter (A -> TMEM)
-        setmaxnreg_dec<kNarrowOtherRegs>();
-        const int row = threadIdx.x - 128;
-        const int q = warp & 3;
-        Ring a, ts;
-        for_each_piece(plan, [&](int, int s0, int s1) -> bool {
-            for (int sg = s0; sg < s1; ++sg) {
-                const int ng = min(2, G - 2 * sg);
-                if (!mbar_wait(bar(NBar::a_full + a.idx), a.phase, s_abort, p.err, ROLE_CONVERT,
-                               1) ||
-                    !mbar_wait(bar(NBar::a_free + ts.idx), ts.phase ^ 1u, s_abort, p.err,
-                               ROLE_CONVERT, 2))
-                    return false;
-                tc_fence_after();
-                for (int j = 0; j < ng; ++j) {
-                    const uint8_t *rowp = smem + kNarrowOffStages + a.idx * kNarrowAStageBytes +
-                                          j * kAStageBytes + row * 128;
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                           a_col0 + ts.idx * 128u + j * 64u;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        uint32_t r16[16];
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            const int c = 2 * jj + cc;
-                            const uint4 v =
-                                *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
-                            i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
-                            i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
-                            i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
-                            i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
-                        }
-                        tmem_st_16cols(taddr + jj * 16, r16);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(NBar::a_empty + a.idx));
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(NBar::ready + ts.idx));
-                a.advance(SA);
-                ts.advance(NSA);
-            }
-            return true;
-        });
-    } else {
-        // -------------------------------------------------------- epilogue
-        setmaxnreg_inc<kNarrowEpiRegs>();
-        const int ewg = wg - 2;                // owns token columns [32 ewg, 32 ewg + 32)
-        const int q = warp & 3;
-        const int lrow = q * 32 + lane;
-        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
-        const int c_self = static_cast<int>(blockIdx.x);
-        float acc[32];
-        Ring st, bs;   // partial slots; token stages handed back
-        // Stream-K bookkeeping of split tiles: the CTAs c_first..c_final
-        // holding a tile's pieces in K order, and the partial slot a CTA's
-        // piece goes to (the first CTA's piece ends its range: slot 1; every
-        // other piece starts its CTA's range: slot 0).
-        auto sk_range = [&](int t, int &c_first, int &c_final) {
-            const long long x0 = static_cast<long long>(t - plan.dp) * plan.S;
-            c_first = sk_owner(x0, plan);
-            c_final = sk_owner(x0 + plan.S - 1, plan);
-        };
-        auto sk_slot = [&](int t, int c) -> float * {
-            int c_first, c_final;
-            sk_range(t, c_first, c_final);
-            const int slot = (c == c_first) ? 1 : 0;
-            return p.sk_part + static_cast<size_t>(2 * c + slot) * p.sk_ld * kTileN;
-        };
-        int split_t0 = 0, split_t1 = 0;   // this CTA's split tiles (at most 2)
-        int n_split = 0;
-        // After a failed wait the warp keeps walking the same piece list with
-        // no waits and no data work, so that all eight epilogue warps take
-        // the same named barriers at the end (a named barrier has no time
-        // limit).
-        bool failed = false;
-        for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-            const int n_eff = (ti.rows + 15) & ~15;
-            const bool owned = 32 * ewg < n_eff;   // warp-uniform
-            const int n_local = ti.n0 + lrow;
-            const bool n_ok = n_local < p.N;
-            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
-            float sa_r[32];
-            if constexpr (!kDebug) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    sa_r[j] = __ldg(p.sa + ti.m0 + min(32 * ewg + j, ti.rows - 1));
-            }
-            // Scales of this row a quad of groups (two steps) ahead; loads are
-            // issued in place and only read after the next quad boundary.
-            auto load_quad = [&](int g) -> float4 {
-                float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (!n_ok || !owned || failed) return v;
-                if (vec_sw) {
-                    if (g < G) v = ldg_nc_f32x4_now(swp + g);
-                } else {
-                    if (g < G) v.x = ldg_nc_f32_now(swp + g);
-                    if (g + 1 < G) v.y = ldg_nc_f32_now(swp + g + 1);
-                    if (g + 2 < G) v.z = ldg_nc_f32_now(swp + g + 2);
-                    if (g + 3 < G) v.w = ldg_nc_f32_now(swp + g + 3);
-                }
-                return v;
-            };
-            const int qb = (2 * s0) & ~3;
-            float4 cur = load_quad(qb);
-            float4 nxt = load_quad(qb + 4);
-            for (int sg = s0; sg < s1; ++sg) {
-                const int g0 = 2 * sg;
-                const int ng = min(2, G - g0);
-                if ((g0 & 3) == 0 && g0 > qb) {
-                    cur = nxt;
-                    nxt = load_quad(g0 + 4);
-                }
-                const float sc0 = (g0 & 3) == 0 ? cur.x : cur.z;
-                const float sc1 = (g0 & 3) == 0 ? cur.y : cur.w;
-                if (!failed) {
-                    const bool waited = *s_abort == 0 &&
-                                        mbar_wait(bar(NBar::done + st.idx), st.phase, s_abort,
-                                                  p.err, ROLE_EPILOGUE, 1);
-                    failed = __any_sync(0xFFFFFFFFu, !waited);
-                }
-                if (failed) continue;
-                tc_fence_after();
-                // The step's MMAs are complete: its token stage is free.
-                if (threadIdx.x == 256) mbar_arrive(bar(NBar::b_empty + bs.idx));
-                bs.advance(NB);
-                if (owned) {
-                    const uint32_t c0 = lane_base + pbuf_col(st.idx, 0) + 32u * ewg;
-                    const uint32_t c1 = lane_base + pbuf_col(st.idx, 1) + 32u * ewg;
-                    uint32_t v0[32], v1[32];
-                    if (ng == 2) {
-                        tmem_ld_2x32cols_sync(c0, c1, v0, v1);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[j] = fmaf(__uint_as_float(v1[j]), sc1,
-                                          fmaf(__uint_as_float(v0[j]), sc0, acc[j]));
-                    } else {
-                        tmem_ld_32cols_sync(c0, v0);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(v0[j]), sc0, acc[j]);
-                    }
-                    if (kDebug && n_ok) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int col = 32 * ewg + j;
-                            if (col < ti.rows) {
-                                const size_t o =
-                                    (static_cast<size_t>(ti.m0 + col) * p.N + n_local) * G + g0;
-                                p.dbg[o] = __float2int_rn(__uint_as_float(v0[j]));
-                                if (ng == 2) p.dbg[o + 1] = __float2int_rn(__uint_as_float(v1[j]));
-                            }
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + st.idx));
-                st.advance(kNarrowSlots);
-            }
-            const bool write = owned && n_ok && !failed;
-            // sa_r: token scales of the chunk's columns (columns past the
-            // tile's rows repeat its last row; they are never stored), loaded
-            // when the piece starts so the final stores do not wait for them;
-            // read at the store in the debug build, which needs the registers.
-            auto store_y = [&](const float (&v)[32]) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int col = 32 * ewg + j;
-                    if (col < ti.rows) {
-                        const int m = ti.m0 + col;
-                        const float out = v[j] * (kDebug ? __ldg(p.sa + m) : sa_r[j]);
-                        const size_t idx = static_cast<size_t>(m) * p.N + n_local;
-                        if (p.out_fp32)
-                            static_cast<float *>(p.y)[idx] = out;
-                        else
-                            static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
-                    }
-                }
-            };
-            if (s0 == 0 && s1 == plan.S) {
-                if (write) store_y(acc);
-                return true;
-            }
-            // Split tile: store this piece's partial now with plain stores;
-            // publishing it (fence, arrival count) and the combine wait for
-            // the CTA's last step, so no fence stalls the pipeline.
-            if (write) {
-                float *dst = sk_slot(t, c_self);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int col = 32 * ewg + j;
-                    if (col < ti.rows) __stcg(dst + col * kTileN + lrow, acc[j]);
-                }
-            }
-            if (n_split == 0) split_t0 = t; else split_t1 = t;
-            n_split = min(n_split + 1, 2);
-            return true;
-        });
-
-        // Publish this CTA's split pieces, count them in, and finish the
-        // tiles whose last piece this CTA delivered: add the pieces in K
-        // order, apply sa and store y.
-        if (n_split > 0) {   // the same for all epilogue warps
-            __threadfence();
-            named_barrier_sync(1, 256);
-            if (threadIdx.x == 256) {
-                int flags = 0;
-                for (int r = 0; r < n_split; ++r) {
-                    const int t = r == 0 ? split_t0 : split_t1;
-                    int c_first, c_final;
-                    sk_range(t, c_first, c_final);
-                    const int arrived = atomicAdd(p.sk_cnt + (t - plan.dp), 1);
-                    if (arrived == c_final - c_first) flags |= 1 << r;
-                }
-                __threadfence();
-                *s_last = flags;
-            }
-            named_barrier_sync(1, 256);
-            const int flags = *s_last;
-            for (int r = 0; r < n_split; ++r) {
-                if (((flags >> r) & 1) == 0 || failed) continue;
-                const int t = r == 0 ? split_t0 : split_t1;
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const int n_local = ti.n0 + lrow;
-                if (32 * ewg >= n_eff || n_local >= p.N) continue;
-                int c_first, c_final;
-                sk_range(t, c_first, c_final);
-                float sum[32], sa_f[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    sum[j] = 0.0f;
-                    sa_f[j] = __ldg(p.sa + ti.m0 + min(32 * ewg + j, ti.rows - 1));
-                }
-                for (int c = c_first; c <= c_final; ++c) {
-                    // Columns past the tile's rows re-read its last column.
-                    const float *src = sk_slot(t, c) + lrow;
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __ldcg(src + min(32 * ewg + j, ti.rows - 1) * kTileN);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) sum[j] += v[j];
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int col = 32 * ewg + j;
-                    if (col < ti.rows) {
-                        const int m = ti.m0 + col;
-                        const float out = sum[j] * sa_f[j];
-                        const size_t idx = static_cast<size_t>(m) * p.N + n_local;
-                        if (p.out_fp32)
-                            static_cast<float *>(p.y)[idx] = out;
-                        else
-                            static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
-                    }
-                }
-            }
-        }
-    }
-
-    __syncwarp();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
-    }
-}
-
 // =============================================================================
 // Decode-sized dense problems (at most 8 token rows): a batched GEMV on the
 // CUDA cores. With at most 8 multiply-adds per weight byte, the exact int8
@@ -1215,7 +1056,10 @@ struct GBar {
 static_assert(GBar::count <= 128, "barrier area");
 static_assert(gemv_stage_bytes(kGemvMaxTokens) % 1024 == 0, "stage alignment");
 
-template <bool kDebug, int MR>
+// Register blocking: a compute thread covers RR weight rows x RM token rows
+// of one group, so a step's loads from shared memory are amortised over
+// RR * RM dot products per word (MR = RR * RM token rows per tile).
+template <bool kDebug, int RR, int RM>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_q, const KParams p) {
@@ -1223,6 +1067,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw_addr);
+    constexpr int MR = RR * RM;
     constexpr uint32_t kStage = static_cast<uint32_t>(gemv_stage_bytes(MR));
     const uint32_t SA = static_cast<uint32_t>(p.a_stages);
     const uint32_t sA = base + kGemvOffStages;
@@ -1293,8 +1138,15 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
     } else {
         // ------------------------------------------------- compute warps
+        // Thread (row block rb, token block tb, group j): rows rb + i*128/RR,
+        // token rows tb*RM + u. The 8 lanes of a shared-memory phase read 8
+        // consecutive rows (conflict-free under the 128-byte swizzle); all
+        // lanes of a half-warp read the same token words (broadcast).
         const int ct = threadIdx.x - 32;
-        const int r = (ct >> 5) * 16 + (lane & 15);   // weight row of the tile
+        const int cw = ct >> 5;
+        constexpr int kWarpsPerTb = 8 / RR;
+        const int tb = cw / kWarpsPerTb;
+        const int rb = (cw % kWarpsPerTb) * 16 + (lane & 15);
         const int j = lane >> 4;                      // group of the step
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
         const int c_self = static_cast<int>(blockIdx.x);
@@ -1315,39 +1167,50 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
         // time limit).
         bool failed = false;
         Ring a;
-        float acc[MR];
+        float acc[RR][RM];
         for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
             const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-            const int n_local = ti.n0 + r;
-            const bool n_ok = n_local < p.N;
-            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            int n_row[RR];
+            bool n_ok[RR];
+            const float *swp[RR];
 #pragma unroll
-            for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
-            auto load_quad = [&](int g) -> float4 {
+            for (int i = 0; i < RR; ++i) {
+                n_row[i] = ti.n0 + rb + i * (128 / RR);
+                n_ok[i] = n_row[i] < p.N;
+                swp[i] = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok[i] ? n_row[i] : 0)) * G;
+#pragma unroll
+                for (int u = 0; u < RM; ++u) acc[i][u] = 0.0f;
+            }
+            auto load_quad = [&](int i, int g) -> float4 {
                 float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (!n_ok || failed) return v;
+                if (!n_ok[i] || failed) return v;
                 if (vec_sw) {
-                    if (g < G) v = ldg_nc_f32x4_now(swp + g);
+                    if (g < G) v = ldg_nc_f32x4_now(swp[i] + g);
                 } else {
-                    if (g < G) v.x = ldg_nc_f32_now(swp + g);
-                    if (g + 1 < G) v.y = ldg_nc_f32_now(swp + g + 1);
-                    if (g + 2 < G) v.z = ldg_nc_f32_now(swp + g + 2);
-                    if (g + 3 < G) v.w = ldg_nc_f32_now(swp + g + 3);
+                    if (g < G) v.x = ldg_nc_f32_now(swp[i] + g);
+                    if (g + 1 < G) v.y = ldg_nc_f32_now(swp[i] + g + 1);
+                    if (g + 2 < G) v.z = ldg_nc_f32_now(swp[i] + g + 2);
+                    if (g + 3 < G) v.w = ldg_nc_f32_now(swp[i] + g + 3);
                 }
                 return v;
             };
             const int qb = (2 * s0) & ~3;
-            float4 cur = load_quad(qb);
-            float4 nxt = load_quad(qb + 4);
+            float4 cur[RR], nxt[RR];
+#pragma unroll
+            for (int i = 0; i < RR; ++i) {
+                cur[i] = load_quad(i, qb);
+                nxt[i] = load_quad(i, qb + 4);
+            }
             for (int sg = s0; sg < s1; ++sg) {
                 const int g0 = 2 * sg;
                 const int ng = min(2, G - g0);
                 if ((g0 & 3) == 0 && g0 > qb) {
-                    cur = nxt;
-                    nxt = load_quad(g0 + 4);
+#pragma unroll
+                    for (int i = 0; i < RR; ++i) {
+                        cur[i] = nxt[i];
+                        nxt[i] = load_quad(i, g0 + 4);
+                    }
                 }
-                const float sc0 = (g0 & 3) == 0 ? cur.x : cur.z;
-                const float sc1 = (g0 & 3) == 0 ? cur.y : cur.w;
                 if (!failed) {
                     const bool waited = *s_abort == 0 &&
                                         mbar_wait_spin(bar(GBar::full + a.idx), a.phase, s_abort,
@@ -1355,58 +1218,82 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     failed = __any_sync(0xFFFFFFFFu, !waited);
                 }
                 if (failed) continue;
-                int P[MR];
+                int P[RR][RM];
 #pragma unroll
-                for (int m = 0; m < MR; ++m) P[m] = 0;
+                for (int i = 0; i < RR; ++i)
+#pragma unroll
+                    for (int u = 0; u < RM; ++u) P[i][u] = 0;
                 if (j < ng) {
                     const uint8_t *stage = smem + kGemvOffStages + a.idx * kStage;
-                    const uint8_t *wrow = stage + j * kAStageBytes + r * 128;
-                    const uint8_t *tok = stage + 2 * kAStageBytes + j * MR * 128;
+                    const uint8_t *wg = stage + j * kAStageBytes;
+                    const uint8_t *tok = stage + 2 * kAStageBytes + (j * MR + tb * RM) * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + ((c ^ (r & 7)) << 4));
+                        uint4 wv[RR], tv[RM];
 #pragma unroll
-                        for (int m = 0; m < MR; ++m) {
-                            const uint4 tv = *reinterpret_cast<const uint4 *>(tok + m * 128 + c * 16);
-                            P[m] = __dp4a(static_cast<int>(wv.x), static_cast<int>(tv.x), P[m]);
-                            P[m] = __dp4a(static_cast<int>(wv.y), static_cast<int>(tv.y), P[m]);
-                            P[m] = __dp4a(static_cast<int>(wv.z), static_cast<int>(tv.z), P[m]);
-                            P[m] = __dp4a(static_cast<int>(wv.w), static_cast<int>(tv.w), P[m]);
+                        for (int i = 0; i < RR; ++i) {
+                            const int r = rb + i * (128 / RR);
+                            wv[i] = *reinterpret_cast<const uint4 *>(wg + r * 128 + ((c ^ (r & 7)) << 4));
                         }
+#pragma unroll
+                        for (int u = 0; u < RM; ++u)
+                            tv[u] = *reinterpret_cast<const uint4 *>(tok + u * 128 + c * 16);
+#pragma unroll
+                        for (int i = 0; i < RR; ++i)
+#pragma unroll
+                            for (int u = 0; u < RM; ++u) {
+                                P[i][u] = __dp4a(static_cast<int>(wv[i].x), static_cast<int>(tv[u].x), P[i][u]);
+                                P[i][u] = __dp4a(static_cast<int>(wv[i].y), static_cast<int>(tv[u].y), P[i][u]);
+                                P[i][u] = __dp4a(static_cast<int>(wv[i].z), static_cast<int>(tv[u].z), P[i][u]);
+                                P[i][u] = __dp4a(static_cast<int>(wv[i].w), static_cast<int>(tv[u].w), P[i][u]);
+                            }
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(GBar::empty + a.idx));
                 a.advance(SA);
 #pragma unroll
-                for (int m = 0; m < MR; ++m) {
-                    const int other = __shfl_xor_sync(0xFFFFFFFFu, P[m], 16);
-                    const int p0 = j ? other : P[m];
-                    const int p1 = j ? P[m] : other;
-                    acc[m] = fmaf(static_cast<float>(p0), sc0, acc[m]);
-                    if (ng == 2) acc[m] = fmaf(static_cast<float>(p1), sc1, acc[m]);
-                }
-                if (kDebug && n_ok && j < ng) {
+                for (int i = 0; i < RR; ++i) {
+                    const float sc0 = (g0 & 3) == 0 ? cur[i].x : cur[i].z;
+                    const float sc1 = (g0 & 3) == 0 ? cur[i].y : cur[i].w;
 #pragma unroll
-                    for (int m = 0; m < MR; ++m)
-                        if (m < ti.rows)
-                            p.dbg[(static_cast<size_t>(ti.m0 + m) * p.N + n_local) * G + g0 + j] = P[m];
+                    for (int u = 0; u < RM; ++u) {
+                        const int other = __shfl_xor_sync(0xFFFFFFFFu, P[i][u], 16);
+                        const int p0 = j ? other : P[i][u];
+                        const int p1 = j ? P[i][u] : other;
+                        acc[i][u] = fmaf(static_cast<float>(p0), sc0, acc[i][u]);
+                        if (ng == 2) acc[i][u] = fmaf(static_cast<float>(p1), sc1, acc[i][u]);
+                    }
+                }
+                if (kDebug && j < ng) {
+#pragma unroll
+                    for (int i = 0; i < RR; ++i)
+#pragma unroll
+                        for (int u = 0; u < RM; ++u) {
+                            const int m = tb * RM + u;
+                            if (n_ok[i] && m < ti.rows)
+                                p.dbg[(static_cast<size_t>(ti.m0 + m) * p.N + n_row[i]) * G + g0 + j] =
+                                    P[i][u];
+                        }
                 }
             }
-            const bool write = j == 0 && n_ok && !failed;
+            auto store_out = [&](int i, int u, float v) {
+                const int m = tb * RM + u;
+                const float out = v * __ldg(p.sa + ti.m0 + m);
+                const size_t idx = static_cast<size_t>(ti.m0 + m) * p.N + n_row[i];
+                if (p.out_fp32)
+                    static_cast<float *>(p.y)[idx] = out;
+                else
+                    static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+            };
+            const bool write = j == 0 && !failed;
             if (s0 == 0 && s1 == plan.S) {
                 if (write) {
 #pragma unroll
-                    for (int m = 0; m < MR; ++m) {
-                        if (m < ti.rows) {
-                            const float out = acc[m] * __ldg(p.sa + ti.m0 + m);
-                            const size_t idx = static_cast<size_t>(ti.m0 + m) * p.N + n_local;
-                            if (p.out_fp32)
-                                static_cast<float *>(p.y)[idx] = out;
-                            else
-                                static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
-                        }
-                    }
+                    for (int i = 0; i < RR; ++i)
+#pragma unroll
+                        for (int u = 0; u < RM; ++u)
+                            if (n_ok[i] && tb * RM + u < ti.rows) store_out(i, u, acc[i][u]);
                 }
                 return true;
             }
@@ -1415,8 +1302,13 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
             if (write) {
                 float *dst = sk_slot(t, c_self);
 #pragma unroll
-                for (int m = 0; m < MR; ++m)
-                    if (m < ti.rows) __stcg(dst + m * kTileN + r, acc[m]);
+                for (int i = 0; i < RR; ++i)
+#pragma unroll
+                    for (int u = 0; u < RM; ++u) {
+                        const int m = tb * RM + u;
+                        if (n_ok[i] && m < ti.rows)
+                            __stcg(dst + m * kTileN + rb + i * (128 / RR), acc[i][u]);
+                    }
             }
             if (n_split == 0) split_t0 = t; else split_t1 = t;
             n_split = min(n_split + 1, 2);
@@ -1444,30 +1336,36 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 if (((flags >> q) & 1) == 0 || failed || j != 0) continue;
                 const int t = q == 0 ? split_t0 : split_t1;
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int n_local = ti.n0 + r;
-                if (n_local >= p.N) continue;
                 int c_first, c_final;
                 sk_range(t, c_first, c_final);
-                float sum[MR];
 #pragma unroll
-                for (int m = 0; m < MR; ++m) sum[m] = 0.0f;
-                for (int c = c_first; c <= c_final; ++c) {
-                    const float *src = sk_slot(t, c) + r;
-                    float v[MR];
+                for (int i = 0; i < RR; ++i) {
+                    const int r = rb + i * (128 / RR);
+                    const int n_local = ti.n0 + r;
+                    if (n_local >= p.N) continue;
+                    float sum[RM];
 #pragma unroll
-                    for (int m = 0; m < MR; ++m) v[m] = __ldcg(src + min(m, ti.rows - 1) * kTileN);
+                    for (int u = 0; u < RM; ++u) sum[u] = 0.0f;
+                    for (int c = c_first; c <= c_final; ++c) {
+                        const float *src = sk_slot(t, c) + r;
+                        float v[RM];
 #pragma unroll
-                    for (int m = 0; m < MR; ++m) sum[m] += v[m];
-                }
+                        for (int u = 0; u < RM; ++u)
+                            v[u] = __ldcg(src + min(tb * RM + u, ti.rows - 1) * kTileN);
 #pragma unroll
-                for (int m = 0; m < MR; ++m) {
-                    if (m < ti.rows) {
-                        const float out = sum[m] * __ldg(p.sa + ti.m0 + m);
-                        const size_t idx = static_cast<size_t>(ti.m0 + m) * p.N + n_local;
-                        if (p.out_fp32)
-                            static_cast<float *>(p.y)[idx] = out;
-                        else
-                            static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                        for (int u = 0; u < RM; ++u) sum[u] += v[u];
+                    }
+#pragma unroll
+                    for (int u = 0; u < RM; ++u) {
+                        const int m = tb * RM + u;
+                        if (m < ti.rows) {
+                            const float out = sum[u] * __ldg(p.sa + ti.m0 + m);
+                            const size_t idx = static_cast<size_t>(ti.m0 + m) * p.N + n_local;
+                            if (p.out_fp32)
+                                static_cast<float *>(p.y)[idx] = out;
+                            else
+                                static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                        }
                     }
                 }
             }
@@ -1524,8 +1422,7 @@ bool encode_2d_plain(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_by
 // stage counts, filling shared memory with weight stages after the token stages.
 struct PipeShape {
     int b_rows, tile_tokens, b_stages, a_stages, p_bufs, smem_bytes;
-    int tab_off = kOffTab;
-    int a_slots = 2;
+
     bool narrow;    // one batch of <= 64 rows per tile: w8a8_gemm_narrow_kernel
 };
 
@@ -1543,23 +1440,15 @@ PipeShape choose_pipe(const GemmProblem &pr) {
     }
     s.narrow = s.tile_tokens == s.b_rows && s.b_rows <= 64;
     if (s.narrow) {
-        // Token ring: stages of two K groups each, 4 deep for tiles of <= 32
-        // rows, 3 deep for 64; the tile table (3 ints per expert + 1) after it.
+        // Two step slots, each holding the token tiles of two K groups.
         s.p_bufs = 2 * kNarrowSlots;
-        s.b_stages = s.b_rows <= 32 ? 4 : 3;
-        // TMEM: 2 partial slots of 2 x b_rows columns, then 128-column
-        // operand slots in the rest of the 512 columns.
-        s.a_slots = (kTmemCols - 2 * kNarrowSlots * s.b_rows) / 128;
-        if (s.a_slots > kNarrowMaxASlots) s.a_slots = kNarrowMaxASlots;
-        const int b_stage_bytes = 4 * s.b_rows * 128;
-        const int tab_bytes = static_cast<int>((3 * (pr.E + 1) * 4 + 15) / 16 * 16);
-        const int avail =
-            kSmemLimit - 1024 - kNarrowOffStages - s.b_stages * b_stage_bytes - tab_bytes;
+        s.b_stages = kNarrowSlots;
+        const int b_slot_bytes = 4 * s.b_rows * 128;
+        const int avail = kSmemLimit - 1024 - kOffStages - kNarrowSlots * b_slot_bytes;
         s.a_stages = avail / kNarrowAStageBytes;
         if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
-        s.tab_off = kNarrowOffStages + s.a_stages * kNarrowAStageBytes +
-                    s.b_stages * b_stage_bytes;
-        s.smem_bytes = s.tab_off + tab_bytes + 1024;
+        s.smem_bytes = kOffStages + s.a_stages * kNarrowAStageBytes +
+                       kNarrowSlots * b_slot_bytes + 1024;
         return s;
     }
     s.p_bufs = 256 / s.b_rows;
@@ -1577,8 +1466,6 @@ template <auto kernel>
 cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sms,
                           cudaStream_t stream) {
     if (ps.a_stages < 2 || ps.b_stages > kMaxBStages || ps.b_rows % kBoxRows != 0 ||
-        (ps.narrow && (ps.a_slots < 2 || ps.a_slots > kNarrowMaxASlots ||
-                       2 * kNarrowSlots * ps.b_rows + 128 * ps.a_slots > kTmemCols)) ||
         ps.b_rows > kMaxBatchRows ||
         ps.smem_bytes > kSmemLimit)
         return cudaErrorInvalidConfiguration;
@@ -1623,8 +1510,7 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     kp.b_rows = ps.b_rows;
     kp.tile_tokens = ps.tile_tokens;
     kp.p_bufs = ps.p_bufs;
-    kp.tab_off = ps.tab_off;
-    kp.a_slots = ps.a_slots;
+    kp.tab_off = kOffTab;
     unsigned long long *err = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
     if (e != cudaSuccess) return e;
@@ -1637,16 +1523,9 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     const int64_t tiles_bound = m_tiles_bound * kp.n_tiles;
     const int64_t grid = tiles_bound < num_sms ? tiles_bound : num_sms;
     if (grid <= 0) return cudaSuccess;
-    kp.sk_cnt = nullptr;
+    kp.sk_cnt = nullptr;   // the tensor-core kernels never split a tile's K range
     kp.sk_part = nullptr;
     kp.sk_ld = 0;
-    // A partial slot must hold every token row of a tile.
-    if (ps.narrow && pr.sk_cnt != nullptr && grid <= kSkMaxCtas &&
-        pr.sk_ld >= (pr.offsets != nullptr ? ps.tile_tokens : pr.R)) {
-        kp.sk_cnt = pr.sk_cnt;
-        kp.sk_part = pr.sk_part;
-        kp.sk_ld = pr.sk_ld;
-    }
 
     // Programmatic dependent launch: the kernel may start while the staging
     // kernel before it in the stream is still running; only its token
@@ -1713,7 +1592,11 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     kp.err = err;
     const int64_t grid = kp.n_tiles < num_sms ? kp.n_tiles : num_sms;
-    if (pr.sk_cnt != nullptr && grid <= kSkMaxCtas && pr.sk_ld >= pr.R) {
+    // Split tile K ranges (stream-K) only where the GEMV is bound by its
+    // arithmetic (8-token tiles): when it is bound by the weight stream, the
+    // SMs of a partial last wave stream faster and the split's publish and
+    // combine cost more than they save (measured on GB300).
+    if (MR >= kGemvSplitRows && pr.sk_cnt != nullptr && grid <= kSkMaxCtas && pr.sk_ld >= pr.R) {
         kp.sk_cnt = pr.sk_cnt;
         kp.sk_part = pr.sk_part;
         kp.sk_ld = pr.sk_ld;
@@ -1722,21 +1605,21 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int MR>
+template <int RR, int RM>
 cudaError_t launch_gemv_mr(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     return pr.debug_partials != nullptr
-               ? launch_gemv<w8a8_gemv_kernel<true, MR>, MR>(pr, num_sms, stream)
-               : launch_gemv<w8a8_gemv_kernel<false, MR>, MR>(pr, num_sms, stream);
+               ? launch_gemv<w8a8_gemv_kernel<true, RR, RM>, RR * RM>(pr, num_sms, stream)
+               : launch_gemv<w8a8_gemv_kernel<false, RR, RM>, RR * RM>(pr, num_sms, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     if (uses_gemv(pr.R, pr.offsets != nullptr)) {
-        if (pr.R <= 1) return launch_gemv_mr<1>(pr, num_sms, stream);
-        if (pr.R <= 2) return launch_gemv_mr<2>(pr, num_sms, stream);
-        if (pr.R <= 4) return launch_gemv_mr<4>(pr, num_sms, stream);
-        return launch_gemv_mr<8>(pr, num_sms, stream);
+        if (pr.R <= 1) return launch_gemv_mr<1, 1>(pr, num_sms, stream);
+        if (pr.R <= 2) return launch_gemv_mr<1, 2>(pr, num_sms, stream);
+        if (pr.R <= 4) return launch_gemv_mr<1, 4>(pr, num_sms, stream);
+        return launch_gemv_mr<1, 8>(pr, num_sms, stream);
     }
     const PipeShape ps = choose_pipe(pr);
     const bool dbg = pr.debug_partials != nullptr;

@@ -14,10 +14,9 @@ cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
                                 cudaStream_t stream);
 
-// int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] in `out`;
-// also zeroes `zero[0, n_zero)` (the GEMM's split-tile counters; may be null).
+// int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] in `out`.
 cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
-                               int *zero, int n_zero, int num_sms, cudaStream_t stream);
+                               int num_sms, cudaStream_t stream);
 
 struct GemmProblem {
     const int8_t *qa;         // [R, K] int8 activation codes
@@ -31,7 +30,7 @@ struct GemmProblem {
     int64_t R, E, N, K;
     bool out_fp32;
     int grouped_batch_rows = 64;  // token rows per MMA batch for grouped calls (32..128)
-    // Stream-K split of narrow-tile calls; null sk_cnt: whole tiles only.
+    // Stream-K split of GEMV calls; null sk_cnt: whole tiles only.
     int *sk_cnt = nullptr;        // [2 * kSkMaxCtas] counters, zeroed before the GEMM
     float *sk_part = nullptr;     // [kSkMaxCtas][2][sk_ld][128] FP32 partials
     int sk_ld = 0;
@@ -42,25 +41,20 @@ struct GemmProblem {
 constexpr int kGemvMaxTokens = 8;
 inline bool uses_gemv(int64_t R, bool grouped) { return !grouped && R <= kGemvMaxTokens; }
 
-// Narrow-tile calls (dense M <= 64, every grouped call) can split tiles
-// across CTAs (stream-K) when the workspace holds the split area: arrival
-// counters and two FP32 partial slots per CTA, for at most kSkMaxCtas CTAs.
+// The GEMV splits tiles across CTAs (stream-K) for tiles of 5..8 token rows
+// when the workspace holds the split area: arrival counters and two FP32
+// partial slots per CTA (token rows x 128 weight rows), for at most
+// kSkMaxCtas CTAs.
 constexpr int kSkMaxCtas = 160;
-constexpr int kNarrowMaxRows = 64;
-inline bool uses_narrow_tiles(int64_t R, bool grouped) {
-    return grouped || R <= kNarrowMaxRows;
-}
-// Token columns of one partial slot: every row of a dense call, one tile's
-// rows of a grouped call.
-inline int64_t sk_slot_cols(int64_t R, bool grouped) {
-    return grouped ? kNarrowMaxRows : R;
+constexpr int kGemvSplitRows = 8;   // token rows per tile (rounded up to 1, 2, 4, 8)
+inline bool uses_split(int64_t R, bool grouped) {
+    return uses_gemv(R, grouped) && R > kGemvSplitRows / 2;
 }
 inline size_t sk_counter_bytes() { return 2 * kSkMaxCtas * sizeof(int); }
 inline size_t sk_area_bytes(int64_t R, bool grouped) {
-    if (R <= 0 || !uses_narrow_tiles(R, grouped)) return 0;
+    if (R <= 0 || !uses_split(R, grouped)) return 0;
     return sk_counter_bytes() +
-           static_cast<size_t>(kSkMaxCtas) * 2 * static_cast<size_t>(sk_slot_cols(R, grouped)) *
-               128 * sizeof(float);
+           static_cast<size_t>(kSkMaxCtas) * 2 * static_cast<size_t>(R) * 128 * sizeof(float);
 }
 
 // Maximum number of experts a grouped call may have.

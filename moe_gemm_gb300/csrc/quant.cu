@@ -178,13 +178,10 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float *__restri
 // int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] (dense).
 __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restrict__ q,
                                                           int64_t rows, int K, int64_t ldq,
-                                                          __half *__restrict__ out, int *zero,
-                                                          int n_zero) {
+                                                          __half *__restrict__ out) {
     // The GEMM that consumes this copy is launched as a programmatic
     // dependent: let it start its set-up and weight stream right away.
     griddep_launch_dependents();
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0;
     const int vec_per_row = K >> 4;  // 16 codes per vector
     const int64_t total = rows * vec_per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -234,15 +231,14 @@ cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw
 }
 
 cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
-                               int *zero, int n_zero, int num_sms, cudaStream_t stream) {
+                               int num_sms, cudaStream_t stream) {
     const int64_t total = rows * (K / 16);
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     widen_codes_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        q, rows, static_cast<int>(K), ldq, static_cast<__half *>(out), zero,
-        zero != nullptr ? n_zero : 0);
+        q, rows, static_cast<int>(K), ldq, static_cast<__half *>(out));
     return cudaGetLastError();
 }
 

@@ -299,9 +299,10 @@ def _staging_only(rows, K):
 
 
 @pytest.mark.parametrize("M,N,K,out", [
-    (1, 4096, 8192, "fp32"),     # 32 tiles of 32 steps over all SMs: ~5 pieces per tile
-    (33, 1000, 1152, "bf16"),    # odd group count, one step per CTA, ragged N
-    (64, 28672, 1024, "fp32"),   # 224 tiles, ranges cross tile boundaries
+    (8, 4096, 8192, "fp32"),     # 32 tiles of 32 steps over all SMs: ~5 pieces per tile
+    (5, 1000, 1152, "bf16"),     # odd group count, one step per CTA, ragged N
+    (6, 28672, 1024, "fp32"),    # 224 tiles, ranges cross tile boundaries
+    (33, 1000, 1152, "bf16"),    # tensor-core path: whole tiles, workspace size irrelevant
 ])
 def test_dense_k_split_matches_oracle_and_unsplit(M, N, K, out):
     rng = np.random.default_rng(M + N + K)
@@ -327,7 +328,7 @@ def test_dense_k_split_matches_oracle_and_unsplit(M, N, K, out):
     assert w8.device_error(clear=True) == 0
 
 
-def test_grouped_k_split_matches_oracle_and_unsplit():
+def test_grouped_minimal_workspace_matches_oracle():
     rng = np.random.default_rng(77)
     R, E, N, K = 300, 6, 256, 1280
     off = workloads.random_offsets(rng, R, E, empty_frac=0.2)
