@@ -7,9 +7,10 @@ Each GEMM of the step reads its own 235 MB weight copy, so every input is
 larger than L2 and no weight bytes are reused from L2 between GEMMs.
 
 Metric: INT8 TOPS = sum of 2*M*N*K over the step / step time (whole job over
-all ranks). The dominant kernel is the GEMM, HBM-bound at these shapes: the
-roofline object reports its algorithmic bytes per launch (int8 weights, FP32
-group scales, int8 activations and scales, BF16 output) over its measured
+all ranks). The dominant kernel is the GEMM (the CUDA-core batched GEMV for
+M <= 8, the tcgen05 narrow-tile kernel for M = 32), HBM-bound at these shapes:
+the roofline object reports its algorithmic bytes per launch (int8 weights,
+FP32 group scales, int8 activations and scales, BF16 output) over its measured
 launch duration, against the measured HBM copy bandwidth.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]

@@ -1037,12 +1037,13 @@ __device__ __forceinline__ void for_each_piece(const WorkPlan &w, F &&f) {
 // stream-K split and FP32 accumulation order are those of the narrow kernel;
 // the int8 token codes are read directly (no fp16 staging copy), in the same
 // stages as the weights.
-// Warp 0 (lane 0) streams the stages; warps 1..8 compute. In a step, thread
-// (row r, group j) forms the exact partials P[m] of its row and group for all
-// token rows m; the two threads of a row swap them and both apply the group
-// scales in K order, acc = fma(P_g0, sw_g0, acc), acc = fma(P_g1, sw_g1, acc).
+// Warp 0 (lane 0) streams the stages; the other warps compute. In a step,
+// a thread forms the exact partials P[m] of its rows, token rows and group;
+// the two threads holding the step's two groups of the same rows swap them
+// and both apply the group scales in K order, acc = fma(P_g0, sw_g0, acc),
+// acc = fma(P_g1, sw_g1, acc).
 // =============================================================================
-constexpr int kGemvThreads = 288;
+constexpr int gemv_threads(int cw) { return 32 * (1 + cw); }   // producer warp + cw
 constexpr int kGemvOffStages = 2048;     // barriers, flags; the tile table follows the stages
 constexpr int gemv_stage_bytes(int mr) {
     return 2 * kAStageBytes + ((2 * mr * 128 + 1023) / 1024) * 1024;
@@ -1058,16 +1059,19 @@ static_assert(gemv_stage_bytes(kGemvMaxTokens) % 1024 == 0, "stage alignment");
 
 // Register blocking: a compute thread covers RR weight rows x RM token rows
 // of one group, so a step's loads from shared memory are amortised over
-// RR * RM dot products per word (MR = RR * RM token rows per tile).
-template <bool kDebug, int RR, int RM>
-__global__ void __launch_bounds__(kGemvThreads, 1)
+// RR * RM dot products per word. CW compute warps cover the tile's 128 rows
+// x 2 groups in CW * RR / 8 token blocks, so MR = CW * RR / 8 * RM token rows.
+template <bool kDebug, int RR, int RM, int CW>
+__global__ void __launch_bounds__(gemv_threads(CW), 1)
 w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_q, const KParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw_addr);
-    constexpr int MR = RR * RM;
+    constexpr int TB = CW * RR / 8;
+    constexpr int MR = TB * RM;
+    static_assert(TB >= 1 && CW * RR % 8 == 0, "compute warps cover whole token blocks");
     constexpr uint32_t kStage = static_cast<uint32_t>(gemv_stage_bytes(MR));
     const uint32_t SA = static_cast<uint32_t>(p.a_stages);
     const uint32_t sA = base + kGemvOffStages;
@@ -1086,7 +1090,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     if (threadIdx.x == 0) {
         for (int i = 0; i < kMaxAStages; ++i) {
             mbar_init(bar(GBar::full + i), 1);
-            mbar_init(bar(GBar::empty + i), 8);
+            mbar_init(bar(GBar::empty + i), CW);
         }
         *s_abort = 0;
         fence_mbarrier_init();
@@ -1317,7 +1321,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
         if (n_split > 0) {   // the same for all compute warps
             __threadfence();
-            named_barrier_sync(1, 256);
+            named_barrier_sync(1, 32 * CW);
             if (ct == 0) {
                 int flags = 0;
                 for (int q = 0; q < n_split; ++q) {
@@ -1330,7 +1334,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 __threadfence();
                 *s_last = flags;
             }
-            named_barrier_sync(1, 256);
+            named_barrier_sync(1, 32 * CW);
             const int flags = *s_last;
             for (int q = 0; q < n_split; ++q) {
                 if (((flags >> q) & 1) == 0 || failed || j != 0) continue;
@@ -1546,7 +1550,7 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
 }
 
 // Batched GEMV on the CUDA cores for dense calls of at most 8 token rows.
-template <auto kernel, int MR>
+template <auto kernel, int MR, int CW>
 cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     constexpr int stage = gemv_stage_bytes(MR);
     const int tab_bytes = static_cast<int>((3 * (pr.E + 1) * 4 + 15) / 16 * 16);
@@ -1601,25 +1605,26 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
         kp.sk_part = pr.sk_part;
         kp.sk_ld = pr.sk_ld;
     }
-    kernel<<<static_cast<unsigned>(grid), kGemvThreads, smem_bytes, stream>>>(tw, tq, kp);
+    kernel<<<static_cast<unsigned>(grid), gemv_threads(CW), smem_bytes, stream>>>(tw, tq, kp);
     return cudaGetLastError();
 }
 
-template <int RR, int RM>
+template <int RR, int RM, int CW>
 cudaError_t launch_gemv_mr(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
+    constexpr int MR = CW * RR / 8 * RM;
     return pr.debug_partials != nullptr
-               ? launch_gemv<w8a8_gemv_kernel<true, RR, RM>, RR * RM>(pr, num_sms, stream)
-               : launch_gemv<w8a8_gemv_kernel<false, RR, RM>, RR * RM>(pr, num_sms, stream);
+               ? launch_gemv<w8a8_gemv_kernel<true, RR, RM, CW>, MR, CW>(pr, num_sms, stream)
+               : launch_gemv<w8a8_gemv_kernel<false, RR, RM, CW>, MR, CW>(pr, num_sms, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     if (uses_gemv(pr.R, pr.offsets != nullptr)) {
-        if (pr.R <= 1) return launch_gemv_mr<1, 1>(pr, num_sms, stream);
-        if (pr.R <= 2) return launch_gemv_mr<1, 2>(pr, num_sms, stream);
-        if (pr.R <= 4) return launch_gemv_mr<1, 4>(pr, num_sms, stream);
-        return launch_gemv_mr<1, 8>(pr, num_sms, stream);
+        if (pr.R <= 1) return launch_gemv_mr<1, 1, 8>(pr, num_sms, stream);
+        if (pr.R <= 2) return launch_gemv_mr<1, 2, 8>(pr, num_sms, stream);
+        if (pr.R <= 4) return launch_gemv_mr<1, 4, 8>(pr, num_sms, stream);
+        return launch_gemv_mr<1, 8, 8>(pr, num_sms, stream);
     }
     const PipeShape ps = choose_pipe(pr);
     const bool dbg = pr.debug_partials != nullptr;
