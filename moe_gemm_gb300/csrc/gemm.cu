@@ -620,6 +620,9 @@ w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
 // Warp roles as in w8a8_gemm_kernel.
 // =============================================================================
 constexpr int kNarrowSlots = 2;
+constexpr int kWideOffTab = kOffMisc + 64;       // wide tiles: tile table in the fixed area
+constexpr int kWideOffStages = 2048;
+constexpr int kWideMaxExperts = (kWideOffStages - kWideOffTab) / 12 - 1;
 constexpr int kNarrowAStageBytes = 2 * kAStageBytes;   // 32 KB
 
 struct NBar {
@@ -629,12 +632,21 @@ struct NBar {
     static constexpr int done = ready + kNarrowSlots;    // [2] MMA commit -> epilogue, converter, TMA
     static constexpr int b_full = done + kNarrowSlots;   // [2] TMA -> admission
     static constexpr int p_empty = b_full + kNarrowSlots;// [2] epilogue -> admission
-    static constexpr int drain = p_empty + kNarrowSlots;
+    static constexpr int p_full = p_empty + kNarrowSlots;  // [2] wide: MMA commit per group -> epilogue
+    static constexpr int drain = p_full + kNarrowSlots;
     static constexpr int count = drain + 1;
 };
 static_assert(NBar::count <= 128, "barrier area");
 
-template <bool kDebug>
+// kWide: 96- or 128-row token tiles. The two steps' partial buffers (2 x 2 x
+// 128 columns) would not fit next to the operand slots in TMEM, so one pair
+// of partial buffers serves every step, one buffer per group with its own
+// commit ("p_full") and release ("p_empty"): the epilogue drains group 0
+// while the MMAs of group 1 issue, and group 0 of the next step waits only
+// for that drain. Each epilogue warpgroup owns two 32-column chunks; the tile
+// table lives in the fixed area so that the weight stages fit beside the two
+// token stages.
+template <bool kDebug, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
 w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
@@ -643,19 +655,23 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw_addr);
 
+    constexpr uint32_t NP = kWide ? 1u : kNarrowSlots;   // partial-buffer slots
+    constexpr int NCH = kWide ? 2 : 1;                    // 32-column chunks per epilogue warpgroup
+    constexpr uint32_t kStagesOff = kWide ? kWideOffStages : kOffStages;
     const uint32_t SA = static_cast<uint32_t>(p.a_stages);
-    const int b_rows = p.b_rows;                          // 32 or 64
+    const int b_rows = p.b_rows;                          // 32 or 64; 128 when kWide
     const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
     const uint32_t b_stage_bytes = 4u * b_atom_bytes;     // 2 groups x 2 atoms
-    const uint32_t sA = base + kOffStages;
+    const uint32_t sA = base + kStagesOff;
     const uint32_t sB = sA + SA * kNarrowAStageBytes;
     const uint32_t sBar = base + kOffBar;
     volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
-    int *s_base = reinterpret_cast<int *>(smem + kOffTab);
-    int *s_lo = s_base + (kMaxExperts + 1);
-    int *s_cnt = s_lo + (kMaxExperts + 1);
+    const int tab_stride = kWide ? p.E + 1 : kMaxExperts + 1;
+    int *s_base = reinterpret_cast<int *>(smem + (kWide ? kWideOffTab : kOffTab));
+    int *s_lo = s_base + tab_stride;
+    int *s_cnt = s_lo + tab_stride;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -672,6 +688,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(bar(NBar::done + i), 1);
             mbar_init(bar(NBar::b_full + i), 1);
             mbar_init(bar(NBar::p_empty + i), 8);
+            mbar_init(bar(NBar::p_full + i), 1);
         }
         mbar_init(bar(NBar::drain), 1);
         *s_abort = 0;
@@ -694,8 +711,9 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const int total = *s_total;
     const int G = p.G;
     const int wg = warp >> 2;
-    // TMEM: partial buffer of (slot s, group j) at column (2 s + j) * b_rows;
-    // fp16 A operand of (slot s, group j) at column 256 + 128 s + 64 j.
+    // TMEM: partial buffer of (partial slot s, group j) at column
+    // (2 s + j) * b_rows; fp16 A operand of (step slot s, group j) at column
+    // 256 + 128 s + 64 j.
     auto pbuf_col = [&](uint32_t s, int j) -> uint32_t {
         return (2u * s + static_cast<uint32_t>(j)) * static_cast<uint32_t>(b_rows);
     };
@@ -728,7 +746,8 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             if (!ok) drain_ring(bar(NBar::a_full), issued, SA);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------- MMA issuer
-            Ring st;
+            Ring st, pr;
+            uint32_t gph[2] = {0u, 0u};   // wide: phase of each group's partial buffer
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
@@ -743,7 +762,16 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     }
                     tc_fence_after();
                     for (int j = 0; j < ng; ++j) {
-                        const uint32_t d_tmem = tmem_base + pbuf_col(st.idx, j);
+                        if constexpr (kWide) {
+                            // group j's partial buffer drained by the epilogue
+                            if (!mbar_wait(bar(NBar::p_empty + j), gph[j] ^ 1u, s_abort, p.err,
+                                           ROLE_MMA, 4)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        const uint32_t d_tmem = tmem_base + pbuf_col(pr.idx, j);
                         const uint32_t a_tmem = tmem_base + kTmemA0 + st.idx * 128u + j * 64u;
                         const uint64_t bdesc0 = smem_desc_sw128(sB + st.idx * b_stage_bytes +
                                                                 j * 2u * b_atom_bytes);
@@ -754,9 +782,15 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                 bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
                             mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
                         }
+                        if constexpr (kWide) {
+                            mma_commit(bar(NBar::p_full + j));
+                            gph[j] ^= 1u;
+                        }
                     }
+                    if (!ok) break;
                     mma_commit(bar(NBar::done + st.idx));
                     st.advance(kNarrowSlots);
+                    pr.advance(NP);
                 }
             }
             mma_commit(bar(NBar::drain));
@@ -794,19 +828,20 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             if (!ok) drain_ring(bar(NBar::b_full), issued, kNarrowSlots);
         } else if (warp == 3 && lane == 0) {
             // --------------------------------------------------- admission
-            Ring st;
+            Ring st, pr;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 for (int g0 = 0; g0 < G; g0 += 2) {
                     if (!mbar_wait(bar(NBar::b_full + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
                                    2) ||
-                        !mbar_wait(bar(NBar::p_empty + st.idx), st.phase ^ 1u, s_abort, p.err,
-                                   ROLE_MMA, 3)) {
+                        (!kWide && !mbar_wait(bar(NBar::p_empty + pr.idx), pr.phase ^ 1u, s_abort,
+                                              p.err, ROLE_MMA, 3))) {
                         ok = false;
                         break;
                     }
                     mbar_arrive(bar(NBar::ready + st.idx));
                     st.advance(kNarrowSlots);
+                    pr.advance(NP);
                 }
             }
         }
@@ -830,7 +865,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 tc_fence_after();
                 for (int j = 0; j < ng; ++j) {
                     const uint8_t *rowp =
-                        smem + kOffStages + a.idx * kNarrowAStageBytes + j * kAStageBytes + row * 128;
+                        smem + kStagesOff + a.idx * kNarrowAStageBytes + j * kAStageBytes + row * 128;
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                            kTmemA0 + st.idx * 128u + j * 64u;
 #pragma unroll
@@ -862,20 +897,23 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     } else {
         // -------------------------------------------------------- epilogue
         setmaxnreg_inc<kEpiRegs>();
-        const int ewg = wg - 2;                // owns token columns [32 ewg, 32 ewg + 32)
+        const int ewg = wg - 2;   // owns token columns [32 c, 32 c + 32) for chunks c = ewg + 2 h
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
-        float acc[32];
+        float acc[NCH][32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
-        Ring st;
+        for (int h = 0; h < NCH; ++h)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[h][j] = 0.0f;
+        Ring st, pr;
+        uint32_t gph[2] = {0u, 0u};   // wide: phase of each group's partial buffer
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
             const int n_eff = (ti.rows + 15) & ~15;
-            const bool owned = 32 * ewg < n_eff;   // warp-uniform
+            const bool owned = 32 * ewg < n_eff;   // warp-uniform (first chunk)
             const int n_local = ti.n0 + lrow;
             const bool n_ok = n_local < p.N;
             const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
@@ -904,31 +942,73 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
                 const float s0 = (g0 & 3) == 0 ? cur.x : cur.z;
                 const float s1 = (g0 & 3) == 0 ? cur.y : cur.w;
+                if constexpr (kWide) {
+                    // One group at a time: wait for its MMAs, drain its buffer,
+                    // release it (group 0 drains while group 1's MMAs issue).
+                    for (int j = 0; j < ng; ++j) {
+                        if (!mbar_wait(bar(NBar::p_full + j), gph[j], s_abort, p.err,
+                                       ROLE_EPILOGUE, 2)) {
+                            ok = false;
+                            break;
+                        }
+                        gph[j] ^= 1u;
+                        tc_fence_after();
+                        const float sj = j == 0 ? s0 : s1;
+#pragma unroll
+                        for (int h = 0; h < NCH; ++h) {
+                            const int chunk = ewg + 2 * h;
+                            if (32 * chunk >= n_eff) continue;   // warp-uniform
+                            uint32_t v[32];
+                            tmem_ld_32cols_sync(lane_base + pbuf_col(0, j) + 32u * chunk, v);
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj)
+                                acc[h][jj] = fmaf(__uint_as_float(v[jj]), sj, acc[h][jj]);
+                            if (kDebug && n_ok) {
+#pragma unroll
+                                for (int jj = 0; jj < 32; ++jj) {
+                                    const int col = 32 * chunk + jj;
+                                    if (col < ti.rows)
+                                        p.dbg[(static_cast<size_t>(ti.m0 + col) * p.N + n_local) * G +
+                                              g0 + j] = __float2int_rn(__uint_as_float(v[jj]));
+                                }
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + j));
+                    }
+                    if (!ok) break;
+                    continue;
+                }
                 if (!mbar_wait(bar(NBar::done + st.idx), st.phase, s_abort, p.err, ROLE_EPILOGUE,
                                1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (owned) {
-                    const uint32_t c0 = lane_base + pbuf_col(st.idx, 0) + 32u * ewg;
-                    const uint32_t c1 = lane_base + pbuf_col(st.idx, 1) + 32u * ewg;
+#pragma unroll
+                for (int h = 0; h < NCH; ++h) {
+                    const int chunk = ewg + 2 * h;
+                    if (32 * chunk >= n_eff) continue;   // warp-uniform
+                    const uint32_t c0 = lane_base + pbuf_col(pr.idx, 0) + 32u * chunk;
+                    const uint32_t c1 = lane_base + pbuf_col(pr.idx, 1) + 32u * chunk;
                     uint32_t v0[32], v1[32];
                     if (ng == 2) {
                         tmem_ld_2x32cols_sync(c0, c1, v0, v1);
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            acc[j] = fmaf(__uint_as_float(v1[j]), s1,
-                                          fmaf(__uint_as_float(v0[j]), s0, acc[j]));
+                            acc[h][j] = fmaf(__uint_as_float(v1[j]), s1,
+                                             fmaf(__uint_as_float(v0[j]), s0, acc[h][j]));
                     } else {
                         tmem_ld_32cols_sync(c0, v0);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(v0[j]), s0, acc[j]);
+                        for (int j = 0; j < 32; ++j)
+                            acc[h][j] = fmaf(__uint_as_float(v0[j]), s0, acc[h][j]);
                     }
                     if (kDebug && n_ok) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const int col = 32 * ewg + j;
+                            const int col = 32 * chunk + j;
                             if (col < ti.rows) {
                                 const size_t o =
                                     (static_cast<size_t>(ti.m0 + col) * p.N + n_local) * G + g0;
@@ -940,27 +1020,33 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + st.idx));
+                if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + pr.idx));
                 st.advance(kNarrowSlots);
+                pr.advance(NP);
             }
             if (!ok) break;
-            if (owned && n_ok) {
+            if (n_ok) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int col = 32 * ewg + j;
-                    if (col < ti.rows) {
-                        const int m = ti.m0 + col;
-                        const float out = acc[j] * __ldg(p.sa + m);
-                        const size_t idx = static_cast<size_t>(m) * p.N + n_local;
-                        if (p.out_fp32)
-                            static_cast<float *>(p.y)[idx] = out;
-                        else
-                            static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                for (int h = 0; h < NCH; ++h) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = 32 * (ewg + 2 * h) + j;
+                        if (col < ti.rows) {
+                            const int m = ti.m0 + col;
+                            const float out = acc[h][j] * __ldg(p.sa + m);
+                            const size_t idx = static_cast<size_t>(m) * p.N + n_local;
+                            if (p.out_fp32)
+                                static_cast<float *>(p.y)[idx] = out;
+                            else
+                                static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+            for (int h = 0; h < NCH; ++h)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[h][j] = 0.0f;
         }
     }
 
@@ -1426,8 +1512,8 @@ bool encode_2d_plain(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_by
 // stage counts, filling shared memory with weight stages after the token stages.
 struct PipeShape {
     int b_rows, tile_tokens, b_stages, a_stages, p_bufs, smem_bytes;
-
     bool narrow;    // one batch of <= 64 rows per tile: w8a8_gemm_narrow_kernel
+    bool wide;      // one batch of 96 or 128 rows per tile: its kWide form
 };
 
 PipeShape choose_pipe(const GemmProblem &pr) {
@@ -1439,10 +1525,27 @@ PipeShape choose_pipe(const GemmProblem &pr) {
         s.b_rows = kMaxBatchRows;
         s.tile_tokens = 2 * kMaxBatchRows;
     } else {
-        s.b_rows = pr.grouped_batch_rows;
-        s.tile_tokens = pr.grouped_batch_rows;
+        // Expert tiles of 128 rows when the tile table fits the wide kernel's
+        // fixed area (fewer tiles, and fewer weight passes, for experts with
+        // 65..128 routed rows), else 64.
+        s.b_rows = pr.E <= kWideMaxExperts ? kMaxBatchRows : 64;
+        s.tile_tokens = s.b_rows;
     }
     s.narrow = s.tile_tokens == s.b_rows && s.b_rows <= 64;
+    s.wide = s.tile_tokens == s.b_rows && s.b_rows > 64;
+    if (s.wide) {
+        // One partial slot; two step slots of token tiles (b_rows x 512 B);
+        // weight stages after the 2 KB fixed area.
+        s.p_bufs = 2;
+        s.b_stages = kNarrowSlots;
+        const int b_slot_bytes = 4 * s.b_rows * 128;
+        const int avail = kSmemLimit - 1024 - kWideOffStages - kNarrowSlots * b_slot_bytes;
+        s.a_stages = avail / kNarrowAStageBytes;
+        if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
+        s.smem_bytes = kWideOffStages + s.a_stages * kNarrowAStageBytes +
+                       kNarrowSlots * b_slot_bytes + 1024;
+        return s;
+    }
     if (s.narrow) {
         // Two step slots, each holding the token tiles of two K groups.
         s.p_bufs = 2 * kNarrowSlots;
@@ -1550,14 +1653,15 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
 }
 
 // Batched GEMV on the CUDA cores for dense calls of at most 8 token rows.
-template <auto kernel, int MR, int CW>
+// kExtra: bytes of shared memory the kernel keeps after its stages.
+template <auto kernel, int MR, int CW, int kExtra>
 cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     constexpr int stage = gemv_stage_bytes(MR);
     const int tab_bytes = static_cast<int>((3 * (pr.E + 1) * 4 + 15) / 16 * 16);
-    int stages = (kSmemLimit - 1024 - kGemvOffStages - tab_bytes) / stage;
+    int stages = (kSmemLimit - 1024 - kGemvOffStages - kExtra - tab_bytes) / stage;
     if (stages > kMaxAStages) stages = kMaxAStages;
     if (stages < 2 || pr.R > MR) return cudaErrorInvalidConfiguration;
-    const int tab_off = kGemvOffStages + stages * stage;
+    const int tab_off = kGemvOffStages + stages * stage + kExtra;
     const int smem_bytes = tab_off + tab_bytes + 1024;
     CUtensorMap tw, tq;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
@@ -1613,8 +1717,8 @@ template <int RR, int RM, int CW>
 cudaError_t launch_gemv_mr(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     constexpr int MR = CW * RR / 8 * RM;
     return pr.debug_partials != nullptr
-               ? launch_gemv<w8a8_gemv_kernel<true, RR, RM, CW>, MR, CW>(pr, num_sms, stream)
-               : launch_gemv<w8a8_gemv_kernel<false, RR, RM, CW>, MR, CW>(pr, num_sms, stream);
+               ? launch_gemv<w8a8_gemv_kernel<true, RR, RM, CW>, MR, CW, 0>(pr, num_sms, stream)
+               : launch_gemv<w8a8_gemv_kernel<false, RR, RM, CW>, MR, CW, 0>(pr, num_sms, stream);
 }
 
 }  // namespace
@@ -1628,9 +1732,14 @@ cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     }
     const PipeShape ps = choose_pipe(pr);
     const bool dbg = pr.debug_partials != nullptr;
+    if (ps.wide) {
+        if (pr.E > kWideMaxExperts) return cudaErrorInvalidConfiguration;
+        return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true, true>>(pr, ps, num_sms, stream)
+                   : launch_kernel<w8a8_gemm_narrow_kernel<false, true>>(pr, ps, num_sms, stream);
+    }
     if (ps.narrow)
-        return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true>>(pr, ps, num_sms, stream)
-                   : launch_kernel<w8a8_gemm_narrow_kernel<false>>(pr, ps, num_sms, stream);
+        return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true, false>>(pr, ps, num_sms, stream)
+                   : launch_kernel<w8a8_gemm_narrow_kernel<false, false>>(pr, ps, num_sms, stream);
     return dbg ? launch_kernel<w8a8_gemm_kernel<true>>(pr, ps, num_sms, stream)
                : launch_kernel<w8a8_gemm_kernel<false>>(pr, ps, num_sms, stream);
 }

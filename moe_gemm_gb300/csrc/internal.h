@@ -29,7 +29,6 @@ struct GemmProblem {
     int32_t *debug_partials;  // nullable [R, N, G]
     int64_t R, E, N, K;
     bool out_fp32;
-    int grouped_batch_rows = 64;  // token rows per MMA batch for grouped calls (32..128)
     // Stream-K split of GEMV calls; null sk_cnt: whole tiles only.
     int *sk_cnt = nullptr;        // [2 * kSkMaxCtas] counters, zeroed before the GEMM
     float *sk_part = nullptr;     // [kSkMaxCtas][2][sk_ld][128] FP32 partials
