@@ -236,7 +236,12 @@ def run_ours(args):
         wsz = (w8.grouped_gemm_workspace_size(shp.M, shp.E, shp.N, shp.K) if d["off"] is not None
                else w8.gemm_workspace_size(shp.M, shp.N, shp.K))
         d["ws"] = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
-        d["launches"] = 2 + (1 if wsz > 0 else 0)
+        # quantizer + GEMM, plus the fp16 staging kernel (tensor-core paths)
+        # or the split-counter reset (CUDA-core path, 5..8 token rows)
+        if d["off"] is None and shp.M <= 8:
+            d["launches"] = 2 + (1 if shp.M > 4 else 0)
+        else:
+            d["launches"] = 3
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
@@ -249,11 +254,15 @@ def run_ours(args):
             w8.gemm(d["qa"], d["sa"], d["qw"], d["sw"], out=d["y"], out_dtype=d["y"].dtype,
                     workspace=d["ws"])
 
+    # Per-GEMM events bracket the quantizer and the GEMM: the GEMM is launched
+    # as a programmatic dependent of the quantizer and overlaps it, which an
+    # event recorded between the two would prevent. The per-launch GEMM time
+    # (roofline) therefore includes any part of the quantizer it does not hide.
     def step(ev=None):
         for i, d in enumerate(per):
-            w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"])
             if ev is not None:
                 ev[i][0].record(stream)
+            w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"])
             gemm_call(d)
             if ev is not None:
                 ev[i][1].record(stream)
@@ -351,6 +360,8 @@ def run_ours(args):
                 "traffic": recorded_traffic(args.workload),
                 "alg_bytes_per_launch": alg,
                 "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
+                "kernel_time": "quantizer start to GEMM end per shape (the GEMM overlaps the "
+                               "quantizer; includes any part of it not hidden)",
                 "peak_source": f"{peaks['source']} HBM copy bandwidth"}
     else:
         flops = [d["shape"].ops for d in per]
@@ -361,6 +372,8 @@ def run_ours(args):
                 "traffic": recorded_traffic(args.workload),
                 "ops_per_launch": flops,
                 "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
+                "kernel_time": "quantizer start to GEMM end per shape (the GEMM overlaps the "
+                               "quantizer; includes any part of it not hidden)",
                 "peak_source": (f"{peaks['source']} dense bf16 burst (the integer path runs "
                                 "on fp16 tensor cores, same rate as bf16)")}
 

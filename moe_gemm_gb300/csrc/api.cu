@@ -110,8 +110,7 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
     if (w8a8::uses_gemv(R, grouped)) {
         // The CUDA-core path reads the int8 codes directly; only the split
         // counters need zeroing.
-        if (p.sk_cnt != nullptr)
-            e = cudaMemsetAsync(p.sk_cnt, 0, w8a8::sk_counter_bytes(), s);
+        if (p.sk_cnt != nullptr) e = w8a8::launch_zero_counters(p.sk_cnt, 2 * w8a8::kSkMaxCtas, s);
     } else {
         e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s);
     }

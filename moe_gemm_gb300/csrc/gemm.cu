@@ -1196,9 +1196,30 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     if (warp == 0) {
         if (lane == 0) {
             // ---------------------------------------------- stage producer
+            // The kernel may start while the quantizer that writes the token
+            // codes still runs (programmatic dependent launch): the first
+            // stage's weight loads go out at once, its token loads (and all
+            // later stages) after griddepcontrol.wait. (Deferring more stages
+            // delays the first token loads more than it gains: measured.)
             Ring a;
             uint32_t issued = 0;
             bool ok = true;
+            bool dep_done = false;
+            uint32_t pend_stage[kMaxAStages], pend_bar[kMaxAStages];
+            int pend_x[kMaxAStages], pend_y[kMaxAStages], pend_ng[kMaxAStages];
+            int n_pend = 0;
+            auto issue_tokens = [&](uint32_t stage, int x, int y, int ng, uint32_t fb) {
+                for (int j = 0; j < ng; ++j)
+                    tma_load_2d(stage + 2 * kAStageBytes + j * MR * 128, &tmap_q, x + j * kGroupK,
+                                y, fb);
+            };
+            auto flush = [&]() {
+                griddep_wait();
+                dep_done = true;
+                for (int i = 0; i < n_pend; ++i)
+                    issue_tokens(pend_stage[i], pend_x[i], pend_y[i], pend_ng[i], pend_bar[i]);
+                n_pend = 0;
+            };
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int wrow = ti.e * p.N + ti.n0;
@@ -1211,19 +1232,27 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         return false;
                     }
                     const uint32_t stage = sA + a.idx * kStage;
-                    mbar_arrive_expect_tx(bar(GBar::full + a.idx),
-                                          static_cast<uint32_t>(ng * (kAStageBytes + MR * 128)));
-                    for (int j = 0; j < ng; ++j) {
-                        tma_load_2d(stage + j * kAStageBytes, &tmap_w, (g0 + j) * kGroupK, wrow,
-                                    bar(GBar::full + a.idx));
-                        tma_load_2d(stage + 2 * kAStageBytes + j * MR * 128, &tmap_q,
-                                    (g0 + j) * kGroupK, ti.m0, bar(GBar::full + a.idx));
+                    const uint32_t fb = bar(GBar::full + a.idx);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng * (kAStageBytes + MR * 128)));
+                    for (int j = 0; j < ng; ++j)
+                        tma_load_2d(stage + j * kAStageBytes, &tmap_w, (g0 + j) * kGroupK, wrow, fb);
+                    if (dep_done) {
+                        issue_tokens(stage, g0 * kGroupK, ti.m0, ng, fb);
+                    } else {
+                        pend_stage[n_pend] = stage;
+                        pend_x[n_pend] = g0 * kGroupK;
+                        pend_y[n_pend] = ti.m0;
+                        pend_ng[n_pend] = ng;
+                        pend_bar[n_pend] = fb;
+                        ++n_pend;
+                        flush();   // the first stage's weights overlap the wait
                     }
                     a.advance(SA);
                     ++issued;
                 }
                 return true;
             });
+            if (!dep_done) flush();   // fewer steps than stages (or an abort)
             if (!ok) drain_ring(bar(GBar::full), issued, SA);
         }
     } else {
@@ -1709,7 +1738,21 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
         kp.sk_part = pr.sk_part;
         kp.sk_ld = pr.sk_ld;
     }
-    kernel<<<static_cast<unsigned>(grid), gemv_threads(CW), smem_bytes, stream>>>(tw, tq, kp);
+    // Programmatic dependent launch: the kernel may start while the kernel
+    // before it in the stream (the quantizer) still runs; its stage producer
+    // waits for that kernel before loading the token codes.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(gemv_threads(CW));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tw, tq, kp);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -18,6 +18,10 @@ cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw
 cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
                                int num_sms, cudaStream_t stream);
 
+// Zeroes n split-tile counters (programmatic dependent of the kernel before
+// it in the stream; see quant.cu).
+cudaError_t launch_zero_counters(int *cnt, int n, cudaStream_t stream);
+
 struct GemmProblem {
     const int8_t *qa;         // [R, K] int8 activation codes
     const float *sa;          // [R]

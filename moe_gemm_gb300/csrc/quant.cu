@@ -109,6 +109,10 @@ template <int VPT>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
     const uint16_t *__restrict__ a, int K, int64_t lda, int8_t *__restrict__ qa, int64_t ldq,
     float *__restrict__ sa) {
+    // A GEMM launched after this kernel as a programmatic dependent may start
+    // its set-up and weight stream now; it waits for this grid (and so for qa
+    // and sa) before it reads the codes.
+    griddep_launch_dependents();
     __shared__ uint32_t red[kQuantThreads / 32];
     const int64_t row = blockIdx.x;
     const uint4 *src = reinterpret_cast<const uint4 *>(a + row * lda);
@@ -180,8 +184,11 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restri
                                                           int64_t rows, int K, int64_t ldq,
                                                           __half *__restrict__ out) {
     // The GEMM that consumes this copy is launched as a programmatic
-    // dependent: let it start its set-up and weight stream right away.
+    // dependent: let it start its set-up and weight stream right away. This
+    // kernel is itself a programmatic dependent of the quantizer: wait for
+    // its codes.
     griddep_launch_dependents();
+    griddep_wait();
     const int vec_per_row = K >> 4;  // 16 codes per vector
     const int64_t total = rows * vec_per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -230,6 +237,31 @@ cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw
     return cudaGetLastError();
 }
 
+// Zeroes the GEMV's split-tile counters. Launched as a programmatic
+// dependent of the quantizer and waiting for it before it completes, so the
+// GEMV after it (itself a programmatic dependent) starts early and its wait
+// still covers the quantizer's codes.
+__global__ void __launch_bounds__(256) zero_counters_kernel(int *__restrict__ cnt, int n) {
+    griddep_launch_dependents();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) cnt[i] = 0;
+    griddep_wait();
+}
+
+cudaError_t launch_zero_counters(int *cnt, int n, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, zero_counters_kernel, cnt, n);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
                                int num_sms, cudaStream_t stream) {
     const int64_t total = rows * (K / 16);
@@ -237,8 +269,18 @@ cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    widen_codes_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        q, rows, static_cast<int>(K), ldq, static_cast<__half *>(out));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, widen_codes_kernel, q, rows, static_cast<int>(K),
+                                             ldq, static_cast<__half *>(out));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
