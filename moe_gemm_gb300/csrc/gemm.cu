@@ -1143,6 +1143,61 @@ struct GBar {
 static_assert(GBar::count <= 128, "barrier area");
 static_assert(gemv_stage_bytes(kGemvMaxTokens) % 1024 == 0, "stage alignment");
 
+// Stage producer of the GEMV kernels (one thread): weights and the token
+// codes of each step into one stage, per the work plan.
+template <int MR>
+__device__ __forceinline__ void gemv_produce(const KParams &p, const WorkPlan &plan,
+                                             const CUtensorMap &tmap_w, const CUtensorMap &tmap_q,
+                                             uint32_t sA, uint32_t kStage, uint32_t SA,
+                                             uint32_t full0, uint32_t empty0, volatile int *s_abort,
+                                             const int *s_base, const int *s_lo, const int *s_cnt,
+                                             int tt) {
+    const int G = p.G;
+    // ---------------------------------------------- stage producer
+    // The kernel may start while the quantizer that writes the token
+    // codes still runs (programmatic dependent launch): the first
+    // stage's weight loads go out at once, its token loads (and all
+    // later stages) after griddepcontrol.wait. (Deferring more stages
+    // delays the first token loads more than it gains: measured.)
+    Ring a;
+    uint32_t issued = 0;
+    bool ok = true;
+    bool dep_done = false;
+    auto issue_tokens = [&](uint32_t stage, int x, int y, int ng, uint32_t fb) {
+        for (int j = 0; j < ng; ++j)
+            tma_load_2d(stage + 2 * kAStageBytes + j * MR * 128, &tmap_q, x + j * kGroupK,
+                        y, fb);
+    };
+    for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
+        const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+        const int wrow = ti.e * p.N + ti.n0;
+        for (int sg = s0; sg < s1; ++sg) {
+            const int g0 = 2 * sg;
+            const int ng = min(2, G - g0);
+            if (!mbar_wait(empty0 + 8u * a.idx, a.phase ^ 1u, s_abort, p.err,
+                           ROLE_PRODUCER, 1)) {
+                ok = false;
+                return false;
+            }
+            const uint32_t stage = sA + a.idx * kStage;
+            const uint32_t fb = full0 + 8u * a.idx;
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng * (kAStageBytes + MR * 128)));
+            for (int j = 0; j < ng; ++j)
+                tma_load_2d(stage + j * kAStageBytes, &tmap_w, (g0 + j) * kGroupK, wrow, fb);
+            if (!dep_done) {
+                griddep_wait();
+                dep_done = true;
+            }
+            issue_tokens(stage, g0 * kGroupK, ti.m0, ng, fb);
+            a.advance(SA);
+            ++issued;
+        }
+        return true;
+    });
+    if (!dep_done) griddep_wait();   // no step at all (or an abort before the first)
+    if (!ok) drain_ring(full0, issued, SA);
+}
+
 // Register blocking: a compute thread covers RR weight rows x RM token rows
 // of one group, so a step's loads from shared memory are amortised over
 // RR * RM dot products per word. CW compute warps cover the tile's 128 rows
@@ -1195,65 +1250,8 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------------------------------------- stage producer
-            // The kernel may start while the quantizer that writes the token
-            // codes still runs (programmatic dependent launch): the first
-            // stage's weight loads go out at once, its token loads (and all
-            // later stages) after griddepcontrol.wait. (Deferring more stages
-            // delays the first token loads more than it gains: measured.)
-            Ring a;
-            uint32_t issued = 0;
-            bool ok = true;
-            bool dep_done = false;
-            uint32_t pend_stage[kMaxAStages], pend_bar[kMaxAStages];
-            int pend_x[kMaxAStages], pend_y[kMaxAStages], pend_ng[kMaxAStages];
-            int n_pend = 0;
-            auto issue_tokens = [&](uint32_t stage, int x, int y, int ng, uint32_t fb) {
-                for (int j = 0; j < ng; ++j)
-                    tma_load_2d(stage + 2 * kAStageBytes + j * MR * 128, &tmap_q, x + j * kGroupK,
-                                y, fb);
-            };
-            auto flush = [&]() {
-                griddep_wait();
-                dep_done = true;
-                for (int i = 0; i < n_pend; ++i)
-                    issue_tokens(pend_stage[i], pend_x[i], pend_y[i], pend_ng[i], pend_bar[i]);
-                n_pend = 0;
-            };
-            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int wrow = ti.e * p.N + ti.n0;
-                for (int sg = s0; sg < s1; ++sg) {
-                    const int g0 = 2 * sg;
-                    const int ng = min(2, G - g0);
-                    if (!mbar_wait(bar(GBar::empty + a.idx), a.phase ^ 1u, s_abort, p.err,
-                                   ROLE_PRODUCER, 1)) {
-                        ok = false;
-                        return false;
-                    }
-                    const uint32_t stage = sA + a.idx * kStage;
-                    const uint32_t fb = bar(GBar::full + a.idx);
-                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng * (kAStageBytes + MR * 128)));
-                    for (int j = 0; j < ng; ++j)
-                        tma_load_2d(stage + j * kAStageBytes, &tmap_w, (g0 + j) * kGroupK, wrow, fb);
-                    if (dep_done) {
-                        issue_tokens(stage, g0 * kGroupK, ti.m0, ng, fb);
-                    } else {
-                        pend_stage[n_pend] = stage;
-                        pend_x[n_pend] = g0 * kGroupK;
-                        pend_y[n_pend] = ti.m0;
-                        pend_ng[n_pend] = ng;
-                        pend_bar[n_pend] = fb;
-                        ++n_pend;
-                        flush();   // the first stage's weights overlap the wait
-                    }
-                    a.advance(SA);
-                    ++issued;
-                }
-                return true;
-            });
-            if (!dep_done) flush();   // fewer steps than stages (or an abort)
-            if (!ok) drain_ring(bar(GBar::full), issued, SA);
+            gemv_produce<MR>(p, plan, tmap_w, tmap_q, sA, kStage, SA, bar(GBar::full),
+                             bar(GBar::empty), s_abort, s_base, s_lo, s_cnt, tt);
         }
     } else {
         // ------------------------------------------------- compute warps
