@@ -196,6 +196,18 @@ const char *w8a8_status_string(w8a8_status status);
  */
 w8a8_status w8a8_device_error(uint64_t *code_out, int clear);
 
+/*
+ * Diagnostic of the device-side failure path (no counterpart on the pages):
+ * launches a one-thread kernel that waits, through the same bounded wait the
+ * GEMM kernels use, on a barrier armed for bytes no copy will deliver. The
+ * wait gives up after limit_us microseconds (1 .. 2,000,000) and records its
+ * code in the error word; w8a8_device_error() then returns
+ * W8A8_ERR_DEVICE_TIMEOUT with code = kernel 2, role 5, site 1, CTA 0
+ * (bits 56..63, 48..55, 32..47, 0..31). Nothing traps or hangs and the
+ * context stays usable. Asynchronous on `stream`.
+ */
+w8a8_status w8a8_selftest_wait_timeout(uint32_t limit_us, w8a8_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int w8a8_version(void);
 

@@ -53,9 +53,10 @@ def _load() -> ctypes.CDLL:
     lib.w8a8_status_string.argtypes = [i32]
     lib.w8a8_status_string.restype = ctypes.c_char_p
     lib.w8a8_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint64), i32]
+    lib.w8a8_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
     lib.w8a8_version.restype = i32
     for name in ("w8a8_quant_act", "w8a8_quant_weight", "w8a8_gemm", "w8a8_grouped_gemm",
-                 "w8a8_gemm_noalloc", "w8a8_device_error"):
+                 "w8a8_gemm_noalloc", "w8a8_device_error", "w8a8_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -207,6 +208,15 @@ def grouped_gemm(qa: torch.Tensor, sa: torch.Tensor, offsets: torch.Tensor, qw: 
                                   _dtype_code(out_dtype), R, E, N, K, _ptr(P), _ptr(workspace),
                                   workspace.numel(), _stream(stream)), "w8a8_grouped_gemm")
     return (y, P) if debug_partials else y
+
+
+def selftest_wait_timeout(limit_us: int = 20000,
+                          stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Drives the device-side bounded-wait failure path: a wait that can never
+    complete gives up after limit_us and records its code (read it with
+    device_error())."""
+    _check(_lib.w8a8_selftest_wait_timeout(limit_us, _stream(stream)),
+           "w8a8_selftest_wait_timeout")
 
 
 def device_error(clear: bool = True) -> int:

@@ -263,6 +263,15 @@ w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *q
                      stream);
 }
 
+w8a8_status w8a8_selftest_wait_timeout(uint32_t limit_us, w8a8_stream_t stream) {
+    if (limit_us == 0 || limit_us > 2000000u) return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_selftest_wait(static_cast<unsigned long long>(limit_us) * 1000ull,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w8a8_status w8a8_device_error(uint64_t *code_out, int clear) {
     if (!code_out) return W8A8_ERR_INVALID_ARG;
     unsigned long long v = 0;

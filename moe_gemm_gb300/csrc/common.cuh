@@ -13,8 +13,10 @@ namespace w8a8 {
 // error word (first writer wins). Layout of the 64-bit code:
 //   bits 56..63 kernel id, 48..55 role, 32..47 wait site, 0..31 CTA index.
 
-enum KernelId : unsigned { KID_GEMM = 1 };
-enum Role : unsigned { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_CONVERT = 3, ROLE_EPILOGUE = 4 };
+enum KernelId : unsigned { KID_GEMM = 1, KID_SELFTEST = 2 };
+enum Role : unsigned {
+    ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_CONVERT = 3, ROLE_EPILOGUE = 4, ROLE_SELFTEST = 5
+};
 
 // A wait gives up after this many nanoseconds of %globaltimer time. Every wait
 // in these kernels normally completes within microseconds.
@@ -107,18 +109,21 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Waits for the phase with the given parity to complete. Returns false (and
-// records a device error) if the wait gives up after kWaitLimitNs, or if
-// another role of this CTA has already given up (*abort != 0).
+// records a device error) if the wait gives up after limit_ns (kWaitLimitNs
+// unless given), or if another role of this CTA has already given up
+// (*abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          unsigned long long *err, unsigned role, unsigned site) {
+                                          unsigned long long *err, unsigned role, unsigned site,
+                                          unsigned long long limit_ns = kWaitLimitNs,
+                                          unsigned kid = KID_GEMM) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
-            record_device_error(err, KID_GEMM, role, site);
+            record_device_error(err, kid, role, site);
             return false;
         }
     }

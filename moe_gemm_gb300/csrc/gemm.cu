@@ -1490,6 +1490,23 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
 }
 
+// Diagnostic of the bounded-wait error path: one thread arms an mbarrier for
+// 16 bytes that no copy will ever deliver (a mis-sized expect-tx) and waits on
+// it through the same bounded wait the GEMM roles use, with a short limit.
+// The wait gives up, writes its code into the error word and the kernel
+// returns; nothing traps or hangs, and no copy is left in flight.
+__global__ void selftest_wait_kernel(unsigned long long *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbarrier_init();
+        mbar_arrive_expect_tx(smem_u32(&bar), 16);
+        mbar_wait(smem_u32(&bar), 0, &abort_flag, err, ROLE_SELFTEST, 1, limit_ns, KID_SELFTEST);
+    }
+}
+
 // ------------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1783,6 +1800,14 @@ cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream)
                    : launch_kernel<w8a8_gemm_narrow_kernel<false, false>>(pr, ps, num_sms, stream);
     return dbg ? launch_kernel<w8a8_gemm_kernel<true>>(pr, ps, num_sms, stream)
                : launch_kernel<w8a8_gemm_kernel<false>>(pr, ps, num_sms, stream);
+}
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
+    unsigned long long *err = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
+    if (e != cudaSuccess) return e;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t read_device_error(unsigned long long *value, bool clear) {

@@ -65,6 +65,10 @@ constexpr int kMaxExperts = 1024;
 
 cudaError_t launch_gemm(const GemmProblem &p, int num_sms, cudaStream_t stream);
 
+// Launches the bounded-wait diagnostic (see gemm.cu): its wait gives up after
+// limit_ns and records a code in the device error word.
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
+
 // Device error word of the GEMM kernel (read/clear; synchronising).
 cudaError_t read_device_error(unsigned long long *value, bool clear);
 

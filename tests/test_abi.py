@@ -133,3 +133,11 @@ def test_no_device_gives_cuda_error(lib):
     # Valid arguments reach the device check, which fails without a GPU; the
     # fake pointers are never used.
     assert lib.w8a8_quant_act(FAKE, 4, 64, 64, FAKE, 64, FAKE, None) in (CUDA_ERR, UNSUPPORTED)
+
+
+def test_selftest_wait_validation(lib):
+    lib.w8a8_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+    lib.w8a8_selftest_wait_timeout.restype = ctypes.c_int
+    # refused on the host: never launches
+    assert lib.w8a8_selftest_wait_timeout(0, None) == INVALID
+    assert lib.w8a8_selftest_wait_timeout(2000001, None) == INVALID
