@@ -15,10 +15,10 @@
 //    Each group gets a FRESH accumulator in tensor memory, so the tensor core
 //    never adds numbers that are not exactly representable.
 //  * Swap-AB: the MMA's M side (128 TMEM lanes) is 128 weight rows n, its N
-//    side is a batch of up to 128 token rows. So the weight scale sw[n, g] is
+//    side is a tile of up to 128 token rows. So the weight scale sw[n, g] is
 //    one register per epilogue thread.
-//  * Weights stay int8 in HBM. TMA lands each 128 x 128 int8 weight tile in
-//    shared memory; a converter warpgroup widens it in registers and writes
+//  * Weights stay int8 in HBM. TMA lands 128 x 256 int8 weight stages in
+//    shared memory; a converter warpgroup widens them in registers and writes
 //    the fp16 A operand straight into tensor memory (tcgen05.st), so the
 //    widening costs no shared-memory bandwidth beyond one read.
 //  * Token operand: an fp16 copy of the int8 codes (written by a staging
@@ -26,16 +26,12 @@
 //    This kernel is launched as a programmatic dependent of the staging
 //    kernel: only the token producer waits for it (griddepcontrol.wait); the
 //    weight stream, the conversion and all set-up start at once.
-//  * Weight tiles and token tiles have separate producers and pipelines whose
-//    depths are chosen per call; narrow token batches (decode) leave room for
-//    ~11 weight tiles in flight per SM.
-//  * Narrow token tiles (<= 64 rows: decode, MoE experts) run a kernel that
-//    moves two K groups per pipeline step, halving the per-group hand-offs.
-//  * Up to 8 partial buffers in TMEM (as many batches as fit in 256 columns)
-//    rotate between the MMA issuer and two epilogue warpgroups, which drain
-//    them (tcgen05.ld), fma the partial with sw[n,g] into register
-//    accumulators, and at the end of the tile multiply by sa[m] and store
-//    BF16 (round to nearest even) or FP32.
+//  * Two K groups move through the pipeline per step (one barrier hand-off,
+//    one commit and one epilogue wait per 32 KB of weights); see the kernel.
+//  * Epilogue warpgroups drain the partial buffers (tcgen05.ld), fma each
+//    partial with sw[n,g] into register accumulators in K order, and at the
+//    end of the tile multiply by sa[m] and store BF16 (round to nearest even)
+//    or FP32.
 //  * Persistent CTAs walk a tile list built on the device from the expert
 //    offsets (no host read, graph-capture safe). Within an (expert, weight
 //    tile) the token tiles are consecutive so CTAs running together share the
@@ -43,6 +39,9 @@
 //  * Every mbarrier wait is bounded (%globaltimer); a wait that gives up sets
 //    the library error word and the CTA drains its copies, frees TMEM and
 //    returns.
+//  * Dense calls of at most 8 token rows run a CUDA-core kernel instead
+//    (w8a8_gemv_kernel, below): exact int8 dot products (dp4a) cost less than
+//    the weight stream there.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -63,16 +62,14 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kMaxAStages = 12;     // weight tiles in flight (shared memory)
-constexpr int kMaxBStages = 8;      // token batches in flight
-constexpr int kTmemSlots = 4;       // fp16 weight operands resident in TMEM
-constexpr int kMaxPBufs = 8;        // fp32 group-partial buffers in TMEM columns [0, 256)
+constexpr int kMaxBStages = 8;      // token stages in flight
 constexpr int kTileN = 128;         // weight rows per tile = MMA M = TMEM lanes
-constexpr int kGroupK = 128;        // K elements per scale group = per pipeline stage
-constexpr int kMaxBatchRows = 128;  // token rows per MMA batch (MMA N <= 128)
+constexpr int kGroupK = 128;        // K elements per scale group
+constexpr int kMaxBatchRows = 128;  // token rows per tile (MMA N <= 128)
 constexpr int kBoxRows = 32;        // token rows per TMA box
 constexpr int kAStageBytes = kTileN * kGroupK;   // 16 KB int8
 constexpr int kTmemCols = 512;
-constexpr int kTmemA0 = 256;        // TMEM weight slot s at columns [256 + 64 s, +64)
+constexpr int kTmemA0 = 256;        // TMEM fp16 weight operands from column 256
 constexpr int kEpiRegs = 200;       // 256 threads x 200 + 256 x 56 = 512 x 128 at launch
 constexpr int kOtherRegs = 56;
 constexpr int kSmemLimit = 232448;
@@ -85,20 +82,6 @@ constexpr int kOffTab = kOffMisc + 64;
 constexpr int kTabBytes = 3 * (kMaxExperts + 1) * 4;
 constexpr int kOffStages = ((kOffTab + kTabBytes + 1023) / 1024) * 1024;
 static_assert((kThreads / 2) * (kEpiRegs + kOtherRegs) == 65536, "register split");
-
-struct BarIdx {
-    static constexpr int a_full = 0;                              // TMA -> weight converter
-    static constexpr int a_empty = a_full + kMaxAStages;          // weight converter -> TMA
-    static constexpr int ready = a_empty + kMaxAStages;           // converter + admission -> MMA
-    static constexpr int ta_empty = ready + kTmemSlots;           // MMA -> weight converter
-    static constexpr int b_full = ta_empty + kTmemSlots;          // TMA -> MMA
-    static constexpr int b_empty = b_full + kMaxBStages;          // MMA -> TMA
-    static constexpr int p_full = b_empty + kMaxBStages;          // MMA -> epilogue
-    static constexpr int p_empty = p_full + kMaxPBufs;            // epilogue -> MMA
-    static constexpr int drain = p_empty + kMaxPBufs;             // MMA completion at exit
-    static constexpr int count = drain + 1;
-};
-static_assert(BarIdx::count <= 128, "barrier area");
 
 struct KParams {
     const float *sa;
@@ -198,11 +181,6 @@ __device__ __forceinline__ void build_tile_table(const KParams &p, int tt, int l
     }
 }
 
-// Token rows of MMA batch h of a tile with n_eff (multiple of 16) rows.
-__device__ __forceinline__ int batch_rows(int n_eff, int nb, int h, int b_rows) {
-    return nb == 2 ? (h == 0 ? b_rows : n_eff - b_rows) : n_eff;
-}
-
 // Bounded wait used only on the exit path, independent of the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer_ns();
@@ -217,407 +195,25 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, uint32_t issued, uint3
         drain_wait(bar0 + 8u * (i % slots), (i / slots) & 1u);
 }
 
-// Warp roles: 0 weight TMA producer, 1 MMA issuer (+ TMEM allocation), 2 token
-// TMA producer, 3 admission (token tiles landed, partial buffers free), 4-7
-// weight converter, 8-15 epilogue (two warpgroups).
-// kDebug additionally writes every exact group partial.
-// Used for tiles of more than 64 token rows; narrow tiles take
-// w8a8_gemm_narrow_kernel below.
-template <bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1)
-w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                 const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    uint8_t *smem = smem_raw + (base - raw_addr);
-
-    const uint32_t SA = static_cast<uint32_t>(p.a_stages);
-    const uint32_t SB = static_cast<uint32_t>(p.b_stages);
-    const int b_rows = p.b_rows;
-    const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
-    const uint32_t b_stage_bytes = 2u * b_atom_bytes;
-    const uint32_t sA = base + kOffStages;
-    const uint32_t sB = sA + SA * kAStageBytes;
-    const uint32_t sBar = base + kOffBar;
-    volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
-    volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
-    int *s_base = reinterpret_cast<int *>(smem + kOffTab);
-    int *s_lo = s_base + (kMaxExperts + 1);
-    int *s_cnt = s_lo + (kMaxExperts + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int tt = p.tile_tokens;
-    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
-
-    // ------------------------------------------------------------ set-up
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kMaxAStages; ++i) {
-            mbar_init(bar(BarIdx::a_full + i), 1);
-            mbar_init(bar(BarIdx::a_empty + i), 4);
-        }
-        for (int i = 0; i < kTmemSlots; ++i) {
-            mbar_init(bar(BarIdx::ready + i), 5);
-            mbar_init(bar(BarIdx::ta_empty + i), 1);
-        }
-        for (int i = 0; i < kMaxBStages; ++i) {
-            mbar_init(bar(BarIdx::b_full + i), 1);
-            mbar_init(bar(BarIdx::b_empty + i), 1);
-        }
-        for (int i = 0; i < kMaxPBufs; ++i) {
-            mbar_init(bar(BarIdx::p_full + i), 1);
-            mbar_init(bar(BarIdx::p_empty + i), 8);
-        }
-        mbar_init(bar(BarIdx::drain), 1);
-        *s_abort = 0;
-        fence_mbarrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmap_w);
-        tma_prefetch_desc(&tmap_x);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == 2) build_tile_table(p, tt, lane, s_base, s_lo, s_cnt, s_total);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    const uint32_t tmem_base = *s_tmem_base;
-    const int total = *s_total;
-    const int G = p.G;
-    const int wg = warp >> 2;
-
-    // Register split: each setmaxnreg sits inside its role's branch so that
-    // the register allocator sees only that role's code in the region.
-    if (warp < 4) {
-        setmaxnreg_dec<kOtherRegs>();
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------- weight TMA producer
-            Ring a;
-            uint32_t issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int wrow = ti.e * p.N + ti.n0;
-                for (int g = 0; g < G; ++g) {
-                    if (!mbar_wait(bar(BarIdx::a_empty + a.idx), a.phase ^ 1u, s_abort, p.err,
-                                   ROLE_PRODUCER, 1)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(BarIdx::a_full + a.idx), kAStageBytes);
-                    tma_load_2d(sA + a.idx * kAStageBytes, &tmap_w, g * kGroupK, wrow,
-                                bar(BarIdx::a_full + a.idx));
-                    a.advance(SA);
-                    ++issued;
-                }
-            }
-            if (!ok) drain_ring(bar(BarIdx::a_full), issued, SA);
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------- MMA issuer
-            // One wait per group (operand ready: weights in TMEM, token tiles
-            // landed, partial buffers free), then the group's MMAs and commits.
-            Ring ts, b, pr;
-            const uint32_t PB = static_cast<uint32_t>(p.p_bufs);
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const int nb = n_eff > b_rows ? 2 : 1;
-                for (int g = 0; g < G; ++g) {
-                    if (!mbar_wait(bar(BarIdx::ready + ts.idx), ts.phase, s_abort, p.err, ROLE_MMA,
-                                   1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_tmem = tmem_base + kTmemA0 + ts.idx * 64u;
-                    for (int h = 0; h < nb; ++h) {
-                        const uint32_t idesc = idesc_f16_f32(
-                            kTileN, static_cast<uint32_t>(batch_rows(n_eff, nb, h, b_rows)));
-                        const uint32_t d_tmem = tmem_base + pr.idx * static_cast<uint32_t>(b_rows);
-                        // Descriptors of the 8 k-steps differ only in the start-address
-                        // field (address >> 4, no carry out of its 14 bits below 256 KB).
-                        const uint64_t bdesc0 = smem_desc_sw128(sB + b.idx * b_stage_bytes);
-                        const uint64_t atom_step = b_atom_bytes >> 4;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t bdesc =
-                                bdesc0 + (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
-                            mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(bar(BarIdx::p_full + pr.idx));
-                        mma_commit(bar(BarIdx::b_empty + b.idx));
-                        b.advance(SB);
-                        pr.advance(PB);
-                    }
-                    mma_commit(bar(BarIdx::ta_empty + ts.idx));
-                    ts.advance(kTmemSlots);
-                }
-            }
-            // All MMAs issued by this thread complete before TMEM is freed.
-            mma_commit(bar(BarIdx::drain));
-            drain_wait(bar(BarIdx::drain), 0);
-        } else if (warp == 3 && lane == 0) {
-            // --------------------------------------------------- admission
-            // Waits, in group order, for the group's token tiles and for the
-            // partial buffers its batches will overwrite (drained by the
-            // epilogue), then adds its arrival to the group's operand-ready
-            // barrier, which the four converter warps complete.
-            Ring ts, b, pr;
-            const uint32_t PB = static_cast<uint32_t>(p.p_bufs);
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const int nb = n_eff > b_rows ? 2 : 1;
-                for (int g = 0; ok && g < G; ++g) {
-                    for (int h = 0; h < nb; ++h) {
-                        if (!mbar_wait(bar(BarIdx::b_full + b.idx), b.phase, s_abort, p.err,
-                                       ROLE_MMA, 2) ||
-                            !mbar_wait(bar(BarIdx::p_empty + pr.idx), pr.phase ^ 1u, s_abort,
-                                       p.err, ROLE_MMA, 3)) {
-                            ok = false;
-                            break;
-                        }
-                        b.advance(SB);
-                        pr.advance(PB);
-                    }
-                    if (!ok) break;
-                    mbar_arrive(bar(BarIdx::ready + ts.idx));
-                    ts.advance(kTmemSlots);
-                }
-            }
-        } else if (warp == 2 && lane == 0) {
-            // -------------------------------------------- token TMA producer
-            // The fp16 token codes are written by the kernel launched just
-            // before this one: wait for it (and only here) before loading them.
-            griddep_wait();
-            Ring b;
-            uint32_t issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                const int n_eff = (ti.rows + 15) & ~15;
-                const int nb = n_eff > b_rows ? 2 : 1;
-                for (int g = 0; ok && g < G; ++g) {
-                    for (int h = 0; h < nb; ++h) {
-                        const int rows_h = batch_rows(n_eff, nb, h, b_rows);
-                        const int nbox = (rows_h + kBoxRows - 1) / kBoxRows;
-                        if (!mbar_wait(bar(BarIdx::b_empty + b.idx), b.phase ^ 1u, s_abort, p.err,
-                                       ROLE_PRODUCER, 2)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t stage = sB + b.idx * b_stage_bytes;
-                        mbar_arrive_expect_tx(bar(BarIdx::b_full + b.idx),
-                                              2u * nbox * kBoxRows * 128u);
-                        for (int a = 0; a < 2; ++a)
-                            for (int i = 0; i < nbox; ++i)
-                                tma_load_2d(stage + a * b_atom_bytes + i * kBoxRows * 128, &tmap_x,
-                                            g * kGroupK + a * 64, ti.m0 + h * b_rows + i * kBoxRows,
-                                            bar(BarIdx::b_full + b.idx));
-                        b.advance(SB);
-                        ++issued;
-                    }
-                }
-            }
-            if (!ok) drain_ring(bar(BarIdx::b_full), issued, SB);
-        }
-    } else if (wg == 1) {
-        // --------------------------------------- weight converter (A -> TMEM)
-        setmaxnreg_dec<kOtherRegs>();
-        const int row = threadIdx.x - 128;     // weight row within the tile = TMEM lane
-        const int q = warp & 3;                // TMEM lane quarter of this warp
-        Ring a, ts;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            for (int g = 0; g < G; ++g) {
-                if (!mbar_wait(bar(BarIdx::a_full + a.idx), a.phase, s_abort, p.err, ROLE_CONVERT,
-                               1) ||
-                    !mbar_wait(bar(BarIdx::ta_empty + ts.idx), ts.phase ^ 1u, s_abort, p.err,
-                               ROLE_CONVERT, 2)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint8_t *rowp = smem + kOffStages + a.idx * kAStageBytes + row * 128;
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kTmemA0 +
-                                       ts.idx * 64u;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t r16[16];
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * j + cc;  // 16-byte chunk = one MMA k-step
-                        const uint4 v =
-                            *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
-                        i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
-                        i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
-                        i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
-                        i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
-                    }
-                    tmem_st_16cols(taddr + j * 16, r16);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BarIdx::a_empty + a.idx));
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BarIdx::ready + ts.idx));
-                a.advance(SA);
-                ts.advance(kTmemSlots);
-            }
-        }
-    } else {
-        // -------------------------------------------------------- epilogue
-        setmaxnreg_inc<kEpiRegs>();
-        const int ewg = wg - 2;                // 0 or 1
-        const int q = warp & 3;
-        const int lrow = q * 32 + lane;        // weight row within the tile = TMEM lane
-        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        const uint32_t PB = static_cast<uint32_t>(p.p_bufs);
-        const int cpb = b_rows / 32;           // 32-column chunks per batch
-        float acc[4][32];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[i][j] = 0.0f;
-        Ring pr;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-            const int n_eff = (ti.rows + 15) & ~15;
-            const int nb = n_eff > b_rows ? 2 : 1;
-            const int n_local = ti.n0 + lrow;
-            const bool n_ok = n_local < p.N;
-            // Column ownership: with two batches, warpgroup w takes batch w;
-            // with one, the 32-column chunks alternate between the warpgroups.
-            // Slot i of acc[] holds tile columns [32 chunk(i), +32).
-            auto chunk_of = [&](int i) { return nb == 2 ? ewg * cpb + i : 2 * i + ewg; };
-            auto owned = [&](int i) {
-                return (nb == 2 ? i < cpb : true) && chunk_of(i) * 32 < n_eff;
-            };
-            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
-            // Weight scales of this row: the current quad of groups in cur,
-            // the next quad in nxt, loaded a whole quad ahead (one 16-byte load
-            // when the row is 16-byte aligned) and only copied at a quad
-            // boundary, so no load latency sits in the drain loop.
-            const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
-            auto load_quad = [&](int g) -> float4 {
-                float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (!n_ok) return v;
-                if (vec_sw) {
-                    if (g < G) v = ldg_nc_f32x4_now(swp + g);
-                } else {
-                    if (g < G) v.x = ldg_nc_f32_now(swp + g);
-                    if (g + 1 < G) v.y = ldg_nc_f32_now(swp + g + 1);
-                    if (g + 2 < G) v.z = ldg_nc_f32_now(swp + g + 2);
-                    if (g + 3 < G) v.w = ldg_nc_f32_now(swp + g + 3);
-                }
-                return v;
-            };
-            float4 cur = load_quad(0);
-            float4 nxt = load_quad(4);
-            for (int g = 0; ok && g < G; ++g) {
-                const int jq = g & 3;
-                if (jq == 0 && g > 0) {
-                    cur = nxt;
-                    nxt = load_quad(g + 4);
-                }
-                const float s = jq == 0 ? cur.x : (jq == 1 ? cur.y : (jq == 2 ? cur.z : cur.w));
-                for (int h = 0; h < nb; ++h) {
-                    if (!mbar_wait(bar(BarIdx::p_full + pr.idx), pr.phase, s_abort, p.err,
-                                   ROLE_EPILOGUE, 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (nb == 1 || h == ewg) {
-                        const uint32_t buf = lane_base + pr.idx * static_cast<uint32_t>(b_rows);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            if (owned(i)) {
-                                const int col = nb == 2 ? i * 32 : chunk_of(i) * 32;
-                                uint32_t v[32];
-                                tmem_ld_32cols_sync(buf + col, v);
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    acc[i][j] = fmaf(__uint_as_float(v[j]), s, acc[i][j]);
-                                if (kDebug && n_ok) {
-#pragma unroll
-                                    for (int j = 0; j < 32; ++j) {
-                                        const int tcol = chunk_of(i) * 32 + j;
-                                        if (tcol < ti.rows)
-                                            p.dbg[(static_cast<size_t>(ti.m0 + tcol) * p.N +
-                                                   n_local) * G + g] =
-                                                __float2int_rn(__uint_as_float(v[j]));
-                                    }
-                                }
-                            }
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_relaxed(bar(BarIdx::p_empty + pr.idx));
-                    pr.advance(PB);
-                }
-            }
-            if (!ok) break;
-            // Token scale and store: Y[m, n] = sa[m] * acc.
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (owned(i) && n_ok) {
-                    const int c0 = chunk_of(i) * 32;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = c0 + j;
-                        if (col < ti.rows) {
-                            const int m = ti.m0 + col;
-                            const float out = acc[i][j] * __ldg(p.sa + m);
-                            const size_t idx = static_cast<size_t>(m) * p.N + n_local;
-                            if (p.out_fp32)
-                                static_cast<float *>(p.y)[idx] = out;
-                            else
-                                static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[i][j] = 0.0f;
-            }
-        }
-    }
-
-    __syncwarp();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
-    }
-}
-
-
 // =============================================================================
-// Narrow tiles (every tile is one MMA batch of at most 64 token rows: decode
-// shapes and MoE experts). Two K groups move through the pipeline per step, so
-// every hand-off (barrier wait, arrive, commit) is paid once per 32 KB of
-// weights instead of once per 16 KB:
+// The tensor-core GEMM: every tile is one MMA batch of up to 128 token rows
+// (decode shapes, MoE experts, 128-row tiles of large problems). Two K groups
+// move through the pipeline per step, so every hand-off (barrier wait,
+// arrive, commit) is paid once per 32 KB of weights instead of once per 16 KB:
 //  * a weight stage is 128 rows x 256 K int8 (two TMA boxes, 256 contiguous
 //    bytes per weight row);
 //  * a step slot (2 of them) holds the fp16 A operands of both groups in TMEM
-//    (128 columns), their two partial buffers (2 x b_rows columns) and the
-//    step's token tiles in shared memory; one commit per step ("done") frees
-//    all of it and tells the epilogue the step's partials are ready;
-//  * each epilogue warpgroup owns one 32-column chunk of the token tile and
+//    (128 columns), their two partial buffers (2 x b_rows columns; one pair
+//    shared by all steps in the wide form, see below) and the step's token
+//    tiles in shared memory; one commit per step ("done") frees them and
+//    tells the epilogue the step's partials are ready;
+//  * each epilogue warpgroup owns 32-column chunks of the token tile and
 //    drains both groups of a step with two loads and a single wait.
-// Warp roles as in w8a8_gemm_kernel.
+// Warp roles (512 threads): 0 weight TMA producer; 1 MMA issuer and TMEM
+// allocation; 2 token TMA producer (the only thread that waits for the
+// staging kernel); 3 admission (token tiles landed, partial buffers free ->
+// "ready"); 4-7 converter (int8 -> fp16 A operand in TMEM); 8-15 epilogue.
+// kDebug additionally writes every exact group partial.
 // =============================================================================
 constexpr int kNarrowSlots = 2;
 constexpr int kWideOffTab = kOffMisc + 64;       // wide tiles: tile table in the fixed area
@@ -1556,60 +1152,37 @@ bool encode_2d_plain(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_by
 // stage counts, filling shared memory with weight stages after the token stages.
 struct PipeShape {
     int b_rows, tile_tokens, b_stages, a_stages, p_bufs, smem_bytes;
-    bool narrow;    // one batch of <= 64 rows per tile: w8a8_gemm_narrow_kernel
-    bool wide;      // one batch of 96 or 128 rows per tile: its kWide form
+    bool narrow;    // tiles of <= 64 token rows: w8a8_gemm_narrow_kernel
+    bool wide;      // tiles of 96 or 128 token rows: its kWide form
 };
 
 PipeShape choose_pipe(const GemmProblem &pr) {
     PipeShape s;
-    if (pr.offsets == nullptr && pr.R <= kMaxBatchRows) {
-        s.b_rows = static_cast<int>((pr.R + kBoxRows - 1) / kBoxRows * kBoxRows);
-        s.tile_tokens = s.b_rows;
-    } else if (pr.offsets == nullptr) {
-        s.b_rows = kMaxBatchRows;
-        s.tile_tokens = 2 * kMaxBatchRows;
+    if (pr.offsets == nullptr) {
+        // Dense: one tile of the rounded-up token count up to 128 rows,
+        // 128-row tiles beyond.
+        s.b_rows = pr.R <= kMaxBatchRows
+                       ? static_cast<int>((pr.R + kBoxRows - 1) / kBoxRows * kBoxRows)
+                       : kMaxBatchRows;
     } else {
-        // Expert tiles of 128 rows when the tile table fits the wide kernel's
+        // Expert tiles of 128 rows when the tile table fits the wide form's
         // fixed area (fewer tiles, and fewer weight passes, for experts with
         // 65..128 routed rows), else 64.
         s.b_rows = pr.E <= kWideMaxExperts ? kMaxBatchRows : 64;
-        s.tile_tokens = s.b_rows;
     }
-    s.narrow = s.tile_tokens == s.b_rows && s.b_rows <= 64;
-    s.wide = s.tile_tokens == s.b_rows && s.b_rows > 64;
-    if (s.wide) {
-        // One partial slot; two step slots of token tiles (b_rows x 512 B);
-        // weight stages after the 2 KB fixed area.
-        s.p_bufs = 2;
-        s.b_stages = kNarrowSlots;
-        const int b_slot_bytes = 4 * s.b_rows * 128;
-        const int avail = kSmemLimit - 1024 - kWideOffStages - kNarrowSlots * b_slot_bytes;
-        s.a_stages = avail / kNarrowAStageBytes;
-        if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
-        s.smem_bytes = kWideOffStages + s.a_stages * kNarrowAStageBytes +
-                       kNarrowSlots * b_slot_bytes + 1024;
-        return s;
-    }
-    if (s.narrow) {
-        // Two step slots, each holding the token tiles of two K groups.
-        s.p_bufs = 2 * kNarrowSlots;
-        s.b_stages = kNarrowSlots;
-        const int b_slot_bytes = 4 * s.b_rows * 128;
-        const int avail = kSmemLimit - 1024 - kOffStages - kNarrowSlots * b_slot_bytes;
-        s.a_stages = avail / kNarrowAStageBytes;
-        if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
-        s.smem_bytes = kOffStages + s.a_stages * kNarrowAStageBytes +
-                       kNarrowSlots * b_slot_bytes + 1024;
-        return s;
-    }
-    s.p_bufs = 256 / s.b_rows;
-    if (s.p_bufs > kMaxPBufs) s.p_bufs = kMaxPBufs;
-    s.b_stages = 4;
-    const int b_stage_bytes = s.b_rows * 256;
-    const int avail = kSmemLimit - 1024 - kOffStages - s.b_stages * b_stage_bytes;
-    s.a_stages = avail / kAStageBytes;
+    s.tile_tokens = s.b_rows;
+    s.narrow = s.b_rows <= 64;
+    s.wide = !s.narrow;
+    s.p_bufs = 2;
+    s.b_stages = kNarrowSlots;   // two step slots of token tiles (b_rows x 512 B)
+    const int b_slot_bytes = 4 * s.b_rows * 128;
+    // Weight stages after the fixed area: 14 KB (tile table for up to 1024
+    // experts) for narrow tiles, 2 KB for wide ones.
+    const int off = s.wide ? kWideOffStages : kOffStages;
+    const int avail = kSmemLimit - 1024 - off - kNarrowSlots * b_slot_bytes;
+    s.a_stages = avail / kNarrowAStageBytes;
     if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
-    s.smem_bytes = kOffStages + s.a_stages * kAStageBytes + s.b_stages * b_stage_bytes + 1024;
+    s.smem_bytes = off + s.a_stages * kNarrowAStageBytes + kNarrowSlots * b_slot_bytes + 1024;
     return s;
 }
 
@@ -1795,11 +1368,8 @@ cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream)
         return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true, true>>(pr, ps, num_sms, stream)
                    : launch_kernel<w8a8_gemm_narrow_kernel<false, true>>(pr, ps, num_sms, stream);
     }
-    if (ps.narrow)
-        return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true, false>>(pr, ps, num_sms, stream)
-                   : launch_kernel<w8a8_gemm_narrow_kernel<false, false>>(pr, ps, num_sms, stream);
-    return dbg ? launch_kernel<w8a8_gemm_kernel<true>>(pr, ps, num_sms, stream)
-               : launch_kernel<w8a8_gemm_kernel<false>>(pr, ps, num_sms, stream);
+    return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true, false>>(pr, ps, num_sms, stream)
+               : launch_kernel<w8a8_gemm_narrow_kernel<false, false>>(pr, ps, num_sms, stream);
 }
 
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
