@@ -86,7 +86,7 @@ w8a8_status w8a8_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, 
 /*
  * Bytes of device workspace w8a8_gemm asks for: an fp16 copy of the M x K
  * int8 activation codes (the tensor-core operand), rounded up to 256 bytes,
- * then, when 5 <= M <= 8, a split area of 1280 + 160 * 2 * M * 128 * 4
+ * then, when 5 <= M <= 64, a split area of 1280 + 160 * 2 * M * 128 * 4
  * bytes (rounded up to 256) in which up to 160 CTAs exchange FP32 partial
  * sums of weight tiles whose K range they share. 0 when M == 0.
  * The split area is optional: a workspace that holds only the staging copy
@@ -112,7 +112,7 @@ size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * K must be a positive multiple of 128; N >= 1. M == 0 is a no-op.
  * The group sums are exact integers; Y is accumulated in FP32 over the
  * groups in K order, acc = fma(P_g, sw[n,g], acc), and Y = sa[m] * acc. When
- * a tile's K range is split into n pieces (only for 5 <= M <= 8 with the
+ * a tile's K range is split into n pieces (only for 5 <= M <= 64 with the
  * split area; n <= ceil(G/2), otherwise n = 1), each piece accumulates its
  * groups from zero and the pieces are added in K order, so
  *   |Y - Y*| <= (G + n + 1) * 2^-24 * sum_g |sa*sw*P_g|  for the exact Y*,

@@ -79,8 +79,8 @@ w8a8_status check_gemm(const int8_t *qa, const float *sa, const void *offsets, c
     return W8A8_OK;
 }
 
-// Full workspace: the staging copy, then (GEMV calls of 5..8 token rows) the
-// stream-K split area at the next 256-byte boundary.
+// Full workspace: the staging copy, then (dense calls of 5..64 token rows)
+// the stream-K split area at the next 256-byte boundary.
 size_t workspace_bytes_for(int64_t R, int64_t K, bool grouped) {
     if (R <= 0) return 0;
     return staging_bytes(R, K) + round_up(w8a8::sk_area_bytes(R, grouped), kWsAlign);
@@ -112,7 +112,8 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
         // counters need zeroing.
         if (p.sk_cnt != nullptr) e = w8a8::launch_zero_counters(p.sk_cnt, 2 * w8a8::kSkMaxCtas, s);
     } else {
-        e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s);
+        e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s, p.sk_cnt,
+                                     p.sk_cnt != nullptr ? 2 * w8a8::kSkMaxCtas : 0);
     }
     if (e != cudaSuccess) return W8A8_ERR_CUDA;
     p.qa = qa;

@@ -72,6 +72,10 @@ constexpr int kTmemCols = 512;
 constexpr int kTmemA0 = 256;        // TMEM fp16 weight operands from column 256
 constexpr int kEpiRegs = 200;       // 256 threads x 200 + 256 x 56 = 512 x 128 at launch
 constexpr int kOtherRegs = 56;
+// Narrow tiles (one 32-column accumulator per epilogue thread) give the other
+// roles room for the stream-K bookkeeping.
+constexpr int kSplitEpiRegs = 184;
+constexpr int kSplitOtherRegs = 72;
 constexpr int kSmemLimit = 232448;
 
 // Shared memory: a fixed area (barriers, flags, tile table), then the weight
@@ -82,6 +86,7 @@ constexpr int kOffTab = kOffMisc + 64;
 constexpr int kTabBytes = 3 * (kMaxExperts + 1) * 4;
 constexpr int kOffStages = ((kOffTab + kTabBytes + 1023) / 1024) * 1024;
 static_assert((kThreads / 2) * (kEpiRegs + kOtherRegs) == 65536, "register split");
+static_assert((kThreads / 2) * (kSplitEpiRegs + kSplitOtherRegs) == 65536, "register split");
 
 struct KParams {
     const float *sa;
@@ -99,7 +104,7 @@ struct KParams {
     int p_bufs;         // partial buffers in TMEM (p_bufs * b_rows <= 256)
     int tab_off;        // byte offset of the tile table in shared memory
     unsigned long long *err;
-    // Stream-K split of the CUDA-core GEMV (null sk_cnt: whole tiles only).
+    // Stream-K split of dense calls (null sk_cnt: whole tiles only).
     int *sk_cnt;        // [2 * grid] arrival counters of split tiles, zero at launch
     float *sk_part;     // [grid][2][sk_ld][128] FP32 piece partials
     int sk_ld;          // token columns per partial slot
@@ -195,6 +200,99 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, uint32_t issued, uint3
         drain_wait(bar0 + 8u * (i % slots), (i / slots) & 1u);
 }
 
+// Stream-K work split (dense calls, when the caller's workspace has room for
+// it): the tiles that fill whole waves go round-robin to the CTAs; the steps
+// of the tiles left over are divided into equal contiguous ranges, one per
+// CTA, so that every SM does the same number of steps. A CTA works on its
+// range first and on its whole tiles after it. A tile whose steps fall into
+// several ranges is finished by the CTA that completes its piece last: each
+// piece stores its FP32 partial sum (before the token scale), and after its
+// last step the CTA bumps the arrival counter of each of its split tiles
+// (deferred publish: one fence for all of them); the last arrival adds the
+// pieces in K order (so the result does not depend on arrival order),
+// applies sa and stores y. No CTA waits for another.
+//
+// WorkPlan: this CTA's share of the work: the step range [u0, u1) of the
+// stream-K part (steps of tiles [dp, total), S per tile, numbered from 0 at
+// tile dp, split over g_sk CTAs), then round-robin whole tiles of [0, dp).
+// All of it in 32-bit arithmetic: U < grid * S fits an int, and
+// floor(c U / g) is formed from U = q g + r as c q + floor(c r / g).
+struct WorkPlan {
+    int dp, S, g_sk, U, u0, u1;
+};
+
+__device__ __forceinline__ WorkPlan make_plan(int total, int G, bool stream_k) {
+    WorkPlan w;
+    w.S = (G + 1) >> 1;
+    const int grid = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    w.u0 = w.u1 = 0;
+    if (!stream_k) {
+        w.dp = total;
+        w.g_sk = 0;
+        w.U = 0;
+        return w;
+    }
+    w.dp = (total / grid) * grid;   // whole waves; fewer than grid tiles are split
+    w.U = (total - w.dp) * w.S;
+    w.g_sk = w.U < grid ? w.U : grid;
+    if (c < w.g_sk) {
+        const int q = w.U / w.g_sk, r = w.U - q * w.g_sk;
+        w.u0 = c * q + (c * r) / w.g_sk;
+        w.u1 = (c + 1) * q + ((c + 1) * r) / w.g_sk;
+    }
+    return w;
+}
+
+// The stream-K CTA whose step range contains step x (0 <= x < U): the largest
+// c with floor(c U / g) <= x, i.e. c U < (x + 1) g. A float estimate is
+// corrected with exact 64-bit products.
+__device__ __forceinline__ int sk_owner(int x, const WorkPlan &w) {
+    const long long rhs = static_cast<long long>(x + 1) * w.g_sk;
+    int c = static_cast<int>(__fdividef(static_cast<float>(rhs), static_cast<float>(w.U)));
+    c = min(max(c, 0), w.g_sk - 1);
+    while (c > 0 && static_cast<long long>(c) * w.U >= rhs) --c;
+    while (c + 1 < w.g_sk && static_cast<long long>(c + 1) * w.U < rhs) ++c;
+    return c;
+}
+
+// Calls f(tile, s0, s1) for every piece of this CTA in order; f returns false
+// to stop. A stream-K range is shorter than a tile (fewer than grid tiles are
+// left over), so it holds at most two pieces: they are formed up front and
+// the walk is one counted loop with one call site. (A walk that advanced a
+// step cursor through the range made every pipeline step ~15% slower in all
+// roles, measured.)
+template <class F>
+__device__ __forceinline__ void for_each_piece(const WorkPlan &w, F &&f) {
+    int t0 = 0, a0 = 0, b0 = 0, b1 = 0, nsk = 0;
+    if (w.u0 < w.u1) {
+        const int ts = w.u0 / w.S;
+        t0 = w.dp + ts;
+        a0 = w.u0 - ts * w.S;
+        b0 = min(w.S, a0 + (w.u1 - w.u0));
+        nsk = 1;
+        const int u = w.u0 + (b0 - a0);   // the range goes on into tile t0 + 1
+        if (u < w.u1) {
+            b1 = min(w.S, w.u1 - u);
+            nsk = 2;
+        }
+    }
+    for (int i = 0;; ++i) {
+        int t, s0, s1;
+        if (i < nsk) {
+            t = t0 + i;
+            s0 = i == 0 ? a0 : 0;
+            s1 = i == 0 ? b0 : b1;
+        } else {
+            t = static_cast<int>(blockIdx.x) + (i - nsk) * static_cast<int>(gridDim.x);
+            if (t >= w.dp) return;
+            s0 = 0;
+            s1 = w.S;
+        }
+        if (!f(t, s0, s1)) return;
+    }
+}
+
 // =============================================================================
 // The tensor-core GEMM: every tile is one MMA batch of up to 128 token rows
 // (decode shapes, MoE experts, 128-row tiles of large problems). Two K groups
@@ -264,6 +362,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    volatile int *s_last = reinterpret_cast<volatile int *>(smem + kOffMisc + 12);
     const int tab_stride = kWide ? p.E + 1 : kMaxExperts + 1;
     int *s_base = reinterpret_cast<int *>(smem + (kWide ? kWideOffTab : kOffTab));
     int *s_lo = s_base + tab_stride;
@@ -307,6 +406,11 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const int total = *s_total;
     const int G = p.G;
     const int wg = warp >> 2;
+    // Wide tiles are never split (their two accumulators leave no registers
+    // for the bookkeeping).
+    const WorkPlan plan = make_plan(total, G, !kWide && p.sk_cnt != nullptr);
+    constexpr int kEpiR = kWide ? kEpiRegs : kSplitEpiRegs;
+    constexpr int kOthR = kWide ? kOtherRegs : kSplitOtherRegs;
     // TMEM: partial buffer of (partial slot s, group j) at column
     // (2 s + j) * b_rows; fp16 A operand of (step slot s, group j) at column
     // 256 + 128 s + 64 j.
@@ -315,21 +419,22 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     };
 
     if (warp < 4) {
-        setmaxnreg_dec<kOtherRegs>();
+        setmaxnreg_dec<kOthR>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------- weight TMA producer
             Ring a;
             uint32_t issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int wrow = ti.e * p.N + ti.n0;
-                for (int g0 = 0; g0 < G; g0 += 2) {
+                for (int sg = s0; sg < s1; ++sg) {
+                    const int g0 = 2 * sg;
                     const int ng = min(2, G - g0);
                     if (!mbar_wait(bar(NBar::a_empty + a.idx), a.phase ^ 1u, s_abort, p.err,
                                    ROLE_PRODUCER, 1)) {
                         ok = false;
-                        break;
+                        return false;
                     }
                     mbar_arrive_expect_tx(bar(NBar::a_full + a.idx), ng * kAStageBytes);
                     for (int j = 0; j < ng; ++j)
@@ -338,23 +443,25 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     a.advance(SA);
                     ++issued;
                 }
-            }
+                return true;
+            });
             if (!ok) drain_ring(bar(NBar::a_full), issued, SA);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------- MMA issuer
             Ring st, pr;
             uint32_t gph[2] = {0u, 0u};   // wide: phase of each group's partial buffer
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int n_eff = (ti.rows + 15) & ~15;
                 const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(n_eff));
-                for (int g0 = 0; g0 < G; g0 += 2) {
+                for (int sg = s0; sg < s1; ++sg) {
+                    const int g0 = 2 * sg;
                     const int ng = min(2, G - g0);
                     if (!mbar_wait(bar(NBar::ready + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
                                    1)) {
                         ok = false;
-                        break;
+                        return false;
                     }
                     tc_fence_after();
                     for (int j = 0; j < ng; ++j) {
@@ -383,12 +490,13 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             gph[j] ^= 1u;
                         }
                     }
-                    if (!ok) break;
+                    if (!ok) return false;
                     mma_commit(bar(NBar::done + st.idx));
                     st.advance(kNarrowSlots);
                     pr.advance(NP);
                 }
-            }
+                return true;
+            });
             mma_commit(bar(NBar::drain));
             drain_wait(bar(NBar::drain), 0);
         } else if (warp == 2 && lane == 0) {
@@ -397,16 +505,17 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             Ring st;
             uint32_t issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int n_eff = (ti.rows + 15) & ~15;
                 const int nbox = (n_eff + kBoxRows - 1) / kBoxRows;
-                for (int g0 = 0; g0 < G; g0 += 2) {
+                for (int sg = s0; sg < s1; ++sg) {
+                    const int g0 = 2 * sg;
                     const int ng = min(2, G - g0);
                     if (!mbar_wait(bar(NBar::done + st.idx), st.phase ^ 1u, s_abort, p.err,
                                    ROLE_PRODUCER, 2)) {
                         ok = false;
-                        break;
+                        return false;
                     }
                     const uint32_t stage = sB + st.idx * b_stage_bytes;
                     mbar_arrive_expect_tx(bar(NBar::b_full + st.idx),
@@ -420,44 +529,41 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     st.advance(kNarrowSlots);
                     ++issued;
                 }
-            }
+                return true;
+            });
             if (!ok) drain_ring(bar(NBar::b_full), issued, kNarrowSlots);
         } else if (warp == 3 && lane == 0) {
             // --------------------------------------------------- admission
             Ring st, pr;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                for (int g0 = 0; g0 < G; g0 += 2) {
+            for_each_piece(plan, [&](int, int s0, int s1) -> bool {
+                for (int sg = s0; sg < s1; ++sg) {
                     if (!mbar_wait(bar(NBar::b_full + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
                                    2) ||
                         (!kWide && !mbar_wait(bar(NBar::p_empty + pr.idx), pr.phase ^ 1u, s_abort,
-                                              p.err, ROLE_MMA, 3))) {
-                        ok = false;
-                        break;
-                    }
+                                              p.err, ROLE_MMA, 3)))
+                        return false;
                     mbar_arrive(bar(NBar::ready + st.idx));
                     st.advance(kNarrowSlots);
                     pr.advance(NP);
                 }
-            }
+                return true;
+            });
         }
     } else if (wg == 1) {
         // --------------------------------------- weight converter (A -> TMEM)
-        setmaxnreg_dec<kOtherRegs>();
+        setmaxnreg_dec<kOthR>();
         const int row = threadIdx.x - 128;
         const int q = warp & 3;
         Ring a, st;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            for (int g0 = 0; g0 < G; g0 += 2) {
+        for_each_piece(plan, [&](int, int s0, int s1) -> bool {
+            for (int sg = s0; sg < s1; ++sg) {
+                const int g0 = 2 * sg;
                 const int ng = min(2, G - g0);
                 if (!mbar_wait(bar(NBar::a_full + a.idx), a.phase, s_abort, p.err, ROLE_CONVERT,
                                1) ||
                     !mbar_wait(bar(NBar::done + st.idx), st.phase ^ 1u, s_abort, p.err,
-                               ROLE_CONVERT, 2)) {
-                    ok = false;
-                    break;
-                }
+                               ROLE_CONVERT, 2))
+                    return false;
                 tc_fence_after();
                 for (int j = 0; j < ng; ++j) {
                     const uint8_t *rowp =
@@ -489,15 +595,24 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 a.advance(SA);
                 st.advance(kNarrowSlots);
             }
-        }
+            return true;
+        });
     } else {
         // -------------------------------------------------------- epilogue
-        setmaxnreg_inc<kEpiRegs>();
+        setmaxnreg_inc<kEpiR>();
         const int ewg = wg - 2;   // owns token columns [32 c, 32 c + 32) for chunks c = ewg + 2 h
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
+        auto store_out = [&](int m, int n_local, float v) {
+            const float out = v * __ldg(p.sa + m);
+            const size_t idx = static_cast<size_t>(m) * p.N + n_local;
+            if (p.out_fp32)
+                static_cast<float *>(p.y)[idx] = out;
+            else
+                static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+        };
         float acc[NCH][32];
 #pragma unroll
         for (int h = 0; h < NCH; ++h)
@@ -505,8 +620,11 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             for (int j = 0; j < 32; ++j) acc[h][j] = 0.0f;
         Ring st, pr;
         uint32_t gph[2] = {0u, 0u};   // wide: phase of each group's partial buffer
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        // After a failed wait the threads keep walking the same pieces with
+        // no waits and no data work, so that every epilogue warp takes the
+        // same named barriers at split pieces.
+        bool failed = false;
+        for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
             const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
             const int n_eff = (ti.rows + 15) & ~15;
             const bool owned = 32 * ewg < n_eff;   // warp-uniform (first chunk)
@@ -517,7 +635,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             // issued in place and only read after the next quad boundary.
             auto load_quad = [&](int g) -> float4 {
                 float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (!n_ok || !owned) return v;
+                if (!n_ok || !owned || failed) return v;
                 if (vec_sw) {
                     if (g < G) v = ldg_nc_f32x4_now(swp + g);
                 } else {
@@ -528,28 +646,31 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
                 return v;
             };
-            float4 cur = load_quad(0);
-            float4 nxt = load_quad(4);
-            for (int g0 = 0; ok && g0 < G; g0 += 2) {
+            const int qb = (2 * s0) & ~3;
+            float4 cur = load_quad(qb);
+            float4 nxt = load_quad(qb + 4);
+            for (int sg = s0; sg < s1; ++sg) {
+                const int g0 = 2 * sg;
                 const int ng = min(2, G - g0);
-                if ((g0 & 3) == 0 && g0 > 0) {
+                if ((g0 & 3) == 0 && g0 > qb) {
                     cur = nxt;
                     nxt = load_quad(g0 + 4);
                 }
-                const float s0 = (g0 & 3) == 0 ? cur.x : cur.z;
-                const float s1 = (g0 & 3) == 0 ? cur.y : cur.w;
+                const float sc0 = (g0 & 3) == 0 ? cur.x : cur.z;
+                const float sc1 = (g0 & 3) == 0 ? cur.y : cur.w;
+                if (failed) continue;
                 if constexpr (kWide) {
                     // One group at a time: wait for its MMAs, drain its buffer,
                     // release it (group 0 drains while group 1's MMAs issue).
                     for (int j = 0; j < ng; ++j) {
                         if (!mbar_wait(bar(NBar::p_full + j), gph[j], s_abort, p.err,
                                        ROLE_EPILOGUE, 2)) {
-                            ok = false;
+                            failed = true;
                             break;
                         }
                         gph[j] ^= 1u;
                         tc_fence_after();
-                        const float sj = j == 0 ? s0 : s1;
+                        const float sj = j == 0 ? sc0 : sc1;
 #pragma unroll
                         for (int h = 0; h < NCH; ++h) {
                             const int chunk = ewg + 2 * h;
@@ -573,13 +694,12 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         __syncwarp();
                         if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + j));
                     }
-                    if (!ok) break;
                     continue;
                 }
                 if (!mbar_wait(bar(NBar::done + st.idx), st.phase, s_abort, p.err, ROLE_EPILOGUE,
                                1)) {
-                    ok = false;
-                    break;
+                    failed = true;
+                    continue;
                 }
                 tc_fence_after();
 #pragma unroll
@@ -593,13 +713,13 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         tmem_ld_2x32cols_sync(c0, c1, v0, v1);
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            acc[h][j] = fmaf(__uint_as_float(v1[j]), s1,
-                                             fmaf(__uint_as_float(v0[j]), s0, acc[h][j]));
+                            acc[h][j] = fmaf(__uint_as_float(v1[j]), sc1,
+                                             fmaf(__uint_as_float(v0[j]), sc0, acc[h][j]));
                     } else {
                         tmem_ld_32cols_sync(c0, v0);
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            acc[h][j] = fmaf(__uint_as_float(v0[j]), s0, acc[h][j]);
+                            acc[h][j] = fmaf(__uint_as_float(v0[j]), sc0, acc[h][j]);
                     }
                     if (kDebug && n_ok) {
 #pragma unroll
@@ -620,17 +740,89 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 st.advance(kNarrowSlots);
                 pr.advance(NP);
             }
-            if (!ok) break;
-            if (n_ok) {
+            if (s0 == 0 && s1 == plan.S) {
+                if (n_ok && !failed) {
 #pragma unroll
-                for (int h = 0; h < NCH; ++h) {
+                    for (int h = 0; h < NCH; ++h) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = 32 * (ewg + 2 * h) + j;
+                            if (col < ti.rows) store_out(ti.m0 + col, n_local, acc[h][j]);
+                        }
+                    }
+                }
+            } else if constexpr (!kWide) {
+                // Split piece: store its partial ([token column][weight row],
+                // FP32, before sa), then count it in. The CTA that brings
+                // the tile's last piece adds all pieces in K order (its own
+                // from registers) and stores y. The other roles run on
+                // meanwhile; the MMAs of the next steps fill the two
+                // partial-buffer slots.
+                const int me = static_cast<int>(blockIdx.x);
+                const int x0 = (t - plan.dp) * plan.S;
+                const int c_first = sk_owner(x0, plan);
+                const int c_final = sk_owner(x0 + plan.S - 1, plan);
+                auto slot = [&](int c) -> const float * {   // slot 1: the tile's first piece
+                    return p.sk_part +
+                           static_cast<size_t>(2 * c + (c == c_first ? 1 : 0)) * p.sk_ld * kTileN;
+                };
+                const int col0 = 32 * ewg;
+                const bool mine = n_ok && !failed && col0 < ti.rows;
+                if (mine) {
+                    float *dst = const_cast<float *>(slot(me)) + lrow;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j < ti.rows) __stcg(dst + (col0 + j) * kTileN, acc[0][j]);
+                }
+                // Release: the barrier orders every epilogue thread's partial
+                // stores before one thread's fence and counter update (fences
+                // are cumulative); the last arrival's fence then orders its
+                // reads of the other pieces after their release.
+                named_barrier_sync(1, 256);
+                if (threadIdx.x == 256) {
+                    int last = 0;
+                    if (*s_abort == 0) {
+                        // Orders the counter update after the kernel before
+                        // this one in the stream, which zeroed the counters
+                        // (returns at once: the token producer has waited).
+                        griddep_wait();
+                        __threadfence();
+                        last = atomicAdd(p.sk_cnt + (t - plan.dp), 1) == c_final - c_first;
+                        if (last) __threadfence();
+                    }
+                    *s_last = last;
+                }
+                named_barrier_sync(1, 256);
+                if (*s_last != 0 && mine) {
+                    // Token scales loaded ahead of the pieces (the debug
+                    // form loads them at the store: fewer live registers).
+                    float sa_r[32], sum[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const int col = 32 * (ewg + 2 * h) + j;
-                        if (col < ti.rows) {
-                            const int m = ti.m0 + col;
-                            const float out = acc[h][j] * __ldg(p.sa + m);
-                            const size_t idx = static_cast<size_t>(m) * p.N + n_local;
+                        sa_r[j] = kDebug ? 0.0f : __ldg(p.sa + ti.m0 + min(col0 + j, ti.rows - 1));
+                        sum[j] = 0.0f;
+                    }
+                    for (int c = c_first; c <= c_final; ++c) {   // K order
+                        if (c == me) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) sum[j] += acc[0][j];
+                        } else {
+                            const float *src = slot(c) + lrow;
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __ldcg(src + min(col0 + j, ti.rows - 1) * kTileN);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) sum[j] += v[j];
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (col0 + j < ti.rows) {
+                            const size_t idx =
+                                static_cast<size_t>(ti.m0 + col0 + j) * p.N + n_local;
+                            const float out =
+                                sum[j] * (kDebug ? __ldg(p.sa + ti.m0 + col0 + j) : sa_r[j]);
                             if (p.out_fp32)
                                 static_cast<float *>(p.y)[idx] = out;
                             else
@@ -643,7 +835,8 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             for (int h = 0; h < NCH; ++h)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc[h][j] = 0.0f;
-        }
+            return true;
+        });
     }
 
     __syncwarp();
@@ -653,60 +846,6 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
-}
-
-// Stream-K work split (used by the CUDA-core GEMV below).
-// This CTA's share of the work: the step range [u0, u1) of the stream-K part
-// (steps of tiles [dp, total), S per tile, numbered from 0 at tile dp, split
-// over g_sk CTAs), then round-robin whole tiles of [0, dp).
-struct WorkPlan {
-    int dp, S, g_sk;
-    long long U, u0, u1;
-};
-
-__device__ __forceinline__ WorkPlan make_plan(int total, int G, bool stream_k) {
-    WorkPlan w;
-    w.S = (G + 1) >> 1;
-    const int grid = static_cast<int>(gridDim.x);
-    const int c = static_cast<int>(blockIdx.x);
-    w.u0 = w.u1 = 0;
-    if (!stream_k) {
-        w.dp = total;
-        w.g_sk = 0;
-        w.U = 0;
-        return w;
-    }
-    w.dp = (total / grid) * grid;   // whole waves; fewer than grid tiles are split
-    w.U = static_cast<long long>(total - w.dp) * w.S;
-    w.g_sk = static_cast<int>(w.U < grid ? w.U : grid);
-    if (c < w.g_sk) {
-        w.u0 = static_cast<long long>(c) * w.U / w.g_sk;
-        w.u1 = static_cast<long long>(c + 1) * w.U / w.g_sk;
-    }
-    return w;
-}
-
-// The stream-K CTA whose step range contains step x: the largest c with
-// floor(c U / g) <= x.
-__device__ __forceinline__ int sk_owner(long long x, const WorkPlan &w) {
-    return static_cast<int>(((x + 1) * w.g_sk + w.U - 1) / w.U) - 1;
-}
-
-// Calls f(tile, s0, s1) for every piece of this CTA in order; f returns false
-// to stop.
-template <class F>
-__device__ __forceinline__ void for_each_piece(const WorkPlan &w, F &&f) {
-    long long u = w.u0;
-    while (u < w.u1) {
-        const int ts = static_cast<int>(u / w.S);
-        const int s0 = static_cast<int>(u - static_cast<long long>(ts) * w.S);
-        const long long left = w.u1 - u;
-        const int s1 = left < w.S - s0 ? s0 + static_cast<int>(left) : w.S;
-        if (!f(w.dp + ts, s0, s1)) return;
-        u += s1 - s0;
-    }
-    for (int t = blockIdx.x; t < w.dp; t += gridDim.x)
-        if (!f(t, 0, w.S)) return;
 }
 
 // =============================================================================
@@ -864,7 +1003,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
         const int c_self = static_cast<int>(blockIdx.x);
         auto sk_range = [&](int t, int &c_first, int &c_final) {
-            const long long x0 = static_cast<long long>(t - plan.dp) * plan.S;
+            const int x0 = (t - plan.dp) * plan.S;
             c_first = sk_owner(x0, plan);
             c_final = sk_owner(x0 + plan.S - 1, plan);
         };
@@ -1033,6 +1172,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
             named_barrier_sync(1, 32 * CW);
             if (ct == 0) {
                 int flags = 0;
+                griddep_wait();   // the counters were zeroed by the kernel before this one
                 for (int q = 0; q < n_split; ++q) {
                     const int t = q == 0 ? split_t0 : split_t1;
                     int c_first, c_final;
@@ -1245,11 +1385,16 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     const int64_t m_tiles_bound = pr.offsets == nullptr ? (pr.R + tt - 1) / tt
                                                         : (pr.R + tt - 1) / tt + pr.E;
     const int64_t tiles_bound = m_tiles_bound * kp.n_tiles;
-    const int64_t grid = tiles_bound < num_sms ? tiles_bound : num_sms;
+    // Dense narrow tiles split their K ranges across CTAs (stream-K) when the
+    // workspace holds the split area: one CTA per SM, or per step if fewer.
+    const bool split = !ps.wide && pr.offsets == nullptr && pr.sk_cnt != nullptr &&
+                       num_sms <= kSkMaxCtas && pr.sk_ld >= pr.R;
+    const int64_t units = split ? tiles_bound * ((kp.G + 1) / 2) : tiles_bound;
+    const int64_t grid = units < num_sms ? units : num_sms;
     if (grid <= 0) return cudaSuccess;
-    kp.sk_cnt = nullptr;   // the tensor-core kernels never split a tile's K range
-    kp.sk_part = nullptr;
-    kp.sk_ld = 0;
+    kp.sk_cnt = split ? pr.sk_cnt : nullptr;
+    kp.sk_part = split ? pr.sk_part : nullptr;
+    kp.sk_ld = split ? pr.sk_ld : 0;
 
     // Programmatic dependent launch: the kernel may start while the staging
     // kernel before it in the stream is still running; only its token

@@ -14,9 +14,12 @@ cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
                                 cudaStream_t stream);
 
-// int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] in `out`.
+// int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] in `out`;
+// also zeroes n_cnt split-tile counters at cnt (if not null) for the GEMM
+// launched after it.
 cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
-                               int num_sms, cudaStream_t stream);
+                               int num_sms, cudaStream_t stream, int *cnt = nullptr,
+                               int n_cnt = 0);
 
 // Zeroes n split-tile counters (programmatic dependent of the kernel before
 // it in the stream; see quant.cu).
@@ -33,7 +36,7 @@ struct GemmProblem {
     int32_t *debug_partials;  // nullable [R, N, G]
     int64_t R, E, N, K;
     bool out_fp32;
-    // Stream-K split of GEMV calls; null sk_cnt: whole tiles only.
+    // Stream-K split of dense calls; null sk_cnt: whole tiles only.
     int *sk_cnt = nullptr;        // [2 * kSkMaxCtas] counters, zeroed before the GEMM
     float *sk_part = nullptr;     // [kSkMaxCtas][2][sk_ld][128] FP32 partials
     int sk_ld = 0;
@@ -44,14 +47,17 @@ struct GemmProblem {
 constexpr int kGemvMaxTokens = 8;
 inline bool uses_gemv(int64_t R, bool grouped) { return !grouped && R <= kGemvMaxTokens; }
 
-// The GEMV splits tiles across CTAs (stream-K) for tiles of 5..8 token rows
-// when the workspace holds the split area: arrival counters and two FP32
-// partial slots per CTA (token rows x 128 weight rows), for at most
-// kSkMaxCtas CTAs.
+// Dense calls of 5..64 token rows split tiles across CTAs (stream-K) when the
+// workspace holds the split area: arrival counters and two FP32 partial
+// slots per CTA (token rows x 128 weight rows), for at most kSkMaxCtas CTAs.
+// Both kernels are bound by their arithmetic there (the GEMV's 8-token
+// tiles; every narrow tensor-core tile), so the steps of a partial last wave
+// are worth spreading over all SMs.
 constexpr int kSkMaxCtas = 160;
-constexpr int kGemvSplitRows = 8;   // token rows per tile (rounded up to 1, 2, 4, 8)
+constexpr int kGemvSplitRows = 8;   // GEMV token rows per tile (rounded up to 1, 2, 4, 8)
+constexpr int kNarrowSplitMaxRows = 64;
 inline bool uses_split(int64_t R, bool grouped) {
-    return uses_gemv(R, grouped) && R > kGemvSplitRows / 2;
+    return !grouped && R > kGemvSplitRows / 2 && R <= kNarrowSplitMaxRows;
 }
 inline size_t sk_counter_bytes() { return 2 * kSkMaxCtas * sizeof(int); }
 inline size_t sk_area_bytes(int64_t R, bool grouped) {

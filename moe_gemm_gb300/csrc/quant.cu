@@ -182,12 +182,16 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float *__restri
 // int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] (dense).
 __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restrict__ q,
                                                           int64_t rows, int K, int64_t ldq,
-                                                          __half *__restrict__ out) {
+                                                          __half *__restrict__ out,
+                                                          int *__restrict__ cnt, int n_cnt) {
     // The GEMM that consumes this copy is launched as a programmatic
     // dependent: let it start its set-up and weight stream right away. This
     // kernel is itself a programmatic dependent of the quantizer: wait for
-    // its codes.
+    // its codes. The GEMM's split counters are free to reset at once: no GEMM
+    // releases its dependents early, so the one before (if any) has exited.
     griddep_launch_dependents();
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
     griddep_wait();
     const int vec_per_row = K >> 4;  // 16 codes per vector
     const int64_t total = rows * vec_per_row;
@@ -263,7 +267,8 @@ cudaError_t launch_zero_counters(int *cnt, int n, cudaStream_t stream) {
 }
 
 cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
-                               int num_sms, cudaStream_t stream) {
+                               int num_sms, cudaStream_t stream, int *cnt, int n_cnt) {
+    if (cnt == nullptr) n_cnt = 0;
     const int64_t total = rows * (K / 16);
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
@@ -279,7 +284,7 @@ cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, widen_codes_kernel, q, rows, static_cast<int>(K),
-                                             ldq, static_cast<__half *>(out));
+                                             ldq, static_cast<__half *>(out), cnt, n_cnt);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

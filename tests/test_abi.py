@@ -63,16 +63,18 @@ def _split_area(rows):
 
 def test_workspace_size(lib):
     # fp16 staging copy of the activation codes (rounded up to 256 bytes), then
-    # the optional K-split area of the CUDA-core path for 5..8 token rows.
+    # the optional K-split area of dense calls of 5..64 token rows.
     assert lib.w8a8_gemm_workspace_size(0, 128, 128) == 0
     assert lib.w8a8_gemm_workspace_size(3, 128, 128) == 768
     assert lib.w8a8_gemm_workspace_size(1, 128, 128) == 256
     assert lib.w8a8_gemm_workspace_size(4, 128, 128) == _staging(4, 128)
     assert lib.w8a8_gemm_workspace_size(5, 128, 128) == _staging(5, 128) + _split_area(5)
     assert lib.w8a8_gemm_workspace_size(8, 28672, 8192) == 8 * 8192 * 2 + _split_area(8)
-    assert lib.w8a8_gemm_workspace_size(9, 128, 128) == _staging(9, 128)
+    assert lib.w8a8_gemm_workspace_size(9, 128, 128) == _staging(9, 128) + _split_area(9)
+    assert lib.w8a8_gemm_workspace_size(64, 128, 256) == _staging(64, 256) + _split_area(64)
+    assert lib.w8a8_gemm_workspace_size(65, 128, 256) == _staging(65, 256)
     assert lib.w8a8_gemm_workspace_size(129, 128, 384) == (129 * 384 * 2 + 255) // 256 * 256
-    assert lib.w8a8_gemm_workspace_size(32, 28672, 8192) == 32 * 8192 * 2
+    assert lib.w8a8_gemm_workspace_size(32, 28672, 8192) == 32 * 8192 * 2 + _split_area(32)
     assert lib.w8a8_grouped_gemm_workspace_size(4096, 64, 3072, 4096) == 4096 * 4096 * 2
     assert lib.w8a8_grouped_gemm_workspace_size(8, 64, 3072, 4096) == 8 * 4096 * 2
     assert lib.w8a8_grouped_gemm_workspace_size(0, 64, 3072, 4096) == 0

@@ -302,7 +302,10 @@ def _staging_only(rows, K):
     (8, 4096, 8192, "fp32"),     # 32 tiles of 32 steps over all SMs: ~5 pieces per tile
     (5, 1000, 1152, "bf16"),     # odd group count, one step per CTA, ragged N
     (6, 28672, 1024, "fp32"),    # 224 tiles, ranges cross tile boundaries
-    (33, 1000, 1152, "bf16"),    # tensor-core path: whole tiles, workspace size irrelevant
+    (33, 1000, 1152, "bf16"),    # tensor-core path: 8 tiles x 5 steps, one step per CTA
+    (9, 2000, 2048, "fp32"),     # tensor-core path: 16 tiles x 8 steps over 128 CTAs
+    (17, 28672, 1024, "bf16"),   # tensor-core path: one whole wave, 72 tiles split
+    (64, 4096, 8192, "fp32"),    # tensor-core path: ~5 pieces per tile, 64-row tiles
 ])
 def test_dense_k_split_matches_oracle_and_unsplit(M, N, K, out):
     rng = np.random.default_rng(M + N + K)
