@@ -35,6 +35,9 @@ sys.path.insert(0, ROOT)
 
 import workloads  # noqa: E402
 
+KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM replayed back to back K times, events "
+                    "around the K launches; the GEMM overlaps the quantizer, so this includes "
+                    "any part of the quantizer it does not hide")
 METRIC = "INT8 TOPS & % of roofline (tensor peak or HBM GB/s) per GEMM shape, 1xGB300"
 GROUP = 128
 
@@ -244,59 +247,100 @@ def run_ours(args):
             d["launches"] = 3
     torch.cuda.synchronize()
 
-    stream = torch.cuda.current_stream()
-
-    def gemm_call(d):
+    def gemm_call(d, s=None):
+        s = stream if s is None else s
         if d["off"] is not None:
             w8.grouped_gemm(d["qa"], d["sa"], d["off"], d["qw"], d["sw"], out=d["y"],
-                            out_dtype=d["y"].dtype, workspace=d["ws"])
+                            out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
         else:
             w8.gemm(d["qa"], d["sa"], d["qw"], d["sw"], out=d["y"], out_dtype=d["y"].dtype,
-                    workspace=d["ws"])
+                    workspace=d["ws"], stream=s)
 
-    # Per-GEMM events bracket the quantizer and the GEMM: the GEMM is launched
-    # as a programmatic dependent of the quantizer and overlaps it, which an
-    # event recorded between the two would prevent. The per-launch GEMM time
-    # (roofline) therefore includes any part of the quantizer it does not hide.
-    def step(ev=None):
-        for i, d in enumerate(per):
-            if ev is not None:
-                ev[i][0].record(stream)
-            w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"])
-            gemm_call(d)
-            if ev is not None:
-                ev[i][1].record(stream)
+    def shape_call(d):
+        w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"], stream=stream)
+        gemm_call(d)
 
-    # ---- warm-up, then the timed region (CUDA events on the launching stream)
-    for _ in range(args.warmup):
-        step()
+    def step():
+        for d in per:
+            shape_call(d)
+
+    # The step runs as one CUDA graph (quantizer, staging/reset kernel and
+    # GEMM of every shape, with their programmatic-dependent-launch edges),
+    # replayed once per step: the launches a serving loop would capture.
+    stream = torch.cuda.Stream(device=dev)
+    graphs = not args.no_graph
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()                       # eager pass on the capture stream first
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        torch.cuda.synchronize()
+        return g
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
     torch.cuda.synchronize()
+    if graphs:
+        g_step = capture(step)
+        run_step = g_step.replay
+        g_shape = [capture(lambda d=d: shape_call(d)) for d in per]
+        run_shape = [g.replay for g in g_shape]
+    else:
+        run_step = step
+        run_shape = [lambda d=d: shape_call(d) for d in per]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run_step()
+    torch.cuda.synchronize()
+
+    # ---- the timed region (CUDA events on the launching stream)
     sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
     if sampler:
         sampler.start()
-    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in per] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for k in range(args.steps):
-        step(kev[k])
-    t1.record(stream)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for k in range(args.steps):
+            run_step()
+        t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     elapsed_ms = t0.elapsed_time(t1)
+
+    # ---- per-shape launch time (roofline): each shape's quantizer + GEMM
+    # replayed K times back to back, timed with events around the K launches
+    # (an event between two launches would cut their programmatic overlap).
+    gemm_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(len(per)):
+            for _ in range(3):
+                run_shape[i]()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(args.steps):
+                run_shape[i]()
+            s1.record(stream)
+            s1.synchronize()
+            gemm_ms.append(s0.elapsed_time(s1) / args.steps)
     # Keep the same step running ~1 s more so the clock sampler sees the load
     # even when the timed region itself is shorter than its sampling period.
     if sampler:
         hold_end = time.time() + 1.0
-        while time.time() < hold_end:
-            for _ in range(50):
-                step()
-            torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            while time.time() < hold_end:
+                for _ in range(50):
+                    run_step()
+                stream.synchronize()
         clocks = sampler.stop()
         clocks["note"] = "sampled every 50 ms over the timed region and a 1 s hold of the same step"
     if world > 1:
@@ -304,8 +348,6 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    gemm_ms = [sum(kev[k][i][0].elapsed_time(kev[k][i][1]) for k in range(args.steps)) /
-               args.steps for i in range(len(per))]
     ops_step = sum(d["shape"].ops for d in per)
     value = ops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
 
@@ -318,11 +360,13 @@ def run_ours(args):
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
 
+        cur = torch.cuda.current_stream()
+
         def e2e_step():
             for d, hi, ho in zip(per, host_in, host_out):
                 d["a"].copy_(hi, non_blocking=True)
-                w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"])
-                gemm_call(d)
+                w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"], stream=cur)
+                gemm_call(d, cur)
                 ho.copy_(d["y"], non_blocking=True)
 
         for _ in range(args.warmup):
@@ -332,10 +376,10 @@ def run_ours(args):
             dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(cur)
         for _ in range(args.steps):
             e2e_step()
-        e1.record(stream)
+        e1.record(cur)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
         if world > 1:
@@ -360,8 +404,7 @@ def run_ours(args):
                 "traffic": recorded_traffic(args.workload),
                 "alg_bytes_per_launch": alg,
                 "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
-                "kernel_time": "quantizer start to GEMM end per shape (the GEMM overlaps the "
-                               "quantizer; includes any part of it not hidden)",
+                "kernel_time": KERNEL_TIME_NOTE,
                 "peak_source": f"{peaks['source']} HBM copy bandwidth"}
     else:
         flops = [d["shape"].ops for d in per]
@@ -372,8 +415,7 @@ def run_ours(args):
                 "traffic": recorded_traffic(args.workload),
                 "ops_per_launch": flops,
                 "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
-                "kernel_time": "quantizer start to GEMM end per shape (the GEMM overlaps the "
-                               "quantizer; includes any part of it not hidden)",
+                "kernel_time": KERNEL_TIME_NOTE,
                 "peak_source": (f"{peaks['source']} dense bf16 burst (the integer path runs "
                                 "on fp16 tensor cores, same rate as bf16)")}
 
@@ -387,7 +429,10 @@ def run_ours(args):
                                                  for d in per],
                    "l2": "inputs larger than L2: each GEMM reads its own weight copy "
                          f"({per[0]['shape'].N * per[0]['shape'].K * per[0]['shape'].E / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "launch": ("one CUDA graph per step (all shapes' kernels with their "
+                              "programmatic-dependent-launch edges), replayed" if graphs
+                              else "stream launches")},
         "roofline": roof,
         "gpu_launches": sum(d["launches"] for d in per) * args.steps,
     }
@@ -504,6 +549,8 @@ def main():
                     choices=["decode", "tiny", "prefill", "stress", "moe"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the step's kernels on a stream instead of replaying a graph")
     ap.add_argument("--no-clocks", action="store_true",
                     help="skip nvidia-smi clock sampling and its 1 s hold (profiler runs)")
     args = ap.parse_args()
