@@ -8,7 +8,7 @@ larger than L2 and no weight bytes are reused from L2 between GEMMs.
 
 Metric: INT8 TOPS = sum of 2*M*N*K over the step / step time (whole job over
 all ranks). The dominant kernel is the GEMM (the CUDA-core batched GEMV for
-M <= 8, the tcgen05 narrow-tile kernel for M = 32), HBM-bound at these shapes:
+M = 1, the tcgen05 narrow-tile kernel with K split for M = 8 and 32), HBM-bound at these shapes:
 the roofline object reports its algorithmic bytes per launch (int8 weights,
 FP32 group scales, int8 activations and scales, BF16 output) over its measured
 launch duration, against the measured HBM copy bandwidth.
@@ -239,12 +239,9 @@ def run_ours(args):
         wsz = (w8.grouped_gemm_workspace_size(shp.M, shp.E, shp.N, shp.K) if d["off"] is not None
                else w8.gemm_workspace_size(shp.M, shp.N, shp.K))
         d["ws"] = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
-        # quantizer + GEMM, plus the fp16 staging kernel (tensor-core paths)
-        # or the split-counter reset (CUDA-core path, 5..8 token rows)
-        if d["off"] is None and shp.M <= 8:
-            d["launches"] = 2 + (1 if shp.M > 4 else 0)
-        else:
-            d["launches"] = 3
+        # quantizer + GEMM, plus the fp16 staging kernel on the tensor-core
+        # paths (the CUDA-core GEMV for <= 4 token rows reads the int8 codes)
+        d["launches"] = 2 if (d["off"] is None and shp.M <= 4) else 3
     torch.cuda.synchronize()
 
     def gemm_call(d, s=None):

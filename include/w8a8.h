@@ -93,7 +93,7 @@ w8a8_status w8a8_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, 
  * (M * K * 2 bytes rounded up to 256) is accepted, and the GEMM then never
  * splits a tile's K range across CTAs (slower when the weight tiles do not
  * divide evenly among the SMs; results agree within the stated bound).
- * Calls with M <= 8 run on the CUDA cores and do not use the staging copy.
+ * Calls with M <= 4 run on the CUDA cores and do not use the staging copy.
  */
 size_t w8a8_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 

@@ -107,11 +107,10 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
         p.sk_ld = static_cast<int>(R);
     }
     cudaError_t e = cudaSuccess;
-    if (w8a8::uses_gemv(R, grouped)) {
-        // The CUDA-core path reads the int8 codes directly; only the split
-        // counters need zeroing.
-        if (p.sk_cnt != nullptr) e = w8a8::launch_zero_counters(p.sk_cnt, 2 * w8a8::kSkMaxCtas, s);
-    } else {
+    if (!w8a8::uses_gemv(R, grouped)) {
+        // The tensor-core path reads an fp16 copy of the codes; the kernel that
+        // writes it also resets the split counters. (The CUDA-core path reads
+        // the int8 codes directly.)
         e = w8a8::launch_widen_codes(qa, R, K, K, workspace, info.num_sms, s, p.sk_cnt,
                                      p.sk_cnt != nullptr ? 2 * w8a8::kSkMaxCtas : 0);
     }

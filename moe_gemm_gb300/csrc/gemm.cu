@@ -39,9 +39,11 @@
 //  * Every mbarrier wait is bounded (%globaltimer); a wait that gives up sets
 //    the library error word and the CTA drains its copies, frees TMEM and
 //    returns.
-//  * Dense calls of at most 8 token rows run a CUDA-core kernel instead
+//  * Dense calls of at most 4 token rows run a CUDA-core kernel instead
 //    (w8a8_gemv_kernel, below): exact int8 dot products (dp4a) cost less than
 //    the weight stream there.
+//  * Dense calls of 5..64 token rows split tile K ranges over all SMs
+//    (stream-K) when the workspace has room for it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -849,15 +851,16 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
 }
 
 // =============================================================================
-// Decode-sized dense problems (at most 8 token rows): a batched GEMV on the
-// CUDA cores. With at most 8 multiply-adds per weight byte, the exact int8
+// Decode-sized dense problems (at most 4 token rows): a batched GEMV on the
+// CUDA cores. With at most 4 multiply-adds per weight byte, the exact int8
 // group sums fit the integer dot-product units (dp4a: four int8 products
 // summed into an int32, exact) in less time than the weights take to stream
-// from HBM, so the tensor cores' fixed cost per instruction is not paid. The
-// weight stream (TMA, 128-byte swizzle, two K groups per step), tile table,
-// stream-K split and FP32 accumulation order are those of the narrow kernel;
-// the int8 token codes are read directly (no fp16 staging copy), in the same
-// stages as the weights.
+// from HBM, so the tensor cores' fixed cost per instruction is not paid, and
+// the kernel runs at the weight-stream rate (whole tiles, no K split). The
+// weight stream (TMA, 128-byte swizzle, two K groups per step), tile table
+// and FP32 accumulation order are those of the narrow kernel; the int8 token
+// codes are read directly (no fp16 staging copy), in the same stages as the
+// weights. (5..8 token rows run faster on the split tensor-core kernel.)
 // Warp 0 (lane 0) streams the stages; the other warps compute. In a step,
 // a thread forms the exact partials P[m] of its rows, token rows and group;
 // the two threads holding the step's two groups of the same rows swap them
@@ -954,7 +957,6 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const uint32_t sBar = base + kOffBar;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
-    volatile int *s_last = reinterpret_cast<volatile int *>(smem + kOffMisc + 12);
     int *s_base = reinterpret_cast<int *>(smem + p.tab_off);
     int *s_lo = s_base + (p.E + 1);
     int *s_cnt = s_lo + (p.E + 1);
@@ -981,7 +983,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     __syncthreads();
     const int total = *s_total;
     const int G = p.G;
-    const WorkPlan plan = make_plan(total, G, p.sk_cnt != nullptr);
+    const WorkPlan plan = make_plan(total, G, false);   // whole tiles (stream-bound)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1001,22 +1003,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int rb = (cw % kWarpsPerTb) * 16 + (lane & 15);
         const int j = lane >> 4;                      // group of the step
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
-        const int c_self = static_cast<int>(blockIdx.x);
-        auto sk_range = [&](int t, int &c_first, int &c_final) {
-            const int x0 = (t - plan.dp) * plan.S;
-            c_first = sk_owner(x0, plan);
-            c_final = sk_owner(x0 + plan.S - 1, plan);
-        };
-        auto sk_slot = [&](int t, int c) -> float * {
-            int c_first, c_final;
-            sk_range(t, c_first, c_final);
-            const int slot = (c == c_first) ? 1 : 0;
-            return p.sk_part + static_cast<size_t>(2 * c + slot) * p.sk_ld * kTileN;
-        };
-        int split_t0 = 0, split_t1 = 0, n_split = 0;
-        // After a failed wait the warp keeps walking the same piece list with
-        // no waits and no data work (the named barrier at the end has no
-        // time limit).
+        // After a failed wait the warp stops waiting and doing data work.
         bool failed = false;
         Ring a;
         float acc[RR][RM];
@@ -1138,91 +1125,15 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 else
                     static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
             };
-            const bool write = j == 0 && !failed;
-            if (s0 == 0 && s1 == plan.S) {
-                if (write) {
-#pragma unroll
-                    for (int i = 0; i < RR; ++i)
-#pragma unroll
-                        for (int u = 0; u < RM; ++u)
-                            if (n_ok[i] && tb * RM + u < ti.rows) store_out(i, u, acc[i][u]);
-                }
-                return true;
-            }
-            // Split tile: store the piece's partial now; publish and combine
-            // after the CTA's last step (as in the narrow kernel).
-            if (write) {
-                float *dst = sk_slot(t, c_self);
+            if (j == 0 && !failed) {
 #pragma unroll
                 for (int i = 0; i < RR; ++i)
 #pragma unroll
-                    for (int u = 0; u < RM; ++u) {
-                        const int m = tb * RM + u;
-                        if (n_ok[i] && m < ti.rows)
-                            __stcg(dst + m * kTileN + rb + i * (128 / RR), acc[i][u]);
-                    }
+                    for (int u = 0; u < RM; ++u)
+                        if (n_ok[i] && tb * RM + u < ti.rows) store_out(i, u, acc[i][u]);
             }
-            if (n_split == 0) split_t0 = t; else split_t1 = t;
-            n_split = min(n_split + 1, 2);
             return true;
         });
-
-        if (n_split > 0) {   // the same for all compute warps
-            __threadfence();
-            named_barrier_sync(1, 32 * CW);
-            if (ct == 0) {
-                int flags = 0;
-                griddep_wait();   // the counters were zeroed by the kernel before this one
-                for (int q = 0; q < n_split; ++q) {
-                    const int t = q == 0 ? split_t0 : split_t1;
-                    int c_first, c_final;
-                    sk_range(t, c_first, c_final);
-                    const int arrived = atomicAdd(p.sk_cnt + (t - plan.dp), 1);
-                    if (arrived == c_final - c_first) flags |= 1 << q;
-                }
-                __threadfence();
-                *s_last = flags;
-            }
-            named_barrier_sync(1, 32 * CW);
-            const int flags = *s_last;
-            for (int q = 0; q < n_split; ++q) {
-                if (((flags >> q) & 1) == 0 || failed || j != 0) continue;
-                const int t = q == 0 ? split_t0 : split_t1;
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-                int c_first, c_final;
-                sk_range(t, c_first, c_final);
-#pragma unroll
-                for (int i = 0; i < RR; ++i) {
-                    const int r = rb + i * (128 / RR);
-                    const int n_local = ti.n0 + r;
-                    if (n_local >= p.N) continue;
-                    float sum[RM];
-#pragma unroll
-                    for (int u = 0; u < RM; ++u) sum[u] = 0.0f;
-                    for (int c = c_first; c <= c_final; ++c) {
-                        const float *src = sk_slot(t, c) + r;
-                        float v[RM];
-#pragma unroll
-                        for (int u = 0; u < RM; ++u)
-                            v[u] = __ldcg(src + min(tb * RM + u, ti.rows - 1) * kTileN);
-#pragma unroll
-                        for (int u = 0; u < RM; ++u) sum[u] += v[u];
-                    }
-#pragma unroll
-                    for (int u = 0; u < RM; ++u) {
-                        const int m = tb * RM + u;
-                        if (m < ti.rows) {
-                            const float out = sum[u] * __ldg(p.sa + ti.m0 + m);
-                            const size_t idx = static_cast<size_t>(ti.m0 + m) * p.N + n_local;
-                            if (p.out_fp32)
-                                static_cast<float *>(p.y)[idx] = out;
-                            else
-                                static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
-                        }
-                    }
-                }
-            }
-        }
     }
 }
 
@@ -1414,7 +1325,7 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     return cudaGetLastError();
 }
 
-// Batched GEMV on the CUDA cores for dense calls of at most 8 token rows.
+// Batched GEMV on the CUDA cores for dense calls of at most 4 token rows.
 // kExtra: bytes of shared memory the kernel keeps after its stages.
 template <auto kernel, int MR, int CW, int kExtra>
 cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
@@ -1462,15 +1373,6 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     kp.err = err;
     const int64_t grid = kp.n_tiles < num_sms ? kp.n_tiles : num_sms;
-    // Split tile K ranges (stream-K) only where the GEMV is bound by its
-    // arithmetic (8-token tiles): when it is bound by the weight stream, the
-    // SMs of a partial last wave stream faster and the split's publish and
-    // combine cost more than they save (measured on GB300).
-    if (MR >= kGemvSplitRows && pr.sk_cnt != nullptr && grid <= kSkMaxCtas && pr.sk_ld >= pr.R) {
-        kp.sk_cnt = pr.sk_cnt;
-        kp.sk_part = pr.sk_part;
-        kp.sk_ld = pr.sk_ld;
-    }
     // Programmatic dependent launch: the kernel may start while the kernel
     // before it in the stream (the quantizer) still runs; its stage producer
     // waits for that kernel before loading the token codes.
@@ -1503,8 +1405,7 @@ cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     if (uses_gemv(pr.R, pr.offsets != nullptr)) {
         if (pr.R <= 1) return launch_gemv_mr<1, 1, 8>(pr, num_sms, stream);
         if (pr.R <= 2) return launch_gemv_mr<1, 2, 8>(pr, num_sms, stream);
-        if (pr.R <= 4) return launch_gemv_mr<1, 4, 8>(pr, num_sms, stream);
-        return launch_gemv_mr<1, 8, 8>(pr, num_sms, stream);
+        return launch_gemv_mr<1, 4, 8>(pr, num_sms, stream);
     }
     const PipeShape ps = choose_pipe(pr);
     const bool dbg = pr.debug_partials != nullptr;

@@ -21,10 +21,6 @@ cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t
                                int num_sms, cudaStream_t stream, int *cnt = nullptr,
                                int n_cnt = 0);
 
-// Zeroes n split-tile counters (programmatic dependent of the kernel before
-// it in the stream; see quant.cu).
-cudaError_t launch_zero_counters(int *cnt, int n, cudaStream_t stream);
-
 struct GemmProblem {
     const int8_t *qa;         // [R, K] int8 activation codes
     const float *sa;          // [R]
@@ -44,20 +40,19 @@ struct GemmProblem {
 
 // Dense calls with at most kGemvMaxTokens token rows run on the CUDA cores
 // (batched GEMV over the int8 codes; no fp16 staging copy is made).
-constexpr int kGemvMaxTokens = 8;
+constexpr int kGemvMaxTokens = 4;
 inline bool uses_gemv(int64_t R, bool grouped) { return !grouped && R <= kGemvMaxTokens; }
 
-// Dense calls of 5..64 token rows split tiles across CTAs (stream-K) when the
-// workspace holds the split area: arrival counters and two FP32 partial
-// slots per CTA (token rows x 128 weight rows), for at most kSkMaxCtas CTAs.
-// Both kernels are bound by their arithmetic there (the GEMV's 8-token
-// tiles; every narrow tensor-core tile), so the steps of a partial last wave
-// are worth spreading over all SMs.
+// Dense calls of 5..64 token rows (narrow tensor-core tiles) split tiles
+// across CTAs (stream-K) when the workspace holds the split area: arrival
+// counters and two FP32 partial slots per CTA (token rows x 128 weight rows),
+// for at most kSkMaxCtas CTAs. A narrow tile is bound by its MMA issue, not
+// by the weight stream, so the steps of a partial last wave are worth
+// spreading over all SMs.
 constexpr int kSkMaxCtas = 160;
-constexpr int kGemvSplitRows = 8;   // GEMV token rows per tile (rounded up to 1, 2, 4, 8)
 constexpr int kNarrowSplitMaxRows = 64;
 inline bool uses_split(int64_t R, bool grouped) {
-    return !grouped && R > kGemvSplitRows / 2 && R <= kNarrowSplitMaxRows;
+    return !grouped && R > kGemvMaxTokens && R <= kNarrowSplitMaxRows;
 }
 inline size_t sk_counter_bytes() { return 2 * kSkMaxCtas * sizeof(int); }
 inline size_t sk_area_bytes(int64_t R, bool grouped) {

@@ -241,31 +241,6 @@ cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw
     return cudaGetLastError();
 }
 
-// Zeroes the GEMV's split-tile counters. Launched as a programmatic
-// dependent of the quantizer and waiting for it before it completes, so the
-// GEMV after it (itself a programmatic dependent) starts early and its wait
-// still covers the quantizer's codes.
-__global__ void __launch_bounds__(256) zero_counters_kernel(int *__restrict__ cnt, int n) {
-    griddep_launch_dependents();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) cnt[i] = 0;
-    griddep_wait();
-}
-
-cudaError_t launch_zero_counters(int *cnt, int n, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(256);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, zero_counters_kernel, cnt, n);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
 cudaError_t launch_widen_codes(const int8_t *q, int64_t rows, int64_t K, int64_t ldq, void *out,
                                int num_sms, cudaStream_t stream, int *cnt, int n_cnt) {
     if (cnt == nullptr) n_cnt = 0;
