@@ -325,9 +325,10 @@ struct NBar {
     static constexpr int a_full = 0;                     // [kMaxAStages] TMA -> converter
     static constexpr int a_empty = a_full + kMaxAStages; // [kMaxAStages] converter -> TMA
     static constexpr int ready = a_empty + kMaxAStages;  // [2] converter (4) + admission (1) -> MMA
-    static constexpr int done = ready + kNarrowSlots;    // [2] MMA commit -> epilogue, converter, TMA
-    static constexpr int b_full = done + kNarrowSlots;   // [2] TMA -> admission
-    static constexpr int p_empty = b_full + kNarrowSlots;// [2] epilogue -> admission
+    static constexpr int done = ready + kNarrowSlots;    // [2] MMA commit -> epilogue, converter
+    static constexpr int b_full = done + kNarrowSlots;   // [kMaxBStages] token TMA -> admission
+    static constexpr int b_empty = b_full + kMaxBStages; // [kMaxBStages] epilogue -> token TMA
+    static constexpr int p_empty = b_empty + kMaxBStages;// [2] epilogue -> admission
     static constexpr int p_full = p_empty + kNarrowSlots;  // [2] wide: MMA commit per group -> epilogue
     static constexpr int drain = p_full + kNarrowSlots;
     static constexpr int count = drain + 1;
@@ -355,6 +356,12 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     constexpr int NCH = kWide ? 2 : 1;                    // 32-column chunks per epilogue warpgroup
     constexpr uint32_t kStagesOff = kWide ? kWideOffStages : kOffStages;
     const uint32_t SA = static_cast<uint32_t>(p.a_stages);
+    // Token stages: a ring of NB (narrow tiles; a stage is freed by the
+    // epilogue once the step's MMAs are complete, so the token producer runs
+    // NB - 1 steps ahead of the MMAs and the L2 latency of the token tiles is
+    // off the critical path), or the two step slots (wide tiles, NB == 2,
+    // freed by the step's commit).
+    const uint32_t NB = static_cast<uint32_t>(p.b_stages);
     const int b_rows = p.b_rows;                          // 32 or 64; 128 when kWide
     const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
     const uint32_t b_stage_bytes = 4u * b_atom_bytes;     // 2 groups x 2 atoms
@@ -383,9 +390,12 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (int i = 0; i < kNarrowSlots; ++i) {
             mbar_init(bar(NBar::ready + i), 5);
             mbar_init(bar(NBar::done + i), 1);
-            mbar_init(bar(NBar::b_full + i), 1);
             mbar_init(bar(NBar::p_empty + i), 8);
             mbar_init(bar(NBar::p_full + i), 1);
+        }
+        for (int i = 0; i < kMaxBStages; ++i) {
+            mbar_init(bar(NBar::b_full + i), 1);
+            mbar_init(bar(NBar::b_empty + i), 1);
         }
         mbar_init(bar(NBar::drain), 1);
         *s_abort = 0;
@@ -450,7 +460,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             if (!ok) drain_ring(bar(NBar::a_full), issued, SA);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------- MMA issuer
-            Ring st, pr;
+            Ring st, pr, bs;
             uint32_t gph[2] = {0u, 0u};   // wide: phase of each group's partial buffer
             bool ok = true;
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
@@ -478,7 +488,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         }
                         const uint32_t d_tmem = tmem_base + pbuf_col(pr.idx, j);
                         const uint32_t a_tmem = tmem_base + kTmemA0 + st.idx * 128u + j * 64u;
-                        const uint64_t bdesc0 = smem_desc_sw128(sB + st.idx * b_stage_bytes +
+                        const uint64_t bdesc0 = smem_desc_sw128(sB + bs.idx * b_stage_bytes +
                                                                 j * 2u * b_atom_bytes);
                         const uint64_t atom_step = b_atom_bytes >> 4;
 #pragma unroll
@@ -496,6 +506,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     mma_commit(bar(NBar::done + st.idx));
                     st.advance(kNarrowSlots);
                     pr.advance(NP);
+                    bs.advance(NB);
                 }
                 return true;
             });
@@ -504,9 +515,11 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         } else if (warp == 2 && lane == 0) {
             // -------------------------------------------- token TMA producer
             griddep_wait();   // the fp16 token codes come from the kernel launched before
-            Ring st;
+            Ring bs;
             uint32_t issued = 0;
             bool ok = true;
+            // wide: the stage is the step slot, free once the slot's commit landed
+            const int free_bar = kWide ? NBar::done : NBar::b_empty;
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int n_eff = (ti.rows + 15) & ~15;
@@ -514,32 +527,32 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 for (int sg = s0; sg < s1; ++sg) {
                     const int g0 = 2 * sg;
                     const int ng = min(2, G - g0);
-                    if (!mbar_wait(bar(NBar::done + st.idx), st.phase ^ 1u, s_abort, p.err,
+                    if (!mbar_wait(bar(free_bar + bs.idx), bs.phase ^ 1u, s_abort, p.err,
                                    ROLE_PRODUCER, 2)) {
                         ok = false;
                         return false;
                     }
-                    const uint32_t stage = sB + st.idx * b_stage_bytes;
-                    mbar_arrive_expect_tx(bar(NBar::b_full + st.idx),
+                    const uint32_t stage = sB + bs.idx * b_stage_bytes;
+                    mbar_arrive_expect_tx(bar(NBar::b_full + bs.idx),
                                           static_cast<uint32_t>(ng * 2 * nbox * kBoxRows * 128));
                     for (int j = 0; j < ng; ++j)
                         for (int a = 0; a < 2; ++a)
                             for (int i = 0; i < nbox; ++i)
                                 tma_load_2d(stage + (2 * j + a) * b_atom_bytes + i * kBoxRows * 128,
                                             &tmap_x, (g0 + j) * kGroupK + a * 64,
-                                            ti.m0 + i * kBoxRows, bar(NBar::b_full + st.idx));
-                    st.advance(kNarrowSlots);
+                                            ti.m0 + i * kBoxRows, bar(NBar::b_full + bs.idx));
+                    bs.advance(NB);
                     ++issued;
                 }
                 return true;
             });
-            if (!ok) drain_ring(bar(NBar::b_full), issued, kNarrowSlots);
+            if (!ok) drain_ring(bar(NBar::b_full), issued, NB);
         } else if (warp == 3 && lane == 0) {
             // --------------------------------------------------- admission
-            Ring st, pr;
+            Ring st, pr, bs;
             for_each_piece(plan, [&](int, int s0, int s1) -> bool {
                 for (int sg = s0; sg < s1; ++sg) {
-                    if (!mbar_wait(bar(NBar::b_full + st.idx), st.phase, s_abort, p.err, ROLE_MMA,
+                    if (!mbar_wait(bar(NBar::b_full + bs.idx), bs.phase, s_abort, p.err, ROLE_MMA,
                                    2) ||
                         (!kWide && !mbar_wait(bar(NBar::p_empty + pr.idx), pr.phase ^ 1u, s_abort,
                                               p.err, ROLE_MMA, 3)))
@@ -547,6 +560,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     mbar_arrive(bar(NBar::ready + st.idx));
                     st.advance(kNarrowSlots);
                     pr.advance(NP);
+                    bs.advance(NB);
                 }
                 return true;
             });
@@ -620,7 +634,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (int h = 0; h < NCH; ++h)
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[h][j] = 0.0f;
-        Ring st, pr;
+        Ring st, pr, bs;
         uint32_t gph[2] = {0u, 0u};   // wide: phase of each group's partial buffer
         // After a failed wait the threads keep walking the same pieces with
         // no waits and no data work, so that every epilogue warp takes the
@@ -703,6 +717,9 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     failed = true;
                     continue;
                 }
+                // The step's MMAs are complete: its token stage is free.
+                if (threadIdx.x == 256) mbar_arrive(bar(NBar::b_empty + bs.idx));
+                bs.advance(NB);
                 tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < NCH; ++h) {
@@ -1225,15 +1242,19 @@ PipeShape choose_pipe(const GemmProblem &pr) {
     s.narrow = s.b_rows <= 64;
     s.wide = !s.narrow;
     s.p_bufs = 2;
-    s.b_stages = kNarrowSlots;   // two step slots of token tiles (b_rows x 512 B)
+    // Token stages (b_rows x 512 B each): the two step slots for wide tiles; a
+    // deeper ring for narrow ones, so that token tiles are requested several
+    // steps ahead (their L2 latency, ~1 us under the weight stream, was on the
+    // critical path with two), at the cost of one weight stage.
+    s.b_stages = s.wide ? kNarrowSlots : (s.b_rows <= 32 ? 4 : 3);
     const int b_slot_bytes = 4 * s.b_rows * 128;
     // Weight stages after the fixed area: 14 KB (tile table for up to 1024
     // experts) for narrow tiles, 2 KB for wide ones.
     const int off = s.wide ? kWideOffStages : kOffStages;
-    const int avail = kSmemLimit - 1024 - off - kNarrowSlots * b_slot_bytes;
+    const int avail = kSmemLimit - 1024 - off - s.b_stages * b_slot_bytes;
     s.a_stages = avail / kNarrowAStageBytes;
     if (s.a_stages > kMaxAStages) s.a_stages = kMaxAStages;
-    s.smem_bytes = off + s.a_stages * kNarrowAStageBytes + kNarrowSlots * b_slot_bytes + 1024;
+    s.smem_bytes = off + s.a_stages * kNarrowAStageBytes + s.b_stages * b_slot_bytes + 1024;
     return s;
 }
 
