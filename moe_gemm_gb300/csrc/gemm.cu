@@ -202,25 +202,26 @@ __device__ __forceinline__ void drain_ring(uint32_t bar0, uint32_t issued, uint3
         drain_wait(bar0 + 8u * (i % slots), (i / slots) & 1u);
 }
 
-// Stream-K work split (dense calls, when the caller's workspace has room for
-// it): the tiles that fill whole waves go round-robin to the CTAs; the steps
-// of the tiles left over are divided into equal contiguous ranges, one per
-// CTA, so that every SM does the same number of steps. A CTA works on its
-// range first and on its whole tiles after it. A tile whose steps fall into
-// several ranges is finished by the CTA that completes its piece last: each
-// piece stores its FP32 partial sum (before the token scale), and after its
-// last step the CTA bumps the arrival counter of each of its split tiles
-// (deferred publish: one fence for all of them); the last arrival adds the
-// pieces in K order (so the result does not depend on arrival order),
-// applies sa and stores y. No CTA waits for another.
+// Stream-K work split (dense narrow tiles, when the caller's workspace has
+// room for it): the tiles that fill whole waves go round-robin to the CTAs;
+// the L tiles left over are split in K. When the grid holds at least two
+// CTAs per left-over tile, each of them is cut into k = min(S, grid / L)
+// equal pieces, one per CTA (a CTA then holds one split piece, so it crosses
+// one piece boundary and combines at most one tile); otherwise their steps
+// are divided into equal contiguous ranges, one per CTA. A CTA works on its
+// split piece(s) first and on its whole tiles after them. Each piece stores
+// its FP32 partial sum (before the token scale) and counts itself in; the
+// CTA that brings a tile's last piece adds the pieces in K order (so the
+// result does not depend on arrival order), applies sa and stores y. No CTA
+// waits for another.
 //
-// WorkPlan: this CTA's share of the work: the step range [u0, u1) of the
-// stream-K part (steps of tiles [dp, total), S per tile, numbered from 0 at
-// tile dp, split over g_sk CTAs), then round-robin whole tiles of [0, dp).
+// WorkPlan: this CTA's split steps [u0, u1) (steps of tiles [dp, total),
+// S per tile, numbered from 0 at tile dp; g_sk CTAs take part), then
+// round-robin whole tiles of [0, dp). k > 0: the aligned cut above.
 // All of it in 32-bit arithmetic: U < grid * S fits an int, and
 // floor(c U / g) is formed from U = q g + r as c q + floor(c r / g).
 struct WorkPlan {
-    int dp, S, g_sk, U, u0, u1;
+    int dp, S, g_sk, U, u0, u1, k;
 };
 
 __device__ __forceinline__ WorkPlan make_plan(int total, int G, bool stream_k) {
@@ -229,6 +230,7 @@ __device__ __forceinline__ WorkPlan make_plan(int total, int G, bool stream_k) {
     const int grid = static_cast<int>(gridDim.x);
     const int c = static_cast<int>(blockIdx.x);
     w.u0 = w.u1 = 0;
+    w.k = 0;
     if (!stream_k) {
         w.dp = total;
         w.g_sk = 0;
@@ -236,7 +238,19 @@ __device__ __forceinline__ WorkPlan make_plan(int total, int G, bool stream_k) {
         return w;
     }
     w.dp = (total / grid) * grid;   // whole waves; fewer than grid tiles are split
-    w.U = (total - w.dp) * w.S;
+    const int L = total - w.dp;
+    w.U = L * w.S;
+    const int k = L > 0 ? min(w.S, grid / L) : 0;
+    if (k >= 2) {
+        w.k = k;
+        w.g_sk = k * L;
+        if (c < w.g_sk) {
+            const int tl = c / k, j = c - tl * k;
+            w.u0 = tl * w.S + (j * w.S) / k;
+            w.u1 = tl * w.S + ((j + 1) * w.S) / k;
+        }
+        return w;
+    }
     w.g_sk = w.U < grid ? w.U : grid;
     if (c < w.g_sk) {
         const int q = w.U / w.g_sk, r = w.U - q * w.g_sk;
@@ -246,9 +260,9 @@ __device__ __forceinline__ WorkPlan make_plan(int total, int G, bool stream_k) {
     return w;
 }
 
-// The stream-K CTA whose step range contains step x (0 <= x < U): the largest
-// c with floor(c U / g) <= x, i.e. c U < (x + 1) g. A float estimate is
-// corrected with exact 64-bit products.
+// Contiguous ranges: the CTA whose range contains step x (0 <= x < U): the
+// largest c with floor(c U / g) <= x, i.e. c U < (x + 1) g. A float estimate
+// is corrected with exact 64-bit products.
 __device__ __forceinline__ int sk_owner(int x, const WorkPlan &w) {
     const long long rhs = static_cast<long long>(x + 1) * w.g_sk;
     int c = static_cast<int>(__fdividef(static_cast<float>(rhs), static_cast<float>(w.U)));
@@ -256,6 +270,19 @@ __device__ __forceinline__ int sk_owner(int x, const WorkPlan &w) {
     while (c > 0 && static_cast<long long>(c) * w.U >= rhs) --c;
     while (c + 1 < w.g_sk && static_cast<long long>(c + 1) * w.U < rhs) ++c;
     return c;
+}
+
+// The CTAs holding the pieces of split tile t, in K order.
+__device__ __forceinline__ void tile_owners(int t, const WorkPlan &w, int &c_first,
+                                            int &c_final) {
+    if (w.k > 0) {
+        c_first = (t - w.dp) * w.k;
+        c_final = c_first + w.k - 1;
+    } else {
+        const int x0 = (t - w.dp) * w.S;
+        c_first = sk_owner(x0, w);
+        c_final = sk_owner(x0 + w.S - 1, w);
+    }
 }
 
 // Calls f(tile, s0, s1) for every piece of this CTA in order; f returns false
@@ -778,9 +805,8 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 // meanwhile; the MMAs of the next steps fill the two
                 // partial-buffer slots.
                 const int me = static_cast<int>(blockIdx.x);
-                const int x0 = (t - plan.dp) * plan.S;
-                const int c_first = sk_owner(x0, plan);
-                const int c_final = sk_owner(x0 + plan.S - 1, plan);
+                int c_first, c_final;
+                tile_owners(t, plan, c_first, c_final);
                 auto slot = [&](int c) -> const float * {   // slot 1: the tile's first piece
                     return p.sk_part +
                            static_cast<size_t>(2 * c + (c == c_first ? 1 : 0)) * p.sk_ld * kTileN;
