@@ -408,6 +408,11 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const int lane = threadIdx.x & 31;
     const int tt = p.tile_tokens;                         // == b_rows
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+    // No griddepcontrol.launch_dependents here: the kernels of the next call
+    // (programmatic dependents) then launch only when this grid completes.
+    // Releasing them at the start, so that the next GEMM's CTAs stream
+    // weights on SMs this grid frees, made a decode step slower (measured:
+    // 162 -> 170 us).
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kMaxAStages; ++i) {

@@ -111,8 +111,12 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
     float *__restrict__ sa) {
     // A GEMM launched after this kernel as a programmatic dependent may start
     // its set-up and weight stream now; it waits for this grid (and so for qa
-    // and sa) before it reads the codes.
+    // and sa) before it reads the codes. This kernel is itself launched as a
+    // programmatic dependent of the kernel before it (which may have written
+    // the activations, or still read qa/sa): it waits for that grid before
+    // touching either.
     griddep_launch_dependents();
+    griddep_wait();
     __shared__ uint32_t red[kQuantThreads / 32];
     const int64_t row = blockIdx.x;
     const uint4 *src = reinterpret_cast<const uint4 *>(a + row * lda);
@@ -143,6 +147,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
 __global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
     const uint16_t *__restrict__ a, int K, int64_t lda, int8_t *__restrict__ qa, int64_t ldq,
     float *__restrict__ sa) {
+    griddep_launch_dependents();   // as in quant_act_vec_kernel
+    griddep_wait();
     __shared__ uint32_t red[kQuantThreads / 32];
     const int64_t row = blockIdx.x;
     const uint16_t *src = a + row * lda;
@@ -187,12 +193,13 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restri
     // The GEMM that consumes this copy is launched as a programmatic
     // dependent: let it start its set-up and weight stream right away. This
     // kernel is itself a programmatic dependent of the quantizer: wait for
-    // its codes. The GEMM's split counters are free to reset at once: no GEMM
-    // releases its dependents early, so the one before (if any) has exited.
+    // its codes (and so, through the quantizer's own wait, for any GEMM
+    // before it, which may still use the split counters and the staging
+    // copy), before it resets or writes either.
     griddep_launch_dependents();
+    griddep_wait();
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
-    griddep_wait();
     const int vec_per_row = K >> 4;  // 16 codes per vector
     const int64_t total = rows * vec_per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -213,6 +220,24 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restri
 
 }  // namespace
 
+// Launch as a programmatic dependent of the previous kernel in the stream.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
                              int64_t ldq, float *sa, cudaStream_t stream) {
     const bool vec_ok = (K % 8 == 0) && (lda % 8 == 0) && (ldq % 8 == 0) &&
@@ -220,17 +245,16 @@ cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t ld
                         (reinterpret_cast<uintptr_t>(qa) % 8 == 0);
     const int k = static_cast<int>(K);
     const dim3 grid(static_cast<unsigned>(M));
+    const dim3 block(kQuantThreads);
     if (vec_ok && K <= 256 * 8 * 1)
-        quant_act_vec_kernel<1><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
-    else if (vec_ok && K <= 256 * 8 * 2)
-        quant_act_vec_kernel<2><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
-    else if (vec_ok && K <= 256 * 8 * 4)
-        quant_act_vec_kernel<4><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
-    else if (vec_ok && K <= 256 * 8 * 8)
-        quant_act_vec_kernel<8><<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
-    else
-        quant_act_generic_kernel<<<grid, kQuantThreads, 0, stream>>>(a, k, lda, qa, ldq, sa);
-    return cudaGetLastError();
+        return launch_pdl(quant_act_vec_kernel<1>, grid, block, stream, a, k, lda, qa, ldq, sa);
+    if (vec_ok && K <= 256 * 8 * 2)
+        return launch_pdl(quant_act_vec_kernel<2>, grid, block, stream, a, k, lda, qa, ldq, sa);
+    if (vec_ok && K <= 256 * 8 * 4)
+        return launch_pdl(quant_act_vec_kernel<4>, grid, block, stream, a, k, lda, qa, ldq, sa);
+    if (vec_ok && K <= 256 * 8 * 8)
+        return launch_pdl(quant_act_vec_kernel<8>, grid, block, stream, a, k, lda, qa, ldq, sa);
+    return launch_pdl(quant_act_generic_kernel, grid, block, stream, a, k, lda, qa, ldq, sa);
 }
 
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
