@@ -2,7 +2,9 @@
 
 One step = one pass of the whole hot path over the decode-shaped dense
 workload: for each token count M in {1, 8, 32} (K=8192, N=28672, BF16 out),
-per-token activation quantization followed by the group-scaled INT8 GEMM.
+per-token activation quantization followed by the group-scaled INT8 GEMM, as
+one library call per shape (w8a8_linear: the quantizer writes the GEMM's
+operand into the workspace, then the GEMM runs).
 Each GEMM of the step reads its own 235 MB weight copy, so every input is
 larger than L2 and no weight bytes are reused from L2 between GEMMs.
 
@@ -232,30 +234,27 @@ def run_ours(args):
                             off=None))
     for d in per:
         shp = d["shape"]
-        d["qa"] = torch.empty((shp.M, shp.K), dtype=torch.int8, device=dev)
-        d["sa"] = torch.empty((shp.M,), dtype=torch.float32, device=dev)
         odt = torch.bfloat16 if shp.out == "bf16" else torch.float32
         d["y"] = torch.empty((shp.M, shp.N), dtype=odt, device=dev)
-        wsz = (w8.grouped_gemm_workspace_size(shp.M, shp.E, shp.N, shp.K) if d["off"] is not None
-               else w8.gemm_workspace_size(shp.M, shp.N, shp.K))
+        wsz = (w8.grouped_linear_workspace_size(shp.M, shp.E, shp.N, shp.K)
+               if d["off"] is not None else w8.linear_workspace_size(shp.M, shp.N, shp.K))
         d["ws"] = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
-        # quantizer + GEMM, plus the fp16 staging kernel on the tensor-core
-        # paths (the CUDA-core GEMV for <= 4 token rows reads the int8 codes)
-        d["launches"] = 2 if (d["off"] is None and shp.M <= 4) else 3
+        # one public call per shape: the quantizer (writing the GEMM's operand
+        # into the workspace) and the GEMM
+        d["launches"] = 2
     torch.cuda.synchronize()
 
-    def gemm_call(d, s=None):
+    def linear_call(d, s=None):
         s = stream if s is None else s
         if d["off"] is not None:
-            w8.grouped_gemm(d["qa"], d["sa"], d["off"], d["qw"], d["sw"], out=d["y"],
-                            out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
+            w8.grouped_linear(d["a"], d["off"], d["qw"], d["sw"], out=d["y"],
+                              out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
         else:
-            w8.gemm(d["qa"], d["sa"], d["qw"], d["sw"], out=d["y"], out_dtype=d["y"].dtype,
-                    workspace=d["ws"], stream=s)
+            w8.linear(d["a"], d["qw"], d["sw"], out=d["y"], out_dtype=d["y"].dtype,
+                      workspace=d["ws"], stream=s)
 
     def shape_call(d):
-        w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"], stream=stream)
-        gemm_call(d)
+        linear_call(d)
 
     def step():
         for d in per:
@@ -362,8 +361,7 @@ def run_ours(args):
         def e2e_step():
             for d, hi, ho in zip(per, host_in, host_out):
                 d["a"].copy_(hi, non_blocking=True)
-                w8.quant_act(d["a"], qa=d["qa"], sa=d["sa"], stream=cur)
-                gemm_call(d, cur)
+                linear_call(d, cur)
                 ho.copy_(d["y"], non_blocking=True)
 
         for _ in range(args.warmup):

@@ -152,6 +152,53 @@ w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *
                               w8a8_stream_t stream);
 
 /*
+ * Bytes of device workspace w8a8_linear asks for: the M x K activation codes
+ * (M * K * 2 bytes, rounded up to 256), the M token scales (M * 4 bytes,
+ * rounded up to 256), then for 5 <= M <= 64 the optional split area of
+ * w8a8_gemm_workspace_size. 0 when M == 0. A workspace without the split
+ * area is accepted (tiles then are never split across CTAs).
+ */
+size_t w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * The quantized linear layer in one call: per-token activation quantization
+ * (w8a8_quant_act, Hunyuan-770B page §3.1: dynamic per-token INT8) followed by
+ * the group-scaled GEMM (w8a8_gemm). The quantizer writes the codes and token
+ * scales into the workspace in the form the GEMM reads (int8 for M <= 4,
+ * fp16 for the tensor-core path), so no staging copy is made in between.
+ *   a_bf16 [M, K] BF16, row stride lda >= K elements (2-byte aligned)
+ *   qw [N, K] int8, sw [N, K/128] float   (from w8a8_quant_weight)
+ *   y  [M, N] BF16 (round to nearest even) or FP32, per y_dtype.
+ *   workspace: device buffer, 256-byte aligned, of w8a8_linear_workspace_size(M,
+ *              N, K) bytes (at least the codes and scales, see above); scratch.
+ * The result is identical to w8a8_quant_act followed by w8a8_gemm with the
+ * same workspace split behaviour (same codes, scales and kernels), with the
+ * error bound stated there. K a positive multiple of 128; N >= 1; M == 0 is
+ * a no-op. Returns W8A8_ERR_WORKSPACE when the workspace is missing, not
+ * 256-byte aligned or smaller than the codes and scales.
+ */
+w8a8_status w8a8_linear(const void *a_bf16, int64_t lda, const int8_t *qw, const float *sw,
+                        void *y, w8a8_dtype y_dtype, int64_t M, int64_t N, int64_t K,
+                        void *workspace, size_t workspace_bytes, w8a8_stream_t stream);
+
+/*
+ * Bytes of device workspace w8a8_grouped_linear needs for R routed rows: the
+ * R x K codes (R * K * 2 bytes) and R token scales, each rounded up to 256.
+ */
+size_t w8a8_grouped_linear_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K);
+
+/*
+ * w8a8_grouped_gemm with the per-token quantization of its routed rows in the
+ * same call (as w8a8_linear): a_bf16 [R, K] BF16 rows sorted by expert (row
+ * stride lda), offsets [E+1] int32 on the device, qw [E, N, K], sw [E, N, K/128],
+ * y [R, N]. Identical result to w8a8_quant_act + w8a8_grouped_gemm.
+ */
+w8a8_status w8a8_grouped_linear(const void *a_bf16, int64_t lda, const int32_t *offsets,
+                                const int8_t *qw, const float *sw, void *y, w8a8_dtype y_dtype,
+                                int64_t R, int64_t E, int64_t N, int64_t K, void *workspace,
+                                size_t workspace_bytes, w8a8_stream_t stream);
+
+/*
  * Size of the scratch array built into the library for w8a8_gemm_noalloc:
  * 8 MiB, enough for M * K <= 4,194,304 activation codes (e.g. M <= 512 at
  * K = 8192, M <= 256 at K = 16384).

@@ -54,9 +54,17 @@ def _load() -> ctypes.CDLL:
     lib.w8a8_status_string.restype = ctypes.c_char_p
     lib.w8a8_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint64), i32]
     lib.w8a8_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+    lib.w8a8_linear_workspace_size.argtypes = [i64, i64, i64]
+    lib.w8a8_linear_workspace_size.restype = ctypes.c_size_t
+    lib.w8a8_grouped_linear_workspace_size.argtypes = [i64, i64, i64, i64]
+    lib.w8a8_grouped_linear_workspace_size.restype = ctypes.c_size_t
+    lib.w8a8_linear.argtypes = [vp, i64, vp, vp, vp, i32, i64, i64, i64, vp, ctypes.c_size_t, vp]
+    lib.w8a8_grouped_linear.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64, i64, i64, i64, vp,
+                                        ctypes.c_size_t, vp]
     lib.w8a8_version.restype = i32
     for name in ("w8a8_quant_act", "w8a8_quant_weight", "w8a8_gemm", "w8a8_grouped_gemm",
-                 "w8a8_gemm_noalloc", "w8a8_device_error", "w8a8_selftest_wait_timeout"):
+                 "w8a8_gemm_noalloc", "w8a8_device_error", "w8a8_selftest_wait_timeout",
+                 "w8a8_linear", "w8a8_grouped_linear"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -208,6 +216,62 @@ def grouped_gemm(qa: torch.Tensor, sa: torch.Tensor, offsets: torch.Tensor, qw: 
                                   _dtype_code(out_dtype), R, E, N, K, _ptr(P), _ptr(workspace),
                                   workspace.numel(), _stream(stream)), "w8a8_grouped_gemm")
     return (y, P) if debug_partials else y
+
+
+def linear_workspace_size(M: int, N: int, K: int) -> int:
+    return int(_lib.w8a8_linear_workspace_size(M, N, K))
+
+
+def grouped_linear_workspace_size(R: int, E: int, N: int, K: int) -> int:
+    return int(_lib.w8a8_grouped_linear_workspace_size(R, E, N, K))
+
+
+def _require_act(a: torch.Tensor) -> int:
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or not a.is_cuda or a.stride(1) != 1:
+        raise ValueError("a must be a CUDA bfloat16 [M, K] tensor with unit column stride")
+    return a.stride(0)
+
+
+def linear(a: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
+           out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+           workspace: Optional[torch.Tensor] = None,
+           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """quant_act + gemm in one call: Y[M,N] from BF16 activations a [M, K]
+    (the quantizer writes the GEMM's operand directly into the workspace)."""
+    lda = _require_act(a)
+    _require(qw, torch.int8, "qw", 2)
+    _require(sw, torch.float32, "sw", 2)
+    M, K = a.shape
+    N = qw.shape[0]
+    y = torch.empty((M, N), dtype=out_dtype, device=a.device) if out is None else out
+    if workspace is None:
+        workspace = torch.empty(max(linear_workspace_size(M, N, K), 1), dtype=torch.uint8,
+                                device=a.device)
+    _check(_lib.w8a8_linear(_ptr(a), lda, _ptr(qw), _ptr(sw), _ptr(y), _dtype_code(out_dtype),
+                            M, N, K, _ptr(workspace), workspace.numel(), _stream(stream)),
+           "w8a8_linear")
+    return y
+
+
+def grouped_linear(a: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
+                   out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """quant_act + grouped_gemm in one call over rows sorted by expert."""
+    lda = _require_act(a)
+    _require(qw, torch.int8, "qw", 3)
+    _require(sw, torch.float32, "sw", 3)
+    _require(offsets, torch.int32, "offsets", 1)
+    R, K = a.shape
+    E, N, _ = qw.shape
+    y = torch.empty((R, N), dtype=out_dtype, device=a.device) if out is None else out
+    if workspace is None:
+        workspace = torch.empty(max(grouped_linear_workspace_size(R, E, N, K), 1),
+                                dtype=torch.uint8, device=a.device)
+    _check(_lib.w8a8_grouped_linear(_ptr(a), lda, _ptr(offsets), _ptr(qw), _ptr(sw), _ptr(y),
+                                    _dtype_code(out_dtype), R, E, N, K, _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "w8a8_grouped_linear")
+    return y
 
 
 def selftest_wait_timeout(limit_us: int = 20000,

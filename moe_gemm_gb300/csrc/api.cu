@@ -132,6 +132,88 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
 }
 
 // ---------------------------------------------------------------------------
+// Fused quantizer + GEMM (w8a8_linear, w8a8_grouped_linear). Workspace: the
+// codes [R, K] (int8 for the CUDA-core GEMV, else fp16 for the tensor-core
+// GEMM, M*K*2 bytes either way), the token scales [R], then the optional
+// split area. The quantizer writes the operand the GEMM reads, so the
+// tensor-core path needs no staging kernel.
+size_t linear_scales_offset(int64_t R, int64_t K) { return staging_bytes(R, K); }
+size_t linear_required_bytes(int64_t R, int64_t K) {
+    if (R <= 0) return 0;
+    return staging_bytes(R, K) + round_up(static_cast<size_t>(R) * 4, kWsAlign);
+}
+size_t linear_bytes_for(int64_t R, int64_t K, bool grouped) {
+    if (R <= 0) return 0;
+    return linear_required_bytes(R, K) + round_up(w8a8::sk_area_bytes(R, grouped), kWsAlign);
+}
+
+w8a8_status check_linear(const void *a, int64_t lda, const void *offsets, const int8_t *qw,
+                         const float *sw, const void *y, w8a8_dtype y_dtype, int64_t R, int64_t E,
+                         int64_t N, int64_t K, bool grouped, void *workspace,
+                         size_t workspace_bytes) {
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    if (R < 0 || N <= 0 || K <= 0 || E <= 0 || lda < K) return W8A8_ERR_INVALID_ARG;
+    if (K % W8A8_GROUP != 0) return W8A8_ERR_INVALID_ARG;
+    if (grouped && E > w8a8::kMaxExperts) return W8A8_ERR_INVALID_ARG;
+    if (R > kMaxElems / lda || E * N > kMaxElems / K || R > kMaxElems / N)
+        return W8A8_ERR_INVALID_ARG;
+    if (R == 0) return W8A8_OK;
+    if (!a || !qw || !sw || !y || (grouped && !offsets)) return W8A8_ERR_INVALID_ARG;
+    if (!aligned(a, 2) || !aligned(qw, 16) || !aligned(sw, 4) || !aligned(y, 4) ||
+        (offsets && !aligned(offsets, 4)))
+        return W8A8_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < linear_required_bytes(R, K) ||
+        !aligned(workspace, kWsAlign))
+        return W8A8_ERR_WORKSPACE;
+    return W8A8_OK;
+}
+
+w8a8_status run_linear(const void *a, int64_t lda, const int32_t *offsets, const int8_t *qw,
+                       const float *sw, void *y, w8a8_dtype y_dtype, int64_t R, int64_t E,
+                       int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                       w8a8_stream_t stream) {
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool grouped = offsets != nullptr;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    float *sa = reinterpret_cast<float *>(ws + linear_scales_offset(R, K));
+    w8a8::GemmProblem p;
+    if (w8a8::sk_area_bytes(R, grouped) > 0 &&
+        workspace_bytes >= linear_bytes_for(R, K, grouped)) {
+        unsigned char *area = ws + linear_required_bytes(R, K);
+        p.sk_cnt = reinterpret_cast<int *>(area);
+        p.sk_part = reinterpret_cast<float *>(area + w8a8::sk_counter_bytes());
+        p.sk_ld = static_cast<int>(R);
+    }
+    const uint16_t *a16 = static_cast<const uint16_t *>(a);
+    cudaError_t e;
+    if (w8a8::uses_gemv(R, grouped)) {
+        e = w8a8::launch_quant_act(a16, R, K, lda, reinterpret_cast<int8_t *>(ws), K, sa, s);
+        p.qa = reinterpret_cast<const int8_t *>(ws);
+    } else {
+        e = w8a8::launch_quant_act_f16(a16, R, K, lda, ws, sa, p.sk_cnt,
+                                       p.sk_cnt != nullptr ? 2 * w8a8::kSkMaxCtas : 0, s);
+        p.qa = nullptr;   // the tensor-core GEMM reads only the fp16 codes
+    }
+    if (e != cudaSuccess) return W8A8_ERR_CUDA;
+    p.sa = sa;
+    p.sw = sw;
+    p.qw = qw;
+    p.x16 = ws;
+    p.offsets = offsets;
+    p.y = y;
+    p.debug_partials = nullptr;
+    p.R = R;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.out_fp32 = (y_dtype == W8A8_FP32);
+    return from_cuda(w8a8::launch_gemm(p, info.num_sms, s));
+}
+
+// ---------------------------------------------------------------------------
 // Built-in scratch for w8a8_gemm_noalloc: the fp16 staging copy of the
 // activation codes lives in this fixed device array instead of a caller
 // workspace. Every GPU that loads the library keeps it until the process
@@ -243,6 +325,40 @@ w8a8_status w8a8_grouped_gemm(const int8_t *qa, const float *sa, const int32_t *
     if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
     return run_gemm(qa, sa, offsets, qw, sw, y, y_dtype, R, E, N, K, debug_partials, workspace,
                     workspace_bytes, stream);
+}
+
+size_t w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    if (K <= 0) return 0;
+    return linear_bytes_for(M, K, false);
+}
+
+size_t w8a8_grouped_linear_workspace_size(int64_t R, int64_t E, int64_t N, int64_t K) {
+    (void)E;
+    (void)N;
+    if (K <= 0) return 0;
+    return linear_bytes_for(R, K, true);
+}
+
+w8a8_status w8a8_linear(const void *a_bf16, int64_t lda, const int8_t *qw, const float *sw,
+                        void *y, w8a8_dtype y_dtype, int64_t M, int64_t N, int64_t K,
+                        void *workspace, size_t workspace_bytes, w8a8_stream_t stream) {
+    w8a8_status st = check_linear(a_bf16, lda, nullptr, qw, sw, y, y_dtype, M, 1, N, K, false,
+                                  workspace, workspace_bytes);
+    if (st != W8A8_OK || M == 0) return st;
+    return run_linear(a_bf16, lda, nullptr, qw, sw, y, y_dtype, M, 1, N, K, workspace,
+                      workspace_bytes, stream);
+}
+
+w8a8_status w8a8_grouped_linear(const void *a_bf16, int64_t lda, const int32_t *offsets,
+                                const int8_t *qw, const float *sw, void *y, w8a8_dtype y_dtype,
+                                int64_t R, int64_t E, int64_t N, int64_t K, void *workspace,
+                                size_t workspace_bytes, w8a8_stream_t stream) {
+    w8a8_status st = check_linear(a_bf16, lda, offsets, qw, sw, y, y_dtype, R, E, N, K, true,
+                                  workspace, workspace_bytes);
+    if (st != W8A8_OK || R == 0) return st;
+    return run_linear(a_bf16, lda, offsets, qw, sw, y, y_dtype, R, E, N, K, workspace,
+                      workspace_bytes, stream);
 }
 
 w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *qw,

@@ -11,6 +11,12 @@ namespace w8a8 {
 cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
                              int64_t ldq, float *sa, cudaStream_t stream);
 
+// The same codes as launch_quant_act, written as fp16 (row stride K) into
+// x16 for the tensor-core GEMM, which then needs no staging kernel; also
+// zeroes n_cnt split counters at cnt (if not null) for that GEMM.
+cudaError_t launch_quant_act_f16(const uint16_t *a, int64_t M, int64_t K, int64_t lda, void *x16,
+                                 float *sa, int *cnt, int n_cnt, cudaStream_t stream);
+
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
                                 cudaStream_t stream);
 

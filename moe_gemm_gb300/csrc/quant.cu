@@ -105,10 +105,14 @@ __device__ __forceinline__ uint32_t amax_bits8(const uint4 v) {
 
 // One CTA per token row; the row stays in registers between the amax pass and
 // the quantize pass (VPT 16-byte vectors per thread, K <= 256 * 8 * VPT).
-template <int VPT>
+// kF16: the codes are written as fp16 (exact integers; the tensor-core GEMM's
+// operand) instead of int8, and block 0 also zeroes n_cnt split counters of
+// the GEMM that follows (after the wait below, so the GEMM before it, which
+// may share them, has finished).
+template <int VPT, bool kF16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
-    const uint16_t *__restrict__ a, int K, int64_t lda, int8_t *__restrict__ qa, int64_t ldq,
-    float *__restrict__ sa) {
+    const uint16_t *__restrict__ a, int K, int64_t lda, void *__restrict__ out, int64_t ldq,
+    float *__restrict__ sa, int *__restrict__ cnt, int n_cnt) {
     // A GEMM launched after this kernel as a programmatic dependent may start
     // its set-up and weight stream now; it waits for this grid (and so for qa
     // and sa) before it reads the codes. This kernel is itself launched as a
@@ -117,10 +121,11 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
     // touching either.
     griddep_launch_dependents();
     griddep_wait();
+    if (kF16 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
     __shared__ uint32_t red[kQuantThreads / 32];
     const int64_t row = blockIdx.x;
     const uint4 *src = reinterpret_cast<const uint4 *>(a + row * lda);
-    uint2 *dst = reinterpret_cast<uint2 *>(qa + row * ldq);
     const int nvec = K >> 3;
     uint4 v[VPT];
     uint32_t m = 0;
@@ -139,16 +144,28 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int idx = threadIdx.x + i * kQuantThreads;
-        if (idx < nvec) __stcs(dst + idx, quantize8(v[i], s, r, fast));
+        if (idx >= nvec) continue;
+        const uint2 q = quantize8(v[i], s, r, fast);
+        if constexpr (kF16) {
+            uint4 h;
+            i8x4_to_f16x4(q.x, h.x, h.y);
+            i8x4_to_f16x4(q.y, h.z, h.w);
+            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldq)[idx] = h;
+        } else {
+            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldq) + idx, q);
+        }
     }
 }
 
 // Any K / stride / alignment: scalar two-pass version (re-reads the row).
+template <bool kF16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
-    const uint16_t *__restrict__ a, int K, int64_t lda, int8_t *__restrict__ qa, int64_t ldq,
-    float *__restrict__ sa) {
+    const uint16_t *__restrict__ a, int K, int64_t lda, void *__restrict__ out, int64_t ldq,
+    float *__restrict__ sa, int *__restrict__ cnt, int n_cnt) {
     griddep_launch_dependents();   // as in quant_act_vec_kernel
     griddep_wait();
+    if (kF16 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
     __shared__ uint32_t red[kQuantThreads / 32];
     const int64_t row = blockIdx.x;
     const uint16_t *src = a + row * lda;
@@ -157,9 +174,13 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
     m = block_max_u32(m, red);
     const float s = __fdiv_rn(bf16_bits_to_f32(m), 127.0f);
     if (threadIdx.x == 0) sa[row] = s;
-    for (int k = threadIdx.x; k < K; k += kQuantThreads)
-        qa[row * ldq + k] =
-            static_cast<int8_t>(s == 0.0f ? 0 : quantize_exact(bf16_bits_to_f32(src[k]), s));
+    for (int k = threadIdx.x; k < K; k += kQuantThreads) {
+        const int q = s == 0.0f ? 0 : quantize_exact(bf16_bits_to_f32(src[k]), s);
+        if constexpr (kF16)
+            static_cast<__half *>(out)[row * ldq + k] = __int2half_rn(q);
+        else
+            static_cast<int8_t *>(out)[row * ldq + k] = static_cast<int8_t>(q);
+    }
 }
 
 // One warp per (row n, group g): 128 floats, 4 per lane.
@@ -218,8 +239,6 @@ __global__ void __launch_bounds__(256) widen_codes_kernel(const int8_t *__restri
     }
 }
 
-}  // namespace
-
 // Launch as a programmatic dependent of the previous kernel in the stream.
 template <typename... Params, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t stream,
@@ -238,23 +257,43 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStr
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
-                             int64_t ldq, float *sa, cudaStream_t stream) {
+template <bool kF16>
+cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, void *out,
+                         int64_t ldq, float *sa, int *cnt, int n_cnt, cudaStream_t stream) {
+    const int align = kF16 ? 16 : 8;   // one 8-code vector per store
     const bool vec_ok = (K % 8 == 0) && (lda % 8 == 0) && (ldq % 8 == 0) &&
                         (reinterpret_cast<uintptr_t>(a) % 16 == 0) &&
-                        (reinterpret_cast<uintptr_t>(qa) % 8 == 0);
+                        (reinterpret_cast<uintptr_t>(out) % align == 0);
     const int k = static_cast<int>(K);
     const dim3 grid(static_cast<unsigned>(M));
     const dim3 block(kQuantThreads);
+    if (cnt == nullptr) n_cnt = 0;
     if (vec_ok && K <= 256 * 8 * 1)
-        return launch_pdl(quant_act_vec_kernel<1>, grid, block, stream, a, k, lda, qa, ldq, sa);
+        return launch_pdl(quant_act_vec_kernel<1, kF16>, grid, block, stream, a, k, lda, out, ldq,
+                          sa, cnt, n_cnt);
     if (vec_ok && K <= 256 * 8 * 2)
-        return launch_pdl(quant_act_vec_kernel<2>, grid, block, stream, a, k, lda, qa, ldq, sa);
+        return launch_pdl(quant_act_vec_kernel<2, kF16>, grid, block, stream, a, k, lda, out, ldq,
+                          sa, cnt, n_cnt);
     if (vec_ok && K <= 256 * 8 * 4)
-        return launch_pdl(quant_act_vec_kernel<4>, grid, block, stream, a, k, lda, qa, ldq, sa);
+        return launch_pdl(quant_act_vec_kernel<4, kF16>, grid, block, stream, a, k, lda, out, ldq,
+                          sa, cnt, n_cnt);
     if (vec_ok && K <= 256 * 8 * 8)
-        return launch_pdl(quant_act_vec_kernel<8>, grid, block, stream, a, k, lda, qa, ldq, sa);
-    return launch_pdl(quant_act_generic_kernel, grid, block, stream, a, k, lda, qa, ldq, sa);
+        return launch_pdl(quant_act_vec_kernel<8, kF16>, grid, block, stream, a, k, lda, out, ldq,
+                          sa, cnt, n_cnt);
+    return launch_pdl(quant_act_generic_kernel<kF16>, grid, block, stream, a, k, lda, out, ldq, sa,
+                      cnt, n_cnt);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
+                             int64_t ldq, float *sa, cudaStream_t stream) {
+    return launch_quant<false>(a, M, K, lda, qa, ldq, sa, nullptr, 0, stream);
+}
+
+cudaError_t launch_quant_act_f16(const uint16_t *a, int64_t M, int64_t K, int64_t lda, void *x16,
+                                 float *sa, int *cnt, int n_cnt, cudaStream_t stream) {
+    return launch_quant<true>(a, M, K, lda, x16, K, sa, cnt, n_cnt, stream);
 }
 
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,

@@ -30,6 +30,13 @@ def lib():
     L.w8a8_grouped_gemm_workspace_size.restype = ctypes.c_size_t
     L.w8a8_status_string.argtypes = [i32]
     L.w8a8_status_string.restype = ctypes.c_char_p
+    L.w8a8_linear_workspace_size.argtypes = [i64, i64, i64]
+    L.w8a8_linear_workspace_size.restype = ctypes.c_size_t
+    L.w8a8_grouped_linear_workspace_size.argtypes = [i64, i64, i64, i64]
+    L.w8a8_grouped_linear_workspace_size.restype = ctypes.c_size_t
+    L.w8a8_linear.argtypes = [vp, i64, vp, vp, vp, i32, i64, i64, i64, vp, ctypes.c_size_t, vp]
+    L.w8a8_grouped_linear.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64, i64, i64, i64, vp,
+                                      ctypes.c_size_t, vp]
     return L
 
 
@@ -143,3 +150,42 @@ def test_selftest_wait_validation(lib):
     # refused on the host: never launches
     assert lib.w8a8_selftest_wait_timeout(0, None) == INVALID
     assert lib.w8a8_selftest_wait_timeout(2000001, None) == INVALID
+
+
+def test_linear_workspace_size(lib):
+    # codes (M*K*2) and scales (M*4), each rounded up to 256 bytes, then the
+    # optional K-split area for 5..64 dense rows
+    def base(M, K):
+        return _staging(M, K) + (M * 4 + 255) // 256 * 256
+    assert lib.w8a8_linear_workspace_size(0, 128, 128) == 0
+    assert lib.w8a8_linear_workspace_size(1, 28672, 8192) == base(1, 8192)
+    assert lib.w8a8_linear_workspace_size(4, 128, 128) == base(4, 128)
+    assert lib.w8a8_linear_workspace_size(32, 28672, 8192) == base(32, 8192) + _split_area(32)
+    assert lib.w8a8_linear_workspace_size(65, 128, 256) == base(65, 256)
+    assert lib.w8a8_grouped_linear_workspace_size(4096, 64, 3072, 4096) == base(4096, 4096)
+    assert lib.w8a8_grouped_linear_workspace_size(8, 64, 3072, 4096) == base(8, 4096)
+
+
+def test_linear_host_validation(lib):
+    def call(a=FAKE, lda=256, qw=FAKE, sw=FAKE, y=FAKE, dt=0, M=16, N=128, K=256, ws=FAKE,
+             wsb=1 << 30):
+        return lib.w8a8_linear(a, lda, qw, sw, y, dt, M, N, K, ws, wsb, None)
+    assert call(K=100, lda=100) == INVALID              # K % 128 != 0
+    assert call(lda=128) == INVALID                     # lda < K
+    assert call(a=None) == INVALID
+    assert call(a=FAKE + 1) == INVALID                  # BF16 rows must be 2-byte aligned
+    assert call(qw=FAKE + 8) == INVALID                 # TMA operand not 16-byte aligned
+    assert call(dt=5) == INVALID
+    assert call(N=0) == INVALID
+    assert call(ws=None) == WORKSPACE
+    assert call(ws=FAKE + 16) == WORKSPACE
+    assert call(wsb=16 * 256 * 2) == WORKSPACE          # no room for the scales
+    assert call(M=0) == OK
+
+    def gcall(off=FAKE, E=4, R=64, wsb=1 << 30):
+        return lib.w8a8_grouped_linear(FAKE, 256, off, FAKE, FAKE, FAKE, 0, R, E, 128, 256,
+                                       FAKE, wsb, None)
+    assert gcall(off=None) == INVALID
+    assert gcall(E=1025) == INVALID
+    assert gcall(wsb=100) == WORKSPACE
+    assert gcall(R=0) == OK

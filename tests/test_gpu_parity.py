@@ -345,3 +345,68 @@ def test_grouped_minimal_workspace_matches_oracle():
         torch.cuda.synchronize()
         check_fp32(y.cpu().numpy()[covered], y_ref[covered], T[covered], K)
     assert w8.device_error(clear=True) == 0
+
+
+# --------------------------------------------- fused quantizer + GEMM entry
+def _linear_only_workspace(M, K):
+    """Codes and scales only: tiles are never split."""
+    n = (M * K * 2 + 255) // 256 * 256 + (M * 4 + 255) // 256 * 256
+    return torch.empty(n, dtype=torch.uint8, device=DEV)
+
+
+@pytest.mark.parametrize("M,N,K,out,lda_pad", [
+    (1, 1000, 1152, "bf16", 0),     # CUDA-core GEMV path (int8 codes in the workspace)
+    (3, 256, 384, "fp32", 8),       # GEMV, strided activations
+    (8, 4096, 2048, "fp32", 0),     # tensor-core path, split
+    (33, 1000, 1152, "bf16", 0),    # tensor-core path, split, ragged N
+    (64, 28672, 1024, "bf16", 16),  # 64-row tiles, strided activations
+    (130, 384, 640, "fp32", 0),     # 128-row tiles (wide form), ragged token tail
+])
+def test_linear_equals_quant_then_gemm(M, N, K, out, lda_pad):
+    rng = np.random.default_rng(M + 3 * N + K)
+    a_bits = workloads.f32_to_bf16_bits(rng.standard_normal((M, K + lda_pad)).astype(np.float32))
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    a_full = to_dev_bf16(a_bits)
+    a = a_full[:, :K]                                   # row stride K + lda_pad
+    qw, sw = w8.quant_weight(torch.from_numpy(np.ascontiguousarray(w)).to(DEV))
+    dt = torch.float32 if out == "fp32" else torch.bfloat16
+    qa, sa = w8.quant_act(a.contiguous())
+    y_two = w8.gemm(qa, sa, qw, sw, out_dtype=dt)
+    for ws in (None, _linear_only_workspace(M, K)):
+        y = torch.full((M, N), float("nan"), dtype=dt, device=DEV)
+        w8.linear(a, qw, sw, out_dtype=dt, out=y, workspace=ws)
+        torch.cuda.synchronize()
+        if ws is None:   # same codes, scales, kernels and split as the two calls
+            assert torch.equal(y, y_two)
+        qa_o, sa_o = oracle.quant_act(np.ascontiguousarray(a_bits[:, :K]))
+        y_ref, T = oracle.gemm(qa_o, sa_o, *oracle.quant_weight(w))
+        if out == "fp32":
+            check_fp32(y.cpu().numpy(), y_ref, T, K)
+        else:
+            check_bf16(bf16_bits_of(y), y_ref, T)
+    assert w8.device_error(clear=True) == 0
+
+
+def test_grouped_linear_equals_quant_then_grouped_gemm():
+    rng = np.random.default_rng(91)
+    R, E, N, K = 700, 9, 256, 512
+    off = workloads.random_offsets(rng, R, E, empty_frac=0.3)
+    a_bits = workloads.f32_to_bf16_bits(rng.standard_normal((R, K)).astype(np.float32))
+    w = (rng.standard_normal((E * N, K)) * 0.02).astype(np.float32)
+    a = to_dev_bf16(a_bits)
+    qw, sw = w8.quant_weight(torch.from_numpy(w).to(DEV))
+    qw, sw = qw.view(E, N, K), sw.view(E, N, K // G)
+    offs = torch.from_numpy(off).to(DEV)
+    qa, sa = w8.quant_act(a)
+    y_two = torch.full((R, N), float("nan"), dtype=torch.float32, device=DEV)
+    w8.grouped_gemm(qa, sa, offs, qw, sw, out_dtype=torch.float32, out=y_two)
+    y = torch.full((R, N), float("nan"), dtype=torch.float32, device=DEV)
+    w8.grouped_linear(a, offs, qw, sw, out_dtype=torch.float32, out=y)
+    torch.cuda.synchronize()
+    covered = slice(int(off[0]), int(off[E]))
+    assert torch.equal(y[covered], y_two[covered])
+    qa_o, sa_o = oracle.quant_act(a_bits)
+    qw_o, sw_o = oracle.quant_weight(w)
+    y_ref, T = oracle.grouped_gemm(qa_o, sa_o, off, qw_o.reshape(E, N, K), sw_o.reshape(E, N, K // G))
+    check_fp32(y.cpu().numpy()[covered], y_ref[covered], T[covered], K)
+    assert w8.device_error(clear=True) == 0
