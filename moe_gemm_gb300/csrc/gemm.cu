@@ -105,6 +105,7 @@ struct KParams {
     int tile_tokens;    // token rows per tile (b_rows or 2 * b_rows)
     int p_bufs;         // partial buffers in TMEM (p_bufs * b_rows <= 256)
     int tab_off;        // byte offset of the tile table in shared memory
+    int group_tokens;   // wide tiles: token stages released per K group (dense calls)
     unsigned long long *err;
     // Stream-K split of dense calls (null sk_cnt: whole tiles only).
     int *sk_cnt;        // [2 * grid] arrival counters of split tiles, zero at launch
@@ -389,6 +390,12 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     // off the critical path), or the two step slots (wide tiles, NB == 2,
     // freed by the step's commit).
     const uint32_t NB = static_cast<uint32_t>(p.b_stages);
+    // Wide dense tiles: each stage's two K-group halves have their own
+    // barriers, so group j's tokens are requested as soon as group j's MMAs of
+    // the step that last used the stage are done (4096x8192x8192 GEMM: 640 ->
+    // 627 us, measured); MoE expert tiles (a few steps each) were slower that
+    // way (gate_up 266 -> 273 us) and keep whole-step stages.
+    const bool gt = kWide && p.group_tokens != 0;
     const int b_rows = p.b_rows;                          // 32 or 64; 128 when kWide
     const uint32_t b_atom_bytes = static_cast<uint32_t>(b_rows) * 128u;
     const uint32_t b_stage_bytes = 4u * b_atom_bytes;     // 2 groups x 2 atoms
@@ -510,9 +517,13 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     tc_fence_after();
                     for (int j = 0; j < ng; ++j) {
                         if constexpr (kWide) {
-                            // group j's partial buffer drained by the epilogue
+                            // group j's partial buffer drained by the epilogue;
+                            // group 1's tokens landed (admission covered group 0's)
                             if (!mbar_wait(bar(NBar::p_empty + j), gph[j] ^ 1u, s_abort, p.err,
-                                           ROLE_MMA, 4)) {
+                                           ROLE_MMA, 4) ||
+                                (gt && j == 1 &&
+                                 !mbar_wait(bar(NBar::b_full + 2 * bs.idx + 1), bs.phase, s_abort,
+                                            p.err, ROLE_MMA, 5))) {
                                 ok = false;
                                 break;
                             }
@@ -550,8 +561,6 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             Ring bs;
             uint32_t issued = 0;
             bool ok = true;
-            // wide: the stage is the step slot, free once the slot's commit landed
-            const int free_bar = kWide ? NBar::done : NBar::b_empty;
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
                 const int n_eff = (ti.rows + 15) & ~15;
@@ -559,12 +568,44 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 for (int sg = s0; sg < s1; ++sg) {
                     const int g0 = 2 * sg;
                     const int ng = min(2, G - g0);
-                    if (!mbar_wait(bar(free_bar + bs.idx), bs.phase ^ 1u, s_abort, p.err,
-                                   ROLE_PRODUCER, 2)) {
+                    const uint32_t stage = sB + bs.idx * b_stage_bytes;
+                    if (kWide && gt) {
+                        // One barrier pair per group half of the stage: group j's
+                        // tokens are requested as soon as group j's MMAs of the
+                        // step that last used the stage are done (a missing
+                        // second group completes its barrier empty).
+                        for (int j = 0; j < 2; ++j) {
+                            const uint32_t gb = 2u * bs.idx + static_cast<uint32_t>(j);
+                            if (!mbar_wait(bar(NBar::b_empty + gb), bs.phase ^ 1u, s_abort,
+                                           p.err, ROLE_PRODUCER, 2)) {
+                                ok = false;
+                                return false;
+                            }
+                            if (j < ng) {
+                                mbar_arrive_expect_tx(
+                                    bar(NBar::b_full + gb),
+                                    static_cast<uint32_t>(2 * nbox * kBoxRows * 128));
+                                for (int a = 0; a < 2; ++a)
+                                    for (int i = 0; i < nbox; ++i)
+                                        tma_load_2d(stage + (2 * j + a) * b_atom_bytes +
+                                                        i * kBoxRows * 128,
+                                                    &tmap_x, (g0 + j) * kGroupK + a * 64,
+                                                    ti.m0 + i * kBoxRows, bar(NBar::b_full + gb));
+                            } else {
+                                mbar_arrive(bar(NBar::b_full + gb));
+                            }
+                            ++issued;
+                        }
+                        bs.advance(NB);
+                        continue;
+                    }
+                    // narrow: the ring stage is freed by the epilogue; wide (whole
+                    // steps): the stage is the step slot, freed by its commit
+                    if (!mbar_wait(bar((kWide ? NBar::done : NBar::b_empty) + bs.idx),
+                                   bs.phase ^ 1u, s_abort, p.err, ROLE_PRODUCER, 2)) {
                         ok = false;
                         return false;
                     }
-                    const uint32_t stage = sB + bs.idx * b_stage_bytes;
                     mbar_arrive_expect_tx(bar(NBar::b_full + bs.idx),
                                           static_cast<uint32_t>(ng * 2 * nbox * kBoxRows * 128));
                     for (int j = 0; j < ng; ++j)
@@ -578,14 +619,15 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
                 return true;
             });
-            if (!ok) drain_ring(bar(NBar::b_full), issued, NB);
+            // wide: group barriers in issue order 0,1,2,3,0,...
+            if (!ok) drain_ring(bar(NBar::b_full), issued, (kWide && gt) ? 2 * NB : NB);
         } else if (warp == 3 && lane == 0) {
             // --------------------------------------------------- admission
             Ring st, pr, bs;
             for_each_piece(plan, [&](int, int s0, int s1) -> bool {
                 for (int sg = s0; sg < s1; ++sg) {
-                    if (!mbar_wait(bar(NBar::b_full + bs.idx), bs.phase, s_abort, p.err, ROLE_MMA,
-                                   2) ||
+                    if (!mbar_wait(bar(NBar::b_full + ((kWide && gt) ? 2 * bs.idx : bs.idx)),
+                                   bs.phase, s_abort, p.err, ROLE_MMA, 2) ||
                         (!kWide && !mbar_wait(bar(NBar::p_empty + pr.idx), pr.phase ^ 1u, s_abort,
                                               p.err, ROLE_MMA, 3)))
                         return false;
@@ -717,6 +759,9 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             break;
                         }
                         gph[j] ^= 1u;
+                        // group j's MMAs are complete: its token half-stage is free
+                        if (gt && threadIdx.x == 256)
+                            mbar_arrive(bar(NBar::b_empty + 2 * bs.idx + j));
                         tc_fence_after();
                         const float sj = j == 0 ? sc0 : sc1;
 #pragma unroll
@@ -741,6 +786,12 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive_relaxed(bar(NBar::p_empty + j));
+                    }
+                    if (!failed) {
+                        // a step with one group releases the unused half at once
+                        if (gt && ng == 1 && threadIdx.x == 256)
+                            mbar_arrive(bar(NBar::b_empty + 2 * bs.idx + 1));
+                        bs.advance(NB);
                     }
                     continue;
                 }
@@ -1338,6 +1389,7 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     kp.tile_tokens = ps.tile_tokens;
     kp.p_bufs = ps.p_bufs;
     kp.tab_off = kOffTab;
+    kp.group_tokens = (ps.wide && pr.offsets == nullptr) ? 1 : 0;
     unsigned long long *err = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
     if (e != cudaSuccess) return e;
