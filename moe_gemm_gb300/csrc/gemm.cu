@@ -980,11 +980,44 @@ struct GBar {
 static_assert(GBar::count <= 128, "barrier area");
 static_assert(gemv_stage_bytes(kGemvMaxTokens) % 1024 == 0, "stage alignment");
 
+// GEMV work of this CTA, f(tile, half): the tiles that fill whole waves go
+// round-robin (half 0); when at most half a wave is left over, each left-over
+// tile is cut into two 64-row halves (half 1: weight rows [0, 64), 2: [64,
+// 128)), one per CTA, taken first, so that every SM streams the same number of
+// weight bytes (a partial last wave of whole tiles streams on fewer SMs). One
+// counted loop with one call site, as for_each_piece.
+template <class F>
+__device__ __forceinline__ void gemv_for_each(int total, F &&f) {
+    const int grid = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    int dp = (total / grid) * grid;
+    const int L = total - dp;
+    int nh = 0;
+    if (L > 0 && 2 * L <= grid)
+        nh = c < 2 * L ? 1 : 0;
+    else
+        dp = total;
+    for (int i = 0;; ++i) {
+        int t, h;
+        if (i < nh) {
+            t = dp + c / 2;
+            h = 1 + (c & 1);
+        } else {
+            t = c + (i - nh) * grid;
+            if (t >= dp) return;
+            h = 0;
+        }
+        if (!f(t, h)) return;
+    }
+}
+
 // Stage producer of the GEMV kernels (one thread): weights and the token
-// codes of each step into one stage, per the work plan.
+// codes of each step into one stage, per the work split above (half tiles
+// load 64 weight rows through tmap_w64).
 template <int MR>
-__device__ __forceinline__ void gemv_produce(const KParams &p, const WorkPlan &plan,
-                                             const CUtensorMap &tmap_w, const CUtensorMap &tmap_q,
+__device__ __forceinline__ void gemv_produce(const KParams &p, int total, const CUtensorMap &tmap_w,
+                                             const CUtensorMap &tmap_w64,
+                                             const CUtensorMap &tmap_q,
                                              uint32_t sA, uint32_t kStage, uint32_t SA,
                                              uint32_t full0, uint32_t empty0, volatile int *s_abort,
                                              const int *s_base, const int *s_lo, const int *s_cnt,
@@ -1005,11 +1038,12 @@ __device__ __forceinline__ void gemv_produce(const KParams &p, const WorkPlan &p
             tma_load_2d(stage + 2 * kAStageBytes + j * MR * 128, &tmap_q, x + j * kGroupK,
                         y, fb);
     };
-    for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
+    gemv_for_each(total, [&](int t, int h) -> bool {
         const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
-        const int wrow = ti.e * p.N + ti.n0;
-        for (int sg = s0; sg < s1; ++sg) {
-            const int g0 = 2 * sg;
+        const int wrow = ti.e * p.N + ti.n0 + (h > 0 ? 64 * (h - 1) : 0);
+        const uint32_t wbytes = h > 0 ? kAStageBytes / 2 : kAStageBytes;
+        const CUtensorMap *tw = h > 0 ? &tmap_w64 : &tmap_w;
+        for (int g0 = 0; g0 < G; g0 += 2) {
             const int ng = min(2, G - g0);
             if (!mbar_wait(empty0 + 8u * a.idx, a.phase ^ 1u, s_abort, p.err,
                            ROLE_PRODUCER, 1)) {
@@ -1018,9 +1052,9 @@ __device__ __forceinline__ void gemv_produce(const KParams &p, const WorkPlan &p
             }
             const uint32_t stage = sA + a.idx * kStage;
             const uint32_t fb = full0 + 8u * a.idx;
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng * (kAStageBytes + MR * 128)));
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng * (wbytes + MR * 128)));
             for (int j = 0; j < ng; ++j)
-                tma_load_2d(stage + j * kAStageBytes, &tmap_w, (g0 + j) * kGroupK, wrow, fb);
+                tma_load_2d(stage + j * kAStageBytes, tw, (g0 + j) * kGroupK, wrow, fb);
             if (!dep_done) {
                 griddep_wait();
                 dep_done = true;
@@ -1042,6 +1076,7 @@ __device__ __forceinline__ void gemv_produce(const KParams &p, const WorkPlan &p
 template <bool kDebug, int RR, int RM, int CW>
 __global__ void __launch_bounds__(gemv_threads(CW), 1)
 w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                 const __grid_constant__ CUtensorMap tmap_w64,
                  const __grid_constant__ CUtensorMap tmap_q, const KParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -1075,6 +1110,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tmap_w);
+            tma_prefetch_desc(&tmap_w64);
             tma_prefetch_desc(&tmap_q);
         }
         build_tile_table(p, tt, lane, s_base, s_lo, s_cnt, s_total);
@@ -1082,11 +1118,10 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     __syncthreads();
     const int total = *s_total;
     const int G = p.G;
-    const WorkPlan plan = make_plan(total, G, false);   // whole tiles (stream-bound)
 
     if (warp == 0) {
         if (lane == 0) {
-            gemv_produce<MR>(p, plan, tmap_w, tmap_q, sA, kStage, SA, bar(GBar::full),
+            gemv_produce<MR>(p, total, tmap_w, tmap_w64, tmap_q, sA, kStage, SA, bar(GBar::full),
                              bar(GBar::empty), s_abort, s_base, s_lo, s_cnt, tt);
         }
     } else {
@@ -1106,15 +1141,19 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
         bool failed = false;
         Ring a;
         float acc[RR][RM];
-        for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
+        gemv_for_each(total, [&](int t, int h) -> bool {
             const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+            // a half tile's 64 rows sit in stage rows [0, 64)
+            const int n0 = ti.n0 + (h > 0 ? 64 * (h - 1) : 0);
+            const int s0 = 0, s1 = (G + 1) >> 1;
             int n_row[RR];
             bool n_ok[RR];
             const float *swp[RR];
 #pragma unroll
             for (int i = 0; i < RR; ++i) {
-                n_row[i] = ti.n0 + rb + i * (128 / RR);
-                n_ok[i] = n_row[i] < p.N;
+                const int lr = rb + i * (128 / RR);
+                n_row[i] = n0 + lr;
+                n_ok[i] = n_row[i] < p.N && (h == 0 || lr < 64);
                 swp[i] = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok[i] ? n_row[i] : 0)) * G;
 #pragma unroll
                 for (int u = 0; u < RM; ++u) acc[i][u] = 0.0f;
@@ -1440,9 +1479,11 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     if (stages < 2 || pr.R > MR) return cudaErrorInvalidConfiguration;
     const int tab_off = kGemvOffStages + stages * stage + kExtra;
     const int smem_bytes = tab_off + tab_bytes + 1024;
-    CUtensorMap tw, tq;
+    CUtensorMap tw, tw64, tq;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
                    (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
+        !encode_2d(&tw64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
+                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN / 2) ||
         !encode_2d_plain(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qa, (uint64_t)pr.K,
                          (uint64_t)pr.R, kGroupK, MR))
         return cudaErrorInvalidValue;
@@ -1490,7 +1531,7 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kernel, tw, tq, kp);
+    e = cudaLaunchKernelEx(&cfg, kernel, tw, tw64, tq, kp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
