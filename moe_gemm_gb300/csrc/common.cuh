@@ -345,6 +345,13 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrives on a named barrier without waiting (the other participants wait
+// with named_barrier_sync; the arrival orders this thread's earlier memory
+// accesses before their later ones, at CTA scope).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 template <uint32_t RegCount>
 __device__ __forceinline__ void setmaxnreg_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegCount));

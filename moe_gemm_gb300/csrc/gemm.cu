@@ -74,10 +74,11 @@ constexpr int kTmemCols = 512;
 constexpr int kTmemA0 = 256;        // TMEM fp16 weight operands from column 256
 constexpr int kEpiRegs = 200;       // 256 threads x 200 + 256 x 56 = 512 x 128 at launch
 constexpr int kOtherRegs = 56;
-// Narrow tiles (one 32-column accumulator per epilogue thread) give the other
-// roles room for the stream-K bookkeeping.
-constexpr int kSplitEpiRegs = 184;
-constexpr int kSplitOtherRegs = 72;
+// Narrow tiles: one 32-column accumulator per epilogue thread, plus the
+// split-tile publish/combine paths; the other roles carry the stream-K
+// bookkeeping in 64.
+constexpr int kSplitEpiRegs = 192;
+constexpr int kSplitOtherRegs = 64;
 constexpr int kSmemLimit = 232448;
 
 // Shared memory: a fixed area (barriers, flags, tile table), then the weight
@@ -429,7 +430,10 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         for (int i = 0; i < kNarrowSlots; ++i) {
             mbar_init(bar(NBar::ready + i), 5);
             mbar_init(bar(NBar::done + i), 1);
-            mbar_init(bar(NBar::p_empty + i), 8);
+            // the epilogue warps that drain partials: both warpgroups, or only
+            // the first for token tiles of <= 32 rows (the second one then
+            // combines split tiles; see the epilogue)
+            mbar_init(bar(NBar::p_empty + i), (!kWide && p.b_rows <= 32) ? 4 : 8);
             mbar_init(bar(NBar::p_full + i), 1);
         }
         for (int i = 0; i < kMaxBStages; ++i) {
@@ -703,6 +707,66 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             else
                 static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
         };
+        // Token tiles of <= 32 rows leave the second epilogue warpgroup without
+        // columns: it takes no part in the steps (the partial-buffer release
+        // counts 4 warps) and instead finishes the split tiles. At the end of
+        // each split piece the first warpgroup stores its partial and goes on
+        // with the next piece at once; this one counts the piece in and, for
+        // the tile's last piece, adds all pieces in K order and stores y, off
+        // the MMA pipeline's critical path.
+        const bool helper = !kWide && p.b_rows <= 32;
+        if (helper && ewg == 1) {
+            for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
+                if (s0 == 0 && s1 == plan.S) return true;
+                named_barrier_sync(2, 256);   // the piece's partial is stored
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                int c_first, c_final;
+                tile_owners(t, plan, c_first, c_final);
+                if (threadIdx.x == 384) {
+                    int last = 0;
+                    if (*s_abort == 0) {
+                        // ordered after the kernel that zeroed the counters
+                        griddep_wait();
+                        __threadfence();
+                        last = atomicAdd(p.sk_cnt + (t - plan.dp), 1) == c_final - c_first;
+                        if (last) __threadfence();
+                    }
+                    *s_last = last;
+                }
+                named_barrier_sync(3, 128);
+                const int n_local = ti.n0 + lrow;
+                if (*s_last == 0 || n_local >= p.N) return true;
+                auto slot = [&](int c) -> const float * {   // slot 1: the tile's first piece
+                    return p.sk_part +
+                           static_cast<size_t>(2 * c + (c == c_first ? 1 : 0)) * p.sk_ld * kTileN +
+                           lrow;
+                };
+                // (off the critical path: one piece per round trip)
+                float sum[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sum[j] = 0.0f;
+                for (int c = c_first; c <= c_final; ++c) {   // K order
+                    const float *src = slot(c);
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __ldcg(src + min(j, ti.rows - 1) * kTileN);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sum[j] += v[j];
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (j < ti.rows) {
+                        const size_t idx = static_cast<size_t>(ti.m0 + j) * p.N + n_local;
+                        const float out = sum[j] * __ldg(p.sa + ti.m0 + j);
+                        if (p.out_fp32)
+                            static_cast<float *>(p.y)[idx] = out;
+                        else
+                            static_cast<__nv_bfloat16 *>(p.y)[idx] = __float2bfloat16_rn(out);
+                    }
+                }
+                return true;
+            });
+        } else {
         float acc[NCH][32];
 #pragma unroll
         for (int h = 0; h < NCH; ++h)
@@ -875,6 +939,13 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     for (int j = 0; j < 32; ++j)
                         if (col0 + j < ti.rows) __stcg(dst + (col0 + j) * kTileN, acc[0][j]);
                 }
+                if (helper) {
+                    // the other warpgroup publishes and combines (above)
+                    named_barrier_arrive(2, 256);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[0][j] = 0.0f;
+                    return true;
+                }
                 // Release: the barrier orders every epilogue thread's partial
                 // stores before one thread's fence and counter update (fences
                 // are cumulative); the last arrival's fence then orders its
@@ -938,6 +1009,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 for (int j = 0; j < 32; ++j) acc[h][j] = 0.0f;
             return true;
         });
+        }   // draining warpgroups
     }
 
     __syncwarp();
