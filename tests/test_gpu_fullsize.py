@@ -1,8 +1,9 @@
 """GPU parity at the full workload sizes, on sampled outputs.
 
-The CUDA path runs the whole problem exactly as bench.py launches it
-(weights quantized on the GPU from the seeded FP32 weights, activations
-quantized on the GPU, one GEMM call). The oracle recomputes sampled output
+The CUDA path runs the whole problem (weights quantized on the GPU from the
+seeded FP32 weights, activations quantized on the GPU, one GEMM call), and
+again exactly as bench.py launches it (one fused quantizer + GEMM call,
+w8a8_linear / w8a8_grouped_linear), which must give the same output bits. The oracle recomputes sampled output
 rows/columns from its own quantization of the same seeded inputs; the
 sampled weight rows and activation rows are also compared bit-exactly.
 """
@@ -45,11 +46,16 @@ def test_dense_full_size_sampled(name, n_rows, n_cols):
     rng = np.random.default_rng(zlib.crc32(name.encode()))
     qw, sw = gpu_quant_weights(workloads.weight_blocks(spec), spec.N, spec.K)
     a_bits = workloads.activations(spec)
-    qa, sa = w8.quant_act(to_dev_bf16(a_bits))
+    a_dev = to_dev_bf16(a_bits)
+    qa, sa = w8.quant_act(a_dev)
     dt = torch.bfloat16 if spec.out_dtype == "bf16" else torch.float32
     y = torch.full((spec.M, spec.N), float("nan"), dtype=dt, device=DEV)
     w8.gemm(qa, sa, qw, sw, out_dtype=dt, out=y)
+    y_lin = torch.full((spec.M, spec.N), float("nan"), dtype=dt, device=DEV)
+    w8.linear(a_dev, qw, sw, out_dtype=dt, out=y_lin)
     torch.cuda.synchronize()
+    assert torch.equal(y_lin, y)
+    del y_lin
 
     rows = np.arange(spec.M) if n_rows is None else np.sort(
         rng.choice(spec.M, n_rows, replace=False))
@@ -87,12 +93,17 @@ def test_moe_full_size_sampled(which):
         qw[e].copy_(q)
         sw[e].copy_(s)
     a_bits = workloads.moe_activations(spec, which, route)
-    qa, sa = w8.quant_act(to_dev_bf16(a_bits))
+    a_dev = to_dev_bf16(a_bits)
+    qa, sa = w8.quant_act(a_dev)
     off = route.offsets
+    off_t = torch.from_numpy(off).to(DEV)
     y = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device=DEV)
-    w8.grouped_gemm(qa, sa, torch.from_numpy(off).to(DEV), qw, sw, out=y)
+    w8.grouped_gemm(qa, sa, off_t, qw, sw, out=y)
+    y_lin = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    w8.grouped_linear(a_dev, off_t, qw, sw, out=y_lin)
     torch.cuda.synchronize()
     assert not torch.isnan(y.float()).any().item()          # every routed row written
+    assert torch.equal(y_lin, y)
 
     counts = np.diff(off)
     rng = np.random.default_rng(7 if which == "up" else 8)
