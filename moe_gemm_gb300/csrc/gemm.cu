@@ -21,11 +21,13 @@
 //    shared memory; a converter warpgroup widens them in registers and writes
 //    the fp16 A operand straight into tensor memory (tcgen05.st), so the
 //    widening costs no shared-memory bandwidth beyond one read.
-//  * Token operand: an fp16 copy of the int8 codes (written by a staging
-//    kernel just before this one) is loaded by TMA with the 128-byte swizzle.
-//    This kernel is launched as a programmatic dependent of the staging
-//    kernel: only the token producer waits for it (griddepcontrol.wait); the
-//    weight stream, the conversion and all set-up start at once.
+//  * Token operand: an fp16 copy of the int8 codes (written just before this
+//    kernel by the fused quantizer or by a staging kernel) is loaded by TMA
+//    with the 128-byte swizzle, through a ring of token stages that runs
+//    ahead of the MMAs. This kernel is launched as a programmatic dependent
+//    of that kernel: only the token producer waits for it
+//    (griddepcontrol.wait); the weight stream, the conversion and all set-up
+//    start at once.
 //  * Two K groups move through the pipeline per step (one barrier hand-off,
 //    one commit and one epilogue wait per 32 KB of weights); see the kernel.
 //  * Epilogue warpgroups drain the partial buffers (tcgen05.ld), fma each
@@ -332,17 +334,18 @@ __device__ __forceinline__ void for_each_piece(const WorkPlan &w, F &&f) {
 //  * a weight stage is 128 rows x 256 K int8 (two TMA boxes, 256 contiguous
 //    bytes per weight row);
 //  * a step slot (2 of them) holds the fp16 A operands of both groups in TMEM
-//    (128 columns), their two partial buffers (2 x b_rows columns; one pair
-//    shared by all steps in the wide form, see below) and the step's token
-//    tiles in shared memory; one commit per step ("done") frees them and
-//    tells the epilogue the step's partials are ready;
+//    (128 columns) and their two partial buffers (2 x b_rows columns; one
+//    pair shared by all steps in the wide form, see below); one commit per
+//    step ("done") frees them and tells the epilogue the step's partials are
+//    ready; token tiles sit in their own ring of shared-memory stages;
 //  * each epilogue warpgroup owns 32-column chunks of the token tile and
 //    drains both groups of a step with two loads and a single wait.
 // Warp roles (512 threads): 0 weight TMA producer; 1 MMA issuer and TMEM
 // allocation; 2 token TMA producer (the only thread that waits for the
-// staging kernel); 3 admission (token tiles landed, partial buffers free ->
-// "ready"); 4-7 converter (int8 -> fp16 A operand in TMEM); 8-15 epilogue.
-// kDebug additionally writes every exact group partial.
+// kernel that wrote the codes); 3 admission (token tiles landed, partial
+// buffers free -> "ready"); 4-7 converter (int8 -> fp16 A operand in TMEM);
+// 8-15 epilogue (for token tiles of <= 32 rows, 12-15 finish the split tiles
+// instead). kDebug additionally writes every exact group partial.
 // =============================================================================
 constexpr int kNarrowSlots = 2;
 constexpr int kWideOffTab = kOffMisc + 64;       // wide tiles: tile table in the fixed area
