@@ -411,3 +411,44 @@ def test_grouped_linear_equals_quant_then_grouped_gemm():
     y_ref, T = oracle.grouped_gemm(qa_o, sa_o, off, qw_o.reshape(E, N, K), sw_o.reshape(E, N, K // G))
     check_fp32(y.cpu().numpy()[covered], y_ref[covered], T[covered], K)
     assert w8.device_error(clear=True) == 0
+
+
+def test_back_to_back_calls_share_workspace_and_graph_replay():
+    """Consecutive calls on one stream reuse one workspace (split counters,
+    partial slots, codes) while the previous GEMM may still be draining; a
+    captured CUDA graph of the calls replays to the same bits."""
+    rng = np.random.default_rng(2024)
+    N, K = 28672, 1024
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    qw, sw = w8.quant_weight(torch.from_numpy(w).to(DEV))
+    qw_o, sw_o = oracle.quant_weight(w)
+    shapes = [1, 32, 8, 32, 3]                       # GEMV and split tensor-core calls mixed
+    acts = [workloads.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+            for M in shapes]
+    a_dev = [to_dev_bf16(b) for b in acts]
+    ws = torch.empty(max(w8.linear_workspace_size(M, N, K) for M in shapes), dtype=torch.uint8,
+                     device=DEV)
+    outs = [torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV) for M in shapes]
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for a, y in zip(a_dev, outs):
+            w8.linear(a, qw, sw, out_dtype=torch.float32, out=y, workspace=ws, stream=st)
+    st.synchronize()
+    for a_bits, y, M in zip(acts, outs, shapes):
+        qa_o, sa_o = oracle.quant_act(a_bits)
+        y_ref, T = oracle.gemm(qa_o, sa_o, qw_o, sw_o)
+        check_fp32(y.cpu().numpy(), y_ref, T, K)
+    first = [y.clone() for y in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            for a, y in zip(a_dev, outs):
+                w8.linear(a, qw, sw, out_dtype=torch.float32, out=y, workspace=ws, stream=st)
+    for y in outs:
+        y.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for y, y0 in zip(outs, first):
+        assert torch.equal(y, y0)
+    assert w8.device_error(clear=True) == 0
