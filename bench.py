@@ -58,7 +58,7 @@ def load_peaks():
 
 def gemm_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh"):
+    for f in ("gemm.cu", "common.cuh", "quant_math.cuh"):
         with open(os.path.join(ROOT, "moe_gemm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -240,8 +240,11 @@ def run_ours(args):
                if d["off"] is not None else w8.linear_workspace_size(shp.M, shp.N, shp.K))
         d["ws"] = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
         # one public call per shape: the quantizer (writing the GEMM's operand
-        # into the workspace) and the GEMM
-        d["launches"] = 2
+        # into the workspace) and the GEMM; for <= 4 dense rows whose codes fit
+        # beside the GEMV's stages, the GEMV quantizes them itself (one kernel)
+        mr = 1 if shp.M <= 1 else (2 if shp.M <= 2 else 4)
+        fused = d["off"] is None and shp.M <= 4 and shp.K * mr <= 96 * 1024
+        d["launches"] = 1 if fused else 2
     torch.cuda.synchronize()
 
     def linear_call(d, s=None):

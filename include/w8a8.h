@@ -163,9 +163,11 @@ size_t w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
 /*
  * The quantized linear layer in one call: per-token activation quantization
  * (w8a8_quant_act, Hunyuan-770B page §3.1: dynamic per-token INT8) followed by
- * the group-scaled GEMM (w8a8_gemm). The quantizer writes the codes and token
- * scales into the workspace in the form the GEMM reads (int8 for M <= 4,
- * fp16 for the tensor-core path), so no staging copy is made in between.
+ * the group-scaled GEMM (w8a8_gemm). For M > 4 the quantizer writes the codes
+ * (fp16, the tensor-core operand) and token scales into the workspace, so no
+ * staging copy is made in between; for M <= 4 the CUDA-core GEMM quantizes
+ * its token rows itself when lda is a multiple of 8 and a_bf16 is 16-byte
+ * aligned (one kernel), else the quantizer writes int8 codes first.
  *   a_bf16 [M, K] BF16, row stride lda >= K elements (2-byte aligned)
  *   qw [N, K] int8, sw [N, K/128] float   (from w8a8_quant_weight)
  *   y  [M, N] BF16 (round to nearest even) or FP32, per y_dtype.

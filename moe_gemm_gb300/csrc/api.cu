@@ -188,8 +188,13 @@ w8a8_status run_linear(const void *a, int64_t lda, const int32_t *offsets, const
         p.sk_ld = static_cast<int>(R);
     }
     const uint16_t *a16 = static_cast<const uint16_t *>(a);
-    cudaError_t e;
-    if (w8a8::uses_gemv(R, grouped)) {
+    cudaError_t e = cudaSuccess;
+    if (w8a8::uses_gemv(R, grouped) && w8a8::gemv_can_fuse_quant(R, K, lda, a)) {
+        // one kernel: the GEMV quantizes its token rows itself
+        p.act = a16;
+        p.lda = lda;
+        p.qa = nullptr;
+    } else if (w8a8::uses_gemv(R, grouped)) {
         e = w8a8::launch_quant_act(a16, R, K, lda, reinterpret_cast<int8_t *>(ws), K, sa, s);
         p.qa = reinterpret_cast<const int8_t *>(ws);
     } else {

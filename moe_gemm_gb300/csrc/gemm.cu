@@ -56,6 +56,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "quant_math.cuh"
 #include "internal.h"
 
 namespace w8a8 {
@@ -109,6 +110,11 @@ struct KParams {
     int p_bufs;         // partial buffers in TMEM (p_bufs * b_rows <= 256)
     int tab_off;        // byte offset of the tile table in shared memory
     int group_tokens;   // wide tiles: token stages released per K group (dense calls)
+    // GEMV that quantizes its own token rows: BF16 activations [R, lda] and
+    // the byte offset of the resident int8 code buffer in shared memory.
+    const uint16_t *act;
+    long long lda;
+    int qbuf_off;
     unsigned long long *err;
     // Stream-K split of dense calls (null sk_cnt: whole tiles only).
     int *sk_cnt;        // [2 * grid] arrival counters of split tiles, zero at launch
@@ -1089,7 +1095,7 @@ __device__ __forceinline__ void gemv_for_each(int total, F &&f) {
 // Stage producer of the GEMV kernels (one thread): weights and the token
 // codes of each step into one stage, per the work split above (half tiles
 // load 64 weight rows through tmap_w64).
-template <int MR>
+template <int MR, bool kFuseQ>
 __device__ __forceinline__ void gemv_produce(const KParams &p, int total, const CUtensorMap &tmap_w,
                                              const CUtensorMap &tmap_w64,
                                              const CUtensorMap &tmap_q,
@@ -1127,9 +1133,14 @@ __device__ __forceinline__ void gemv_produce(const KParams &p, int total, const 
             }
             const uint32_t stage = sA + a.idx * kStage;
             const uint32_t fb = full0 + 8u * a.idx;
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng * (wbytes + MR * 128)));
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(ng * (wbytes + (kFuseQ ? 0 : MR * 128))));
             for (int j = 0; j < ng; ++j)
                 tma_load_2d(stage + j * kAStageBytes, tw, (g0 + j) * kGroupK, wrow, fb);
+            if constexpr (kFuseQ) {   // the compute warps quantize the token rows themselves
+                a.advance(SA);
+                ++issued;
+                continue;
+            }
             if (!dep_done) {
                 griddep_wait();
                 dep_done = true;
@@ -1140,7 +1151,7 @@ __device__ __forceinline__ void gemv_produce(const KParams &p, int total, const 
         }
         return true;
     });
-    if (!dep_done) griddep_wait();   // no step at all (or an abort before the first)
+    if (!kFuseQ && !dep_done) griddep_wait();   // no step at all (or an abort before the first)
     if (!ok) drain_ring(full0, issued, SA);
 }
 
@@ -1148,7 +1159,12 @@ __device__ __forceinline__ void gemv_produce(const KParams &p, int total, const 
 // of one group, so a step's loads from shared memory are amortised over
 // RR * RM dot products per word. CW compute warps cover the tile's 128 rows
 // x 2 groups in CW * RR / 8 token blocks, so MR = CW * RR / 8 * RM token rows.
-template <bool kDebug, int RR, int RM, int CW>
+// kFuseQ: the kernel quantizes its token rows itself (per-token scale and
+// codes exactly as the quantizer kernel computes them) from the BF16
+// activations into a resident shared-memory code buffer, so a fused
+// quantizer + GEMM call of <= 4 token rows is one kernel; the stages then
+// carry weights only.
+template <bool kDebug, int RR, int RM, int CW, bool kFuseQ = false>
 __global__ void __launch_bounds__(gemv_threads(CW), 1)
 w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_w64,
@@ -1160,7 +1176,9 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
     constexpr int TB = CW * RR / 8;
     constexpr int MR = TB * RM;
     static_assert(TB >= 1 && CW * RR % 8 == 0, "compute warps cover whole token blocks");
-    constexpr uint32_t kStage = static_cast<uint32_t>(gemv_stage_bytes(MR));
+    constexpr uint32_t kStage =
+        kFuseQ ? 2u * kAStageBytes : static_cast<uint32_t>(gemv_stage_bytes(MR));
+    static_assert(!kFuseQ || (TB == 1 && !kDebug), "fused quantization: one token block");
     const uint32_t SA = static_cast<uint32_t>(p.a_stages);
     const uint32_t sA = base + kGemvOffStages;
     const uint32_t sBar = base + kOffBar;
@@ -1196,8 +1214,9 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     if (warp == 0) {
         if (lane == 0) {
-            gemv_produce<MR>(p, total, tmap_w, tmap_w64, tmap_q, sA, kStage, SA, bar(GBar::full),
-                             bar(GBar::empty), s_abort, s_base, s_lo, s_cnt, tt);
+            gemv_produce<MR, kFuseQ>(p, total, tmap_w, tmap_w64, tmap_q, sA, kStage, SA,
+                                     bar(GBar::full), bar(GBar::empty), s_abort, s_base, s_lo,
+                                     s_cnt, tt);
         }
     } else {
         // ------------------------------------------------- compute warps
@@ -1212,6 +1231,52 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int rb = (cw % kWarpsPerTb) * 16 + (lane & 15);
         const int j = lane >> 4;                      // group of the step
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
+        float s_tok[MR];   // kFuseQ: the token rows' scales
+        const uint8_t *qbuf = smem + p.qbuf_off;
+        if constexpr (kFuseQ) {
+            // The activations may come from the kernel launched before this
+            // one (programmatic dependent launch): wait for it, then form each
+            // row's scale (block max of |x|) and its codes, group by group in
+            // the layout the stages use ([group][token row][128 codes]).
+            griddep_wait();
+            uint32_t *red = reinterpret_cast<uint32_t *>(smem + 512);   // [MR][CW], spare barrier area
+            const int nvec = p.K >> 3;
+            constexpr int kCT = 32 * CW;
+#pragma unroll
+            for (int u = 0; u < MR; ++u) {
+                uint32_t m = 0;
+                if (u < p.R) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.act + u * p.lda);
+                    for (int v = ct; v < nvec; v += kCT) m = max(m, amax_bits8(__ldg(src + v)));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                if (lane == 0) red[u * CW + cw] = m;
+            }
+            named_barrier_sync(1, kCT);
+            float r_tok[MR];
+            bool fast[MR];
+#pragma unroll
+            for (int u = 0; u < MR; ++u) {
+                uint32_t m = 0;
+                for (int w = 0; w < CW; ++w) m = max(m, red[u * CW + w]);
+                s_tok[u] = __fdiv_rn(bf16_bits_to_f32(m), 127.0f);
+                fast[u] = s_tok[u] >= 1.17549435e-38f;   // normal scale: 1/s is finite
+                r_tok[u] = fast[u] ? __frcp_rn(s_tok[u]) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < MR; ++u) {
+                if (u >= p.R) continue;
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.act + u * p.lda);
+                for (int v = ct; v < nvec; v += kCT) {
+                    const int k = v << 3;
+                    *reinterpret_cast<uint2 *>(const_cast<uint8_t *>(qbuf) +
+                                               ((k >> 7) * MR + u) * 128 + (k & 127)) =
+                        quantize8(__ldg(src + v), s_tok[u], r_tok[u], fast[u]);
+                }
+            }
+            named_barrier_sync(1, kCT);   // codes complete before the first step reads them
+        }
         // After a failed wait the warp stops waiting and doing data work.
         bool failed = false;
         Ring a;
@@ -1278,7 +1343,9 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 if (j < ng) {
                     const uint8_t *stage = smem + kGemvOffStages + a.idx * kStage;
                     const uint8_t *wg = stage + j * kAStageBytes;
-                    const uint8_t *tok = stage + 2 * kAStageBytes + (j * MR + tb * RM) * 128;
+                    const uint8_t *tok =
+                        kFuseQ ? qbuf + ((g0 + j) * MR + tb * RM) * 128
+                               : stage + 2 * kAStageBytes + (j * MR + tb * RM) * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         uint4 wv[RR], tv[RM];
@@ -1331,7 +1398,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
             auto store_out = [&](int i, int u, float v) {
                 const int m = tb * RM + u;
-                const float out = v * __ldg(p.sa + ti.m0 + m);
+                const float out = v * (kFuseQ ? s_tok[u] : __ldg(p.sa + ti.m0 + m));
                 const size_t idx = static_cast<size_t>(ti.m0 + m) * p.N + n_row[i];
                 if (p.out_fp32)
                     static_cast<float *>(p.y)[idx] = out;
@@ -1545,23 +1612,30 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
 
 // Batched GEMV on the CUDA cores for dense calls of at most 4 token rows.
 // kExtra: bytes of shared memory the kernel keeps after its stages.
-template <auto kernel, int MR, int CW, int kExtra>
+template <auto kernel, int MR, int CW, int kExtra, bool kFuseQ = false>
 cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
-    constexpr int stage = gemv_stage_bytes(MR);
+    // kFuseQ: weight-only stages plus a resident code buffer of all K groups
+    constexpr int stage = kFuseQ ? 2 * kAStageBytes : gemv_stage_bytes(MR);
+    const int qbuf_bytes = kFuseQ ? static_cast<int>(pr.K / kGroupK) * MR * 128 : 0;
     const int tab_bytes = static_cast<int>((3 * (pr.E + 1) * 4 + 15) / 16 * 16);
-    int stages = (kSmemLimit - 1024 - kGemvOffStages - kExtra - tab_bytes) / stage;
+    int stages = (kSmemLimit - 1024 - kGemvOffStages - kExtra - qbuf_bytes - tab_bytes) / stage;
     if (stages > kMaxAStages) stages = kMaxAStages;
     if (stages < 2 || pr.R > MR) return cudaErrorInvalidConfiguration;
-    const int tab_off = kGemvOffStages + stages * stage + kExtra;
+    const int qbuf_off = kGemvOffStages + stages * stage + kExtra;
+    const int tab_off = qbuf_off + qbuf_bytes;
     const int smem_bytes = tab_off + tab_bytes + 1024;
     CUtensorMap tw, tw64, tq;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
                    (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
         !encode_2d(&tw64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
-                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN / 2) ||
-        !encode_2d_plain(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qa, (uint64_t)pr.K,
-                         (uint64_t)pr.R, kGroupK, MR))
+                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN / 2))
         return cudaErrorInvalidValue;
+    if (kFuseQ) {
+        tq = tw;   // not read: the kernel quantizes the token rows itself
+    } else if (!encode_2d_plain(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qa, (uint64_t)pr.K,
+                                (uint64_t)pr.R, kGroupK, MR)) {
+        return cudaErrorInvalidValue;
+    }
     static int attr_done[64] = {0};   // per device, per kernel instance
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1585,6 +1659,9 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     kp.n_tiles = static_cast<int>((pr.N + kTileN - 1) / kTileN);
     kp.out_fp32 = pr.out_fp32 ? 1 : 0;
     kp.a_stages = stages;
+    kp.act = pr.act;
+    kp.lda = pr.lda;
+    kp.qbuf_off = qbuf_off;
     kp.b_rows = MR;
     kp.tile_tokens = MR;
     kp.tab_off = tab_off;
@@ -1614,6 +1691,9 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
 template <int RR, int RM, int CW>
 cudaError_t launch_gemv_mr(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
     constexpr int MR = CW * RR / 8 * RM;
+    if (pr.act != nullptr)   // fused quantizer (no debug partials on that path)
+        return launch_gemv<w8a8_gemv_kernel<false, RR, RM, CW, true>, MR, CW, 0, true>(
+            pr, num_sms, stream);
     return pr.debug_partials != nullptr
                ? launch_gemv<w8a8_gemv_kernel<true, RR, RM, CW>, MR, CW, 0>(pr, num_sms, stream)
                : launch_gemv<w8a8_gemv_kernel<false, RR, RM, CW>, MR, CW, 0>(pr, num_sms, stream);

@@ -38,6 +38,10 @@ struct GemmProblem {
     int32_t *debug_partials;  // nullable [R, N, G]
     int64_t R, E, N, K;
     bool out_fp32;
+    // Dense calls of <= kGemvMaxTokens rows only: BF16 activations [R, lda]
+    // that the GEMV quantizes itself (then qa and sa are not read).
+    const uint16_t *act = nullptr;
+    int64_t lda = 0;
     // Stream-K split of dense calls; null sk_cnt: whole tiles only.
     int *sk_cnt = nullptr;        // [2 * kSkMaxCtas] counters, zeroed before the GEMM
     float *sk_part = nullptr;     // [kSkMaxCtas][2][sk_ld][128] FP32 partials
@@ -48,6 +52,15 @@ struct GemmProblem {
 // (batched GEMV over the int8 codes; no fp16 staging copy is made).
 constexpr int kGemvMaxTokens = 4;
 inline bool uses_gemv(int64_t R, bool grouped) { return !grouped && R <= kGemvMaxTokens; }
+
+// The GEMV can quantize its token rows itself when their codes for all of K
+// (K * MR bytes, MR = R rounded up to 1, 2 or 4) fit beside its weight
+// stages, and the activation rows allow 16-byte vector loads.
+inline bool gemv_can_fuse_quant(int64_t R, int64_t K, int64_t lda, const void *a) {
+    const int64_t mr = R <= 1 ? 1 : (R <= 2 ? 2 : 4);
+    return R >= 1 && R <= kGemvMaxTokens && K * mr <= 96 * 1024 && lda % 8 == 0 &&
+           (reinterpret_cast<uintptr_t>(a) % 16) == 0;
+}
 
 // Dense calls of 5..64 token rows (narrow tensor-core tiles) split tiles
 // across CTAs (stream-K) when the workspace holds the split area: arrival

@@ -357,7 +357,8 @@ def _linear_only_workspace(M, K):
 @pytest.mark.parametrize("M,N,K,out,lda_pad", [
     (1, 1000, 1152, "bf16", 0),     # CUDA-core GEMV path (int8 codes in the workspace)
     (2, 20480, 512, "fp32", 0),     # GEMV: 160 tiles, 8 left over cut in 64-row halves
-    (3, 256, 384, "fp32", 8),       # GEMV, strided activations
+    (3, 256, 384, "fp32", 8),       # GEMV quantizing its own rows, strided activations
+    (4, 512, 256, "bf16", 4),       # row stride not a multiple of 8: quantizer kernel + GEMV
     (8, 4096, 2048, "fp32", 0),     # tensor-core path, split
     (33, 1000, 1152, "bf16", 0),    # tensor-core path, split, ragged N
     (64, 28672, 1024, "bf16", 16),  # 64-row tiles, strided activations
