@@ -176,6 +176,25 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# ------------------------------------------------------ cross-rank timing
+def slowest_rank_ms(ms, world, device=None):
+    """The largest of the ranks' times (the job ends with its slowest rank).
+    Needs an initialised process group when world > 1 (nccl: a CUDA device;
+    gloo: the CPU)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tops(ops_per_step, steps, world, ms):
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return ops_per_step * steps * world / (ms * 1e-3) / 1e12
+
+
 # -------------------------------------------------------------- ours (GPU)
 def run_ours(args):
     import torch
@@ -342,13 +361,10 @@ def run_ours(args):
                 stream.synchronize()
         clocks = sampler.stop()
         clocks["note"] = "sampled every 50 ms over the timed region and a 1 s hold of the same step"
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, world, dev)
 
     ops_step = sum(d["shape"].ops for d in per)
-    value = ops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = job_tops(ops_step, args.steps, world, elapsed_ms)
 
     # ---- end to end through the public API with host buffers (rank-local)
     e2e = None
@@ -379,12 +395,8 @@ def run_ours(args):
             e2e_step()
         e1.record(cur)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": ops_step * args.steps * world / (ems * 1e-3) / 1e12, "unit": "TOPS",
+        ems = slowest_rank_ms(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": job_tops(ops_step, args.steps, world, ems), "unit": "TOPS",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": ems / args.steps}
 
