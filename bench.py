@@ -350,6 +350,30 @@ def run_ours(args):
             s1.record(stream)
             s1.synchronize()
             gemm_ms.append(s0.elapsed_time(s1) / args.steps)
+
+    # ---- the quantizer alone (step a1, HBM-bound: 2 B read + 1 B written per
+    # element + 4 B per row), per shape, the same way
+    quant_ms = []
+    qbufs = [(torch.empty((d["shape"].M, d["shape"].K), dtype=torch.int8, device=dev),
+              torch.empty((d["shape"].M,), dtype=torch.float32, device=dev)) for d in per]
+
+    def quant_call(i):
+        w8.quant_act(per[i]["a"], qa=qbufs[i][0], sa=qbufs[i][1], stream=stream)
+
+    run_quant = ([capture(lambda i=i: quant_call(i)).replay for i in range(len(per))]
+                 if graphs else [lambda i=i: quant_call(i) for i in range(len(per))])
+    with torch.cuda.stream(stream):
+        for i in range(len(per)):
+            for _ in range(3):
+                run_quant[i]()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(args.steps):
+                run_quant[i]()
+            s1.record(stream)
+            s1.synchronize()
+            quant_ms.append(s0.elapsed_time(s1) / args.steps)
     # Keep the same step running ~1 s more so the clock sampler sees the load
     # even when the timed region itself is shorter than its sampling period.
     if sampler:
@@ -415,6 +439,7 @@ def run_ours(args):
                 "alg_bytes_per_launch": alg,
                 "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
                 "kernel_time": KERNEL_TIME_NOTE,
+                "quantizer_ms_per_launch": [round(x, 5) for x in quant_ms],
                 "peak_source": f"{peaks['source']} HBM copy bandwidth"}
     else:
         flops = [d["shape"].ops for d in per]
@@ -426,6 +451,7 @@ def run_ours(args):
                 "ops_per_launch": flops,
                 "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
                 "kernel_time": KERNEL_TIME_NOTE,
+                "quantizer_ms_per_launch": [round(x, 5) for x in quant_ms],
                 "peak_source": (f"{peaks['source']} dense bf16 burst (the integer path runs "
                                 "on fp16 tensor cores, same rate as bf16)")}
 
