@@ -107,7 +107,6 @@ struct KParams {
     int b_stages;       // token pipeline depth (<= kMaxBStages)
     int b_rows;         // token rows per MMA batch and per token stage (32, 64, 96 or 128)
     int tile_tokens;    // token rows per tile (b_rows or 2 * b_rows)
-    int p_bufs;         // partial buffers in TMEM (p_bufs * b_rows <= 256)
     int tab_off;        // byte offset of the tile table in shared memory
     int group_tokens;   // wide tiles: token stages released per K group (dense calls)
     // GEMV that quantizes its own token rows: BF16 activations [R, lda] and
@@ -1482,7 +1481,7 @@ bool encode_2d_plain(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_by
 // Pipeline shape of one call: batch width, tile rows, partial buffers and
 // stage counts, filling shared memory with weight stages after the token stages.
 struct PipeShape {
-    int b_rows, tile_tokens, b_stages, a_stages, p_bufs, smem_bytes;
+    int b_rows, tile_tokens, b_stages, a_stages, smem_bytes;
     bool narrow;    // tiles of <= 64 token rows: w8a8_gemm_narrow_kernel
     bool wide;      // tiles of 96 or 128 token rows: its kWide form
 };
@@ -1504,7 +1503,6 @@ PipeShape choose_pipe(const GemmProblem &pr) {
     s.tile_tokens = s.b_rows;
     s.narrow = s.b_rows <= 64;
     s.wide = !s.narrow;
-    s.p_bufs = 2;
     // Token stages (b_rows x 512 B each): the two step slots for wide tiles; a
     // deeper ring for narrow ones, so that token tiles are requested several
     // steps ahead (their L2 latency, ~1 us under the weight stream, was on the
@@ -1568,7 +1566,6 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     kp.b_stages = ps.b_stages;
     kp.b_rows = ps.b_rows;
     kp.tile_tokens = ps.tile_tokens;
-    kp.p_bufs = ps.p_bufs;
     kp.tab_off = kOffTab;
     kp.group_tokens = (ps.wide && pr.offsets == nullptr) ? 1 : 0;
     unsigned long long *err = nullptr;
