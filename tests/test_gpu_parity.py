@@ -306,6 +306,8 @@ def _staging_only(rows, K):
     (9, 2000, 2048, "fp32"),     # tensor-core path: 16 tiles x 8 steps over 128 CTAs
     (17, 28672, 1024, "bf16"),   # tensor-core path: one whole wave, 72 tiles split
     (64, 4096, 8192, "fp32"),    # tensor-core path: ~5 pieces per tile, 64-row tiles
+    (20, 32256, 1024, "fp32"),   # 252 tiles: 100 left over > half a wave -> contiguous ranges,
+    (40, 32256, 1024, "bf16"),   #   CTAs with two split pieces (32-row and 64-row tiles)
 ])
 def test_dense_k_split_matches_oracle_and_unsplit(M, N, K, out):
     rng = np.random.default_rng(M + N + K)
