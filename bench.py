@@ -1,22 +1,27 @@
 """Benchmark of the W8A8 group-scaled quantized linear layer on GB300.
 
-One step = one pass of the whole hot path over the decode-shaped dense
-workload: for each token count M in {1, 8, 32} (K=8192, N=28672, BF16 out),
-per-token activation quantization followed by the group-scaled INT8 GEMM, as
-one library call per shape (w8a8_linear: the quantizer writes the GEMM's
-operand into the workspace, then the GEMM runs).
-Each GEMM of the step reads its own 235 MB weight copy, so every input is
-larger than L2 and no weight bytes are reused from L2 between GEMMs.
+Metric: INT8 TOPS (2*M*N*K per GEMM, 2*R*N*K grouped) and the fraction of the
+roofline that binds each GEMM shape (tensor peak for large M, HBM bandwidth
+for decode and MoE), on one GPU.
 
-Metric: INT8 TOPS = sum of 2*M*N*K over the step / step time (whole job over
-all ranks). The dominant kernel is the GEMM (the CUDA-core batched GEMV for
-M = 1, the tcgen05 narrow-tile kernel with K split for M = 8 and 32), HBM-bound at these shapes:
-the roofline object reports its algorithmic bytes per launch (int8 weights,
-FP32 group scales, int8 activations and scales, BF16 output) over its measured
-launch duration, against the measured HBM copy bandwidth.
+A default run measures every workload and prints one JSON line:
+  * the headline ("value", "roofline", "e2e", "cpu_baseline", "config") is the
+    large stress workload, M=8192, K=16384, N=16384, FP32 out: the largest
+    single-GPU configuration;
+  * "per_config" holds the same measurement for each workload: dense tiny
+    16x1024x1024, decode M in {1, 8, 32} x 8192 x 28672, prefill
+    4096x8192x8192, MoE grouped (64 experts, top-8 of 512 tokens; gate_up
+    3072x4096 and down 4096x1536) and stress, each with its throughput, the
+    roofline of its dominant kernel, the quantizer's time, the end-to-end
+    number through the public API with host buffers, and the CPU oracle timed
+    on the host cores on a fixed slice of the same workload.
+One step of a workload = one pass of the whole hot path over it: for each of
+its GEMM shapes, one fused library call (per-token quantization of the BF16
+activations, then the group-scaled GEMM; w8a8_linear / w8a8_grouped_linear),
+the step's calls replayed as one CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --workload prefill|stress|moe|tiny    (other shapes, same line format)
+  python bench.py --workload tiny|decode|prefill|moe|stress   (one workload)
 """
 from __future__ import annotations
 
@@ -37,11 +42,23 @@ sys.path.insert(0, ROOT)
 
 import workloads  # noqa: E402
 
-KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM replayed back to back K times, events "
-                    "around the K launches; the GEMM overlaps the quantizer, so this includes "
-                    "any part of the quantizer it does not hide")
 METRIC = "INT8 TOPS & % of roofline (tensor peak or HBM GB/s) per GEMM shape, 1xGB300"
 GROUP = 128
+WORKLOADS = ("tiny", "decode", "prefill", "moe", "stress")
+HEADLINE = "stress"
+# Workloads whose inputs fit in L2 (129 MB) get an L2 flush (a 256 MB write,
+# outside the timed events) before every timed step; the others read more
+# than L2 holds every step.
+FLUSH_L2 = ("tiny", "prefill")
+L2_FLUSH_BYTES = 256 << 20
+# The CPU oracle's sample of each workload (cpu_baseline and --impl
+# reference time the same slice): every row and all of K, output columns
+# [0, ORACLE_COLS) of every GEMM of the step (of every expert for MoE).
+ORACLE_COLS = {"tiny": 1024, "decode": 2048, "prefill": 512, "moe": 256, "stress": 512}
+KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM (one library call) replayed back to back "
+                    "K times, events around the K launches, median of 3 such batches; the "
+                    "GEMM overlaps the quantizer, so this includes any part of the quantizer "
+                    "it does not hide")
 
 
 def load_peaks():
@@ -102,7 +119,7 @@ class Shape:
 
 
 def build_workload(name):
-    """Returns (description, [Shape], weight spec, kind)."""
+    """Returns (description, [Shape], weight spec, roofline bound)."""
     if name == "decode":
         shapes = [Shape(m, 28672, 8192, "bf16", workloads.DENSE[f"decode_m{m}"])
                   for m in workloads.DECODE_MS]
@@ -126,6 +143,20 @@ def build_workload(name):
                         route.offsets)]
         return desc, shapes, spec, "hbm"
     raise SystemExit(f"unknown workload {name}")
+
+
+def workload_config(name):
+    """The `config` object of a workload's line (identical in both arms)."""
+    desc, shapes, _, _ = build_workload(name)
+    return {"workload": desc, "shapes": [[s.M, s.N, s.K] for s in shapes],
+            "oracle_sample": oracle_sample_desc(name, shapes)}
+
+
+def oracle_sample_desc(name, shapes):
+    n = min(ORACLE_COLS[name], shapes[0].N)
+    per = "of every expert, " if name == "moe" else ""
+    return (f"all rows and all of K of every GEMM of the step, output columns [0, {n}) "
+            f"{per}of N")
 
 
 # ------------------------------------------------------------------ clocks
@@ -169,11 +200,12 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "power_w_max": max(pw) if pw else None, "samples": len(rows)}
 
 
 # ------------------------------------------------------ cross-rank timing
@@ -196,33 +228,85 @@ def job_tops(ops_per_step, steps, world, ms):
 
 
 # -------------------------------------------------------------- ours (GPU)
-def run_ours(args):
-    import torch
-    import torch.distributed as dist
+class GpuContext:
+    def __init__(self, args):
+        import torch
+        import torch.distributed as dist
+        self.torch = torch
+        self.dist = dist
+        self.args = args
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(self.local_rank)
+        if self.world > 1:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local_rank))
+        import __graft_entry__
+        if self.rank == 0 or self.world == 1:
+            __graft_entry__.build()
+        if self.world > 1:
+            dist.barrier()
+        import moe_gemm_gb300 as w8
+        self.w8 = w8
+        self.dev = torch.device("cuda", self.local_rank)
+        self.stream = torch.cuda.Stream(device=self.dev)
+        self.peaks = load_peaks()
+        self.flush_buf = None
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    import __graft_entry__
-    if rank == 0 or world == 1:
-        __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
-    import moe_gemm_gb300 as w8
-    dev = torch.device("cuda", local_rank)
-    peaks = load_peaks()
-    desc, shapes, wspec, bound = build_workload(args.workload)
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
 
-    # ---- resident inputs (weights quantized on the GPU, offline step)
-    def upload_bf16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(
-            torch.bfloat16)
+    def flush_l2(self):
+        torch = self.torch
+        if self.flush_buf is None:
+            self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=self.dev)
+        with torch.cuda.stream(self.stream):
+            self.flush_buf.fill_(1)
 
+    def capture(self, fn):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            fn()                       # eager pass on the capture stream first
+            self.stream.synchronize()
+            with torch.cuda.graph(g, stream=self.stream):
+                fn()
+        torch.cuda.synchronize()
+        return g
+
+    def batch_ms(self, run, reps, batches=3):
+        """Median over `batches` of the mean time of `reps` back-to-back
+        calls of run() on the stream (events around each batch)."""
+        torch = self.torch
+        out = []
+        with torch.cuda.stream(self.stream):
+            for _ in range(3):
+                run()
+            for _ in range(batches):
+                s0 = torch.cuda.Event(enable_timing=True)
+                s1 = torch.cuda.Event(enable_timing=True)
+                s0.record(self.stream)
+                for _ in range(reps):
+                    run()
+                s1.record(self.stream)
+                s1.synchronize()
+                out.append(s0.elapsed_time(s1) / reps)
+        return statistics.median(out)
+
+
+def upload_bf16(torch, dev, bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def setup_workload(ctx, name):
+    """Resident inputs of a workload: per shape the BF16 activations, the
+    quantized weights (quantized on the GPU by the library, an offline step),
+    the output and the workspace of its fused call."""
+    torch, w8, dev = ctx.torch, ctx.w8, ctx.dev
+    desc, shapes, wspec, bound = build_workload(name)
     per = []
-    if args.workload == "moe":
+    if name == "moe":
         spec = wspec
         for shp in shapes:
             which, _, route = shp.act_spec
@@ -235,8 +319,8 @@ def run_ours(args):
                 qw[e].copy_(q)
                 sw[e].copy_(s)
             a_host = workloads.moe_activations(spec, which, route)
-            per.append(dict(shape=shp, qw=qw, sw=sw, a=upload_bf16(a_host), a_host=a_host,
-                            off=torch.from_numpy(route.offsets).to(dev)))
+            per.append(dict(shape=shp, qw=qw, sw=sw, a=upload_bf16(torch, dev, a_host),
+                            a_host=a_host, off=torch.from_numpy(route.offsets).to(dev)))
     else:
         K, N = shapes[0].K, shapes[0].N
         qw0 = torch.empty((N, K), dtype=torch.int8, device=dev)
@@ -245,12 +329,13 @@ def run_ours(args):
             q, s = w8.quant_weight(torch.from_numpy(wb).to(dev))
             qw0[r0:r0 + wb.shape[0]].copy_(q)
             sw0[r0:r0 + wb.shape[0]].copy_(s)
+            del q, s
         for i, shp in enumerate(shapes):
             a_host = workloads.activations(shp.act_spec)
             qw = qw0 if i == 0 else qw0.clone()     # a weight copy per GEMM of the step
             sw = sw0 if i == 0 else sw0.clone()
-            per.append(dict(shape=shp, qw=qw, sw=sw, a=upload_bf16(a_host), a_host=a_host,
-                            off=None))
+            per.append(dict(shape=shp, qw=qw, sw=sw, a=upload_bf16(torch, dev, a_host),
+                            a_host=a_host, off=None))
     for d in per:
         shp = d["shape"]
         odt = torch.bfloat16 if shp.out == "bf16" else torch.float32
@@ -258,139 +343,121 @@ def run_ours(args):
         wsz = (w8.grouped_linear_workspace_size(shp.M, shp.E, shp.N, shp.K)
                if d["off"] is not None else w8.linear_workspace_size(shp.M, shp.N, shp.K))
         d["ws"] = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
-        # one public call per shape: the quantizer (writing the GEMM's operand
+        # one fused call per shape: the quantizer (writing the GEMM's operand
         # into the workspace) and the GEMM; for <= 4 dense rows whose codes fit
         # beside the GEMV's stages, the GEMV quantizes them itself (one kernel)
         mr = 1 if shp.M <= 1 else (2 if shp.M <= 2 else 4)
         fused = d["off"] is None and shp.M <= 4 and shp.K * mr <= 96 * 1024
         d["launches"] = 1 if fused else 2
     torch.cuda.synchronize()
+    return desc, shapes, wspec, bound, per
 
-    def linear_call(d, s=None):
-        s = stream if s is None else s
-        if d["off"] is not None:
-            w8.grouped_linear(d["a"], d["off"], d["qw"], d["sw"], out=d["y"],
-                              out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
-        else:
-            w8.linear(d["a"], d["qw"], d["sw"], out=d["y"], out_dtype=d["y"].dtype,
-                      workspace=d["ws"], stream=s)
 
-    def shape_call(d):
-        linear_call(d)
+def linear_call(ctx, d, s):
+    w8 = ctx.w8
+    if d["off"] is not None:
+        w8.grouped_linear(d["a"], d["off"], d["qw"], d["sw"], out=d["y"],
+                          out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
+    else:
+        w8.linear(d["a"], d["qw"], d["sw"], out=d["y"], out_dtype=d["y"].dtype,
+                  workspace=d["ws"], stream=s)
+
+
+def measure_workload(ctx, name, headline):
+    """One workload: throughput over K timed steps, per-shape kernel times,
+    the quantizer alone, the roofline of the dominant kernel, the end-to-end
+    number with host buffers and (rank 0, one rank) the CPU oracle."""
+    torch, w8, args = ctx.torch, ctx.w8, ctx.args
+    stream = ctx.stream
+    desc, shapes, wspec, bound, per = setup_workload(ctx, name)
 
     def step():
         for d in per:
-            shape_call(d)
+            linear_call(ctx, d, stream)
 
-    # The step runs as one CUDA graph (quantizer, staging/reset kernel and
-    # GEMM of every shape, with their programmatic-dependent-launch edges),
-    # replayed once per step: the launches a serving loop would capture.
-    stream = torch.cuda.Stream(device=dev)
     graphs = not args.no_graph
-
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            fn()                       # eager pass on the capture stream first
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                fn()
-        torch.cuda.synchronize()
-        return g
-
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
     if graphs:
-        g_step = capture(step)
-        run_step = g_step.replay
-        g_shape = [capture(lambda d=d: shape_call(d)) for d in per]
-        run_shape = [g.replay for g in g_shape]
+        run_step = ctx.capture(step).replay
+        run_shape = [ctx.capture(lambda d=d: linear_call(ctx, d, stream)).replay for d in per]
     else:
         run_step = step
-        run_shape = [lambda d=d: shape_call(d) for d in per]
+        run_shape = [lambda d=d: linear_call(ctx, d, stream) for d in per]
     with torch.cuda.stream(stream):
         for _ in range(3):
             run_step()
     torch.cuda.synchronize()
 
-    # ---- the timed region (CUDA events on the launching stream)
-    sampler = ClockSampler(local_rank) if (rank == 0 and not args.no_clocks) else None
-    if sampler:
+    # ---- the timed region: K steps, CUDA events on the launching stream
+    sampler = None
+    if headline and ctx.rank == 0 and not args.no_clocks:
+        sampler = ClockSampler(ctx.local_rank)
         sampler.start()
-    if world > 1:
-        dist.barrier()
+    flush = name in FLUSH_L2
+    ctx.barrier()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for k in range(args.steps):
-            run_step()
-        t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = t0.elapsed_time(t1)
-
-    # ---- per-shape launch time (roofline): each shape's quantizer + GEMM
-    # replayed K times back to back, timed with events around the K launches
-    # (an event between two launches would cut their programmatic overlap).
-    gemm_ms = []
-    with torch.cuda.stream(stream):
-        for i in range(len(per)):
-            for _ in range(3):
-                run_shape[i]()
-            s0 = torch.cuda.Event(enable_timing=True)
-            s1 = torch.cuda.Event(enable_timing=True)
-            s0.record(stream)
+    if flush:
+        # inputs fit in L2: flush it before every step, time each step alone
+        step_ms = []
+        with torch.cuda.stream(stream):
             for _ in range(args.steps):
-                run_shape[i]()
-            s1.record(stream)
-            s1.synchronize()
-            gemm_ms.append(s0.elapsed_time(s1) / args.steps)
+                ctx.flush_l2()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                run_step()
+                e1.record(stream)
+                e1.synchronize()
+                step_ms.append(e0.elapsed_time(e1))
+        elapsed_ms = sum(step_ms)
+    else:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(args.steps):
+                run_step()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = t0.elapsed_time(t1)
+    torch.cuda.synchronize()
+    ctx.barrier()
 
-    # ---- the quantizer alone (step a1, HBM-bound: 2 B read + 1 B written per
-    # element + 4 B per row), per shape, the same way
-    quant_ms = []
-    qbufs = [(torch.empty((d["shape"].M, d["shape"].K), dtype=torch.int8, device=dev),
-              torch.empty((d["shape"].M,), dtype=torch.float32, device=dev)) for d in per]
+    # ---- per-shape time of the fused call (the GEMM dominates it)
+    gemm_ms = [ctx.batch_ms(r, args.steps) for r in run_shape]
+    # ---- the quantizer alone (step a1; HBM-bound: 2 B read + 1 B written
+    # per element + 4 B per row), per shape
+    qbufs = [(torch.empty((d["shape"].M, d["shape"].K), dtype=torch.int8, device=ctx.dev),
+              torch.empty((d["shape"].M,), dtype=torch.float32, device=ctx.dev)) for d in per]
 
     def quant_call(i):
         w8.quant_act(per[i]["a"], qa=qbufs[i][0], sa=qbufs[i][1], stream=stream)
 
-    run_quant = ([capture(lambda i=i: quant_call(i)).replay for i in range(len(per))]
+    run_quant = ([ctx.capture(lambda i=i: quant_call(i)).replay for i in range(len(per))]
                  if graphs else [lambda i=i: quant_call(i) for i in range(len(per))])
-    with torch.cuda.stream(stream):
-        for i in range(len(per)):
-            for _ in range(3):
-                run_quant[i]()
-            s0 = torch.cuda.Event(enable_timing=True)
-            s1 = torch.cuda.Event(enable_timing=True)
-            s0.record(stream)
-            for _ in range(args.steps):
-                run_quant[i]()
-            s1.record(stream)
-            s1.synchronize()
-            quant_ms.append(s0.elapsed_time(s1) / args.steps)
-    # Keep the same step running ~1 s more so the clock sampler sees the load
-    # even when the timed region itself is shorter than its sampling period.
+    quant_ms = [ctx.batch_ms(r, args.steps) for r in run_quant]
+    del qbufs
+
+    clocks = None
     if sampler:
+        # the same step ~1 s more, so the sampler sees the load even when the
+        # timed region is shorter than its sampling period
         hold_end = time.time() + 1.0
         with torch.cuda.stream(stream):
             while time.time() < hold_end:
-                for _ in range(50):
+                for _ in range(10):
                     run_step()
                 stream.synchronize()
         clocks = sampler.stop()
         clocks["note"] = "sampled every 50 ms over the timed region and a 1 s hold of the same step"
-    elapsed_ms = slowest_rank_ms(elapsed_ms, world, dev)
-
+    elapsed_ms = slowest_rank_ms(elapsed_ms, ctx.world, ctx.dev)
     ops_step = sum(d["shape"].ops for d in per)
-    value = job_tops(ops_step, args.steps, world, elapsed_ms)
+    value = job_tops(ops_step, args.steps, ctx.world, elapsed_ms)
 
-    # ---- end to end through the public API with host buffers (rank-local)
+    # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
         host_in = [torch.from_numpy(np.ascontiguousarray(d["a_host"]).view(np.int16)).view(
@@ -398,20 +465,18 @@ def run_ours(args):
         host_out = [torch.empty(d["y"].shape, dtype=d["y"].dtype).pin_memory() for d in per]
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
-
         cur = torch.cuda.current_stream()
 
         def e2e_step():
             for d, hi, ho in zip(per, host_in, host_out):
                 d["a"].copy_(hi, non_blocking=True)
-                linear_call(d, cur)
+                linear_call(ctx, d, cur)
                 ho.copy_(d["y"], non_blocking=True)
 
         for _ in range(args.warmup):
             e2e_step()
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        ctx.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(cur)
@@ -419,85 +484,152 @@ def run_ours(args):
             e2e_step()
         e1.record(cur)
         torch.cuda.synchronize()
-        ems = slowest_rank_ms(e0.elapsed_time(e1), world, dev)
-        e2e = {"value": job_tops(ops_step, args.steps, world, ems), "unit": "TOPS",
+        ems = slowest_rank_ms(e0.elapsed_time(e1), ctx.world, ctx.dev)
+        e2e = {"value": round(job_tops(ops_step, args.steps, ctx.world, ems), 3), "unit": "TOPS",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": ems / args.steps}
+               "ms_per_step": round(ems / args.steps, 5),
+               "how": "per GEMM of the step: pinned host activations -> device, the fused "
+                      "library call, output -> pinned host; stream launches"}
+        del host_in, host_out
 
     # ---- roofline of the dominant kernel (the GEMM)
+    peaks = ctx.peaks
     if bound == "hbm":
         active = None
-        if args.workload == "moe":
+        if name == "moe":
             cnt = np.diff(workloads.routing(wspec).offsets)
             active = int((cnt > 0).sum())
         alg = [d["shape"].alg_bytes(active) for d in per]
         achieved = sum(alg) / (sum(gemm_ms) * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4),
-                "traffic": recorded_traffic(args.workload),
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": recorded_traffic(name),
                 "alg_bytes_per_launch": alg,
-                "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
-                "kernel_time": KERNEL_TIME_NOTE,
-                "quantizer_ms_per_launch": [round(x, 5) for x in quant_ms],
                 "peak_source": f"{peaks['source']} HBM copy bandwidth"}
     else:
         flops = [d["shape"].ops for d in per]
         achieved = sum(flops) / (sum(gemm_ms) * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": recorded_traffic(args.workload),
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": recorded_traffic(name),
                 "ops_per_launch": flops,
-                "kernel_ms_per_launch": [round(x, 5) for x in gemm_ms],
-                "kernel_time": KERNEL_TIME_NOTE,
-                "quantizer_ms_per_launch": [round(x, 5) for x in quant_ms],
-                "peak_source": (f"{peaks['source']} dense bf16 burst (the integer path runs "
-                                "on fp16 tensor cores, same rate as bf16)")}
+                "peak_source": (f"{peaks['source']} dense bf16 burst (the integer-exact path "
+                                "runs on the fp16 tensor cores, whose dense rate equals bf16's)")}
+    roof["kernel_ms_per_launch"] = [round(x, 5) for x in gemm_ms]
+    roof["kernel_time"] = KERNEL_TIME_NOTE
+    roof["quantizer_ms_per_launch"] = [round(x, 5) for x in quant_ms]
 
-    out = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
+    entry = {
+        "workload": desc,
+        "shapes": [[d["shape"].M, d["shape"].N, d["shape"].K] for d in per],
+        "value": round(value, 3), "unit": "TOPS",
         "ms_per_step": round(elapsed_ms / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
-        "data": "synthetic (seeded numpy PCG64, distributions of the workload)",
-        "config": {"workload": desc, "shapes": [[d["shape"].M, d["shape"].N, d["shape"].K]
-                                                 for d in per],
-                   "l2": "inputs larger than L2: each GEMM reads its own weight copy "
-                         f"({per[0]['shape'].N * per[0]['shape'].K * per[0]['shape'].E / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}",
-                   "launch": ("one CUDA graph per step (all shapes' kernels with their "
-                              "programmatic-dependent-launch edges), replayed" if graphs
-                              else "stream launches")},
+        "l2": ("flushed before every timed step (256 MB write outside the events); inputs "
+               "fit in L2" if flush else
+               "inputs larger than L2: each step streams "
+               f"{sum(d['qw'].numel() for d in per) / 1e6:.0f} MB of weights"
+               + (" (a weight copy per GEMM)" if len(per) > 1 and name != "moe" else "")),
         "roofline": roof,
-        "gpu_launches": sum(d["launches"] for d in per) * args.steps,
+        "gpu_launches_per_step": sum(d["launches"] for d in per),
     }
     if e2e:
-        out["e2e"] = e2e
-    if sampler:
-        out["clocks"] = clocks
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.workload, shapes, wspec)
-    if rank == 0:
+        entry["e2e"] = e2e
+    if clocks:
+        entry["clocks"] = clocks
+    if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
+        entry["cpu_baseline"] = cpu_baseline(name, 8.0 if headline else 3.0)
+    del per
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def measure_int_path_peak(ctx):
+    """Rate of the integer-exact arithmetic the GEMMs run: tcgen05.mma
+    kind::f16 on exact int8 integers at the instruction shapes the GEMMs
+    issue, and dp4a (the CUDA-core GEMV). Timed with CUDA events."""
+    torch, w8 = ctx.torch, ctx.w8
+    out = {}
+    for n, chains, steps in ((256, 1, 4000), (128, 2, 4000), (32, 2, 8000)):
+        macs = [0]
+
+        def run(n=n, chains=chains, steps=steps):
+            macs[0] = w8.probe_tc_rate(n, chains, steps, stream=ctx.stream)
+
+        ms = ctx.batch_ms(run, 1, batches=3)
+        out[f"tcgen05_f16_m128_n{n}_x{chains}_tflops"] = round(2 * macs[0] / (ms * 1e-3) / 1e12, 1)
+    macs = [0]
+
+    def run_dp4a():
+        macs[0] = w8.probe_dp4a_rate(20000, stream=ctx.stream)
+
+    ms = ctx.batch_ms(run_dp4a, 1, batches=3)
+    out["dp4a_tops"] = round(2 * macs[0] / (ms * 1e-3) / 1e12, 1)
+    out["how"] = ("w8a8_probe_tc_rate / w8a8_probe_dp4a_rate: one CTA per SM issuing the "
+                  "instruction back to back (zero operands), CUDA events, median of 3; "
+                  "tensor-core entries are M=128 x N x K=16 with `x` accumulators taking turns")
+    if w8.device_error(clear=True) != 0:
+        out["error"] = "a probe's bounded wait gave up"
+    return out
+
+
+def run_ours(args):
+    ctx = GpuContext(args)
+    names = WORKLOADS if args.workload == "all" else (args.workload,)
+    head = HEADLINE if args.workload == "all" else args.workload
+    int_peak = None
+    if not args.no_probe:
+        int_peak = measure_int_path_peak(ctx)
+    entries = {}
+    for name in names:
+        entries[name] = measure_workload(ctx, name, name == head)
+    h = entries[head]
+    roof = dict(h["roofline"])
+    if int_peak and roof["bound"] == "tensor":
+        ip = int_peak["tcgen05_f16_m128_n256_x1_tflops"]
+        roof["int_path_peak"] = ip
+        roof["frac_of_int_path_peak"] = round(roof["achieved"] / ip, 4)
+    out = {
+        "metric": METRIC, "value": h["value"], "unit": "TOPS", "n_gpus": ctx.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": h["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded numpy PCG64, distributions of the workload)",
+        "config": workload_config(head),
+        "timing": {"l2": h["l2"], "parallelism": f"replicas x{ctx.world}",
+                   "launch": ("one CUDA graph per step (all shapes' kernels with their "
+                              "programmatic-dependent-launch edges), replayed"
+                              if not args.no_graph else "stream launches")},
+        "roofline": roof,
+        "gpu_launches": h["gpu_launches_per_step"] * args.steps,
+    }
+    for k in ("e2e", "clocks", "cpu_baseline"):
+        if k in h:
+            out[k] = h[k]
+    if int_peak:
+        out["int_path_peak"] = int_peak
+    if len(entries) > 1:
+        out["per_config"] = entries
+    if ctx.rank == 0:
         print(json.dumps(out))
-    if world > 1:
-        dist.destroy_process_group()
+    if ctx.world > 1:
+        ctx.dist.destroy_process_group()
 
 
 # ----------------------------------------------------- oracle (CPU) timing
-def oracle_sample(workload, shapes, wspec, n_cols):
-    """Inputs for the oracle on a column slice [0, n_cols) of every GEMM."""
+def oracle_items(name):
+    """Inputs of the oracle's sample of a workload (ORACLE_COLS)."""
     import oracle
+    _, shapes, wspec, _ = build_workload(name)
+    n_cols = min(ORACLE_COLS[name], shapes[0].N)
     items = []
-    if workload == "moe":
+    if name == "moe":
         spec = wspec
         for shp in shapes:
             which, _, route = shp.act_spec
             a = workloads.moe_activations(spec, which, route)
-            per_e = []
-            for e in range(spec.E):
-                per_e.append(oracle.quant_weight(
-                    workloads.moe_weights(spec, which, e, rows=np.arange(n_cols))))
+            per_e = [oracle.quant_weight(workloads.moe_weights(spec, which, e,
+                                                               rows=np.arange(n_cols)))
+                     for e in range(spec.E)]
             qw = np.stack([p[0] for p in per_e])
             sw = np.stack([p[1] for p in per_e])
             items.append((a, qw, sw, route.offsets))
@@ -505,7 +637,8 @@ def oracle_sample(workload, shapes, wspec, n_cols):
         qw, sw = oracle.quant_weight(workloads.weights(wspec, rows=np.arange(n_cols)))
         for shp in shapes:
             items.append((workloads.activations(shp.act_spec), qw, sw, None))
-    return items
+    ops = sum(2 * s.M * n_cols * s.K for s in shapes)
+    return items, ops
 
 
 def oracle_step(items):
@@ -518,27 +651,21 @@ def oracle_step(items):
             oracle.grouped_gemm(qa, sa, off, qw, sw)
 
 
-def cpu_baseline(workload, shapes, wspec, target_s=10.0):
+def cpu_baseline(name, target_s):
+    """The oracle as it stands, on the host cores, over whole passes of the
+    workload's fixed sample until about target_s seconds have passed."""
     import oracle
-    cores = oracle.max_threads()
-    n_full = shapes[0].N
-    n0 = min(128, n_full)
-    items = oracle_sample(workload, shapes, wspec, n0)
-    t = time.perf_counter()
-    oracle_step(items)
-    t_small = time.perf_counter() - t
-    n_cols = int(min(n_full, max(n0, n0 * target_s / max(t_small, 1e-6))) // 128 * 128) or n0
-    items = oracle_sample(workload, shapes, wspec, n_cols)
+    _, shapes, _, _ = build_workload(name)
+    items, ops = oracle_items(name)
     reps, dt = 0, 0.0
     t = time.perf_counter()
-    while reps == 0 or dt < target_s:          # whole passes until ~target_s of CPU work
+    while reps == 0 or dt < target_s:
         oracle_step(items)
         reps += 1
         dt = time.perf_counter() - t
-    ops = reps * sum(2 * s.M * n_cols * s.K for s in shapes)
-    return {"value": round(ops / dt / 1e12, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} pass(es) over all rows of every GEMM of the step, output columns "
-                      f"[0, {n_cols}) of {n_full}; {dt:.1f} s", "seconds": round(dt, 2)}
+    return {"value": round(ops * reps / dt / 1e12, 6), "unit": "TOPS",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": oracle_sample_desc(name, shapes), "passes": reps, "seconds": round(dt, 2)}
 
 
 def run_reference(args):
@@ -548,28 +675,26 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    desc, shapes, wspec, _ = build_workload(args.workload)
-    n_cols = min(shapes[0].N, 4096)
-    items = oracle_sample(args.workload, shapes, wspec, n_cols)
+    name = HEADLINE if args.workload == "all" else args.workload
+    _, shapes, _, _ = build_workload(name)
+    items, ops = oracle_items(name)
     for _ in range(args.warmup):
         oracle_step(items)
     t = time.perf_counter()
     for _ in range(args.steps):
         oracle_step(items)
     dt = time.perf_counter() - t
-    ops = sum(2 * s.M * n_cols * s.K for s in shapes)
     value = ops * args.steps / dt / 1e12
     cores = oracle.max_threads()
-    sample = (f"every GEMM of the step with output columns [0, {n_cols}) of {shapes[0].N} "
-              f"(all rows, full K)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": desc, "parallelism": "oracle on host cores (rank 0)"},
+        "config": workload_config(name),
+        "timing": {"parallelism": "the CPU oracle on the host cores (rank 0)"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": cores,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": oracle_sample_desc(name, shapes)},
         "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
@@ -578,13 +703,14 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode",
-                    choices=["decode", "tiny", "prefill", "stress", "moe"])
+    ap.add_argument("--workload", default="all", choices=("all",) + WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-probe", action="store_true",
+                    help="skip the integer-path rate probes")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the step's kernels on a stream instead of replaying a graph")
     ap.add_argument("--no-clocks", action="store_true",

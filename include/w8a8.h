@@ -213,21 +213,31 @@ w8a8_status w8a8_grouped_linear(const void *a_bf16, int64_t lda, const int32_t *
  * inference engine that hands a plug-in only a stream and buffers it planned
  * ahead of time, a runtime whose memory pool forbids allocation on its hot
  * path, or code running where a cudaMalloc would synchronise the device. It
- * computes exactly what w8a8_gemm computes (same kernels, same results), but
- * stages the fp16 copy of the activation codes in a fixed 8 MiB array that is
- * part of the library (W8A8_NOALLOC_SCRATCH_BYTES), so it allocates nothing:
- * no cudaMalloc, no cudaFree, no allocating library routine.
+ * runs the kernels of w8a8_gemm, but its scratch is a fixed 8 MiB array that
+ * is part of the library (W8A8_NOALLOC_SCRATCH_BYTES), so it allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  * There is no counterpart of this call on the source pages; it is a
  * deployment convenience.
  *   Arguments: as w8a8_gemm, without debug_partials and workspace.
- *   Returns W8A8_ERR_WORKSPACE when M * K * 2 bytes (rounded up to 256) do not
- *   fit in the built-in scratch.
+ *   Returns W8A8_ERR_WORKSPACE when the fp16 copy of the activation codes,
+ *   M * K * 2 bytes rounded up to 256, does not fit in the built-in scratch.
+ *   What it computes: for M <= 4, and for M > 64, exactly what w8a8_gemm
+ *   computes (same kernels, same results). For 5 <= M <= 64, w8a8_gemm splits
+ *   tile K ranges over the SMs when its workspace holds the split area; here
+ *   that area (1280 + 163,840 * M bytes, rounded up to 256) must fit in the
+ *   scratch after the codes. When it does (e.g. M <= 46 at K = 8192, M <= 50
+ *   at K = 1024) the result is again identical to w8a8_gemm's; when it does
+ *   not (e.g. M >= 47 at K = 8192) the call runs unsplit, and its FP32 result
+ *   may differ from w8a8_gemm's in the last bits: both are within the bound
+ *   stated for w8a8_gemm (here with n = 1).
  *   The first call on a device looks up the scratch's device address (once,
- *   with that device current); make that first call before any stream
- *   capture. All calls on a device share the one scratch array and it keeps
- *   the last call's contents: calls that can overlap on the GPU (different
- *   streams without ordering between them) race on it and must be ordered by
- *   the caller.
+ *   with that device current; make that first call before any stream
+ *   capture) and keeps it for the life of the device's primary context: do
+ *   not call this function again on a device after resetting it
+ *   (cudaDeviceReset) in the same process. All calls on a device share the
+ *   one scratch array and it keeps the last call's contents: calls that can
+ *   overlap on the GPU (different streams without ordering between them)
+ *   race on it and must be ordered by the caller.
  */
 w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *qw,
                               const float *sw, void *y, w8a8_dtype y_dtype, int64_t M, int64_t N,
@@ -256,6 +266,26 @@ w8a8_status w8a8_device_error(uint64_t *code_out, int clear);
  * context stays usable. Asynchronous on `stream`.
  */
 w8a8_status w8a8_selftest_wait_timeout(uint32_t limit_us, w8a8_stream_t stream);
+
+/*
+ * Rate probes of the integer-exact arithmetic the GEMMs run (diagnostics; no
+ * counterpart on the pages). Each launches one kernel, asynchronously on
+ * `stream`, and stores in *macs_out the number of int8 multiply-adds it
+ * performs; the caller times the launch (CUDA events) to obtain the rate.
+ * The operands are zeros (the rate does not depend on the values).
+ *   w8a8_probe_tc_rate: one CTA per SM issues 8 * chains * steps
+ *     tcgen05.mma kind::f16 instructions of shape M = 128, N = n, K = 16
+ *     (A in tensor memory, B in shared memory: the instruction of the
+ *     tensor-core GEMM), `chains` independent accumulators taking turns.
+ *     16 <= n <= 256, n % 16 == 0, chains >= 1, chains * n <= 256,
+ *     1 <= steps <= 2^24 (keep one launch well under a second).
+ *   w8a8_probe_dp4a_rate: 4 CTAs of 512 threads per SM, each thread 16 *
+ *     iters dp4a (four int8 products into an int32; the CUDA-core GEMV's
+ *     arithmetic). 1 <= iters <= 2^26.
+ */
+w8a8_status w8a8_probe_tc_rate(int32_t n, int32_t chains, int64_t steps, int64_t *macs_out,
+                               w8a8_stream_t stream);
+w8a8_status w8a8_probe_dp4a_rate(int64_t iters, int64_t *macs_out, w8a8_stream_t stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int w8a8_version(void);

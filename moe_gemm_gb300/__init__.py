@@ -61,10 +61,13 @@ def _load() -> ctypes.CDLL:
     lib.w8a8_linear.argtypes = [vp, i64, vp, vp, vp, i32, i64, i64, i64, vp, ctypes.c_size_t, vp]
     lib.w8a8_grouped_linear.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64, i64, i64, i64, vp,
                                         ctypes.c_size_t, vp]
+    lib.w8a8_probe_tc_rate.argtypes = [i32, i32, i64, ctypes.POINTER(i64), vp]
+    lib.w8a8_probe_dp4a_rate.argtypes = [i64, ctypes.POINTER(i64), vp]
     lib.w8a8_version.restype = i32
     for name in ("w8a8_quant_act", "w8a8_quant_weight", "w8a8_gemm", "w8a8_grouped_gemm",
                  "w8a8_gemm_noalloc", "w8a8_device_error", "w8a8_selftest_wait_timeout",
-                 "w8a8_linear", "w8a8_grouped_linear"):
+                 "w8a8_linear", "w8a8_grouped_linear", "w8a8_probe_tc_rate",
+                 "w8a8_probe_dp4a_rate"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -95,10 +98,37 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _require(t: torch.Tensor, dtype: torch.dtype, name: str, ndim: int) -> None:
+def _require(t: torch.Tensor, dtype: torch.dtype, name: str, ndim: int,
+             shape: Optional[Tuple[int, ...]] = None,
+             device: Optional[torch.device] = None) -> None:
     if not t.is_cuda or t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of rank {ndim}, "
                          f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
+def _require_out(out: torch.Tensor, out_dtype: torch.dtype, shape: Tuple[int, int],
+                 device: torch.device) -> None:
+    """The kernels write exactly shape[0] * shape[1] elements of out_dtype
+    into `out`: anything else would be written past its end or half-filled."""
+    _require(out, out_dtype, "out", 2, shape, device)
+
+
+def _require_workspace(ws: torch.Tensor, device: torch.device) -> None:
+    if not ws.is_cuda or ws.dtype != torch.uint8 or not ws.is_contiguous() or ws.device != device:
+        raise ValueError(f"workspace: expected a contiguous uint8 tensor on {device}")
+
+
+def _on_device(device: torch.device, stream: Optional[torch.cuda.Stream]):
+    """Makes the operands' device current for the call (the library resolves
+    per-device state, such as its built-in scratch, on the current device);
+    a stream of another device is refused."""
+    if stream is not None and stream.device != device:
+        raise ValueError(f"stream belongs to {stream.device}, the operands to {device}")
+    return torch.cuda.device(device)
 
 
 def quant_act(a: torch.Tensor, qa: Optional[torch.Tensor] = None,
@@ -108,10 +138,19 @@ def quant_act(a: torch.Tensor, qa: Optional[torch.Tensor] = None,
     if not a.is_cuda or a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
         raise ValueError("a: expected a CUDA bf16 [M, K] tensor with unit column stride")
     M, K = a.shape
-    qa = torch.empty((M, K), dtype=torch.int8, device=a.device) if qa is None else qa
-    sa = torch.empty((M,), dtype=torch.float32, device=a.device) if sa is None else sa
-    _check(_lib.w8a8_quant_act(_ptr(a), M, K, a.stride(0), _ptr(qa), qa.stride(0), _ptr(sa),
-                               _stream(stream)), "w8a8_quant_act")
+    dev = a.device
+    if qa is None:
+        qa = torch.empty((M, K), dtype=torch.int8, device=dev)
+    elif (not qa.is_cuda or qa.dtype != torch.int8 or qa.dim() != 2 or tuple(qa.shape) != (M, K)
+          or qa.stride(1) != 1 or qa.device != dev):
+        raise ValueError(f"qa: expected an int8 [{M}, {K}] tensor with unit column stride on {dev}")
+    if sa is None:
+        sa = torch.empty((M,), dtype=torch.float32, device=dev)
+    else:
+        _require(sa, torch.float32, "sa", 1, (M,), dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_quant_act(_ptr(a), M, K, a.stride(0), _ptr(qa), qa.stride(0), _ptr(sa),
+                                   _stream(stream)), "w8a8_quant_act")
     return qa, sa
 
 
@@ -122,8 +161,9 @@ def quant_weight(w: torch.Tensor, stream: Optional[torch.cuda.Stream] = None
     N, K = w.shape
     qw = torch.empty((N, K), dtype=torch.int8, device=w.device)
     sw = torch.empty((N, K // GROUP), dtype=torch.float32, device=w.device)
-    _check(_lib.w8a8_quant_weight(_ptr(w), N, K, _ptr(qw), _ptr(sw), _stream(stream)),
-           "w8a8_quant_weight")
+    with _on_device(w.device, stream):
+        _check(_lib.w8a8_quant_weight(_ptr(w), N, K, _ptr(qw), _ptr(sw), _stream(stream)),
+               "w8a8_quant_weight")
     return qw, sw
 
 
@@ -143,28 +183,44 @@ def _dtype_code(out_dtype: torch.dtype) -> int:
     raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
 
 
+def _dense_operands(qa, sa, qw, sw):
+    """Checks the dense GEMM operands against each other; returns M, N, K."""
+    _require(qa, torch.int8, "qa", 2)
+    dev = qa.device
+    M, K = qa.shape
+    _require(qw, torch.int8, "qw", 2, device=dev)
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError(f"qw: expected K = {K} columns, got {qw.shape[1]}")
+    _require(sa, torch.float32, "sa", 1, (M,), dev)
+    _require(sw, torch.float32, "sw", 2, (N, K // GROUP), dev)
+    return M, N, K
+
+
 def gemm(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
          out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
          workspace: Optional[torch.Tensor] = None, debug_partials: bool = False,
          stream: Optional[torch.cuda.Stream] = None):
     """Y[M,N] = sa[m] * sum_g sw[n,g] * P[m,n,g]; returns y, or (y, P) with
     debug_partials=True (P int32 [M, N, K/128])."""
-    _require(qa, torch.int8, "qa", 2)
-    _require(qw, torch.int8, "qw", 2)
-    _require(sa, torch.float32, "sa", 1)
-    _require(sw, torch.float32, "sw", 2)
-    M, K = qa.shape
-    N = qw.shape[0]
+    M, N, K = _dense_operands(qa, sa, qw, sw)
+    code = _dtype_code(out_dtype)
     dev = qa.device
-    y = torch.empty((M, N), dtype=out_dtype, device=dev) if out is None else out
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (M, N), dev)
     if workspace is None:
         workspace = torch.empty(max(gemm_workspace_size(M, N, K), 1), dtype=torch.uint8,
                                 device=dev)
+    else:
+        _require_workspace(workspace, dev)
     P = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=dev) if debug_partials else None
-    _check(_lib.w8a8_gemm(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(y), _dtype_code(out_dtype),
-                          M, N, K, _ptr(P), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "w8a8_gemm")
-    return (y, P) if debug_partials else y
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_gemm(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(out), code, M, N, K,
+                              _ptr(P), _ptr(workspace), workspace.numel(), _stream(stream)),
+               "w8a8_gemm")
+    return (out, P) if debug_partials else out
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -173,21 +229,19 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 def gemm_noalloc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
                  out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Same result as gemm(), for callers that cannot allocate device memory
-    when the layer runs: the library stages the activation codes in its own
-    fixed 8 MiB scratch array instead of a workspace (M*K*2 bytes must fit).
-    Calls that may overlap on the GPU share that array and must be ordered."""
-    _require(qa, torch.int8, "qa", 2)
-    _require(qw, torch.int8, "qw", 2)
-    _require(sa, torch.float32, "sa", 1)
-    _require(sw, torch.float32, "sw", 2)
-    M, K = qa.shape
-    N = qw.shape[0]
+    """The GEMM for callers that cannot allocate device memory when the layer
+    runs: the library stages the activation codes (and, when they fit, the
+    K-split partial sums) in its own fixed 8 MiB scratch array instead of a
+    workspace (M*K*2 bytes must fit). Writes into the caller's `out`. Calls
+    that may overlap on the GPU share that array and must be ordered."""
+    M, N, K = _dense_operands(qa, sa, qw, sw)
+    code = _dtype_code(out_dtype)
     if out is None:
         raise ValueError("gemm_noalloc writes into a caller-provided `out` tensor")
-    _check(_lib.w8a8_gemm_noalloc(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(out),
-                                  _dtype_code(out_dtype), M, N, K, _stream(stream)),
-           "w8a8_gemm_noalloc")
+    _require_out(out, out_dtype, (M, N), qa.device)
+    with _on_device(qa.device, stream):
+        _check(_lib.w8a8_gemm_noalloc(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(out), code,
+                                      M, N, K, _stream(stream)), "w8a8_gemm_noalloc")
     return out
 
 
@@ -197,25 +251,31 @@ def grouped_gemm(qa: torch.Tensor, sa: torch.Tensor, offsets: torch.Tensor, qw: 
                  debug_partials: bool = False, stream: Optional[torch.cuda.Stream] = None):
     """MoE grouped GEMM over rows sorted by expert; offsets int32 [E+1] on device."""
     _require(qa, torch.int8, "qa", 2)
-    _require(qw, torch.int8, "qw", 3)
-    _require(sa, torch.float32, "sa", 1)
-    _require(sw, torch.float32, "sw", 3)
-    _require(offsets, torch.int32, "offsets", 1)
-    R, K = qa.shape
-    E, N, _ = qw.shape
     dev = qa.device
+    R, K = qa.shape
+    _require(qw, torch.int8, "qw", 3, device=dev)
+    E, N, K2 = qw.shape
+    if K2 != K:
+        raise ValueError(f"qw: expected K = {K} columns, got {K2}")
+    _require(sa, torch.float32, "sa", 1, (R,), dev)
+    _require(sw, torch.float32, "sw", 3, (E, N, K // GROUP), dev)
+    _require(offsets, torch.int32, "offsets", 1, (E + 1,), dev)
+    code = _dtype_code(out_dtype)
     if out is None:
-        y = torch.empty((R, N), dtype=out_dtype, device=dev)
+        out = torch.empty((R, N), dtype=out_dtype, device=dev)
     else:
-        y = out
+        _require_out(out, out_dtype, (R, N), dev)
     if workspace is None:
         workspace = torch.empty(max(grouped_gemm_workspace_size(R, E, N, K), 1),
                                 dtype=torch.uint8, device=dev)
+    else:
+        _require_workspace(workspace, dev)
     P = torch.empty((R, N, K // GROUP), dtype=torch.int32, device=dev) if debug_partials else None
-    _check(_lib.w8a8_grouped_gemm(_ptr(qa), _ptr(sa), _ptr(offsets), _ptr(qw), _ptr(sw), _ptr(y),
-                                  _dtype_code(out_dtype), R, E, N, K, _ptr(P), _ptr(workspace),
-                                  workspace.numel(), _stream(stream)), "w8a8_grouped_gemm")
-    return (y, P) if debug_partials else y
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_grouped_gemm(_ptr(qa), _ptr(sa), _ptr(offsets), _ptr(qw), _ptr(sw),
+                                      _ptr(out), code, R, E, N, K, _ptr(P), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)), "w8a8_grouped_gemm")
+    return (out, P) if debug_partials else out
 
 
 def linear_workspace_size(M: int, N: int, K: int) -> int:
@@ -239,18 +299,28 @@ def linear(a: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
     """quant_act + gemm in one call: Y[M,N] from BF16 activations a [M, K]
     (the quantizer writes the GEMM's operand directly into the workspace)."""
     lda = _require_act(a)
-    _require(qw, torch.int8, "qw", 2)
-    _require(sw, torch.float32, "sw", 2)
+    dev = a.device
     M, K = a.shape
+    _require(qw, torch.int8, "qw", 2, device=dev)
     N = qw.shape[0]
-    y = torch.empty((M, N), dtype=out_dtype, device=a.device) if out is None else out
+    if qw.shape[1] != K:
+        raise ValueError(f"qw: expected K = {K} columns, got {qw.shape[1]}")
+    _require(sw, torch.float32, "sw", 2, (N, K // GROUP), dev)
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (M, N), dev)
     if workspace is None:
         workspace = torch.empty(max(linear_workspace_size(M, N, K), 1), dtype=torch.uint8,
-                                device=a.device)
-    _check(_lib.w8a8_linear(_ptr(a), lda, _ptr(qw), _ptr(sw), _ptr(y), _dtype_code(out_dtype),
-                            M, N, K, _ptr(workspace), workspace.numel(), _stream(stream)),
-           "w8a8_linear")
-    return y
+                                device=dev)
+    else:
+        _require_workspace(workspace, dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_linear(_ptr(a), lda, _ptr(qw), _ptr(sw), _ptr(out), code, M, N, K,
+                                _ptr(workspace), workspace.numel(), _stream(stream)),
+               "w8a8_linear")
+    return out
 
 
 def grouped_linear(a: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
@@ -259,19 +329,30 @@ def grouped_linear(a: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor, sw:
                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """quant_act + grouped_gemm in one call over rows sorted by expert."""
     lda = _require_act(a)
-    _require(qw, torch.int8, "qw", 3)
-    _require(sw, torch.float32, "sw", 3)
-    _require(offsets, torch.int32, "offsets", 1)
+    dev = a.device
     R, K = a.shape
-    E, N, _ = qw.shape
-    y = torch.empty((R, N), dtype=out_dtype, device=a.device) if out is None else out
+    _require(qw, torch.int8, "qw", 3, device=dev)
+    E, N, K2 = qw.shape
+    if K2 != K:
+        raise ValueError(f"qw: expected K = {K} columns, got {K2}")
+    _require(sw, torch.float32, "sw", 3, (E, N, K // GROUP), dev)
+    _require(offsets, torch.int32, "offsets", 1, (E + 1,), dev)
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((R, N), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (R, N), dev)
     if workspace is None:
         workspace = torch.empty(max(grouped_linear_workspace_size(R, E, N, K), 1),
-                                dtype=torch.uint8, device=a.device)
-    _check(_lib.w8a8_grouped_linear(_ptr(a), lda, _ptr(offsets), _ptr(qw), _ptr(sw), _ptr(y),
-                                    _dtype_code(out_dtype), R, E, N, K, _ptr(workspace),
-                                    workspace.numel(), _stream(stream)), "w8a8_grouped_linear")
-    return y
+                                dtype=torch.uint8, device=dev)
+    else:
+        _require_workspace(workspace, dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_grouped_linear(_ptr(a), lda, _ptr(offsets), _ptr(qw), _ptr(sw),
+                                        _ptr(out), code, R, E, N, K, _ptr(workspace),
+                                        workspace.numel(), _stream(stream)),
+               "w8a8_grouped_linear")
+    return out
 
 
 def selftest_wait_timeout(limit_us: int = 20000,
@@ -281,6 +362,25 @@ def selftest_wait_timeout(limit_us: int = 20000,
     device_error())."""
     _check(_lib.w8a8_selftest_wait_timeout(limit_us, _stream(stream)),
            "w8a8_selftest_wait_timeout")
+
+
+def probe_tc_rate(n: int, chains: int, steps: int,
+                  stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Launches the tcgen05 kind::f16 rate probe (M=128, N=n, K=16 per
+    instruction, `chains` accumulators taking turns); returns the int8
+    multiply-adds it performs (time the launch to get the rate)."""
+    macs = ctypes.c_int64(0)
+    _check(_lib.w8a8_probe_tc_rate(n, chains, steps, ctypes.byref(macs), _stream(stream)),
+           "w8a8_probe_tc_rate")
+    return int(macs.value)
+
+
+def probe_dp4a_rate(iters: int, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Launches the dp4a rate probe; returns the int8 multiply-adds it performs."""
+    macs = ctypes.c_int64(0)
+    _check(_lib.w8a8_probe_dp4a_rate(iters, ctypes.byref(macs), _stream(stream)),
+           "w8a8_probe_dp4a_rate")
+    return int(macs.value)
 
 
 def device_error(clear: bool = True) -> int:

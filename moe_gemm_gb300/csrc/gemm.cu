@@ -1723,6 +1723,10 @@ cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t strea
     return cudaGetLastError();
 }
 
+cudaError_t device_error_word(unsigned long long **out) {
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(out), g_device_error);
+}
+
 cudaError_t read_device_error(unsigned long long *value, bool clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return e;
