@@ -83,6 +83,11 @@ constexpr int kOtherRegs = 56;
 constexpr int kSplitEpiRegs = 192;
 constexpr int kSplitOtherRegs = 64;
 constexpr int kSmemLimit = 232448;
+// Dense problems with wide token tiles walk their tiles in bands of this many
+// weight tiles (see decode_tile).
+constexpr int kRasterBand = 8;
+// Narrow tiles issue the MMAs of a step's two K groups alternately.
+constexpr bool kInterleaveGroups = true;
 
 // Shared memory: a fixed area (barriers, flags, tile table), then the weight
 // stages, then the token stages (offsets from a 1024-byte aligned base).
@@ -109,6 +114,7 @@ struct KParams {
     int tile_tokens;    // token rows per tile (b_rows or 2 * b_rows)
     int tab_off;        // byte offset of the tile table in shared memory
     int group_tokens;   // wide tiles: token stages released per K group (dense calls)
+    int gw;             // tile order: bands of gw weight tiles (0: expert-major, see decode_tile)
     // GEMV that quantizes its own token rows: BF16 activations [R, lda] and
     // the byte offset of the resident int8 code buffer in shared memory.
     const uint16_t *act;
@@ -136,8 +142,16 @@ struct Ring {
     }
 };
 
+// Tile t of the list: the expert e whose tiles [s_base[e], s_base[e+1])
+// contain t, then its weight tile nt and token tile mt. gw == 0: the token
+// tiles of one weight tile are consecutive (an expert's few token tiles share
+// its weight tile through L2). gw > 0 (one dense segment): bands of gw weight
+// tiles, and within a band the weight tiles of one token tile consecutive, so
+// the CTAs running at the same time share a few token tiles and a few weight
+// tiles instead of every token tile of the problem.
 __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const int *s_lo,
-                                                const int *s_cnt, int E, int tt) {
+                                                const int *s_cnt, int E, int tt, int n_tiles = 0,
+                                                int gw = 0) {
     int lo = 0, hi = E;  // s_base[lo] <= t < s_base[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -146,8 +160,18 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_base, const 
     const int local = t - s_base[lo];
     const int cnt = s_cnt[lo];
     const int m_tiles = (cnt + tt - 1) / tt;
-    const int nt = local / m_tiles;
-    const int mt = local - nt * m_tiles;
+    int nt, mt;
+    if (gw > 0) {
+        const int band_tiles = gw * m_tiles;
+        const int band = local / band_tiles;
+        const int w = min(gw, n_tiles - band * gw);
+        const int r = local - band * band_tiles;
+        mt = r / w;
+        nt = band * gw + (r - mt * w);
+    } else {
+        nt = local / m_tiles;
+        mt = local - nt * m_tiles;
+    }
     TileInfo ti;
     ti.e = lo;
     ti.n0 = nt * kTileN;
@@ -489,7 +513,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             uint32_t issued = 0;
             bool ok = true;
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
                 const int wrow = ti.e * p.N + ti.n0;
                 for (int sg = s0; sg < s1; ++sg) {
                     const int g0 = 2 * sg;
@@ -515,7 +539,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             uint32_t gph[2] = {0u, 0u};   // wide: phase of each group's partial buffer
             bool ok = true;
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
                 const int n_eff = (ti.rows + 15) & ~15;
                 const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(n_eff));
                 for (int sg = s0; sg < s1; ++sg) {
@@ -527,6 +551,26 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         return false;
                     }
                     tc_fence_after();
+                    if constexpr (!kWide && kInterleaveGroups) {
+                        // The two groups' accumulators are independent: their
+                        // MMAs take turns, so that one group's instruction
+                        // runs while the other's accumulator is busy.
+                        const uint64_t atom_step = b_atom_bytes >> 4;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            for (int j = 0; j < ng; ++j) {
+                                const uint32_t d_tmem = tmem_base + pbuf_col(pr.idx, j);
+                                const uint32_t a_tmem =
+                                    tmem_base + kTmemA0 + st.idx * 128u + j * 64u;
+                                const uint64_t bdesc =
+                                    smem_desc_sw128(sB + bs.idx * b_stage_bytes +
+                                                    j * 2u * b_atom_bytes) +
+                                    (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
+                                mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc,
+                                              kk > 0 ? 1u : 0u);
+                            }
+                        }
+                    } else
                     for (int j = 0; j < ng; ++j) {
                         if constexpr (kWide) {
                             // group j's partial buffer drained by the epilogue;
@@ -574,7 +618,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             uint32_t issued = 0;
             bool ok = true;
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
                 const int n_eff = (ti.rows + 15) & ~15;
                 const int nbox = (n_eff + kBoxRows - 1) / kBoxRows;
                 for (int sg = s0; sg < s1; ++sg) {
@@ -727,7 +771,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 if (s0 == 0 && s1 == plan.S) return true;
                 named_barrier_sync(2, 256);   // the piece's partial is stored
-                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+                const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
                 int c_first, c_final;
                 tile_owners(t, plan, c_first, c_final);
                 if (threadIdx.x == 384) {
@@ -787,7 +831,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         // same named barriers at split pieces.
         bool failed = false;
         for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
-            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
             const int n_eff = (ti.rows + 15) & ~15;
             const bool owned = 32 * ewg < n_eff;   // warp-uniform (first chunk)
             const int n_local = ti.n0 + lrow;
@@ -1119,7 +1163,7 @@ __device__ __forceinline__ void gemv_produce(const KParams &p, int total, const 
                         y, fb);
     };
     gemv_for_each(total, [&](int t, int h) -> bool {
-        const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+        const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
         const int wrow = ti.e * p.N + ti.n0 + (h > 0 ? 64 * (h - 1) : 0);
         const uint32_t wbytes = h > 0 ? kAStageBytes / 2 : kAStageBytes;
         const CUtensorMap *tw = h > 0 ? &tmap_w64 : &tmap_w;
@@ -1281,7 +1325,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
         Ring a;
         float acc[RR][RM];
         gemv_for_each(total, [&](int t, int h) -> bool {
-            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt);
+            const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
             // a half tile's 64 rows sit in stage rows [0, 64)
             const int n0 = ti.n0 + (h > 0 ? 64 * (h - 1) : 0);
             const int s0 = 0, s1 = (G + 1) >> 1;
@@ -1568,6 +1612,7 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     kp.tile_tokens = ps.tile_tokens;
     kp.tab_off = kOffTab;
     kp.group_tokens = (ps.wide && pr.offsets == nullptr) ? 1 : 0;
+    kp.gw = (ps.wide && pr.offsets == nullptr) ? kRasterBand : 0;
     unsigned long long *err = nullptr;
     cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
     if (e != cudaSuccess) return e;
