@@ -11,8 +11,14 @@ Functions follow "Deploying Hunyuan 770B in INT8 on domestic accelerators"
 INT8 x INT8 into INT32, FP32 scales applied at the end) and §1.3/§4.4 (MoE
 tokens processed by their routed experts).
 
-Pins: every function is checked by ``tests/test_oracle_pins.py`` against
-exact rational arithmetic, closed forms, brute force and invariants.
+MoE expert FFN (same page §4.4: count tokens per destination expert first,
+then transfer them; §4.1: SwiGLU between the two expert GEMMs; §3.1: every
+INT8 GEMM input quantized per token): ``moe_route``, ``swiglu_quant``,
+``moe_unpermute`` and their composition ``moe_ffn``.
+
+Pins: every function is checked by ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_moe_pins.py`` against exact rational arithmetic, closed
+forms, brute force and invariants.
 """
 from __future__ import annotations
 
@@ -63,6 +69,11 @@ def _load():
         lib.oracle_bf16_round.argtypes = [p, i64, p]
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        lib.oracle_moe_route.argtypes = [p, i64, i64, i64, p, p, p, p]
+        lib.oracle_exp_f32_n.argtypes = [p, i64, p]
+        lib.oracle_silu_f32_n.argtypes = [p, i64, p]
+        lib.oracle_swiglu_quant.argtypes = [p, i64, i64, p, p]
+        lib.oracle_moe_unpermute.argtypes = [p, p, p, i64, i64, i64, p]
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_group_size.restype = ctypes.c_int
@@ -176,3 +187,97 @@ def bf16_ulp(h: np.ndarray) -> np.ndarray:
     bexp = (u >> 7) & 0xFF
     e = np.where(bexp == 0, -126, bexp - 127)
     return np.ldexp(1.0, (e - 7).astype(np.int64))
+
+
+# ------------------------------------------------------------ MoE expert FFN
+def moe_route(ids: np.ndarray, E: int):
+    """Routing histogram, offsets and permutation of the top-k expert ids
+    ([T, k] int32). Returns (offsets [E+1], row_of [T*k], token_of_row [T*k],
+    pair_of_row [T*k]) as int32; entries with ids outside [0, E) are not
+    routed (row_of = -1); rows >= offsets[E] have token/pair -1."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    n = T * k
+    offsets = np.empty(E + 1, dtype=np.int32)
+    row_of = np.empty(n, dtype=np.int32)
+    tok = np.empty(n, dtype=np.int32)
+    pair = np.empty(n, dtype=np.int32)
+    _load().oracle_moe_route(_ptr(ids), T, k, E, _ptr(offsets), _ptr(row_of), _ptr(tok),
+                             _ptr(pair))
+    return offsets, row_of, tok, pair
+
+
+def exp_f32(x: np.ndarray) -> np.ndarray:
+    """The SwiGLU's binary32 exponential, element-wise."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    _load().oracle_exp_f32_n(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def silu_f32(x: np.ndarray) -> np.ndarray:
+    """silu(x) = x / (1 + e^-x) in binary32, element-wise."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    _load().oracle_silu_f32_n(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def swiglu_quant(U: np.ndarray, nrows: Optional[int] = None):
+    """h = silu(U[:, :I]) * U[:, I:] (binary32), then per-row quantization:
+    returns (qh int8 [R, I], sh float32 [R]); rows >= nrows are zero."""
+    U = np.ascontiguousarray(U, dtype=np.float32)
+    R, I2 = U.shape
+    assert I2 % 2 == 0
+    I = I2 // 2
+    nrows = R if nrows is None else int(nrows)
+    qh = np.zeros((R, I), dtype=np.int8)
+    sh = np.zeros(R, dtype=np.float32)
+    _load().oracle_swiglu_quant(_ptr(U), nrows, I, _ptr(qh), _ptr(sh))
+    return qh, sh
+
+
+def moe_unpermute(D: np.ndarray, row_of: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """Y[t] = sum_j w[t, j] * D[row_of[t, j]] (FP64); w and row_of [T, k]."""
+    D = np.ascontiguousarray(D, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    T, k = w.shape
+    row_of = np.ascontiguousarray(row_of, dtype=np.int32).reshape(T * k)
+    H = D.shape[1]
+    Y = np.empty((T, H), dtype=np.float64)
+    _load().oracle_moe_unpermute(_ptr(D), _ptr(row_of), _ptr(w), T, k, H, _ptr(Y))
+    return Y
+
+
+def moe_ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, qw_up: np.ndarray,
+            sw_up: np.ndarray, qw_down: np.ndarray, sw_down: np.ndarray) -> dict:
+    """The MoE expert FFN, step by step: route -> per-token quantization of
+    the permuted token rows -> gate_up grouped GEMM (FP32 output: the FP64
+    result rounded to binary32) -> SwiGLU + per-token requantization -> down
+    grouped GEMM (FP64) -> weighted un-permute (FP64). x_bits [T, H] BF16 bit
+    patterns; ids, w [T, k]; qw_up [E, 2I, H], qw_down [E, H, I]. Returns every
+    intermediate and y [T, H] (FP64)."""
+    E = qw_up.shape[0]
+    T, k = ids.shape
+    offsets, row_of, tok, pair = moe_route(ids, E)
+    R = int(offsets[E])
+    n = T * k
+    H = x_bits.shape[1]
+    xr = np.zeros((n, H), dtype=np.uint16)
+    xr[:R] = x_bits[tok[:R]]
+    qa, sa = quant_act(xr)
+    qa[R:] = 0
+    sa[R:] = 0
+    U64, T_up = grouped_gemm(qa, sa, offsets, qw_up, sw_up)
+    U = np.zeros(U64.shape, dtype=np.float32)
+    U[:R] = U64[:R].astype(np.float32)
+    qh, sh = swiglu_quant(U, R)
+    D64, T_down = grouped_gemm(qh, sh, offsets, qw_down, sw_down)
+    D = np.where(np.isnan(D64), 0.0, D64)
+    Tdn = np.where(np.isnan(T_down), 0.0, T_down)
+    y = moe_unpermute(D, row_of.reshape(T, k), w)
+    # sum_j |w| * T_down[row]: the magnitude the output's error is measured against
+    Ty = moe_unpermute(Tdn, row_of.reshape(T, k), np.abs(w).astype(np.float32))
+    return {"offsets": offsets, "row_of": row_of, "token_of_row": tok, "pair_of_row": pair,
+            "R": R, "qa": qa, "sa": sa, "U": U, "T_up": T_up, "qh": qh, "sh": sh, "D": D,
+            "T_down": Tdn, "y": y, "T_y": Ty}

@@ -210,3 +210,141 @@ void oracle_bf16_round(const double *v, int64_t n, uint16_t *out) {
     fesetround(FE_TONEAREST);
     for (int64_t i = 0; i < n; i++) out[i] = oracle_bf16_from_double(v[i]);
 }
+
+/* ======================================================================
+ * MoE expert FFN: the steps either side of the two grouped GEMMs
+ * ("Deploying Hunyuan 770B in INT8 on domestic accelerators", §4.4: a
+ * global count of tokens per destination expert is staged first, then the
+ * tokens are transferred in bulk; §4.1 operator table: SwiGLU next to the
+ * INT8 GEMMs; §3.1: every INT8 GEMM input is quantized per token,
+ * dynamically, so the gate_up output is re-quantized before the down GEMM).
+ * ====================================================================== */
+
+/* Routing: ids [T*k] holds the k experts of each token (flattened in (t, j)
+ * order). Entries whose id lies outside [0, E) are not routed (row_of = -1).
+ * counts per expert -> offsets [E+1] (exclusive prefix sum); each routed
+ * entry i gets row row_of[i] = offsets[e] + (number of earlier entries with
+ * the same expert), so rows are sorted by expert and, within an expert, by
+ * flattened index (token order). token_of_row[r] = i / k and pair_of_row[r]
+ * = i for the R = offsets[E] routed rows; rows >= R are set to -1. */
+void oracle_moe_route(const int32_t *ids, int64_t T, int64_t k, int64_t E, int32_t *offsets,
+                      int32_t *row_of, int32_t *token_of_row, int32_t *pair_of_row) {
+    const int64_t n = T * k;
+    for (int64_t e = 0; e <= E; e++) offsets[e] = 0;
+    for (int64_t i = 0; i < n; i++)
+        if (ids[i] >= 0 && ids[i] < E) offsets[ids[i] + 1] += 1;   /* histogram */
+    for (int64_t e = 0; e < E; e++) offsets[e + 1] += offsets[e];  /* prefix sum */
+    for (int64_t r = 0; r < n; r++) {
+        token_of_row[r] = -1;
+        pair_of_row[r] = -1;
+    }
+    for (int64_t e = 0; e < E; e++) {
+        int32_t fill = offsets[e];
+        for (int64_t i = 0; i < n; i++) {
+            if (ids[i] != e) continue;
+            row_of[i] = fill;
+            token_of_row[fill] = (int32_t)(i / k);
+            pair_of_row[fill] = (int32_t)i;
+            fill++;
+        }
+    }
+    for (int64_t i = 0; i < n; i++)
+        if (ids[i] < 0 || ids[i] >= E) row_of[i] = -1;
+}
+
+/* 2^n as a binary32 number, -126 <= n <= 127 (exact). */
+static float pow2_f32(int n) {
+    uint32_t u = (uint32_t)(n + 127) << 23;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* e^x in binary32 (the SwiGLU's exponential), by the textbook method of
+ * Cody and Waite: x is clamped to [-87, 88] (where e^x and e^-x stay normal
+ * binary32 numbers), n = round-to-nearest-even(x * log2(e)), the reduced
+ * argument r = x - n*ln2 is formed with ln2 split into a 15-bit head and a
+ * tail (so n*head is exact), e^r (|r| <= 0.35) is the Taylor series of degree
+ * 7 evaluated by Horner's rule, and the result is scaled by 2^n. Every step is
+ * one separately rounded binary32 operation (no fused multiply-add), so any
+ * implementation of these steps produces the same bits. */
+float oracle_exp_f32(float x) {
+    if (x > 88.0f) x = 88.0f;
+    if (x < -87.0f) x = -87.0f;
+    const float log2e = 1.44269502163f;
+    const float ln2_hi = 0.693145751953125f;        /* 0x3F317200 */
+    const float ln2_lo = 1.42860676533018e-06f;     /* ln2 - ln2_hi */
+    float t = x * log2e;
+    float n = nearbyintf(t);
+    float r = x - n * ln2_hi;
+    r = r - n * ln2_lo;
+    float p = 1.0f / 5040.0f;                       /* 1/7! */
+    p = p * r + 1.0f / 720.0f;
+    p = p * r + 1.0f / 120.0f;
+    p = p * r + 1.0f / 24.0f;
+    p = p * r + 1.0f / 6.0f;
+    p = p * r + 0.5f;
+    p = p * r + 1.0f;
+    p = p * r + 1.0f;
+    return p * pow2_f32((int)n);
+}
+
+/* silu(g) = g / (1 + e^-g) in binary32 with IEEE division. */
+float oracle_silu_f32(float g) {
+    float e = oracle_exp_f32(-g);
+    float d = 1.0f + e;
+    return g / d;
+}
+
+/* SwiGLU of the gate_up output followed by per-token quantization of the
+ * result for the down GEMM. U [R, 2I] FP32: gate in columns [0, I), up in
+ * [I, 2I). h = silu(gate) * up (binary32), then per row s = amax|h| / 127
+ * and q = clamp(round-half-even(h / s)) as in oracle_quant_act. Rows >= nrows
+ * (the routed rows) are left untouched. qh [R, I] int8, sh [R] float. */
+void oracle_swiglu_quant(const float *U, int64_t nrows, int64_t I, int8_t *qh, float *sh) {
+    fesetround(FE_TONEAREST);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrows; r++) {
+        const float *g = U + r * 2 * I;
+        const float *u = g + I;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < I; i++) {
+            float h = oracle_silu_f32(g[i]) * u[i];
+            if (fabsf(h) > amax) amax = fabsf(h);
+        }
+        float s = amax / 127.0f;
+        sh[r] = s;
+        for (int64_t i = 0; i < I; i++) {
+            float h = oracle_silu_f32(g[i]) * u[i];
+            qh[r * I + i] = quantize_value(h, s);
+        }
+    }
+}
+
+/* Weighted un-permute: Y[t, n] = sum_j w[t*k+j] * D[row_of[t*k+j], n] over the
+ * routed entries of token t (FP64; unrouted entries contribute nothing).
+ * D [R, H] double, Y [T, H] double. */
+void oracle_moe_unpermute(const double *D, const int32_t *row_of, const float *w, int64_t T,
+                          int64_t k, int64_t H, double *Y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; t++) {
+        for (int64_t n = 0; n < H; n++) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < k; j++) {
+                int32_t r = row_of[t * k + j];
+                if (r < 0) continue;
+                acc += (double)w[t * k + j] * D[(int64_t)r * H + n];
+            }
+            Y[t * H + n] = acc;
+        }
+    }
+}
+
+/* Element-wise array forms of the two functions above (for the tests). */
+void oracle_exp_f32_n(const float *x, int64_t n, float *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_exp_f32(x[i]);
+}
+
+void oracle_silu_f32_n(const float *x, int64_t n, float *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = oracle_silu_f32(x[i]);
+}
