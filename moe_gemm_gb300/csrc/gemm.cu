@@ -86,8 +86,6 @@ constexpr int kSmemLimit = 232448;
 // Dense problems with wide token tiles walk their tiles in bands of this many
 // weight tiles (see decode_tile).
 constexpr int kRasterBand = 8;
-// Narrow tiles issue the MMAs of a step's two K groups alternately.
-constexpr bool kInterleaveGroups = true;
 
 // Shared memory: a fixed area (barriers, flags, tile table), then the weight
 // stages, then the token stages (offsets from a 1024-byte aligned base).
@@ -551,26 +549,6 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         return false;
                     }
                     tc_fence_after();
-                    if constexpr (!kWide && kInterleaveGroups) {
-                        // The two groups' accumulators are independent: their
-                        // MMAs take turns, so that one group's instruction
-                        // runs while the other's accumulator is busy.
-                        const uint64_t atom_step = b_atom_bytes >> 4;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            for (int j = 0; j < ng; ++j) {
-                                const uint32_t d_tmem = tmem_base + pbuf_col(pr.idx, j);
-                                const uint32_t a_tmem =
-                                    tmem_base + kTmemA0 + st.idx * 128u + j * 64u;
-                                const uint64_t bdesc =
-                                    smem_desc_sw128(sB + bs.idx * b_stage_bytes +
-                                                    j * 2u * b_atom_bytes) +
-                                    (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
-                                mma_f16_tmemA(d_tmem, a_tmem + kk * 8, bdesc, idesc,
-                                              kk > 0 ? 1u : 0u);
-                            }
-                        }
-                    } else
                     for (int j = 0; j < ng; ++j) {
                         if constexpr (kWide) {
                             // group j's partial buffer drained by the epilogue;
@@ -1062,6 +1040,336 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             return true;
         });
         }   // draining warpgroups
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// =============================================================================
+// Large dense problems (at least 256 token rows): tiles of 128 weight rows x
+// 256 token rows, one K group per pipeline step, and one tcgen05.mma of
+// N = 256 per 16 K. On this part an MMA instruction costs about the same
+// whether it covers 128 or 256 token columns (~130 vs ~137 cycles at M = 128,
+// K = 16, measured with w8a8_probe_tc_rate), so the 256-column form does
+// nearly twice the work per instruction.
+// Tensor memory: the group's exact partial sums in columns [0, 256) (one
+// buffer; the epilogue drains it before the next group's MMAs), the fp16 A
+// operand (weights) of four groups in columns [256, 512), 64 each, so the
+// converter runs up to four groups ahead of the MMAs.
+// Shared memory: three 64 KB token stages (256 rows x 128 K fp16, two
+// 128-byte swizzle atom columns) and two 16 KB weight stages.
+// Warp roles: 0 weight TMA producer; 1 MMA issuer and TMEM allocation; 2
+// token TMA producer (waits for the kernel that wrote the codes); 4-7
+// converter (int8 -> fp16 A operand in TMEM); 8-15 epilogue: warpgroup h
+// drains token columns [128 h, 128 h + 128) of every lane (weight row),
+// fma with sw[n, g] into 128 register accumulators per thread, and at the end
+// of the tile multiplies by sa[m] and stores.
+// =============================================================================
+constexpr int kW2Tokens = 256;
+constexpr int kW2TokStages = 3;
+constexpr int kW2WStages = 2;
+constexpr int kW2ASlots = 4;
+constexpr int kW2OffStages = 2048;
+constexpr int kW2AtomBytes = kW2Tokens * 128;              // one 128-byte atom column, 32 KB
+constexpr int kW2TokStageBytes = 2 * kW2AtomBytes;          // one K group of tokens, 64 KB
+constexpr int kW2SmemBytes =
+    kW2OffStages + kW2TokStages * kW2TokStageBytes + kW2WStages * kAStageBytes + 1024;
+static_assert(kW2SmemBytes <= kSmemLimit, "wide-tile shared memory");
+constexpr uint32_t kW2TmemA0 = 256;
+
+struct W2Bar {
+    static constexpr int a_full = 0;                       // [kW2WStages] weight TMA -> converter
+    static constexpr int a_empty = a_full + kW2WStages;    // [kW2WStages] converter (4) -> weight TMA
+    static constexpr int b_full = a_empty + kW2WStages;    // [kW2TokStages] token TMA -> MMA
+    static constexpr int b_empty = b_full + kW2TokStages;  // [kW2TokStages] MMA commit -> token TMA
+    static constexpr int a_ready = b_empty + kW2TokStages; // [kW2ASlots] converter (4) -> MMA
+    static constexpr int a_free = a_ready + kW2ASlots;     // [kW2ASlots] MMA commit -> converter
+    static constexpr int d_full = a_free + kW2ASlots;      // MMA commit -> epilogue
+    static constexpr int d_empty = d_full + 1;             // epilogue (8 warps) -> MMA
+    static constexpr int drain = d_empty + 1;
+    static constexpr int count = drain + 1;
+};
+static_assert(W2Bar::count <= 128, "barrier area");
+
+template <bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1)
+w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                      const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw_addr);
+    const uint32_t sTok = base + kW2OffStages;
+    const uint32_t sW = sTok + kW2TokStages * kW2TokStageBytes;
+    const uint32_t sBar = base + kOffBar;
+    volatile uint32_t *s_tmem_base = reinterpret_cast<volatile uint32_t *>(smem + kOffMisc);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    volatile int *s_total = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    int *s_base = reinterpret_cast<int *>(smem + kWideOffTab);
+    int *s_lo = s_base + (p.E + 1);
+    int *s_cnt = s_lo + (p.E + 1);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kW2WStages; ++i) {
+            mbar_init(bar(W2Bar::a_full + i), 1);
+            mbar_init(bar(W2Bar::a_empty + i), 4);
+        }
+        for (int i = 0; i < kW2TokStages; ++i) {
+            mbar_init(bar(W2Bar::b_full + i), 1);
+            mbar_init(bar(W2Bar::b_empty + i), 1);
+        }
+        for (int i = 0; i < kW2ASlots; ++i) {
+            mbar_init(bar(W2Bar::a_ready + i), 4);
+            mbar_init(bar(W2Bar::a_free + i), 1);
+        }
+        mbar_init(bar(W2Bar::d_full), 1);
+        mbar_init(bar(W2Bar::d_empty), 8);
+        mbar_init(bar(W2Bar::drain), 1);
+        *s_abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(smem + kOffMisc), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 2) build_tile_table(p, kW2Tokens, lane, s_base, s_lo, s_cnt, s_total);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *s_tmem_base;
+    const int total = *s_total;
+    const int G = p.G;
+    const int grid = static_cast<int>(gridDim.x);
+    const int wg = warp >> 2;
+    auto tile_of = [&](int t) -> TileInfo {
+        return decode_tile(t, s_base, s_lo, s_cnt, p.E, kW2Tokens, p.n_tiles, p.gw);
+    };
+
+    if (warp < 4) {
+        setmaxnreg_dec<kOtherRegs>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------- weight TMA producer
+            Ring a;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += grid) {
+                const TileInfo ti = tile_of(t);
+                const int wrow = ti.e * p.N + ti.n0;
+                for (int g = 0; g < G; ++g) {
+                    if (!mbar_wait(bar(W2Bar::a_empty + a.idx), a.phase ^ 1u, s_abort, p.err,
+                                   ROLE_PRODUCER, 11)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(W2Bar::a_full + a.idx), kAStageBytes);
+                    tma_load_2d(sW + a.idx * kAStageBytes, &tmap_w, g * kGroupK, wrow,
+                                bar(W2Bar::a_full + a.idx));
+                    a.advance(kW2WStages);
+                    ++issued;
+                }
+            }
+            if (!ok) drain_ring(bar(W2Bar::a_full), issued, kW2WStages);
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            Ring b, sl;
+            uint32_t dph = 0;
+            bool ok = true;
+            const uint32_t idesc = idesc_f16_f32(kTileN, kW2Tokens);
+            for (int t = blockIdx.x; t < total && ok; t += grid) {
+                for (int g = 0; g < G; ++g) {
+                    if (!mbar_wait(bar(W2Bar::a_ready + sl.idx), sl.phase, s_abort, p.err,
+                                   ROLE_MMA, 11) ||
+                        !mbar_wait(bar(W2Bar::b_full + b.idx), b.phase, s_abort, p.err, ROLE_MMA,
+                                   12) ||
+                        !mbar_wait(bar(W2Bar::d_empty), dph ^ 1u, s_abort, p.err, ROLE_MMA, 13)) {
+                        ok = false;
+                        break;
+                    }
+                    dph ^= 1u;
+                    tc_fence_after();
+                    const uint32_t stage = sTok + b.idx * kW2TokStageBytes;
+                    const uint32_t a_tmem = tmem_base + kW2TmemA0 + sl.idx * 64u;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bdesc = smem_desc_sw128(stage + (kk >> 2) * kW2AtomBytes) +
+                                               static_cast<uint64_t>((kk & 3) * 2);
+                        mma_f16_tmemA(tmem_base, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(W2Bar::d_full));
+                    mma_commit(bar(W2Bar::a_free + sl.idx));
+                    mma_commit(bar(W2Bar::b_empty + b.idx));
+                    sl.advance(kW2ASlots);
+                    b.advance(kW2TokStages);
+                }
+            }
+            mma_commit(bar(W2Bar::drain));
+            drain_wait(bar(W2Bar::drain), 0);
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------- token TMA producer
+            griddep_wait();   // the fp16 token codes come from the kernel launched before
+            Ring b;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += grid) {
+                const TileInfo ti = tile_of(t);
+                for (int g = 0; g < G; ++g) {
+                    if (!mbar_wait(bar(W2Bar::b_empty + b.idx), b.phase ^ 1u, s_abort, p.err,
+                                   ROLE_PRODUCER, 12)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t stage = sTok + b.idx * kW2TokStageBytes;
+                    mbar_arrive_expect_tx(bar(W2Bar::b_full + b.idx), kW2TokStageBytes);
+                    for (int a = 0; a < 2; ++a)
+                        tma_load_2d(stage + a * kW2AtomBytes, &tmap_x, g * kGroupK + a * 64, ti.m0,
+                                    bar(W2Bar::b_full + b.idx));
+                    b.advance(kW2TokStages);
+                    ++issued;
+                }
+            }
+            if (!ok) drain_ring(bar(W2Bar::b_full), issued, kW2TokStages);
+        }
+    } else if (wg == 1) {
+        // --------------------------------------- weight converter (A -> TMEM)
+        setmaxnreg_dec<kOtherRegs>();
+        const int row = threadIdx.x - 128;
+        const int q = warp & 3;
+        Ring a, sl;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += grid) {
+            for (int g = 0; g < G; ++g) {
+                if (!mbar_wait(bar(W2Bar::a_full + a.idx), a.phase, s_abort, p.err, ROLE_CONVERT,
+                               11) ||
+                    !mbar_wait(bar(W2Bar::a_free + sl.idx), sl.phase ^ 1u, s_abort, p.err,
+                               ROLE_CONVERT, 12)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *rowp = smem + kW2OffStages + kW2TokStages * kW2TokStageBytes +
+                                      a.idx * kAStageBytes + row * 128;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       kW2TmemA0 + sl.idx * 64u;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    uint32_t r16[16];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * jj + cc;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
+                        i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
+                        i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
+                        i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
+                        i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
+                    }
+                    tmem_st_16cols(taddr + jj * 16, r16);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(W2Bar::a_empty + a.idx));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(W2Bar::a_ready + sl.idx));
+                a.advance(kW2WStages);
+                sl.advance(kW2ASlots);
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        setmaxnreg_inc<kEpiRegs>();
+        const int h = wg - 2;   // token columns [128 h, 128 h + 128)
+        const int q = warp & 3;
+        const int lrow = q * 32 + lane;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        float acc[128];
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+        uint32_t dph = 0;
+        bool failed = false;
+        for (int t = blockIdx.x; t < total && !failed; t += grid) {
+            const TileInfo ti = tile_of(t);
+            const int n_local = ti.n0 + lrow;
+            const bool n_ok = n_local < p.N;
+            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            // this row's weight scales two groups ahead (loads issued in place)
+            float sc0 = n_ok ? ldg_nc_f32_now(swp) : 0.0f;
+            float sc1 = (n_ok && G > 1) ? ldg_nc_f32_now(swp + 1) : 0.0f;
+            const int col0 = 128 * h;
+            for (int g = 0; g < G; ++g) {
+                const float sc = sc0;
+                sc0 = sc1;
+                sc1 = (n_ok && g + 2 < G) ? ldg_nc_f32_now(swp + g + 2) : 0.0f;
+                if (!mbar_wait(bar(W2Bar::d_full), dph, s_abort, p.err, ROLE_EPILOGUE, 11)) {
+                    failed = true;
+                    break;
+                }
+                dph ^= 1u;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32cols_sync(lane_base + col0 + 32u * c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[32 * c + j] = fmaf(__uint_as_float(v[j]), sc, acc[32 * c + j]);
+                    if (kDebug && n_ok) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = col0 + 32 * c + j;
+                            if (col < ti.rows)
+                                p.dbg[(static_cast<size_t>(ti.m0 + col) * p.N + n_local) * G + g] =
+                                    __float2int_rn(__uint_as_float(v[j]));
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed(bar(W2Bar::d_empty));
+            }
+            if (failed) break;
+            if (n_ok) {
+                // Token rows [m0 + col0, m0 + col0 + 128) of output column
+                // n_local: one running pointer, and chunks of 16 rows so that
+                // the token-scale loads are not all hoisted ahead of the
+                // stores (registers).
+                const int rows_here = ti.rows - col0;
+                const float *sap = p.sa + ti.m0 + col0;
+                const size_t first = static_cast<size_t>(ti.m0 + col0) * p.N + n_local;
+                if (p.out_fp32) {
+                    float *yp = static_cast<float *>(p.y) + first;
+#pragma unroll
+                    for (int j = 0; j < 128; ++j) {
+                        if (j < rows_here) *yp = acc[j] * __ldg(sap + j);
+                        yp += p.N;
+                        if ((j & 15) == 15) asm volatile("" ::: "memory");
+                    }
+                } else {
+                    __nv_bfloat16 *yp = static_cast<__nv_bfloat16 *>(p.y) + first;
+#pragma unroll
+                    for (int j = 0; j < 128; ++j) {
+                        if (j < rows_here) *yp = __float2bfloat16_rn(acc[j] * __ldg(sap + j));
+                        yp += p.N;
+                        if ((j & 15) == 15) asm volatile("" ::: "memory");
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+        }
     }
 
     __syncwarp();
@@ -1652,6 +1960,67 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     return cudaGetLastError();
 }
 
+// Dense calls of at least kW2Tokens token rows: w8a8_gemm_wide_kernel.
+template <auto kernel>
+cudaError_t launch_wide(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
+    CUtensorMap tw, tx;
+    if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
+                   (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
+        !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x16, (uint64_t)pr.K,
+                   (uint64_t)pr.R, 64, kW2Tokens))
+        return cudaErrorInvalidValue;
+    static int attr_done[64] = {0};   // per device, per kernel instance
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        // setmaxnreg.inc can only take registers the CTA was launched with.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs * kThreads < (kThreads / 2) * (kEpiRegs + kOtherRegs))
+            return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kW2SmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = 1;
+    }
+    KParams kp = {};
+    kp.sa = pr.sa;
+    kp.sw = pr.sw;
+    kp.offsets = nullptr;
+    kp.y = pr.y;
+    kp.dbg = pr.debug_partials;
+    kp.R = static_cast<int>(pr.R);
+    kp.E = 1;
+    kp.N = static_cast<int>(pr.N);
+    kp.K = static_cast<int>(pr.K);
+    kp.G = static_cast<int>(pr.K / kGroupK);
+    kp.n_tiles = static_cast<int>((pr.N + kTileN - 1) / kTileN);
+    kp.out_fp32 = pr.out_fp32 ? 1 : 0;
+    kp.tile_tokens = kW2Tokens;
+    kp.gw = kRasterBand;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&kp.err), g_device_error);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (pr.R + kW2Tokens - 1) / kW2Tokens * kp.n_tiles;
+    const int64_t grid = tiles < num_sms ? tiles : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    // Programmatic dependent launch: only the token producer waits for the
+    // kernel before it (which writes the fp16 codes).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(kW2SmemBytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tw, tx, kp);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // Batched GEMV on the CUDA cores for dense calls of at most 4 token rows.
 // kExtra: bytes of shared memory the kernel keeps after its stages.
 template <auto kernel, int MR, int CW, int kExtra, bool kFuseQ = false>
@@ -1749,8 +2118,11 @@ cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream)
         if (pr.R <= 2) return launch_gemv_mr<1, 2, 8>(pr, num_sms, stream);
         return launch_gemv_mr<1, 4, 8>(pr, num_sms, stream);
     }
-    const PipeShape ps = choose_pipe(pr);
     const bool dbg = pr.debug_partials != nullptr;
+    if (uses_wide256(pr.R, pr.offsets != nullptr))
+        return dbg ? launch_wide<w8a8_gemm_wide_kernel<true>>(pr, num_sms, stream)
+                   : launch_wide<w8a8_gemm_wide_kernel<false>>(pr, num_sms, stream);
+    const PipeShape ps = choose_pipe(pr);
     if (ps.wide) {
         if (pr.E > kWideMaxExperts) return cudaErrorInvalidConfiguration;
         return dbg ? launch_kernel<w8a8_gemm_narrow_kernel<true, true>>(pr, ps, num_sms, stream)

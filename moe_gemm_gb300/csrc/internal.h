@@ -20,6 +20,27 @@ cudaError_t launch_quant_act_f16(const uint16_t *a, int64_t M, int64_t K, int64_
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
                                 cudaStream_t stream);
 
+// Per-token quantization with a row gather: output row r (row stride K)
+// quantizes input row src_rows[r] of a (row stride lda); rows whose entry is
+// negative are skipped. Codes as fp16 (f16) or int8.
+cudaError_t launch_quant_act_rows(const uint16_t *a, int64_t rows, int64_t K, int64_t lda,
+                                  const int32_t *src_rows, void *out, bool f16, float *sa,
+                                  cudaStream_t stream);
+
+// MoE expert FFN steps (moe.cu).
+constexpr int kMoeMaxTopK = 64;
+constexpr int64_t kSwigluMaxI = 8192;
+cudaError_t launch_moe_route(const int32_t *ids, int64_t T, int64_t k, int64_t E, int32_t *offsets,
+                             int32_t *row_of, int32_t *token_of_row, int32_t *pair_of_row,
+                             cudaStream_t stream);
+// out_kind: 0 int8 codes, 1 fp16 codes (+ scales sh), 2 h itself (FP32)
+cudaError_t launch_swiglu_quant(const float *U, int64_t rows, int64_t I, const int32_t *offsets,
+                                int64_t E, void *out, int out_kind, float *sh,
+                                cudaStream_t stream);
+cudaError_t launch_moe_unpermute(const float *D, const int32_t *row_of, const float *w, int64_t T,
+                                 int64_t k, int64_t H, void *y, bool out_fp32,
+                                 cudaStream_t stream);
+
 // int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] in `out`;
 // also zeroes n_cnt split-tile counters at cnt (if not null) for the GEMM
 // launched after it.
@@ -79,6 +100,11 @@ inline size_t sk_area_bytes(int64_t R, bool grouped) {
     return sk_counter_bytes() +
            static_cast<size_t>(kSkMaxCtas) * 2 * static_cast<size_t>(R) * 128 * sizeof(float);
 }
+
+// Dense calls of at least this many token rows run tiles of 128 weight rows x
+// 256 token rows (one 256-column MMA per 16 K).
+constexpr int kWide256MinRows = 256;
+inline bool uses_wide256(int64_t R, bool grouped) { return !grouped && R >= kWide256MinRows; }
 
 // Maximum number of experts a grouped call may have.
 constexpr int kMaxExperts = 1024;

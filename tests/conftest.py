@@ -24,3 +24,13 @@ def pytest_sessionstart(session):
     if torch.cuda.is_available():
         import __graft_entry__
         __graft_entry__.build()
+
+
+def pytest_terminal_summary(terminalreporter):
+    import parity_stats
+    b = parity_stats.BF16
+    if b["checked"]:
+        terminalreporter.write_line(
+            f"BF16 parity: {b['checked']} outputs checked, {b['within_1ulp']} within one ulp of "
+            f"the correctly rounded exact value, {b['by_cancellation_clause']} accepted by the "
+            f"cancellation clause only")

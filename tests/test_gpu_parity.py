@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import oracle
+import parity_stats
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -60,6 +61,7 @@ def check_bf16(y_bits: np.ndarray, y_ref: np.ndarray, T: np.ndarray):
     ok1 = np.abs(yv - rv) <= ulp
     ok2 = np.abs(yv - y_ref) <= 1e-5 * T + 0.5 * oracle.bf16_ulp(y_bits)
     bad = ~(ok1 | ok2)
+    parity_stats.record_bf16(ok1.size, ok1.sum(), (ok2 & ~ok1).sum())
     assert not bad.any(), f"{bad.sum()} BF16 outputs out of tolerance"
     return ok1.mean()
 
@@ -192,6 +194,8 @@ def test_dense_ragged_shapes(M, N, K, out):
     dt = torch.float32 if out == "fp32" else torch.bfloat16
     y, P = run_gemm(qa, sa, qw, sw, dt, debug=True)
     np.testing.assert_array_equal(P.cpu().numpy(), oracle.group_partials(qa_o, qw_o))
+    # the kernel without the partials output computes the same outputs
+    assert torch.equal(run_gemm(qa, sa, qw, sw, dt), y)
     y_ref, T = oracle.gemm(qa_o, sa_o, qw_o, sw_o)
     if out == "fp32":
         check_fp32(y.cpu().numpy(), y_ref, T, K)
