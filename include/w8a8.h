@@ -200,6 +200,107 @@ w8a8_status w8a8_grouped_linear(const void *a_bf16, int64_t lda, const int32_t *
                                 int64_t R, int64_t E, int64_t N, int64_t K, void *workspace,
                                 size_t workspace_bytes, w8a8_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * MoE expert FFN ("Deploying Hunyuan 770B in INT8 on domestic accelerators":
+ * §4.4, tokens are counted per destination expert first and then
+ * transferred; §4.1 operator table, SwiGLU between the INT8 expert GEMMs;
+ * §3.1, every INT8 GEMM input is quantized per token, dynamically). Each
+ * token t has k (expert id, gate weight) pairs from its router, topk_ids and
+ * topk_w [T, k] (row-major, on the device). The FFN of an expert e is
+ *   h = silu(x W_gate[e]^T) * (x W_up[e]^T),   out_e(x) = h W_down[e]^T,
+ * with W_gate_up[e] = [W_gate[e]; W_up[e]] ([2I, H], gate rows first) and
+ * W_down[e] [H, I], both INT8 with per-row per-128-K-group scales, and
+ *   y[t] = sum_j topk_w[t, j] * out_{topk_ids[t, j]}(x[t]).
+ * Entries whose id lies outside [0, E) are not routed: they contribute
+ * nothing. Numerics of each step are stated at its entry point below.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Routing: per-expert counts of the n = T * k entries of topk_ids, their
+ * exclusive prefix sum offsets [E+1] (offsets[E] = number of routed entries
+ * R), and the permutation that sorts the routed entries by expert, ties in
+ * entry order i = t * k + j (so by token): row_of [n] (the row of entry i,
+ * -1 if not routed), token_of_row [n] and pair_of_row [n] (entry i of each
+ * row; -1 for rows >= R). One CTA; all outputs are device int32 arrays. No
+ * host read of any of them (the call can be captured in a CUDA graph).
+ * 1 <= E <= 1024, k >= 1. T == 0 writes offsets = 0 only.
+ */
+w8a8_status w8a8_moe_route(const int32_t *topk_ids, int64_t T, int64_t k, int64_t E,
+                           int32_t *offsets, int32_t *row_of, int32_t *token_of_row,
+                           int32_t *pair_of_row, w8a8_stream_t stream);
+
+/*
+ * The transfer step fused with the per-token quantization: output row r of
+ * qa [rows, K] (row stride K) and sa [rows] holds the w8a8_quant_act codes
+ * and scale of row src_rows[r] of a_bf16 (row stride lda); rows whose
+ * src_rows entry is negative are left untouched. Bit-identical to
+ * w8a8_quant_act on the gathered rows.
+ */
+w8a8_status w8a8_quant_act_rows(const void *a_bf16, int64_t lda, const int32_t *src_rows,
+                                int64_t rows, int64_t K, int8_t *qa, float *sa,
+                                w8a8_stream_t stream);
+
+/*
+ * SwiGLU of the gate_up output followed by per-token requantization (the
+ * down GEMM's input). U [rows, 2I] FP32 (gate in columns [0, I), up in
+ * [I, 2I)); per row, in binary32:
+ *   h = silu(gate) * up,  silu(g) = g / (1 + e^-g),
+ * where e^x is evaluated by Cody and Waite's range reduction (x clamped to
+ * [-87, 88], n = round-half-even(x log2 e), r = x - n ln2 with ln2 split into
+ * 0.693145751953125 + 1.42860676533018e-06) and the degree-7 Taylor series of
+ * e^r by Horner's rule, then scaled by 2^n; every step is a separately
+ * rounded binary32 operation, so h is a fixed function of (gate, up). Then
+ * sh[r] = amax|h| / 127 and qh[r, i] = clamp(round-half-even(h / sh[r]))
+ * exactly as w8a8_quant_act. offsets (nullable) [E+1]: rows >= offsets[E]
+ * are skipped (not routed). I % 4 == 0, I <= 8192.
+ */
+w8a8_status w8a8_swiglu_quant(const float *U, int64_t rows, int64_t I, const int32_t *offsets,
+                              int64_t E, int8_t *qh, float *sh, w8a8_stream_t stream);
+
+/*
+ * h = silu(gate) * up alone (the first half of w8a8_swiglu_quant, same
+ * arithmetic), FP32 [rows, I]; U and h 16-byte aligned.
+ */
+w8a8_status w8a8_swiglu(const float *U, int64_t rows, int64_t I, float *h, w8a8_stream_t stream);
+
+/*
+ * Weighted un-permute: y[t, :] = sum_{j < k} topk_w[t, j] * D[row_of[t*k + j], :]
+ * over the routed entries (row_of >= 0), accumulated in FP32 in order of j
+ * (fused multiply-add), then stored as BF16 (round to nearest even) or FP32.
+ * D [R, H] FP32, row_of and topk_w [T, k], y [T, H]; H % 4 == 0; D and y
+ * 16-byte aligned; k <= 64.
+ */
+w8a8_status w8a8_moe_unpermute(const float *D, const int32_t *row_of, const float *topk_w,
+                               int64_t T, int64_t k, int64_t H, void *y, w8a8_dtype y_dtype,
+                               w8a8_stream_t stream);
+
+/*
+ * Bytes of workspace w8a8_moe_ffn needs (n = T * k): offsets, the routing
+ * arrays, the fp16 codes and scales of both GEMM inputs, and the FP32 outputs
+ * of both GEMMs ([n, 2I] and [n, H]), each rounded up to 256 bytes. 0 for
+ * invalid shapes or T == 0.
+ */
+size_t w8a8_moe_ffn_workspace_size(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E);
+
+/*
+ * The MoE expert FFN in one call, six kernels on `stream`: w8a8_moe_route;
+ * the transfer of the token rows into expert order fused with their
+ * per-token quantization (w8a8_quant_act_rows, fp16 codes); the gate_up
+ * grouped GEMM (FP32 output, as w8a8_grouped_gemm); w8a8_swiglu_quant (fp16
+ * codes); the down grouped GEMM (FP32); w8a8_moe_unpermute into y.
+ *   x_bf16 [T, ldx] BF16 tokens; topk_ids, topk_w [T, k] device arrays;
+ *   qw_up [E, 2I, H] int8, sw_up [E, 2I, H/128]; qw_down [E, H, I] int8,
+ *   sw_down [E, H, I/128]; y [T, H] BF16 or FP32 (16-byte aligned).
+ * Results are identical to those separate calls (same kernels and codes).
+ * H and I positive multiples of 128, I <= 8192, 1 <= k <= 64, 1 <= E <= 1024.
+ * No host read of device data: the call can be captured in a CUDA graph.
+ */
+w8a8_status w8a8_moe_ffn(const void *x_bf16, int64_t ldx, const int32_t *topk_ids,
+                         const float *topk_w, int64_t T, int64_t k, int64_t H, int64_t I,
+                         int64_t E, const int8_t *qw_up, const float *sw_up,
+                         const int8_t *qw_down, const float *sw_down, void *y, w8a8_dtype y_dtype,
+                         void *workspace, size_t workspace_bytes, w8a8_stream_t stream);
+
 /*
  * Size of the scratch array built into the library for w8a8_gemm_noalloc:
  * 8 MiB, enough for M * K <= 4,194,304 activation codes (e.g. M <= 512 at

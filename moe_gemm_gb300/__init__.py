@@ -63,11 +63,21 @@ def _load() -> ctypes.CDLL:
                                         ctypes.c_size_t, vp]
     lib.w8a8_probe_tc_rate.argtypes = [i32, i32, i64, ctypes.POINTER(i64), vp]
     lib.w8a8_probe_dp4a_rate.argtypes = [i64, ctypes.POINTER(i64), vp]
+    lib.w8a8_moe_route.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.w8a8_quant_act_rows.argtypes = [vp, i64, vp, i64, i64, vp, vp, vp]
+    lib.w8a8_swiglu_quant.argtypes = [vp, i64, i64, vp, i64, vp, vp, vp]
+    lib.w8a8_swiglu.argtypes = [vp, i64, i64, vp, vp]
+    lib.w8a8_moe_unpermute.argtypes = [vp, vp, vp, i64, i64, i64, vp, i32, vp]
+    lib.w8a8_moe_ffn_workspace_size.argtypes = [i64, i64, i64, i64, i64]
+    lib.w8a8_moe_ffn_workspace_size.restype = ctypes.c_size_t
+    lib.w8a8_moe_ffn.argtypes = [vp, i64, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
+                                 i32, vp, ctypes.c_size_t, vp]
     lib.w8a8_version.restype = i32
     for name in ("w8a8_quant_act", "w8a8_quant_weight", "w8a8_gemm", "w8a8_grouped_gemm",
                  "w8a8_gemm_noalloc", "w8a8_device_error", "w8a8_selftest_wait_timeout",
                  "w8a8_linear", "w8a8_grouped_linear", "w8a8_probe_tc_rate",
-                 "w8a8_probe_dp4a_rate"):
+                 "w8a8_probe_dp4a_rate", "w8a8_moe_route", "w8a8_quant_act_rows",
+                 "w8a8_swiglu_quant", "w8a8_swiglu", "w8a8_moe_unpermute", "w8a8_moe_ffn"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -352,6 +362,146 @@ def grouped_linear(a: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor, sw:
                                         _ptr(out), code, R, E, N, K, _ptr(workspace),
                                         workspace.numel(), _stream(stream)),
                "w8a8_grouped_linear")
+    return out
+
+
+# ------------------------------------------------------------ MoE expert FFN
+def moe_route(topk_ids: torch.Tensor, E: int, stream: Optional[torch.cuda.Stream] = None):
+    """Routing of topk_ids [T, k] (int32): returns (offsets [E+1], row_of
+    [T*k], token_of_row [T*k], pair_of_row [T*k]), all int32 on the device."""
+    _require(topk_ids, torch.int32, "topk_ids", 2)
+    dev = topk_ids.device
+    T, k = topk_ids.shape
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = torch.empty(T * k, dtype=torch.int32, device=dev)
+    tok = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pair = torch.empty(T * k, dtype=torch.int32, device=dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_moe_route(_ptr(topk_ids), T, k, E, _ptr(offsets), _ptr(row_of),
+                                   _ptr(tok), _ptr(pair), _stream(stream)), "w8a8_moe_route")
+    return offsets, row_of, tok, pair
+
+
+def quant_act_rows(a: torch.Tensor, src_rows: torch.Tensor, qa: Optional[torch.Tensor] = None,
+                   sa: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-token quantization of the gathered rows a[src_rows[r]] (rows with a
+    negative entry are left untouched in qa / sa)."""
+    lda = _require_act(a)
+    dev = a.device
+    _require(src_rows, torch.int32, "src_rows", 1, device=dev)
+    rows, K = src_rows.shape[0], a.shape[1]
+    if qa is None:
+        qa = torch.zeros((rows, K), dtype=torch.int8, device=dev)
+    else:
+        _require(qa, torch.int8, "qa", 2, (rows, K), dev)
+    if sa is None:
+        sa = torch.zeros((rows,), dtype=torch.float32, device=dev)
+    else:
+        _require(sa, torch.float32, "sa", 1, (rows,), dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_quant_act_rows(_ptr(a), lda, _ptr(src_rows), rows, K, _ptr(qa), _ptr(sa),
+                                        _stream(stream)), "w8a8_quant_act_rows")
+    return qa, sa
+
+
+def swiglu_quant(U: torch.Tensor, offsets: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """h = silu(U[:, :I]) * U[:, I:] then per-row quantization: (qh int8
+    [R, I], sh float32 [R]); with offsets [E+1], rows >= offsets[E] are
+    skipped (left zero)."""
+    _require(U, torch.float32, "U", 2)
+    dev = U.device
+    R, I2 = U.shape
+    if I2 % 2:
+        raise ValueError("U must have an even number of columns (gate | up)")
+    I = I2 // 2
+    E = 0
+    if offsets is not None:
+        _require(offsets, torch.int32, "offsets", 1, device=dev)
+        E = offsets.shape[0] - 1
+    qh = torch.zeros((R, I), dtype=torch.int8, device=dev)
+    sh = torch.zeros((R,), dtype=torch.float32, device=dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_swiglu_quant(_ptr(U), R, I, _ptr(offsets), E, _ptr(qh), _ptr(sh),
+                                      _stream(stream)), "w8a8_swiglu_quant")
+    return qh, sh
+
+
+def swiglu(U: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """h = silu(U[:, :I]) * U[:, I:] (FP32, the arithmetic of swiglu_quant)."""
+    _require(U, torch.float32, "U", 2)
+    R, I2 = U.shape
+    h = torch.empty((R, I2 // 2), dtype=torch.float32, device=U.device)
+    with _on_device(U.device, stream):
+        _check(_lib.w8a8_swiglu(_ptr(U), R, I2 // 2, _ptr(h), _stream(stream)), "w8a8_swiglu")
+    return h
+
+
+def moe_unpermute(D: torch.Tensor, row_of: torch.Tensor, topk_w: torch.Tensor,
+                  out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """y[t] = sum_j topk_w[t, j] * D[row_of[t*k + j]] over routed entries."""
+    _require(D, torch.float32, "D", 2)
+    dev = D.device
+    _require(topk_w, torch.float32, "topk_w", 2, device=dev)
+    T, k = topk_w.shape
+    _require(row_of, torch.int32, "row_of", 1, (T * k,), dev)
+    H = D.shape[1]
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (T, H), dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_moe_unpermute(_ptr(D), _ptr(row_of), _ptr(topk_w), T, k, H, _ptr(out),
+                                       code, _stream(stream)), "w8a8_moe_unpermute")
+    return out
+
+
+def moe_ffn_workspace_size(T: int, k: int, H: int, I: int, E: int) -> int:
+    return int(_lib.w8a8_moe_ffn_workspace_size(T, k, H, I, E))
+
+
+def moe_ffn(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,
+            qw_up: torch.Tensor, sw_up: torch.Tensor, qw_down: torch.Tensor,
+            sw_down: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
+            out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The MoE expert FFN: y [T, H] from tokens x [T, H] (BF16), the router's
+    topk_ids / topk_w [T, k], qw_up [E, 2I, H] (gate rows first) and
+    qw_down [E, H, I] with their group scales."""
+    ldx = _require_act(x)
+    dev = x.device
+    T, H = x.shape
+    _require(topk_ids, torch.int32, "topk_ids", 2, device=dev)
+    k = topk_ids.shape[1]
+    _require(topk_w, torch.float32, "topk_w", 2, (T, k), dev)
+    if topk_ids.shape[0] != T:
+        raise ValueError("topk_ids must have one row per token")
+    _require(qw_up, torch.int8, "qw_up", 3, device=dev)
+    E, I2, H2 = qw_up.shape
+    if H2 != H or I2 % 2:
+        raise ValueError("qw_up must be [E, 2I, H]")
+    I = I2 // 2
+    _require(sw_up, torch.float32, "sw_up", 3, (E, I2, H // GROUP), dev)
+    _require(qw_down, torch.int8, "qw_down", 3, (E, H, I), dev)
+    _require(sw_down, torch.float32, "sw_down", 3, (E, H, I // GROUP), dev)
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (T, H), dev)
+    if workspace is None:
+        workspace = torch.empty(max(moe_ffn_workspace_size(T, k, H, I, E), 1), dtype=torch.uint8,
+                                device=dev)
+    else:
+        _require_workspace(workspace, dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_moe_ffn(_ptr(x), ldx, _ptr(topk_ids), _ptr(topk_w), T, k, H, I, E,
+                                 _ptr(qw_up), _ptr(sw_up), _ptr(qw_down), _ptr(sw_down),
+                                 _ptr(out), code, _ptr(workspace), workspace.numel(),
+                                 _stream(stream)), "w8a8_moe_ffn")
     return out
 
 

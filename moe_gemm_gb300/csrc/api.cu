@@ -247,6 +247,53 @@ cudaError_t noalloc_scratch_ptr(void **out) {
     return cudaSuccess;
 }
 
+// ---------------------------------------------------------------------------
+// MoE expert FFN (w8a8_moe_ffn): workspace layout, every part 256-byte aligned,
+// n = T * k routed-row slots:
+//   offsets [E+1] int32, row_of [n], token_of_row [n], pair_of_row [n] int32,
+//   gate_up operand: fp16 codes [n, H] + token scales [n],
+//   gate_up output U [n, 2I] FP32,
+//   down operand: fp16 codes [n, I] + scales [n],
+//   down output D [n, H] FP32.
+struct FfnLayout {
+    size_t offsets, row_of, tok, pair, x_up, sa_up, u, x_dn, sa_dn, d, total;
+};
+
+FfnLayout ffn_layout(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E) {
+    const size_t n = static_cast<size_t>(T) * static_cast<size_t>(k);
+    FfnLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += round_up(bytes, kWsAlign);
+        return at;
+    };
+    L.offsets = take(static_cast<size_t>(E + 1) * 4);
+    L.row_of = take(n * 4);
+    L.tok = take(n * 4);
+    L.pair = take(n * 4);
+    L.x_up = take(n * static_cast<size_t>(H) * 2);
+    L.sa_up = take(n * 4);
+    L.u = take(n * static_cast<size_t>(2 * I) * 4);
+    L.x_dn = take(n * static_cast<size_t>(I) * 2);
+    L.sa_dn = take(n * 4);
+    L.d = take(n * static_cast<size_t>(H) * 4);
+    L.total = off;
+    return L;
+}
+
+w8a8_status check_ffn_shape(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E) {
+    if (T < 0 || k < 1 || k > w8a8::kMoeMaxTopK || E < 1 || E > w8a8::kMaxExperts)
+        return W8A8_ERR_INVALID_ARG;
+    if (H <= 0 || I <= 0 || H % W8A8_GROUP != 0 || I % W8A8_GROUP != 0 || I > w8a8::kSwigluMaxI)
+        return W8A8_ERR_INVALID_ARG;
+    const int64_t n = T * k;
+    if (T > kMaxElems / k || n > kMaxElems / H || n > kMaxElems / (2 * I) ||
+        E * 2 * I > kMaxElems / H || E * H > kMaxElems / I)
+        return W8A8_ERR_INVALID_ARG;
+    return W8A8_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -382,6 +429,177 @@ w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *q
     if (noalloc_scratch_ptr(&scratch) != cudaSuccess) return W8A8_ERR_CUDA;
     return w8a8_gemm(qa, sa, qw, sw, y, y_dtype, M, N, K, nullptr, scratch, kNoallocScratchBytes,
                      stream);
+}
+
+w8a8_status w8a8_moe_route(const int32_t *topk_ids, int64_t T, int64_t k, int64_t E,
+                           int32_t *offsets, int32_t *row_of, int32_t *token_of_row,
+                           int32_t *pair_of_row, w8a8_stream_t stream) {
+    if (T < 0 || k < 1 || E < 1 || E > w8a8::kMaxExperts || T > kMaxElems / k)
+        return W8A8_ERR_INVALID_ARG;
+    if (!offsets) return W8A8_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !row_of || !token_of_row || !pair_of_row))
+        return W8A8_ERR_INVALID_ARG;
+    if (!aligned(topk_ids, 4) || !aligned(offsets, 4) || !aligned(row_of, 4) ||
+        !aligned(token_of_row, 4) || !aligned(pair_of_row, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_moe_route(topk_ids, T, k, E, offsets, row_of, token_of_row,
+                                            pair_of_row, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_quant_act_rows(const void *a_bf16, int64_t lda, const int32_t *src_rows,
+                                int64_t rows, int64_t K, int8_t *qa, float *sa,
+                                w8a8_stream_t stream) {
+    if (rows < 0 || K <= 0 || lda < K || rows > kMaxElems / K) return W8A8_ERR_INVALID_ARG;
+    if (rows == 0) return W8A8_OK;
+    if (!a_bf16 || !src_rows || !qa || !sa || !aligned(a_bf16, 2) || !aligned(src_rows, 4) ||
+        !aligned(sa, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_quant_act_rows(static_cast<const uint16_t *>(a_bf16), rows, K,
+                                                 lda, src_rows, qa, false, sa,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_swiglu_quant(const float *U, int64_t rows, int64_t I, const int32_t *offsets,
+                              int64_t E, int8_t *qh, float *sh, w8a8_stream_t stream) {
+    if (rows < 0 || I <= 0 || I % 4 != 0 || I > w8a8::kSwigluMaxI || rows > kMaxElems / (2 * I))
+        return W8A8_ERR_INVALID_ARG;
+    if (offsets && (E < 1 || E > w8a8::kMaxExperts)) return W8A8_ERR_INVALID_ARG;
+    if (rows == 0) return W8A8_OK;
+    if (!U || !qh || !sh || !aligned(U, 16) || !aligned(qh, 4) || !aligned(sh, 4) ||
+        !aligned(offsets, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_swiglu_quant(U, rows, I, offsets, offsets ? E : 0, qh, 0, sh,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_swiglu(const float *U, int64_t rows, int64_t I, float *h, w8a8_stream_t stream) {
+    if (rows < 0 || I <= 0 || I % 4 != 0 || I > w8a8::kSwigluMaxI || rows > kMaxElems / (2 * I))
+        return W8A8_ERR_INVALID_ARG;
+    if (rows == 0) return W8A8_OK;
+    if (!U || !h || !aligned(U, 16) || !aligned(h, 16)) return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_swiglu_quant(U, rows, I, nullptr, 0, h, 2, nullptr,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_moe_unpermute(const float *D, const int32_t *row_of, const float *topk_w,
+                               int64_t T, int64_t k, int64_t H, void *y, w8a8_dtype y_dtype,
+                               w8a8_stream_t stream) {
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    if (T < 0 || k < 1 || k > w8a8::kMoeMaxTopK || H <= 0 || H % 4 != 0 || T > kMaxElems / H ||
+        T > kMaxElems / k)
+        return W8A8_ERR_INVALID_ARG;
+    if (T == 0) return W8A8_OK;
+    if (!D || !row_of || !topk_w || !y || !aligned(D, 16) || !aligned(row_of, 4) ||
+        !aligned(topk_w, 4) || !aligned(y, 16))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_moe_unpermute(D, row_of, topk_w, T, k, H, y,
+                                                y_dtype == W8A8_FP32,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w8a8_moe_ffn_workspace_size(int64_t T, int64_t k, int64_t H, int64_t I, int64_t E) {
+    if (check_ffn_shape(T, k, H, I, E) != W8A8_OK || T == 0) return 0;
+    return ffn_layout(T, k, H, I, E).total;
+}
+
+w8a8_status w8a8_moe_ffn(const void *x_bf16, int64_t ldx, const int32_t *topk_ids,
+                         const float *topk_w, int64_t T, int64_t k, int64_t H, int64_t I,
+                         int64_t E, const int8_t *qw_up, const float *sw_up,
+                         const int8_t *qw_down, const float *sw_down, void *y, w8a8_dtype y_dtype,
+                         void *workspace, size_t workspace_bytes, w8a8_stream_t stream) {
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    w8a8_status st = check_ffn_shape(T, k, H, I, E);
+    if (st != W8A8_OK) return st;
+    if (ldx < H || T > kMaxElems / ldx) return W8A8_ERR_INVALID_ARG;
+    if (T == 0) return W8A8_OK;
+    if (!x_bf16 || !topk_ids || !topk_w || !qw_up || !sw_up || !qw_down || !sw_down || !y)
+        return W8A8_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 2) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) ||
+        !aligned(qw_up, 16) || !aligned(qw_down, 16) || !aligned(sw_up, 4) ||
+        !aligned(sw_down, 4) || !aligned(y, 16))
+        return W8A8_ERR_INVALID_ARG;
+    const FfnLayout L = ffn_layout(T, k, H, I, E);
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, kWsAlign))
+        return W8A8_ERR_WORKSPACE;
+    w8a8::DeviceInfo info;
+    st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *row_of = reinterpret_cast<int32_t *>(ws + L.row_of);
+    int32_t *tok = reinterpret_cast<int32_t *>(ws + L.tok);
+    int32_t *pair = reinterpret_cast<int32_t *>(ws + L.pair);
+    float *sa_up = reinterpret_cast<float *>(ws + L.sa_up);
+    float *U = reinterpret_cast<float *>(ws + L.u);
+    float *sa_dn = reinterpret_cast<float *>(ws + L.sa_dn);
+    float *D = reinterpret_cast<float *>(ws + L.d);
+    const int64_t n = T * k;
+    // 1. routing histogram -> offsets -> permutation (one CTA)
+    cudaError_t e = w8a8::launch_moe_route(topk_ids, T, k, E, offsets, row_of, tok, pair, s);
+    // 2. transfer + per-token quantization of the permuted token rows (fp16
+    //    codes: the gate_up GEMM's operand)
+    if (e == cudaSuccess)
+        e = w8a8::launch_quant_act_rows(static_cast<const uint16_t *>(x_bf16), n, H, ldx, tok,
+                                        ws + L.x_up, true, sa_up, s);
+    // 3. gate_up grouped GEMM, FP32 output U [n, 2I]
+    if (e == cudaSuccess) {
+        w8a8::GemmProblem p;
+        p.qa = nullptr;
+        p.sa = sa_up;
+        p.sw = sw_up;
+        p.qw = qw_up;
+        p.x16 = ws + L.x_up;
+        p.offsets = offsets;
+        p.y = U;
+        p.debug_partials = nullptr;
+        p.R = n;
+        p.E = E;
+        p.N = 2 * I;
+        p.K = H;
+        p.out_fp32 = true;
+        e = w8a8::launch_gemm(p, info.num_sms, s);
+    }
+    // 4. SwiGLU + per-token requantization (fp16 codes: the down GEMM's operand)
+    if (e == cudaSuccess)
+        e = w8a8::launch_swiglu_quant(U, n, I, offsets, E, ws + L.x_dn, 1, sa_dn, s);
+    // 5. down grouped GEMM, FP32 output D [n, H]
+    if (e == cudaSuccess) {
+        w8a8::GemmProblem p;
+        p.qa = nullptr;
+        p.sa = sa_dn;
+        p.sw = sw_down;
+        p.qw = qw_down;
+        p.x16 = ws + L.x_dn;
+        p.offsets = offsets;
+        p.y = D;
+        p.debug_partials = nullptr;
+        p.R = n;
+        p.E = E;
+        p.N = H;
+        p.K = I;
+        p.out_fp32 = true;
+        e = w8a8::launch_gemm(p, info.num_sms, s);
+    }
+    // 6. weighted un-permute into y [T, H]
+    if (e == cudaSuccess)
+        e = w8a8::launch_moe_unpermute(D, row_of, topk_w, T, k, H, y, y_dtype == W8A8_FP32, s);
+    return from_cuda(e);
 }
 
 w8a8_status w8a8_selftest_wait_timeout(uint32_t limit_us, w8a8_stream_t stream) {

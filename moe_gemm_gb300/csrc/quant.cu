@@ -41,10 +41,14 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
 // operand) instead of int8, and block 0 also zeroes n_cnt split counters of
 // the GEMM that follows (after the wait below, so the GEMM before it, which
 // may share them, has finished).
+// src_rows (nullable): output row r quantizes input row src_rows[r] (a
+// gather, e.g. tokens into expert-sorted order); rows whose entry is
+// negative are skipped.
 template <int VPT, bool kF16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
-    const uint16_t *__restrict__ a, int K, int64_t lda, void *__restrict__ out, int64_t ldq,
-    float *__restrict__ sa, int *__restrict__ cnt, int n_cnt) {
+    const uint16_t *__restrict__ a, int K, int64_t lda, const int32_t *__restrict__ src_rows,
+    void *__restrict__ out, int64_t ldq, float *__restrict__ sa, int *__restrict__ cnt,
+    int n_cnt) {
     // A GEMM launched after this kernel as a programmatic dependent may start
     // its set-up and weight stream now; it waits for this grid (and so for qa
     // and sa) before it reads the codes. This kernel is itself launched as a
@@ -57,7 +61,9 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
         for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
     __shared__ uint32_t red[kQuantThreads / 32];
     const int64_t row = blockIdx.x;
-    const uint4 *src = reinterpret_cast<const uint4 *>(a + row * lda);
+    const int64_t in_row = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
+    if (in_row < 0) return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a + in_row * lda);
     const int nvec = K >> 3;
     uint4 v[VPT];
     uint32_t m = 0;
@@ -92,15 +98,18 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
 // Any K / stride / alignment: scalar two-pass version (re-reads the row).
 template <bool kF16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
-    const uint16_t *__restrict__ a, int K, int64_t lda, void *__restrict__ out, int64_t ldq,
-    float *__restrict__ sa, int *__restrict__ cnt, int n_cnt) {
+    const uint16_t *__restrict__ a, int K, int64_t lda, const int32_t *__restrict__ src_rows,
+    void *__restrict__ out, int64_t ldq, float *__restrict__ sa, int *__restrict__ cnt,
+    int n_cnt) {
     griddep_launch_dependents();   // as in quant_act_vec_kernel
     griddep_wait();
     if (kF16 && blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
     __shared__ uint32_t red[kQuantThreads / 32];
     const int64_t row = blockIdx.x;
-    const uint16_t *src = a + row * lda;
+    const int64_t in_row = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
+    if (in_row < 0) return;
+    const uint16_t *src = a + in_row * lda;
     uint32_t m = 0;
     for (int k = threadIdx.x; k < K; k += kQuantThreads) m = max(m, (uint32_t)src[k] & 0x7FFFu);
     m = block_max_u32(m, red);
@@ -191,7 +200,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStr
 
 template <bool kF16>
 cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, void *out,
-                         int64_t ldq, float *sa, int *cnt, int n_cnt, cudaStream_t stream) {
+                         int64_t ldq, float *sa, int *cnt, int n_cnt, cudaStream_t stream,
+                         const int32_t *src_rows = nullptr) {
     const int align = kF16 ? 16 : 8;   // one 8-code vector per store
     const bool vec_ok = (K % 8 == 0) && (lda % 8 == 0) && (ldq % 8 == 0) &&
                         (reinterpret_cast<uintptr_t>(a) % 16 == 0) &&
@@ -201,19 +211,19 @@ cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, v
     const dim3 block(kQuantThreads);
     if (cnt == nullptr) n_cnt = 0;
     if (vec_ok && K <= 256 * 8 * 1)
-        return launch_pdl(quant_act_vec_kernel<1, kF16>, grid, block, stream, a, k, lda, out, ldq,
-                          sa, cnt, n_cnt);
+        return launch_pdl(quant_act_vec_kernel<1, kF16>, grid, block, stream, a, k, lda, src_rows,
+                          out, ldq, sa, cnt, n_cnt);
     if (vec_ok && K <= 256 * 8 * 2)
-        return launch_pdl(quant_act_vec_kernel<2, kF16>, grid, block, stream, a, k, lda, out, ldq,
-                          sa, cnt, n_cnt);
+        return launch_pdl(quant_act_vec_kernel<2, kF16>, grid, block, stream, a, k, lda, src_rows,
+                          out, ldq, sa, cnt, n_cnt);
     if (vec_ok && K <= 256 * 8 * 4)
-        return launch_pdl(quant_act_vec_kernel<4, kF16>, grid, block, stream, a, k, lda, out, ldq,
-                          sa, cnt, n_cnt);
+        return launch_pdl(quant_act_vec_kernel<4, kF16>, grid, block, stream, a, k, lda, src_rows,
+                          out, ldq, sa, cnt, n_cnt);
     if (vec_ok && K <= 256 * 8 * 8)
-        return launch_pdl(quant_act_vec_kernel<8, kF16>, grid, block, stream, a, k, lda, out, ldq,
-                          sa, cnt, n_cnt);
-    return launch_pdl(quant_act_generic_kernel<kF16>, grid, block, stream, a, k, lda, out, ldq, sa,
-                      cnt, n_cnt);
+        return launch_pdl(quant_act_vec_kernel<8, kF16>, grid, block, stream, a, k, lda, src_rows,
+                          out, ldq, sa, cnt, n_cnt);
+    return launch_pdl(quant_act_generic_kernel<kF16>, grid, block, stream, a, k, lda, src_rows,
+                      out, ldq, sa, cnt, n_cnt);
 }
 
 }  // namespace
@@ -226,6 +236,13 @@ cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_quant_act_f16(const uint16_t *a, int64_t M, int64_t K, int64_t lda, void *x16,
                                  float *sa, int *cnt, int n_cnt, cudaStream_t stream) {
     return launch_quant<true>(a, M, K, lda, x16, K, sa, cnt, n_cnt, stream);
+}
+
+cudaError_t launch_quant_act_rows(const uint16_t *a, int64_t rows, int64_t K, int64_t lda,
+                                  const int32_t *src_rows, void *out, bool f16, float *sa,
+                                  cudaStream_t stream) {
+    return f16 ? launch_quant<true>(a, rows, K, lda, out, K, sa, nullptr, 0, stream, src_rows)
+               : launch_quant<false>(a, rows, K, lda, out, K, sa, nullptr, 0, stream, src_rows);
 }
 
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,

@@ -41,7 +41,7 @@ DEFAULT_SEED = 0
 
 # Stable integer tags for the seed spawn keys.
 _TENSOR_TAGS = {"act": 1, "weight": 2, "outlier_channels": 3, "routing": 4,
-                "act_down": 5, "weight_down": 6}
+                "act_down": 5, "weight_down": 6, "gate_weight": 7}
 
 
 @dataclass(frozen=True)
@@ -202,6 +202,7 @@ class Routing:
     token_of_row: np.ndarray   # [R] token id of each routed row (sorted by expert, then token)
     expert_of_row: np.ndarray  # [R]
     offsets: np.ndarray        # [E+1] int32, rows of expert e are [off[e], off[e+1])
+    choice: np.ndarray         # [T, k] int32: each token's experts in the order they were drawn
 
     @property
     def counts(self) -> np.ndarray:
@@ -237,7 +238,7 @@ def routing(spec: MoESpec, seed: int = DEFAULT_SEED) -> Routing:
     counts = np.bincount(exp, minlength=spec.E)
     offsets = np.zeros(spec.E + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
-    return Routing(tok.astype(np.int64), exp.astype(np.int64), offsets)
+    return Routing(tok.astype(np.int64), exp.astype(np.int64), offsets, choice.astype(np.int32))
 
 
 def moe_spec_as_dense(spec: MoESpec, which: str) -> DenseSpec:
@@ -290,3 +291,18 @@ def random_offsets(rng: np.random.Generator, R: int, E: int, empty_frac: float =
     off = np.zeros(E + 1, dtype=np.int32)
     off[1:] = np.cumsum(counts)
     return off
+
+
+# -------------------------------------------------------- MoE expert FFN inputs
+def moe_tokens(spec: MoESpec, seed: int = DEFAULT_SEED) -> np.ndarray:
+    """The T token vectors (BF16 bit patterns [T, K_up]) entering the FFN: the
+    same draws the gate_up workload routes (row t of the token matrix)."""
+    return activations(moe_spec_as_dense(spec, "up"), M=spec.T, seed=seed)
+
+
+def moe_gate_weights(spec: MoESpec, seed: int = DEFAULT_SEED) -> np.ndarray:
+    """Router gate weights [T, k] float32: positive draws U(0.05, 1) scaled so
+    each token's k weights sum to 1."""
+    rng = _rng(seed, spec.tag, "gate_weight", 0)
+    w = rng.uniform(0.05, 1.0, size=(spec.T, spec.topk))
+    return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
