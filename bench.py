@@ -11,7 +11,9 @@ A default run measures every workload and prints one JSON line:
   * "per_config" holds the same measurement for each workload: dense tiny
     16x1024x1024, decode M in {1, 8, 32} x 8192 x 28672, prefill
     4096x8192x8192, MoE grouped (64 experts, top-8 of 512 tokens; gate_up
-    3072x4096 and down 4096x1536) and stress, each with its throughput, the
+    3072x4096 and down 4096x1536), the whole MoE expert FFN of those 512
+    tokens (routing, both grouped GEMMs, SwiGLU, un-permute) and stress, each
+    with its throughput, the
     roofline of its dominant kernel, the quantizer's time, the end-to-end
     number through the public API with host buffers, and the CPU oracle timed
     on the host cores on a fixed slice of the same workload.
@@ -21,7 +23,7 @@ activations, then the group-scaled GEMM; w8a8_linear / w8a8_grouped_linear),
 the step's calls replayed as one CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --workload tiny|decode|prefill|moe|stress   (one workload)
+  python bench.py --workload tiny|decode|prefill|moe|moe_ffn|stress   (one workload)
 """
 from __future__ import annotations
 
@@ -44,7 +46,7 @@ import workloads  # noqa: E402
 
 METRIC = "INT8 TOPS & % of roofline (tensor peak or HBM GB/s) per GEMM shape, 1xGB300"
 GROUP = 128
-WORKLOADS = ("tiny", "decode", "prefill", "moe", "stress")
+WORKLOADS = ("tiny", "decode", "prefill", "moe", "moe_ffn", "stress")
 HEADLINE = "stress"
 # Workloads whose inputs fit in L2 (129 MB) get an L2 flush (a 256 MB write,
 # outside the timed events) before every timed step; the others read more
@@ -55,6 +57,8 @@ L2_FLUSH_BYTES = 256 << 20
 # reference time the same slice): every row and all of K, output columns
 # [0, ORACLE_COLS) of every GEMM of the step (of every expert for MoE).
 ORACLE_COLS = {"tiny": 1024, "decode": 2048, "prefill": 512, "moe": 256, "stress": 512}
+# The MoE expert FFN's oracle sample: its first FFN_ORACLE_TOKENS tokens, whole.
+FFN_ORACLE_TOKENS = 64
 KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM (one library call) replayed back to back "
                     "K times, events around the K launches, median of 3 such batches; the "
                     "GEMM overlaps the quantizer, so this includes any part of the quantizer "
@@ -118,8 +122,40 @@ class Shape:
         return w + a + y
 
 
+class FfnShape:
+    """The MoE expert FFN of T tokens (top-k of E experts, hidden H,
+    intermediate I): its two grouped GEMMs' ops, and its algorithmic bytes
+    (weights and group scales of the active experts of both GEMMs, the BF16
+    tokens in and out, the routing)."""
+
+    def __init__(self, spec):
+        self.spec = spec
+        self.M, self.N, self.K = spec.T, spec.K_up, spec.K_up   # tokens in, tokens out
+        self.out = "bf16"
+        self.E = spec.E
+
+    @property
+    def ops(self):
+        s = self.spec
+        return 2 * s.R * (s.N_up * s.K_up + s.N_down * s.K_down)
+
+    def alg_bytes(self, active_experts=None):
+        s = self.spec
+        e = s.E if active_experts is None else active_experts
+        w = e * (s.N_up * s.K_up + s.N_down * s.K_down)
+        sc = e * 4 * (s.N_up * s.K_up // GROUP + s.N_down * s.K_down // GROUP)
+        return w + sc + 2 * s.T * s.K_up * 2 + s.T * s.topk * 8
+
+
 def build_workload(name):
     """Returns (description, [Shape], weight spec, roofline bound)."""
+    if name == "moe_ffn":
+        spec = workloads.MOE["moe"]
+        desc = ("MoE expert FFN: 64 experts, top-8 of T=512 tokens, H=4096, I=1536 (routing, "
+                "transfer + quantization, gate_up GEMM, SwiGLU + requantization, down GEMM, "
+                "weighted un-permute), BF16 out")
+        return desc, [Shape(spec.R, spec.N_up, spec.K_up, "fp32", None),
+                      Shape(spec.R, spec.N_down, spec.K_down, "fp32", None)], spec, "hbm"
     if name == "decode":
         shapes = [Shape(m, 28672, 8192, "bf16", workloads.DENSE[f"decode_m{m}"])
                   for m in workloads.DECODE_MS]
@@ -153,6 +189,9 @@ def workload_config(name):
 
 
 def oracle_sample_desc(name, shapes):
+    if name == "moe_ffn":
+        return (f"the whole FFN of the first {FFN_ORACLE_TOKENS} tokens (all their routed rows, "
+                "every column of both GEMMs)")
     n = min(ORACLE_COLS[name], shapes[0].N)
     per = "of every expert, " if name == "moe" else ""
     return (f"all rows and all of K of every GEMM of the step, output columns [0, {n}) "
@@ -257,6 +296,25 @@ class GpuContext:
         if self.world > 1:
             self.dist.barrier()
 
+    def moe_weights(self, spec):
+        """The quantized expert weights of the MoE workload, [(qw, sw) of
+        gate_up, (qw, sw) of down], made once and shared by the grouped-GEMM
+        and FFN workloads (quantized on the GPU, an offline step)."""
+        if getattr(self, "_moe_w", None) is None:
+            torch, w8, dev = self.torch, self.w8, self.dev
+            out = []
+            for which, N, K in (("up", spec.N_up, spec.K_up), ("down", spec.N_down, spec.K_down)):
+                qw = torch.empty((spec.E, N, K), dtype=torch.int8, device=dev)
+                sw = torch.empty((spec.E, N, K // GROUP), dtype=torch.float32, device=dev)
+                for e in range(spec.E):
+                    q, sc = w8.quant_weight(torch.from_numpy(
+                        workloads.moe_weights(spec, which, e)).to(dev))
+                    qw[e].copy_(q)
+                    sw[e].copy_(sc)
+                out.append((qw, sw))
+            self._moe_w = out
+        return self._moe_w
+
     def flush_l2(self):
         torch = self.torch
         if self.flush_buf is None:
@@ -306,18 +364,27 @@ def setup_workload(ctx, name):
     torch, w8, dev = ctx.torch, ctx.w8, ctx.dev
     desc, shapes, wspec, bound = build_workload(name)
     per = []
+    if name == "moe_ffn":
+        spec = wspec
+        route = workloads.routing(spec)
+        up, dn = ctx.moe_weights(spec)
+        x_host = workloads.moe_tokens(spec)
+        d = dict(shape=FfnShape(spec), a=upload_bf16(torch, dev, x_host), a_host=x_host,
+                 off=None, ffn=True, qw=up[0], sw=up[1], qw_dn=dn[0], sw_dn=dn[1],
+                 ids=torch.from_numpy(route.choice).to(dev),
+                 w=torch.from_numpy(workloads.moe_gate_weights(spec)).to(dev))
+        d["y"] = torch.empty((spec.T, spec.K_up), dtype=torch.bfloat16, device=dev)
+        d["ws"] = torch.empty(max(w8.moe_ffn_workspace_size(spec.T, spec.topk, spec.K_up,
+                                                            spec.K_down, spec.E), 1),
+                              dtype=torch.uint8, device=dev)
+        d["launches"] = 6
+        torch.cuda.synchronize()
+        return desc, shapes, wspec, bound, [d]
     if name == "moe":
         spec = wspec
-        for shp in shapes:
+        cached = ctx.moe_weights(spec)
+        for shp, (qw, sw) in zip(shapes, cached):
             which, _, route = shp.act_spec
-            N, K = shp.N, shp.K
-            qw = torch.empty((spec.E, N, K), dtype=torch.int8, device=dev)
-            sw = torch.empty((spec.E, N, K // GROUP), dtype=torch.float32, device=dev)
-            for e in range(spec.E):
-                q, s = w8.quant_weight(torch.from_numpy(
-                    workloads.moe_weights(spec, which, e)).to(dev))
-                qw[e].copy_(q)
-                sw[e].copy_(s)
             a_host = workloads.moe_activations(spec, which, route)
             per.append(dict(shape=shp, qw=qw, sw=sw, a=upload_bf16(torch, dev, a_host),
                             a_host=a_host, off=torch.from_numpy(route.offsets).to(dev)))
@@ -355,7 +422,10 @@ def setup_workload(ctx, name):
 
 def linear_call(ctx, d, s):
     w8 = ctx.w8
-    if d["off"] is not None:
+    if d.get("ffn"):
+        w8.moe_ffn(d["a"], d["ids"], d["w"], d["qw"], d["sw"], d["qw_dn"], d["sw_dn"], out=d["y"],
+                   out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
+    elif d["off"] is not None:
         w8.grouped_linear(d["a"], d["off"], d["qw"], d["sw"], out=d["y"],
                           out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
     else:
@@ -496,7 +566,7 @@ def measure_workload(ctx, name, headline):
     peaks = ctx.peaks
     if bound == "hbm":
         active = None
-        if name == "moe":
+        if name in ("moe", "moe_ffn"):
             cnt = np.diff(workloads.routing(wspec).offsets)
             active = int((cnt > 0).sum())
         alg = [d["shape"].alg_bytes(active) for d in per]
@@ -521,13 +591,13 @@ def measure_workload(ctx, name, headline):
 
     entry = {
         "workload": desc,
-        "shapes": [[d["shape"].M, d["shape"].N, d["shape"].K] for d in per],
+        "shapes": [[sh.M, sh.N, sh.K] for sh in shapes],
         "value": round(value, 3), "unit": "TOPS",
         "ms_per_step": round(elapsed_ms / args.steps, 5),
         "l2": ("flushed before every timed step (256 MB write outside the events); inputs "
                "fit in L2" if flush else
                "inputs larger than L2: each step streams "
-               f"{sum(d['qw'].numel() for d in per) / 1e6:.0f} MB of weights"
+               f"{sum(d['qw'].numel() + d.get('qw_dn', d['qw'][:0]).numel() for d in per) / 1e6:.0f} MB of weights"
                + (" (a weight copy per GEMM)" if len(per) > 1 and name != "moe" else "")),
         "roofline": roof,
         "gpu_launches_per_step": sum(d["launches"] for d in per),
@@ -620,6 +690,22 @@ def oracle_items(name):
     """Inputs of the oracle's sample of a workload (ORACLE_COLS)."""
     import oracle
     _, shapes, wspec, _ = build_workload(name)
+    if name == "moe_ffn":
+        # the whole FFN of the first FFN_ORACLE_TOKENS tokens, with the
+        # weights of the experts they use (ids renumbered over those experts)
+        spec = wspec
+        nt = FFN_ORACLE_TOKENS
+        ids = workloads.routing(spec).choice[:nt]
+        used = np.unique(ids)
+        local = np.searchsorted(used, ids).astype(np.int32)
+        W = []
+        for which in ("up", "down"):
+            qs = [oracle.quant_weight(workloads.moe_weights(spec, which, int(e))) for e in used]
+            W += [np.stack([q for q, _ in qs]), np.stack([s for _, s in qs])]
+        item = ("ffn", workloads.moe_tokens(spec)[:nt], local,
+                workloads.moe_gate_weights(spec)[:nt], W)
+        ops = 2 * nt * spec.topk * (spec.N_up * spec.K_up + spec.N_down * spec.K_down)
+        return [item], ops
     n_cols = min(ORACLE_COLS[name], shapes[0].N)
     items = []
     if name == "moe":
@@ -643,7 +729,12 @@ def oracle_items(name):
 
 def oracle_step(items):
     import oracle
-    for a, qw, sw, off in items:
+    for it in items:
+        if it[0] == "ffn":
+            _, x, ids, w, W = it
+            oracle.moe_ffn(x, ids, w, *W)
+            continue
+        a, qw, sw, off = it
         qa, sa = oracle.quant_act(a)
         if off is None:
             oracle.gemm(qa, sa, qw, sw, want_T=False)
