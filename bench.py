@@ -620,11 +620,13 @@ def measure_int_path_peak(ctx):
     issue, and dp4a (the CUDA-core GEMV). Timed with CUDA events."""
     torch, w8 = ctx.torch, ctx.w8
     out = {}
-    for n, chains, steps in ((256, 1, 4000), (128, 2, 4000), (32, 2, 8000)):
+    # the GEMMs' instruction streams: N=256 (large dense tiles), N=128 and N=32
+    # (wide and narrow tiles), each instruction on operands of its own
+    for n, chains, steps in ((256, 1, 4000), (128, 1, 4000), (32, 1, 8000), (128, 2, 4000)):
         macs = [0]
 
         def run(n=n, chains=chains, steps=steps):
-            macs[0] = w8.probe_tc_rate(n, chains, steps, stream=ctx.stream)
+            macs[0] = w8.probe_tc_rate(n, chains, steps, distinct=True, stream=ctx.stream)
 
         ms = ctx.batch_ms(run, 1, batches=3)
         out[f"tcgen05_f16_m128_n{n}_x{chains}_tflops"] = round(2 * macs[0] / (ms * 1e-3) / 1e12, 1)
@@ -637,7 +639,8 @@ def measure_int_path_peak(ctx):
     out["dp4a_tops"] = round(2 * macs[0] / (ms * 1e-3) / 1e12, 1)
     out["how"] = ("w8a8_probe_tc_rate / w8a8_probe_dp4a_rate: one CTA per SM issuing the "
                   "instruction back to back (zero operands), CUDA events, median of 3; "
-                  "tensor-core entries are M=128 x N x K=16 with `x` accumulators taking turns")
+                  "tensor-core entries are M=128 x N x K=16 with `x` accumulators taking turns, "
+                  "each instruction on its own A and B operands")
     if w8.device_error(clear=True) != 0:
         out["error"] = "a probe's bounded wait gave up"
     return out
@@ -730,7 +733,7 @@ def oracle_items(name):
 def oracle_step(items):
     import oracle
     for it in items:
-        if it[0] == "ffn":
+        if isinstance(it[0], str) and it[0] == "ffn":
             _, x, ids, w, W = it
             oracle.moe_ffn(x, ids, w, *W)
             continue

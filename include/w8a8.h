@@ -377,15 +377,16 @@ w8a8_status w8a8_selftest_wait_timeout(uint32_t limit_us, w8a8_stream_t stream);
  *   w8a8_probe_tc_rate: one CTA per SM issues 8 * chains * steps
  *     tcgen05.mma kind::f16 instructions of shape M = 128, N = n, K = 16
  *     (A in tensor memory, B in shared memory: the instruction of the
- *     tensor-core GEMM), `chains` independent accumulators taking turns.
- *     16 <= n <= 256, n % 16 == 0, chains >= 1, chains * n <= 256,
+ *     tensor-core GEMM), `chains` independent accumulators taking turns, all
+ *     on the same A and B (distinct == 0) or each on its own (distinct != 0).
+ *     16 <= n <= 256, n % 16 == 0, 1 <= chains <= 4, chains * n <= 256,
  *     1 <= steps <= 2^24 (keep one launch well under a second).
  *   w8a8_probe_dp4a_rate: 4 CTAs of 512 threads per SM, each thread 16 *
  *     iters dp4a (four int8 products into an int32; the CUDA-core GEMV's
  *     arithmetic). 1 <= iters <= 2^26.
  */
-w8a8_status w8a8_probe_tc_rate(int32_t n, int32_t chains, int64_t steps, int64_t *macs_out,
-                               w8a8_stream_t stream);
+w8a8_status w8a8_probe_tc_rate(int32_t n, int32_t chains, int32_t distinct, int64_t steps,
+                               int64_t *macs_out, w8a8_stream_t stream);
 w8a8_status w8a8_probe_dp4a_rate(int64_t iters, int64_t *macs_out, w8a8_stream_t stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */

@@ -61,7 +61,7 @@ def _load() -> ctypes.CDLL:
     lib.w8a8_linear.argtypes = [vp, i64, vp, vp, vp, i32, i64, i64, i64, vp, ctypes.c_size_t, vp]
     lib.w8a8_grouped_linear.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64, i64, i64, i64, vp,
                                         ctypes.c_size_t, vp]
-    lib.w8a8_probe_tc_rate.argtypes = [i32, i32, i64, ctypes.POINTER(i64), vp]
+    lib.w8a8_probe_tc_rate.argtypes = [i32, i32, i32, i64, ctypes.POINTER(i64), vp]
     lib.w8a8_probe_dp4a_rate.argtypes = [i64, ctypes.POINTER(i64), vp]
     lib.w8a8_moe_route.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
     lib.w8a8_quant_act_rows.argtypes = [vp, i64, vp, i64, i64, vp, vp, vp]
@@ -514,13 +514,15 @@ def selftest_wait_timeout(limit_us: int = 20000,
            "w8a8_selftest_wait_timeout")
 
 
-def probe_tc_rate(n: int, chains: int, steps: int,
+def probe_tc_rate(n: int, chains: int, steps: int, distinct: bool = False,
                   stream: Optional[torch.cuda.Stream] = None) -> int:
     """Launches the tcgen05 kind::f16 rate probe (M=128, N=n, K=16 per
-    instruction, `chains` accumulators taking turns); returns the int8
-    multiply-adds it performs (time the launch to get the rate)."""
+    instruction, `chains` accumulators taking turns, on shared or distinct
+    operands); returns the int8 multiply-adds it performs (time the launch
+    to get the rate)."""
     macs = ctypes.c_int64(0)
-    _check(_lib.w8a8_probe_tc_rate(n, chains, steps, ctypes.byref(macs), _stream(stream)),
+    _check(_lib.w8a8_probe_tc_rate(n, chains, 1 if distinct else 0, steps, ctypes.byref(macs),
+                                   _stream(stream)),
            "w8a8_probe_tc_rate")
     return int(macs.value)
 

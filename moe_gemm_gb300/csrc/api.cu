@@ -611,16 +611,16 @@ w8a8_status w8a8_selftest_wait_timeout(uint32_t limit_us, w8a8_stream_t stream) 
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
-w8a8_status w8a8_probe_tc_rate(int32_t n, int32_t chains, int64_t steps, int64_t *macs_out,
-                               w8a8_stream_t stream) {
-    if (!macs_out || n < 16 || n > 256 || n % 16 != 0 || chains < 1 || chains * n > 256 ||
-        steps < 1 || steps > (int64_t(1) << 24))
+w8a8_status w8a8_probe_tc_rate(int32_t n, int32_t chains, int32_t distinct, int64_t steps,
+                               int64_t *macs_out, w8a8_stream_t stream) {
+    if (!macs_out || n < 16 || n > 256 || n % 16 != 0 || chains < 1 || chains > 4 ||
+        chains * n > 256 || steps < 1 || steps > (int64_t(1) << 24))
         return W8A8_ERR_INVALID_ARG;
     w8a8::DeviceInfo info;
     w8a8_status st = check_device(&info);
     if (st != W8A8_OK) return st;
     *macs_out = int64_t(info.num_sms) * steps * 8 * chains * 128 * n * 16;
-    return from_cuda(w8a8::launch_probe_tc(n, chains, steps, info.num_sms,
+    return from_cuda(w8a8::launch_probe_tc(n, chains, distinct != 0 ? 1 : 0, steps, info.num_sms,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 

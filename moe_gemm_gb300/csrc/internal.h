@@ -122,10 +122,12 @@ cudaError_t read_device_error(unsigned long long *value, bool clear);
 cudaError_t device_error_word(unsigned long long **out);
 
 // Rate probes of the MMA paths (probe.cu): tcgen05.mma kind::f16, M = 128,
-// N = n, K = 16, A in tensor memory, `chains` accumulators taking turns,
+// N = n, K = 16, A in tensor memory, `chains` accumulators taking turns (on
+// the same operands, or each on its own when distinct),
 // 8 * chains * steps instructions per CTA on num_sms CTAs; and dp4a,
 // 16 * iters per thread on 4 * num_sms CTAs of 512 threads.
-cudaError_t launch_probe_tc(int n, int chains, long long steps, int num_sms, cudaStream_t stream);
+cudaError_t launch_probe_tc(int n, int chains, int distinct, long long steps, int num_sms,
+                            cudaStream_t stream);
 cudaError_t launch_probe_dp4a(long long iters, int num_sms, cudaStream_t stream);
 
 // Per-device properties cached on first use.

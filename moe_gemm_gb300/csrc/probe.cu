@@ -6,8 +6,8 @@
 //    accumulate), M = 128 weight rows, A from tensor memory, B (tokens) from
 //    shared memory with the 128-byte swizzle, N token columns, K = 16 per
 //    instruction: the instruction of w8a8_gemm_narrow_kernel. `chains`
-//    independent accumulators take turns, as the K groups of a pipeline step
-//    do in the GEMM;
+//    independent accumulators take turns, reading the same A and B operands
+//    (distinct = 0) or each its own (distinct = 1);
 //  * dp4a (four int8 products summed into an int32): the CUDA-core GEMV.
 // The operands are zeros; timing does not depend on the values.
 #include <cuda_runtime.h>
@@ -25,7 +25,7 @@ namespace {
 constexpr int kProbeSmemBytes = 128 * 1024;
 
 __global__ void __launch_bounds__(128, 1)
-probe_tc_kernel(int n, int chains, long long steps, unsigned long long *err) {
+probe_tc_kernel(int n, int chains, int distinct, long long steps, unsigned long long *err) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t s_tmem;
@@ -33,7 +33,7 @@ probe_tc_kernel(int n, int chains, long long steps, unsigned long long *err) {
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sB = (raw + 1023u) & ~1023u;
     uint8_t *b_ptr = smem_raw + (sB - raw);
-    for (int i = threadIdx.x; i < n * 128 / 16; i += blockDim.x)
+    for (int i = threadIdx.x; i < 256 * 128 / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(b_ptr)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     const int warp = threadIdx.x >> 5;
@@ -55,7 +55,7 @@ probe_tc_kernel(int n, int chains, long long steps, unsigned long long *err) {
         uint32_t z[16] = {0};
         const uint32_t lane_base = tb + ((static_cast<uint32_t>(warp) * 32u) << 16);
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) tmem_st_16cols(lane_base + 256 + c, z);
+        for (int c = 0; c < 256; c += 16) tmem_st_16cols(lane_base + 256 + c, z);
         tmem_wait_st();
     }
     tc_fence_before();
@@ -67,10 +67,14 @@ probe_tc_kernel(int n, int chains, long long steps, unsigned long long *err) {
         for (long long s = 0; s < steps; ++s) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bdesc = b0 + static_cast<uint64_t>((kk & 3) * 2);
-                for (int c = 0; c < chains; ++c)
-                    mma_f16_tmemA(tb + static_cast<uint32_t>(c * n), tb + 256 + kk * 8, bdesc,
-                                  idesc, kk > 0 ? 1u : 0u);
+                for (int c = 0; c < chains; ++c) {
+                    // distinct: chain c reads its own A columns and B rows
+                    const uint32_t a_off = distinct ? static_cast<uint32_t>(c * 64) : 0u;
+                    const uint64_t b_off = distinct ? static_cast<uint64_t>((c * n * 128) >> 4) : 0u;
+                    const uint64_t bdesc = b0 + b_off + static_cast<uint64_t>((kk & 3) * 2);
+                    mma_f16_tmemA(tb + static_cast<uint32_t>(c * n), tb + 256 + a_off + kk * 8,
+                                  bdesc, idesc, kk > 0 ? 1u : 0u);
+                }
             }
         }
         mma_commit(smem_u32(&bar));
@@ -102,7 +106,8 @@ __device__ int g_probe_sink;
 
 }  // namespace
 
-cudaError_t launch_probe_tc(int n, int chains, long long steps, int num_sms, cudaStream_t stream) {
+cudaError_t launch_probe_tc(int n, int chains, int distinct, long long steps, int num_sms,
+                            cudaStream_t stream) {
     static int attr_done[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -116,7 +121,7 @@ cudaError_t launch_probe_tc(int n, int chains, long long steps, int num_sms, cud
     unsigned long long *err = nullptr;
     e = device_error_word(&err);
     if (e != cudaSuccess) return e;
-    probe_tc_kernel<<<num_sms, 128, kProbeSmemBytes, stream>>>(n, chains, steps, err);
+    probe_tc_kernel<<<num_sms, 128, kProbeSmemBytes, stream>>>(n, chains, distinct, steps, err);
     return cudaGetLastError();
 }
 
