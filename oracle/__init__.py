@@ -74,6 +74,10 @@ def _load():
         lib.oracle_silu_f32_n.argtypes = [p, i64, p]
         lib.oracle_swiglu_quant.argtypes = [p, i64, i64, p, p]
         lib.oracle_moe_unpermute.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.oracle_quant_act_pow2.argtypes = [p, i64, i64, i64, p, i64, p]
+        lib.oracle_quant_weight_blocks.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
+        lib.oracle_gemm_blocks.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p]
+        lib.oracle_w8a16_gemm.argtypes = [p, p, p, i64, i64, i64, i64, p, p]
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_group_size.restype = ctypes.c_int
@@ -281,3 +285,64 @@ def moe_ffn(x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray, qw_up: np.ndarra
     return {"offsets": offsets, "row_of": row_of, "token_of_row": tok, "pair_of_row": pair,
             "R": R, "qa": qa, "sa": sa, "U": U, "T_up": T_up, "qh": qh, "sh": sh, "D": D,
             "T_down": Tdn, "y": y, "T_y": Ty}
+
+
+# ------------------------------------------- scale formats and W8A16 (NEXT)
+def quant_act_pow2(a_bf16: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-token quantization with power-of-two (UE8M0) scales."""
+    a = np.ascontiguousarray(a_bf16, dtype=np.uint16)
+    M, K = a.shape
+    qa = np.empty((M, K), dtype=np.int8)
+    sa = np.empty(M, dtype=np.float32)
+    _load().oracle_quant_act_pow2(_ptr(a), M, K, K, _ptr(qa), K, _ptr(sa))
+    return qa, sa
+
+
+def quant_weight_blocks(w: np.ndarray, block_rows: int = 1,
+                        pow2: bool = False) -> Tuple[np.ndarray, np.ndarray]:
+    """Weight quantization over [block_rows x 128] blocks (1: per-row
+    groups, 128: [128, 128] blocks), amax/127 or power-of-two scales.
+    Returns (qw int8 [N, K], sw float32 [ceil(N/block_rows), K/128])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    nb = (N + block_rows - 1) // block_rows
+    qw = np.empty((N, K), dtype=np.int8)
+    sw = np.empty((nb, K // GROUP), dtype=np.float32)
+    _load().oracle_quant_weight_blocks(_ptr(w), N, K, block_rows, 1 if pow2 else 0, _ptr(qw),
+                                       _ptr(sw))
+    return qw, sw
+
+
+def gemm_blocks(qa: np.ndarray, sa: np.ndarray, qw: np.ndarray, sw: np.ndarray,
+                block_rows: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The group-scaled GEMM with one weight scale per [block_rows x 128]
+    block: y* (FP64) and T."""
+    qa = np.ascontiguousarray(qa, dtype=np.int8)
+    qw = np.ascontiguousarray(qw, dtype=np.int8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = qa.shape
+    N = qw.shape[0]
+    assert sw.shape == ((N + block_rows - 1) // block_rows, K // GROUP)
+    y = np.empty((M, N), dtype=np.float64)
+    T = np.empty((M, N), dtype=np.float64)
+    _load().oracle_gemm_blocks(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, block_rows,
+                               _ptr(y), _ptr(T))
+    return y, T
+
+
+def w8a16_gemm(a_bf16: np.ndarray, qw: np.ndarray, sw: np.ndarray,
+               block_rows: int = 1) -> Tuple[np.ndarray, np.ndarray]:
+    """Weight-only INT8 GEMM with BF16 activations: y* (FP64) and T."""
+    a = np.ascontiguousarray(a_bf16, dtype=np.uint16)
+    qw = np.ascontiguousarray(qw, dtype=np.int8)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = a.shape
+    N = qw.shape[0]
+    assert qw.shape[1] == K and sw.shape == ((N + block_rows - 1) // block_rows, K // GROUP)
+    y = np.empty((M, N), dtype=np.float64)
+    T = np.empty((M, N), dtype=np.float64)
+    _load().oracle_w8a16_gemm(_ptr(a), _ptr(qw), _ptr(sw), M, N, K, block_rows, _ptr(y), _ptr(T))
+    return y, T

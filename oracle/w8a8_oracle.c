@@ -348,3 +348,129 @@ void oracle_exp_f32_n(const float *x, int64_t n, float *out) {
 void oracle_silu_f32_n(const float *x, int64_t n, float *out) {
     for (int64_t i = 0; i < n; i++) out[i] = oracle_silu_f32(x[i]);
 }
+
+/* ======================================================================
+ * Scale formats of the DeepSeek-V4 checkpoints ("Running DeepSeek-V4-Flash-
+ * Vision on 4xA800", §一: weights in [128, 128] blocks with power-of-two
+ * UE8M0 scales), applied to INT8 codes.
+ * ====================================================================== */
+
+/* The UE8M0 (power-of-two) scale of a group with the given amax: the
+ * smallest 2^e >= amax / 127 (compared exactly), e clamped to [-127, 127];
+ * an all-zero group gets 2^-127. The division x / 2^e is then exact, so the
+ * codes are round-half-even(x * 2^-e), |code| <= 127. */
+static float pow2_scale(float amax) {
+    int e = -127;
+    if (amax > 0.0f) {
+        int ex;
+        (void)frexp((double)amax / 127.0, &ex);   /* amax/127 in [2^(ex-1), 2^ex) approx */
+        e = ex - 2;
+        while ((double)amax > 127.0 * ldexp(1.0, e)) e++;          /* exact comparisons */
+        while (e > -127 && (double)amax <= 127.0 * ldexp(1.0, e - 1)) e--;
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+    }
+    return (float)ldexp(1.0, e);
+}
+
+/* Per-token activation quantization with UE8M0 scales (the amax mode is
+ * oracle_quant_act): s_m = pow2_scale(amax_m), qa = rne(a / s_m). */
+void oracle_quant_act_pow2(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
+                           int64_t ldq, float *sa) {
+    fesetround(FE_TONEAREST);
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; k++) {
+            float x = fabsf(bf16_bits_to_float(a[m * lda + k]));
+            if (x > amax) amax = x;
+        }
+        float s = pow2_scale(amax);
+        sa[m] = s;
+        for (int64_t k = 0; k < K; k++)
+            qa[m * ldq + k] = quantize_value(bf16_bits_to_float(a[m * lda + k]), s);
+    }
+}
+
+/* Weight quantization over blocks of block_rows rows x 128 K (block_rows 1:
+ * the per-row groups of oracle_quant_weight; 128: the [128, 128] blocks),
+ * scale amax / 127 (pow2 == 0) or UE8M0 (pow2 != 0).
+ * w [N, K]; qw [N, K]; sw [ceil(N / block_rows), K / 128]. */
+void oracle_quant_weight_blocks(const float *w, int64_t N, int64_t K, int64_t block_rows,
+                                int pow2, int8_t *qw, float *sw) {
+    const int64_t G = K / W8A8_ORACLE_GROUP;
+    const int64_t NB = (N + block_rows - 1) / block_rows;
+    fesetround(FE_TONEAREST);
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < NB; b++) {
+        const int64_t n0 = b * block_rows;
+        const int64_t n1 = n0 + block_rows < N ? n0 + block_rows : N;
+        for (int64_t g = 0; g < G; g++) {
+            float amax = 0.0f;
+            for (int64_t n = n0; n < n1; n++)
+                for (int64_t j = 0; j < W8A8_ORACLE_GROUP; j++) {
+                    float x = fabsf(w[n * K + g * W8A8_ORACLE_GROUP + j]);
+                    if (x > amax) amax = x;
+                }
+            float s = pow2 ? pow2_scale(amax) : amax / 127.0f;
+            sw[b * G + g] = s;
+            for (int64_t n = n0; n < n1; n++)
+                for (int64_t j = 0; j < W8A8_ORACLE_GROUP; j++) {
+                    const int64_t i = n * K + g * W8A8_ORACLE_GROUP + j;
+                    qw[i] = quantize_value(w[i], s);
+                }
+        }
+    }
+}
+
+/* The group-scaled GEMM with one weight scale per block of block_rows output
+ * rows: y[m, n] = sum_g sa[m] * sw[n / block_rows, g] * P[m, n, g] (FP64),
+ * T = sum_g |...|. */
+void oracle_gemm_blocks(const int8_t *qa, const float *sa, const int8_t *qw, const float *sw,
+                        int64_t M, int64_t N, int64_t K, int64_t block_rows, double *y,
+                        double *T) {
+    const int64_t G = K / W8A8_ORACLE_GROUP;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t n = 0; n < N; n++) {
+            double ysum = 0.0, tsum = 0.0;
+            for (int64_t g = 0; g < G; g++) {
+                int32_t p = group_partial(qa + m * K, qw + n * K, g);
+                double term = (double)sa[m] * (double)sw[(n / block_rows) * G + g] * (double)p;
+                ysum += term;
+                tsum += fabs(term);
+            }
+            y[m * N + n] = ysum;
+            if (T) T[m * N + n] = tsum;
+        }
+    }
+}
+
+/* Weight-only INT8 with BF16 activations (the "WNA16" reading of the MoE
+ * runner on the same page, §二): y[m, n] = sum_g sw[n / block_rows, g] *
+ * sum_{k in g} a[m, k] * qw[n, k] (FP64; the products of a BF16 value and an
+ * integer of at most 7 bits are exact), T = sum_g |sw| * sum_k |a * qw|. */
+void oracle_w8a16_gemm(const uint16_t *a, const int8_t *qw, const float *sw, int64_t M, int64_t N,
+                       int64_t K, int64_t block_rows, double *y, double *T) {
+    const int64_t G = K / W8A8_ORACLE_GROUP;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++) {
+        for (int64_t n = 0; n < N; n++) {
+            double ysum = 0.0, tsum = 0.0;
+            for (int64_t g = 0; g < G; g++) {
+                double ps = 0.0, pa = 0.0;
+                for (int64_t j = 0; j < W8A8_ORACLE_GROUP; j++) {
+                    const int64_t k = g * W8A8_ORACLE_GROUP + j;
+                    double prod = (double)bf16_bits_to_float(a[m * K + k]) * (double)qw[n * K + k];
+                    ps += prod;
+                    pa += fabs(prod);
+                }
+                const double s = (double)sw[(n / block_rows) * G + g];
+                ysum += s * ps;
+                tsum += fabs(s) * pa;
+            }
+            y[m * N + n] = ysum;
+            if (T) T[m * N + n] = tsum;
+        }
+    }
+}
