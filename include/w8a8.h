@@ -57,6 +57,12 @@ typedef enum {
 
 typedef enum { W8A8_BF16 = 0, W8A8_FP32 = 1 } w8a8_dtype;
 
+/* How a quantization scale is chosen from the group's largest magnitude amax:
+ * amax / 127 (IEEE FP32 division), or the smallest power of two >= amax / 127
+ * (exponent clamped to [-127, 127]; 2^-127 for an all-zero group), i.e. a
+ * scale that the 8-bit exponent-only UE8M0 format holds exactly. */
+typedef enum { W8A8_SCALE_AMAX = 0, W8A8_SCALE_POW2 = 1 } w8a8_scale_mode;
+
 #define W8A8_GROUP 128
 
 /*
@@ -199,6 +205,58 @@ w8a8_status w8a8_grouped_linear(const void *a_bf16, int64_t lda, const int32_t *
                                 const int8_t *qw, const float *sw, void *y, w8a8_dtype y_dtype,
                                 int64_t R, int64_t E, int64_t N, int64_t K, void *workspace,
                                 size_t workspace_bytes, w8a8_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Scale formats of the DeepSeek-V4 checkpoints ("Running DeepSeek-V4-Flash-
+ * Vision on 4xA800", §一: weights in [128, 128] blocks, power-of-two UE8M0
+ * scales), applied to the INT8 codes of this library.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * w8a8_quant_act with a choice of scale: mode W8A8_SCALE_AMAX is
+ * w8a8_quant_act; W8A8_SCALE_POW2 sets sa[m] to the power of two above
+ * (see w8a8_scale_mode), and the codes are then round-half-even(a / sa[m])
+ * with an exact division (|code| <= 127, the largest |code| of a non-zero
+ * row at least 64).
+ */
+w8a8_status w8a8_quant_act_ex(const void *a_bf16, int64_t M, int64_t K, int64_t lda,
+                              int8_t *qa, int64_t ldq, float *sa, w8a8_scale_mode mode,
+                              w8a8_stream_t stream);
+
+/*
+ * Weight quantization over blocks of block_rows rows x 128 K: block_rows 1 is
+ * w8a8_quant_weight's per-row groups, 128 the [128, 128] blocks (one scale
+ * per block; a ragged last block of rows has its own scale). sw has
+ * ceil(N / block_rows) rows of K / 128 scales; mode as above.
+ */
+w8a8_status w8a8_quant_weight_ex(const float *w, int64_t N, int64_t K, int32_t block_rows,
+                                 w8a8_scale_mode mode, int8_t *qw, float *sw,
+                                 w8a8_stream_t stream);
+
+/*
+ * w8a8_gemm / w8a8_grouped_gemm with weight scales per [sw_block_rows x 128]
+ * block: sw[n / sw_block_rows, g] scales P[m, n, g] (sw_block_rows 1 or 128;
+ * sw [E * ceil(N / sw_block_rows), K / 128] for grouped calls). Everything
+ * else, including the accuracy bound, as w8a8_gemm / w8a8_grouped_gemm.
+ */
+w8a8_status w8a8_gemm_ex(const int8_t *qa, const float *sa, const int8_t *qw, const float *sw,
+                         int32_t sw_block_rows, void *y, w8a8_dtype y_dtype, int64_t M, int64_t N,
+                         int64_t K, int32_t *debug_partials, void *workspace,
+                         size_t workspace_bytes, w8a8_stream_t stream);
+w8a8_status w8a8_grouped_gemm_ex(const int8_t *qa, const float *sa, const int32_t *offsets,
+                                 const int8_t *qw, const float *sw, int32_t sw_block_rows,
+                                 void *y, w8a8_dtype y_dtype, int64_t R, int64_t E, int64_t N,
+                                 int64_t K, int32_t *debug_partials, void *workspace,
+                                 size_t workspace_bytes, w8a8_stream_t stream);
+
+/*
+ * w8a8_linear with the activation scale mode and the weight block size as
+ * above (same workspace as w8a8_linear).
+ */
+w8a8_status w8a8_linear_ex(const void *a_bf16, int64_t lda, w8a8_scale_mode act_mode,
+                           const int8_t *qw, const float *sw, int32_t sw_block_rows, void *y,
+                           w8a8_dtype y_dtype, int64_t M, int64_t N, int64_t K, void *workspace,
+                           size_t workspace_bytes, w8a8_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * MoE expert FFN ("Deploying Hunyuan 770B in INT8 on domestic accelerators":

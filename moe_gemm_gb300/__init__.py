@@ -23,6 +23,7 @@ from . import _build
 
 GROUP = 128
 W8A8_BF16, W8A8_FP32 = 0, 1
+SCALE_AMAX, SCALE_POW2 = 0, 1     # w8a8_scale_mode
 _STATUS = {0: "W8A8_OK", 1: "W8A8_ERR_INVALID_ARG", 2: "W8A8_ERR_UNSUPPORTED",
            3: "W8A8_ERR_CUDA", 4: "W8A8_ERR_WORKSPACE", 5: "W8A8_ERR_DEVICE_TIMEOUT"}
 
@@ -63,6 +64,14 @@ def _load() -> ctypes.CDLL:
                                         ctypes.c_size_t, vp]
     lib.w8a8_probe_tc_rate.argtypes = [i32, i32, i32, i64, ctypes.POINTER(i64), vp]
     lib.w8a8_probe_dp4a_rate.argtypes = [i64, ctypes.POINTER(i64), vp]
+    lib.w8a8_quant_act_ex.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp]
+    lib.w8a8_quant_weight_ex.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp]
+    lib.w8a8_gemm_ex.argtypes = [vp, vp, vp, vp, i32, vp, i32, i64, i64, i64, vp, vp,
+                                 ctypes.c_size_t, vp]
+    lib.w8a8_grouped_gemm_ex.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i64, i64, i64, i64,
+                                         vp, vp, ctypes.c_size_t, vp]
+    lib.w8a8_linear_ex.argtypes = [vp, i64, i32, vp, vp, i32, vp, i32, i64, i64, i64, vp,
+                                   ctypes.c_size_t, vp]
     lib.w8a8_moe_route.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
     lib.w8a8_quant_act_rows.argtypes = [vp, i64, vp, i64, i64, vp, vp, vp]
     lib.w8a8_swiglu_quant.argtypes = [vp, i64, i64, vp, i64, vp, vp, vp]
@@ -77,7 +86,9 @@ def _load() -> ctypes.CDLL:
                  "w8a8_gemm_noalloc", "w8a8_device_error", "w8a8_selftest_wait_timeout",
                  "w8a8_linear", "w8a8_grouped_linear", "w8a8_probe_tc_rate",
                  "w8a8_probe_dp4a_rate", "w8a8_moe_route", "w8a8_quant_act_rows",
-                 "w8a8_swiglu_quant", "w8a8_swiglu", "w8a8_moe_unpermute", "w8a8_moe_ffn"):
+                 "w8a8_swiglu_quant", "w8a8_swiglu", "w8a8_moe_unpermute", "w8a8_moe_ffn",
+                 "w8a8_quant_act_ex", "w8a8_quant_weight_ex", "w8a8_gemm_ex",
+                 "w8a8_grouped_gemm_ex", "w8a8_linear_ex"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -143,8 +154,10 @@ def _on_device(device: torch.device, stream: Optional[torch.cuda.Stream]):
 
 def quant_act(a: torch.Tensor, qa: Optional[torch.Tensor] = None,
               sa: Optional[torch.Tensor] = None,
-              stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Per-token dynamic INT8 quantization of BF16 activations [M, K]."""
+              stream: Optional[torch.cuda.Stream] = None,
+              scale_mode: int = SCALE_AMAX) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-token dynamic INT8 quantization of BF16 activations [M, K]
+    (scale amax/127, or a power of two with scale_mode=SCALE_POW2)."""
     if not a.is_cuda or a.dtype != torch.bfloat16 or a.dim() != 2 or a.stride(1) != 1:
         raise ValueError("a: expected a CUDA bf16 [M, K] tensor with unit column stride")
     M, K = a.shape
@@ -159,21 +172,34 @@ def quant_act(a: torch.Tensor, qa: Optional[torch.Tensor] = None,
     else:
         _require(sa, torch.float32, "sa", 1, (M,), dev)
     with _on_device(dev, stream):
-        _check(_lib.w8a8_quant_act(_ptr(a), M, K, a.stride(0), _ptr(qa), qa.stride(0), _ptr(sa),
-                                   _stream(stream)), "w8a8_quant_act")
+        if scale_mode == SCALE_AMAX:
+            _check(_lib.w8a8_quant_act(_ptr(a), M, K, a.stride(0), _ptr(qa), qa.stride(0),
+                                       _ptr(sa), _stream(stream)), "w8a8_quant_act")
+        else:
+            _check(_lib.w8a8_quant_act_ex(_ptr(a), M, K, a.stride(0), _ptr(qa), qa.stride(0),
+                                          _ptr(sa), scale_mode, _stream(stream)),
+                   "w8a8_quant_act_ex")
     return qa, sa
 
 
-def quant_weight(w: torch.Tensor, stream: Optional[torch.cuda.Stream] = None
+def quant_weight(w: torch.Tensor, stream: Optional[torch.cuda.Stream] = None,
+                 block_rows: int = 1, scale_mode: int = SCALE_AMAX
                  ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Per-row, per-128-K-group INT8 quantization of FP32 weights [N, K]."""
+    """INT8 quantization of FP32 weights [N, K] over [block_rows x 128]
+    blocks (1: per-row groups; 128: [128, 128] blocks); returns (qw [N, K],
+    sw [ceil(N / block_rows), K / 128])."""
     _require(w, torch.float32, "w", 2)
     N, K = w.shape
+    nb = (N + block_rows - 1) // block_rows
     qw = torch.empty((N, K), dtype=torch.int8, device=w.device)
-    sw = torch.empty((N, K // GROUP), dtype=torch.float32, device=w.device)
+    sw = torch.empty((nb, K // GROUP), dtype=torch.float32, device=w.device)
     with _on_device(w.device, stream):
-        _check(_lib.w8a8_quant_weight(_ptr(w), N, K, _ptr(qw), _ptr(sw), _stream(stream)),
-               "w8a8_quant_weight")
+        if block_rows == 1 and scale_mode == SCALE_AMAX:
+            _check(_lib.w8a8_quant_weight(_ptr(w), N, K, _ptr(qw), _ptr(sw), _stream(stream)),
+                   "w8a8_quant_weight")
+        else:
+            _check(_lib.w8a8_quant_weight_ex(_ptr(w), N, K, block_rows, scale_mode, _ptr(qw),
+                                             _ptr(sw), _stream(stream)), "w8a8_quant_weight_ex")
     return qw, sw
 
 
@@ -193,8 +219,10 @@ def _dtype_code(out_dtype: torch.dtype) -> int:
     raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
 
 
-def _dense_operands(qa, sa, qw, sw):
+def _dense_operands(qa, sa, qw, sw, sw_block_rows=1):
     """Checks the dense GEMM operands against each other; returns M, N, K."""
+    if sw_block_rows not in (1, 128):
+        raise ValueError("sw_block_rows must be 1 or 128")
     _require(qa, torch.int8, "qa", 2)
     dev = qa.device
     M, K = qa.shape
@@ -203,17 +231,18 @@ def _dense_operands(qa, sa, qw, sw):
     if qw.shape[1] != K:
         raise ValueError(f"qw: expected K = {K} columns, got {qw.shape[1]}")
     _require(sa, torch.float32, "sa", 1, (M,), dev)
-    _require(sw, torch.float32, "sw", 2, (N, K // GROUP), dev)
+    nb = (N + sw_block_rows - 1) // sw_block_rows
+    _require(sw, torch.float32, "sw", 2, (nb, K // GROUP), dev)
     return M, N, K
 
 
 def gemm(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
          out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
          workspace: Optional[torch.Tensor] = None, debug_partials: bool = False,
-         stream: Optional[torch.cuda.Stream] = None):
-    """Y[M,N] = sa[m] * sum_g sw[n,g] * P[m,n,g]; returns y, or (y, P) with
-    debug_partials=True (P int32 [M, N, K/128])."""
-    M, N, K = _dense_operands(qa, sa, qw, sw)
+         stream: Optional[torch.cuda.Stream] = None, sw_block_rows: int = 1):
+    """Y[M,N] = sa[m] * sum_g sw[n / sw_block_rows, g] * P[m,n,g]; returns y,
+    or (y, P) with debug_partials=True (P int32 [M, N, K/128])."""
+    M, N, K = _dense_operands(qa, sa, qw, sw, sw_block_rows)
     code = _dtype_code(out_dtype)
     dev = qa.device
     if out is None:
@@ -227,9 +256,14 @@ def gemm(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
         _require_workspace(workspace, dev)
     P = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=dev) if debug_partials else None
     with _on_device(dev, stream):
-        _check(_lib.w8a8_gemm(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(out), code, M, N, K,
-                              _ptr(P), _ptr(workspace), workspace.numel(), _stream(stream)),
-               "w8a8_gemm")
+        if sw_block_rows == 1:
+            _check(_lib.w8a8_gemm(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(out), code, M, N,
+                                  K, _ptr(P), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)), "w8a8_gemm")
+        else:
+            _check(_lib.w8a8_gemm_ex(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), sw_block_rows,
+                                     _ptr(out), code, M, N, K, _ptr(P), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "w8a8_gemm_ex")
     return (out, P) if debug_partials else out
 
 
@@ -258,8 +292,10 @@ def gemm_noalloc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch
 def grouped_gemm(qa: torch.Tensor, sa: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor,
                  sw: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
                  out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                 debug_partials: bool = False, stream: Optional[torch.cuda.Stream] = None):
-    """MoE grouped GEMM over rows sorted by expert; offsets int32 [E+1] on device."""
+                 debug_partials: bool = False, stream: Optional[torch.cuda.Stream] = None,
+                 sw_block_rows: int = 1):
+    """MoE grouped GEMM over rows sorted by expert; offsets int32 [E+1] on
+    device; sw [E, ceil(N / sw_block_rows), K/128]."""
     _require(qa, torch.int8, "qa", 2)
     dev = qa.device
     R, K = qa.shape
@@ -268,7 +304,10 @@ def grouped_gemm(qa: torch.Tensor, sa: torch.Tensor, offsets: torch.Tensor, qw: 
     if K2 != K:
         raise ValueError(f"qw: expected K = {K} columns, got {K2}")
     _require(sa, torch.float32, "sa", 1, (R,), dev)
-    _require(sw, torch.float32, "sw", 3, (E, N, K // GROUP), dev)
+    if sw_block_rows not in (1, 128):
+        raise ValueError("sw_block_rows must be 1 or 128")
+    nb = (N + sw_block_rows - 1) // sw_block_rows
+    _require(sw, torch.float32, "sw", 3, (E, nb, K // GROUP), dev)
     _require(offsets, torch.int32, "offsets", 1, (E + 1,), dev)
     code = _dtype_code(out_dtype)
     if out is None:
@@ -282,9 +321,16 @@ def grouped_gemm(qa: torch.Tensor, sa: torch.Tensor, offsets: torch.Tensor, qw: 
         _require_workspace(workspace, dev)
     P = torch.empty((R, N, K // GROUP), dtype=torch.int32, device=dev) if debug_partials else None
     with _on_device(dev, stream):
-        _check(_lib.w8a8_grouped_gemm(_ptr(qa), _ptr(sa), _ptr(offsets), _ptr(qw), _ptr(sw),
-                                      _ptr(out), code, R, E, N, K, _ptr(P), _ptr(workspace),
-                                      workspace.numel(), _stream(stream)), "w8a8_grouped_gemm")
+        if sw_block_rows == 1:
+            _check(_lib.w8a8_grouped_gemm(_ptr(qa), _ptr(sa), _ptr(offsets), _ptr(qw), _ptr(sw),
+                                          _ptr(out), code, R, E, N, K, _ptr(P), _ptr(workspace),
+                                          workspace.numel(), _stream(stream)),
+                   "w8a8_grouped_gemm")
+        else:
+            _check(_lib.w8a8_grouped_gemm_ex(_ptr(qa), _ptr(sa), _ptr(offsets), _ptr(qw),
+                                             _ptr(sw), sw_block_rows, _ptr(out), code, R, E, N,
+                                             K, _ptr(P), _ptr(workspace), workspace.numel(),
+                                             _stream(stream)), "w8a8_grouped_gemm_ex")
     return (out, P) if debug_partials else out
 
 
@@ -305,7 +351,8 @@ def _require_act(a: torch.Tensor) -> int:
 def linear(a: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
            out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
            workspace: Optional[torch.Tensor] = None,
-           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+           stream: Optional[torch.cuda.Stream] = None, act_scale_mode: int = SCALE_AMAX,
+           sw_block_rows: int = 1) -> torch.Tensor:
     """quant_act + gemm in one call: Y[M,N] from BF16 activations a [M, K]
     (the quantizer writes the GEMM's operand directly into the workspace)."""
     lda = _require_act(a)
@@ -315,7 +362,10 @@ def linear(a: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
     N = qw.shape[0]
     if qw.shape[1] != K:
         raise ValueError(f"qw: expected K = {K} columns, got {qw.shape[1]}")
-    _require(sw, torch.float32, "sw", 2, (N, K // GROUP), dev)
+    if sw_block_rows not in (1, 128):
+        raise ValueError("sw_block_rows must be 1 or 128")
+    _require(sw, torch.float32, "sw", 2, ((N + sw_block_rows - 1) // sw_block_rows, K // GROUP),
+             dev)
     code = _dtype_code(out_dtype)
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=dev)
@@ -327,9 +377,14 @@ def linear(a: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
     else:
         _require_workspace(workspace, dev)
     with _on_device(dev, stream):
-        _check(_lib.w8a8_linear(_ptr(a), lda, _ptr(qw), _ptr(sw), _ptr(out), code, M, N, K,
-                                _ptr(workspace), workspace.numel(), _stream(stream)),
-               "w8a8_linear")
+        if act_scale_mode == SCALE_AMAX and sw_block_rows == 1:
+            _check(_lib.w8a8_linear(_ptr(a), lda, _ptr(qw), _ptr(sw), _ptr(out), code, M, N, K,
+                                    _ptr(workspace), workspace.numel(), _stream(stream)),
+                   "w8a8_linear")
+        else:
+            _check(_lib.w8a8_linear_ex(_ptr(a), lda, act_scale_mode, _ptr(qw), _ptr(sw),
+                                       sw_block_rows, _ptr(out), code, M, N, K, _ptr(workspace),
+                                       workspace.numel(), _stream(stream)), "w8a8_linear_ex")
     return out
 
 

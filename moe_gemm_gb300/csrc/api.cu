@@ -89,7 +89,7 @@ size_t workspace_bytes_for(int64_t R, int64_t K, bool grouped) {
 w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, const int8_t *qw,
                      const float *sw, void *y, w8a8_dtype y_dtype, int64_t R, int64_t E,
                      int64_t N, int64_t K, int32_t *dbg, void *workspace, size_t workspace_bytes,
-                     w8a8_stream_t stream) {
+                     w8a8_stream_t stream, int sw_block_rows = 1) {
     w8a8::DeviceInfo info;
     w8a8_status st = check_device(&info);
     if (st != W8A8_OK) return st;
@@ -128,6 +128,7 @@ w8a8_status run_gemm(const int8_t *qa, const float *sa, const int32_t *offsets, 
     p.N = N;
     p.K = K;
     p.out_fp32 = (y_dtype == W8A8_FP32);
+    p.sw_block_rows = sw_block_rows;
     return from_cuda(w8a8::launch_gemm(p, info.num_sms, s));
 }
 
@@ -171,7 +172,7 @@ w8a8_status check_linear(const void *a, int64_t lda, const void *offsets, const 
 w8a8_status run_linear(const void *a, int64_t lda, const int32_t *offsets, const int8_t *qw,
                        const float *sw, void *y, w8a8_dtype y_dtype, int64_t R, int64_t E,
                        int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
-                       w8a8_stream_t stream) {
+                       w8a8_stream_t stream, int sw_block_rows = 1, bool pow2 = false) {
     w8a8::DeviceInfo info;
     w8a8_status st = check_device(&info);
     if (st != W8A8_OK) return st;
@@ -189,17 +190,18 @@ w8a8_status run_linear(const void *a, int64_t lda, const int32_t *offsets, const
     }
     const uint16_t *a16 = static_cast<const uint16_t *>(a);
     cudaError_t e = cudaSuccess;
-    if (w8a8::uses_gemv(R, grouped) && w8a8::gemv_can_fuse_quant(R, K, lda, a)) {
+    if (w8a8::uses_gemv(R, grouped) && !pow2 && w8a8::gemv_can_fuse_quant(R, K, lda, a)) {
         // one kernel: the GEMV quantizes its token rows itself
         p.act = a16;
         p.lda = lda;
         p.qa = nullptr;
     } else if (w8a8::uses_gemv(R, grouped)) {
-        e = w8a8::launch_quant_act(a16, R, K, lda, reinterpret_cast<int8_t *>(ws), K, sa, s);
+        e = w8a8::launch_quant_act_ex(a16, R, K, lda, reinterpret_cast<int8_t *>(ws), K, sa, pow2,
+                                      s);
         p.qa = reinterpret_cast<const int8_t *>(ws);
     } else {
-        e = w8a8::launch_quant_act_f16(a16, R, K, lda, ws, sa, p.sk_cnt,
-                                       p.sk_cnt != nullptr ? 2 * w8a8::kSkMaxCtas : 0, s);
+        e = w8a8::launch_quant_act_f16_ex(a16, R, K, lda, ws, sa, p.sk_cnt,
+                                          p.sk_cnt != nullptr ? 2 * w8a8::kSkMaxCtas : 0, pow2, s);
         p.qa = nullptr;   // the tensor-core GEMM reads only the fp16 codes
     }
     if (e != cudaSuccess) return W8A8_ERR_CUDA;
@@ -215,6 +217,7 @@ w8a8_status run_linear(const void *a, int64_t lda, const int32_t *offsets, const
     p.N = N;
     p.K = K;
     p.out_fp32 = (y_dtype == W8A8_FP32);
+    p.sw_block_rows = sw_block_rows;
     return from_cuda(w8a8::launch_gemm(p, info.num_sms, s));
 }
 
@@ -429,6 +432,84 @@ w8a8_status w8a8_gemm_noalloc(const int8_t *qa, const float *sa, const int8_t *q
     if (noalloc_scratch_ptr(&scratch) != cudaSuccess) return W8A8_ERR_CUDA;
     return w8a8_gemm(qa, sa, qw, sw, y, y_dtype, M, N, K, nullptr, scratch, kNoallocScratchBytes,
                      stream);
+}
+
+w8a8_status w8a8_quant_act_ex(const void *a_bf16, int64_t M, int64_t K, int64_t lda,
+                              int8_t *qa, int64_t ldq, float *sa, w8a8_scale_mode mode,
+                              w8a8_stream_t stream) {
+    if (mode != W8A8_SCALE_AMAX && mode != W8A8_SCALE_POW2) return W8A8_ERR_INVALID_ARG;
+    if (M < 0 || K <= 0 || lda < K || ldq < K) return W8A8_ERR_INVALID_ARG;
+    if (M > kMaxElems / lda || M > kMaxElems / ldq || M > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
+    if (M == 0) return W8A8_OK;
+    if (!a_bf16 || !qa || !sa || !aligned(a_bf16, 2) || !aligned(sa, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_quant_act_ex(static_cast<const uint16_t *>(a_bf16), M, K, lda,
+                                               qa, ldq, sa, mode == W8A8_SCALE_POW2,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_quant_weight_ex(const float *w, int64_t N, int64_t K, int32_t block_rows,
+                                 w8a8_scale_mode mode, int8_t *qw, float *sw,
+                                 w8a8_stream_t stream) {
+    if (mode != W8A8_SCALE_AMAX && mode != W8A8_SCALE_POW2) return W8A8_ERR_INVALID_ARG;
+    if (block_rows != 1 && block_rows != 128) return W8A8_ERR_INVALID_ARG;
+    if (N < 0 || K <= 0 || K % W8A8_GROUP != 0 || N > kMaxElems / K) return W8A8_ERR_INVALID_ARG;
+    if (N == 0) return W8A8_OK;
+    if (!w || !qw || !sw || !aligned(w, 16) || !aligned(qw, 4) || !aligned(sw, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (block_rows == 1 && mode == W8A8_SCALE_AMAX)
+        return from_cuda(w8a8::launch_quant_weight(w, N, K, qw, sw, s));
+    return from_cuda(w8a8::launch_quant_weight_blocks(w, N, K, block_rows,
+                                                      mode == W8A8_SCALE_POW2, qw, sw, s));
+}
+
+w8a8_status w8a8_gemm_ex(const int8_t *qa, const float *sa, const int8_t *qw, const float *sw,
+                         int32_t sw_block_rows, void *y, w8a8_dtype y_dtype, int64_t M, int64_t N,
+                         int64_t K, int32_t *debug_partials, void *workspace,
+                         size_t workspace_bytes, w8a8_stream_t stream) {
+    if (sw_block_rows != 1 && sw_block_rows != 128) return W8A8_ERR_INVALID_ARG;
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    w8a8_status st = check_gemm(qa, sa, nullptr, qw, sw, y, M, 1, N, K, false, workspace,
+                                workspace_bytes);
+    if (st != W8A8_OK || M == 0) return st;
+    if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
+    return run_gemm(qa, sa, nullptr, qw, sw, y, y_dtype, M, 1, N, K, debug_partials, workspace,
+                    workspace_bytes, stream, sw_block_rows);
+}
+
+w8a8_status w8a8_grouped_gemm_ex(const int8_t *qa, const float *sa, const int32_t *offsets,
+                                 const int8_t *qw, const float *sw, int32_t sw_block_rows,
+                                 void *y, w8a8_dtype y_dtype, int64_t R, int64_t E, int64_t N,
+                                 int64_t K, int32_t *debug_partials, void *workspace,
+                                 size_t workspace_bytes, w8a8_stream_t stream) {
+    if (sw_block_rows != 1 && sw_block_rows != 128) return W8A8_ERR_INVALID_ARG;
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    w8a8_status st = check_gemm(qa, sa, offsets, qw, sw, y, R, E, N, K, true, workspace,
+                                workspace_bytes);
+    if (st != W8A8_OK || R == 0) return st;
+    if (debug_partials && !aligned(debug_partials, 4)) return W8A8_ERR_INVALID_ARG;
+    return run_gemm(qa, sa, offsets, qw, sw, y, y_dtype, R, E, N, K, debug_partials, workspace,
+                    workspace_bytes, stream, sw_block_rows);
+}
+
+w8a8_status w8a8_linear_ex(const void *a_bf16, int64_t lda, w8a8_scale_mode act_mode,
+                           const int8_t *qw, const float *sw, int32_t sw_block_rows, void *y,
+                           w8a8_dtype y_dtype, int64_t M, int64_t N, int64_t K, void *workspace,
+                           size_t workspace_bytes, w8a8_stream_t stream) {
+    if (act_mode != W8A8_SCALE_AMAX && act_mode != W8A8_SCALE_POW2) return W8A8_ERR_INVALID_ARG;
+    if (sw_block_rows != 1 && sw_block_rows != 128) return W8A8_ERR_INVALID_ARG;
+    w8a8_status st = check_linear(a_bf16, lda, nullptr, qw, sw, y, y_dtype, M, 1, N, K, false,
+                                  workspace, workspace_bytes);
+    if (st != W8A8_OK || M == 0) return st;
+    return run_linear(a_bf16, lda, nullptr, qw, sw, y, y_dtype, M, 1, N, K, workspace,
+                      workspace_bytes, stream, sw_block_rows, act_mode == W8A8_SCALE_POW2);
 }
 
 w8a8_status w8a8_moe_route(const int32_t *topk_ids, int64_t T, int64_t k, int64_t E,

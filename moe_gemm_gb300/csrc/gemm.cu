@@ -86,6 +86,10 @@ constexpr int kSmemLimit = 232448;
 // Dense problems with wide token tiles walk their tiles in bands of this many
 // weight tiles (see decode_tile).
 constexpr int kRasterBand = 8;
+// Narrow tiles of at most this many token rows issue the MMAs of a step's two
+// K groups alternately (two independent accumulators in flight: decode M=8
+// and M=32 ~1 us faster per GEMM; 64-row tiles were not, measured).
+constexpr int kInterleaveMaxRows = 32;
 
 // Shared memory: a fixed area (barriers, flags, tile table), then the weight
 // stages, then the token stages (offsets from a 1024-byte aligned base).
@@ -113,6 +117,10 @@ struct KParams {
     int tab_off;        // byte offset of the tile table in shared memory
     int group_tokens;   // wide tiles: token stages released per K group (dense calls)
     int gw;             // tile order: bands of gw weight tiles (0: expert-major, see decode_tile)
+    // Weight scales: one row of G scales per 2^sw_shift weight rows (0: per
+    // row; 7: [128, 128] blocks), sw_rows rows of scales per expert.
+    int sw_shift;
+    int sw_rows;
     // GEMV that quantizes its own token rows: BF16 activations [R, lda] and
     // the byte offset of the resident int8 code buffer in shared memory.
     const uint16_t *act;
@@ -549,6 +557,33 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         return false;
                     }
                     tc_fence_after();
+                    if (!kWide && b_rows <= kInterleaveMaxRows) {
+                        // the two groups' accumulators are independent: their
+                        // MMAs take turns (descriptors formed once per step)
+                        const uint32_t d0 = tmem_base + pbuf_col(pr.idx, 0);
+                        const uint32_t d1 = tmem_base + pbuf_col(pr.idx, 1);
+                        const uint32_t a0 = tmem_base + kTmemA0 + st.idx * 128u;
+                        const uint64_t b0 = smem_desc_sw128(sB + bs.idx * b_stage_bytes);
+                        const uint64_t b1 = b0 + static_cast<uint64_t>((2u * b_atom_bytes) >> 4);
+                        const uint64_t atom_step = b_atom_bytes >> 4;
+                        if (ng == 2) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bd =
+                                    (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
+                                mma_f16_tmemA(d0, a0 + kk * 8, b0 + bd, idesc, kk > 0 ? 1u : 0u);
+                                mma_f16_tmemA(d1, a0 + 64u + kk * 8, b1 + bd, idesc,
+                                              kk > 0 ? 1u : 0u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bd =
+                                    (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
+                                mma_f16_tmemA(d0, a0 + kk * 8, b0 + bd, idesc, kk > 0 ? 1u : 0u);
+                            }
+                        }
+                    } else
                     for (int j = 0; j < ng; ++j) {
                         if constexpr (kWide) {
                             // group j's partial buffer drained by the epilogue;
@@ -814,7 +849,8 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const bool owned = 32 * ewg < n_eff;   // warp-uniform (first chunk)
             const int n_local = ti.n0 + lrow;
             const bool n_ok = n_local < p.N;
-            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            const float *swp =
+                p.sw + (static_cast<size_t>(ti.e) * p.sw_rows + ((n_ok ? n_local : 0) >> p.sw_shift)) * G;
             // Scales of this row a quad of groups (two steps) ahead; loads are
             // issued in place and only read after the next quad boundary.
             auto load_quad = [&](int g) -> float4 {
@@ -1304,7 +1340,8 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const TileInfo ti = tile_of(t);
             const int n_local = ti.n0 + lrow;
             const bool n_ok = n_local < p.N;
-            const float *swp = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok ? n_local : 0)) * G;
+            const float *swp =
+                p.sw + (static_cast<size_t>(ti.e) * p.sw_rows + ((n_ok ? n_local : 0) >> p.sw_shift)) * G;
             // this row's weight scales two groups ahead (loads issued in place)
             float sc0 = n_ok ? ldg_nc_f32_now(swp) : 0.0f;
             float sc1 = (n_ok && G > 1) ? ldg_nc_f32_now(swp + 1) : 0.0f;
@@ -1645,7 +1682,8 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 const int lr = rb + i * (128 / RR);
                 n_row[i] = n0 + lr;
                 n_ok[i] = n_row[i] < p.N && (h == 0 || lr < 64);
-                swp[i] = p.sw + (static_cast<size_t>(ti.e) * p.N + (n_ok[i] ? n_row[i] : 0)) * G;
+                swp[i] = p.sw + (static_cast<size_t>(ti.e) * p.sw_rows +
+                                 ((n_ok[i] ? n_row[i] : 0) >> p.sw_shift)) * G;
 #pragma unroll
                 for (int u = 0; u < RM; ++u) acc[i][u] = 0.0f;
             }
@@ -1904,6 +1942,8 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     KParams kp;
     kp.sa = pr.sa;
     kp.sw = pr.sw;
+    kp.sw_shift = pr.sw_block_rows == 128 ? 7 : 0;
+    kp.sw_rows = static_cast<int>((pr.N + (1 << kp.sw_shift) - 1) >> kp.sw_shift);
     kp.offsets = pr.offsets;
     kp.y = pr.y;
     kp.dbg = pr.debug_partials;
@@ -1987,6 +2027,8 @@ cudaError_t launch_wide(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     KParams kp = {};
     kp.sa = pr.sa;
     kp.sw = pr.sw;
+    kp.sw_shift = pr.sw_block_rows == 128 ? 7 : 0;
+    kp.sw_rows = static_cast<int>((pr.N + (1 << kp.sw_shift) - 1) >> kp.sw_shift);
     kp.offsets = nullptr;
     kp.y = pr.y;
     kp.dbg = pr.debug_partials;
@@ -2059,6 +2101,8 @@ cudaError_t launch_gemv(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     KParams kp = {};
     kp.sa = pr.sa;
     kp.sw = pr.sw;
+    kp.sw_shift = pr.sw_block_rows == 128 ? 7 : 0;
+    kp.sw_rows = static_cast<int>((pr.N + (1 << kp.sw_shift) - 1) >> kp.sw_shift);
     kp.offsets = nullptr;
     kp.y = pr.y;
     kp.dbg = pr.debug_partials;

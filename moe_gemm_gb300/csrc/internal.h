@@ -20,6 +20,18 @@ cudaError_t launch_quant_act_f16(const uint16_t *a, int64_t M, int64_t K, int64_
 cudaError_t launch_quant_weight(const float *w, int64_t N, int64_t K, int8_t *qw, float *sw,
                                 cudaStream_t stream);
 
+// Scale-format variants: activations with power-of-two (UE8M0) scales
+// (int8 codes, or fp16 codes into a GEMM workspace), and weights over
+// [block_rows x 128] blocks (block_rows 1 or 128) with amax/127 or
+// power-of-two scales, sw [ceil(N / block_rows), K / 128].
+cudaError_t launch_quant_act_ex(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
+                                int64_t ldq, float *sa, bool pow2, cudaStream_t stream);
+cudaError_t launch_quant_act_f16_ex(const uint16_t *a, int64_t M, int64_t K, int64_t lda,
+                                    void *x16, float *sa, int *cnt, int n_cnt, bool pow2,
+                                    cudaStream_t stream);
+cudaError_t launch_quant_weight_blocks(const float *w, int64_t N, int64_t K, int block_rows,
+                                       bool pow2, int8_t *qw, float *sw, cudaStream_t stream);
+
 // Per-token quantization with a row gather: output row r (row stride K)
 // quantizes input row src_rows[r] of a (row stride lda); rows whose entry is
 // negative are skipped. Codes as fp16 (f16) or int8.
@@ -64,6 +76,8 @@ struct GemmProblem {
     const uint16_t *act = nullptr;
     int64_t lda = 0;
     // Stream-K split of dense calls; null sk_cnt: whole tiles only.
+    // Weight scales per [sw_block_rows x 128] block: 1 (per row) or 128.
+    int sw_block_rows = 1;
     int *sk_cnt = nullptr;        // [2 * kSkMaxCtas] counters, zeroed before the GEMM
     float *sk_part = nullptr;     // [kSkMaxCtas][2][sk_ld][128] FP32 partials
     int sk_ld = 0;

@@ -44,11 +44,12 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
 // src_rows (nullable): output row r quantizes input row src_rows[r] (a
 // gather, e.g. tokens into expert-sorted order); rows whose entry is
 // negative are skipped.
+// pow2: power-of-two (UE8M0) scales instead of amax / 127.
 template <int VPT, bool kF16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
     const uint16_t *__restrict__ a, int K, int64_t lda, const int32_t *__restrict__ src_rows,
     void *__restrict__ out, int64_t ldq, float *__restrict__ sa, int *__restrict__ cnt,
-    int n_cnt) {
+    int n_cnt, int pow2) {
     // A GEMM launched after this kernel as a programmatic dependent may start
     // its set-up and weight stream now; it waits for this grid (and so for qa
     // and sa) before it reads the codes. This kernel is itself launched as a
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
     }
     m = block_max_u32(m, red);
     const float amax = bf16_bits_to_f32(m);
-    const float s = __fdiv_rn(amax, 127.0f);
+    const float s = pow2 ? pow2_scale(amax) : __fdiv_rn(amax, 127.0f);
     const bool fast = s >= 1.17549435e-38f;  // normal scale: 1/s is finite
     const float r = fast ? __frcp_rn(s) : 0.0f;
     if (threadIdx.x == 0) sa[row] = s;
@@ -100,7 +101,7 @@ template <bool kF16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
     const uint16_t *__restrict__ a, int K, int64_t lda, const int32_t *__restrict__ src_rows,
     void *__restrict__ out, int64_t ldq, float *__restrict__ sa, int *__restrict__ cnt,
-    int n_cnt) {
+    int n_cnt, int pow2) {
     griddep_launch_dependents();   // as in quant_act_vec_kernel
     griddep_wait();
     if (kF16 && blockIdx.x == 0)
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
     uint32_t m = 0;
     for (int k = threadIdx.x; k < K; k += kQuantThreads) m = max(m, (uint32_t)src[k] & 0x7FFFu);
     m = block_max_u32(m, red);
-    const float s = __fdiv_rn(bf16_bits_to_f32(m), 127.0f);
+    const float s = pow2 ? pow2_scale(bf16_bits_to_f32(m)) : __fdiv_rn(bf16_bits_to_f32(m), 127.0f);
     if (threadIdx.x == 0) sa[row] = s;
     for (int k = threadIdx.x; k < K; k += kQuantThreads) {
         const int q = s == 0.0f ? 0 : quantize_exact(bf16_bits_to_f32(src[k]), s);
@@ -145,6 +146,45 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float *__restri
         packed = pack4(quantize_exact(x.x, s), quantize_exact(x.y, s), quantize_exact(x.z, s),
                        quantize_exact(x.w, s));
     *reinterpret_cast<uint32_t *>(qw + n * K + g * 128 + lane * 4) = packed;
+}
+
+// One CTA per block of `rows` weight rows x 128 K (grid: blocks x groups):
+// amax over the block, scale amax / 127 or power of two, codes (second pass
+// re-reads the block). Offline input preparation.
+__global__ void __launch_bounds__(256) quant_weight_block_kernel(const float *__restrict__ w,
+                                                                 int64_t N, int K, int rows,
+                                                                 int pow2, int8_t *__restrict__ qw,
+                                                                 float *__restrict__ sw) {
+    __shared__ float red[8];
+    const int G = K / 128;
+    const int64_t b = blockIdx.x;
+    const int g = blockIdx.y;
+    const int64_t n0 = b * rows;
+    const int nr = static_cast<int>(min(static_cast<int64_t>(rows), N - n0));
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < nr * 32; i += 256) {
+        const float4 x = *reinterpret_cast<const float4 *>(w + (n0 + i / 32) * K + g * 128 +
+                                                           (i % 32) * 4);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
+    const float s = pow2 ? pow2_scale(m) : __fdiv_rn(m, 127.0f);
+    if (threadIdx.x == 0) sw[b * G + g] = s;
+    for (int i = threadIdx.x; i < nr * 32; i += 256) {
+        const int64_t off = (n0 + i / 32) * K + g * 128 + (i % 32) * 4;
+        const float4 x = *reinterpret_cast<const float4 *>(w + off);
+        uint32_t packed = 0;
+        if (s != 0.0f)
+            packed = pack4(quantize_exact(x.x, s), quantize_exact(x.y, s), quantize_exact(x.z, s),
+                           quantize_exact(x.w, s));
+        *reinterpret_cast<uint32_t *>(qw + off) = packed;
+    }
 }
 
 // int8 codes [rows, K] (row stride ldq) -> fp16 codes [rows, K] (dense).
@@ -201,7 +241,7 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStr
 template <bool kF16>
 cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, void *out,
                          int64_t ldq, float *sa, int *cnt, int n_cnt, cudaStream_t stream,
-                         const int32_t *src_rows = nullptr) {
+                         const int32_t *src_rows = nullptr, int pow2 = 0) {
     const int align = kF16 ? 16 : 8;   // one 8-code vector per store
     const bool vec_ok = (K % 8 == 0) && (lda % 8 == 0) && (ldq % 8 == 0) &&
                         (reinterpret_cast<uintptr_t>(a) % 16 == 0) &&
@@ -212,18 +252,18 @@ cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, v
     if (cnt == nullptr) n_cnt = 0;
     if (vec_ok && K <= 256 * 8 * 1)
         return launch_pdl(quant_act_vec_kernel<1, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt);
+                          out, ldq, sa, cnt, n_cnt, pow2);
     if (vec_ok && K <= 256 * 8 * 2)
         return launch_pdl(quant_act_vec_kernel<2, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt);
+                          out, ldq, sa, cnt, n_cnt, pow2);
     if (vec_ok && K <= 256 * 8 * 4)
         return launch_pdl(quant_act_vec_kernel<4, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt);
+                          out, ldq, sa, cnt, n_cnt, pow2);
     if (vec_ok && K <= 256 * 8 * 8)
         return launch_pdl(quant_act_vec_kernel<8, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt);
+                          out, ldq, sa, cnt, n_cnt, pow2);
     return launch_pdl(quant_act_generic_kernel<kF16>, grid, block, stream, a, k, lda, src_rows,
-                      out, ldq, sa, cnt, n_cnt);
+                      out, ldq, sa, cnt, n_cnt, pow2);
 }
 
 }  // namespace
@@ -236,6 +276,27 @@ cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_quant_act_f16(const uint16_t *a, int64_t M, int64_t K, int64_t lda, void *x16,
                                  float *sa, int *cnt, int n_cnt, cudaStream_t stream) {
     return launch_quant<true>(a, M, K, lda, x16, K, sa, cnt, n_cnt, stream);
+}
+
+cudaError_t launch_quant_act_ex(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
+                                int64_t ldq, float *sa, bool pow2, cudaStream_t stream) {
+    return launch_quant<false>(a, M, K, lda, qa, ldq, sa, nullptr, 0, stream, nullptr,
+                               pow2 ? 1 : 0);
+}
+
+cudaError_t launch_quant_act_f16_ex(const uint16_t *a, int64_t M, int64_t K, int64_t lda,
+                                    void *x16, float *sa, int *cnt, int n_cnt, bool pow2,
+                                    cudaStream_t stream) {
+    return launch_quant<true>(a, M, K, lda, x16, K, sa, cnt, n_cnt, stream, nullptr, pow2 ? 1 : 0);
+}
+
+cudaError_t launch_quant_weight_blocks(const float *w, int64_t N, int64_t K, int block_rows,
+                                       bool pow2, int8_t *qw, float *sw, cudaStream_t stream) {
+    const int64_t nb = (N + block_rows - 1) / block_rows;
+    const dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(K / 128));
+    quant_weight_block_kernel<<<grid, 256, 0, stream>>>(w, N, static_cast<int>(K), block_rows,
+                                                         pow2 ? 1 : 0, qw, sw);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quant_act_rows(const uint16_t *a, int64_t rows, int64_t K, int64_t lda,

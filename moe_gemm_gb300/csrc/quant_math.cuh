@@ -77,6 +77,23 @@ __device__ __forceinline__ uint32_t amax_bits8(const uint4 v) {
     return m;
 }
 
-// One CTA per token row; the row stays in registers between the amax pass and
-// the quantize pass (VPT 16-byte vectors per thread, K <= 256 * 8 * VPT).
+// Power-of-two (UE8M0) scale of a group whose largest magnitude is amax: the
+// smallest 2^e >= amax / 127 (decided exactly: amax <= 127 * 2^e), e clamped
+// to [-127, 127]; 2^-127 for amax == 0. For a normal amax in [2^E, 2^(E+1)),
+// 127 * 2^(E-7) < amax <= 127 * 2^(E-5), so e is E - 6 or E - 5. Dividing
+// by the scale is then exact, so the codes are round-half-even(x * 2^-e).
+__device__ __forceinline__ float pow2_from_exponent(int e) {
+    return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                     : __uint_as_float(0x00400000u);   // 2^-127 (subnormal)
+}
+
+__device__ __forceinline__ float pow2_scale(float amax) {
+    const uint32_t bits = __float_as_uint(amax);
+    const int bexp = static_cast<int>((bits >> 23) & 0xFFu);
+    if (bexp == 0) return pow2_from_exponent(-127);   // zero or subnormal amax
+    int e = bexp - 127 - 6;
+    if (e >= -127 && !(amax <= 127.0f * pow2_from_exponent(e))) ++e;
+    e = max(-127, min(127, e));
+    return pow2_from_exponent(e);
+}
 }  // namespace w8a8
