@@ -258,6 +258,32 @@ w8a8_status w8a8_linear_ex(const void *a_bf16, int64_t lda, w8a8_scale_mode act_
                            w8a8_dtype y_dtype, int64_t M, int64_t N, int64_t K, void *workspace,
                            size_t workspace_bytes, w8a8_stream_t stream);
 
+/*
+ * Weight-only INT8 GEMM with BF16 activations (the "WNA16" reading of the
+ * MoE runner on "Running DeepSeek-V4-Flash-Vision on 4xA800", §二: INT8
+ * weights with one scale per group of 128 K, 16-bit activations that are not
+ * quantized):
+ *   Y[m, n] = sum_g sw[n / sw_block_rows, g] * P16[m, n, g],
+ *   P16[m, n, g] = sum_{k in g} a[m, k] * qw[n, k]
+ * a_bf16 [M, lda] BF16 (lda % 8 == 0, 16-byte aligned), qw [N, K] int8,
+ * sw [ceil(N / sw_block_rows), K/128], y [M, N] BF16 or FP32. Each product of
+ * a BF16 value and an integer of at most 7 bits is exact in FP32; the tensor
+ * cores sum each group's products in FP32 (not exactly, unlike the integer
+ * partials of w8a8_gemm), then the group scales are applied in the epilogue
+ * in K order as in w8a8_gemm. FP32 outputs are within 1e-5 * T of the exact
+ * value, T = sum_g |sw| * sum_k |a * qw| (tested). No workspace.
+ */
+w8a8_status w8a8_w8a16_gemm(const void *a_bf16, int64_t lda, const int8_t *qw, const float *sw,
+                            int32_t sw_block_rows, void *y, w8a8_dtype y_dtype, int64_t M,
+                            int64_t N, int64_t K, w8a8_stream_t stream);
+
+/* The grouped (MoE) form over rows sorted by expert, offsets as in
+ * w8a8_grouped_gemm; qw [E, N, K], sw [E, ceil(N / sw_block_rows), K/128]. */
+w8a8_status w8a8_w8a16_grouped_gemm(const void *a_bf16, int64_t lda, const int32_t *offsets,
+                                    const int8_t *qw, const float *sw, int32_t sw_block_rows,
+                                    void *y, w8a8_dtype y_dtype, int64_t R, int64_t E, int64_t N,
+                                    int64_t K, w8a8_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * MoE expert FFN ("Deploying Hunyuan 770B in INT8 on domestic accelerators":
  * §4.4, tokens are counted per destination expert first and then

@@ -72,6 +72,9 @@ def _load() -> ctypes.CDLL:
                                          vp, vp, ctypes.c_size_t, vp]
     lib.w8a8_linear_ex.argtypes = [vp, i64, i32, vp, vp, i32, vp, i32, i64, i64, i64, vp,
                                    ctypes.c_size_t, vp]
+    lib.w8a8_w8a16_gemm.argtypes = [vp, i64, vp, vp, i32, vp, i32, i64, i64, i64, vp]
+    lib.w8a8_w8a16_grouped_gemm.argtypes = [vp, i64, vp, vp, vp, i32, vp, i32, i64, i64, i64, i64,
+                                            vp]
     lib.w8a8_moe_route.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
     lib.w8a8_quant_act_rows.argtypes = [vp, i64, vp, i64, i64, vp, vp, vp]
     lib.w8a8_swiglu_quant.argtypes = [vp, i64, i64, vp, i64, vp, vp, vp]
@@ -88,7 +91,8 @@ def _load() -> ctypes.CDLL:
                  "w8a8_probe_dp4a_rate", "w8a8_moe_route", "w8a8_quant_act_rows",
                  "w8a8_swiglu_quant", "w8a8_swiglu", "w8a8_moe_unpermute", "w8a8_moe_ffn",
                  "w8a8_quant_act_ex", "w8a8_quant_weight_ex", "w8a8_gemm_ex",
-                 "w8a8_grouped_gemm_ex", "w8a8_linear_ex"):
+                 "w8a8_grouped_gemm_ex", "w8a8_linear_ex", "w8a8_w8a16_gemm",
+                 "w8a8_w8a16_grouped_gemm"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -417,6 +421,60 @@ def grouped_linear(a: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor, sw:
                                         _ptr(out), code, R, E, N, K, _ptr(workspace),
                                         workspace.numel(), _stream(stream)),
                "w8a8_grouped_linear")
+    return out
+
+
+# ------------------------------------------------- weight-only INT8 (W8A16)
+def w8a16_gemm(a: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
+               out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+               sw_block_rows: int = 1,
+               stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Y = a (BF16, not quantized) x dequantized INT8 weights, the group
+    scales applied per group in the epilogue."""
+    lda = _require_act(a)
+    dev = a.device
+    M, K = a.shape
+    _require(qw, torch.int8, "qw", 2, device=dev)
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError(f"qw: expected K = {K} columns, got {qw.shape[1]}")
+    _require(sw, torch.float32, "sw", 2, ((N + sw_block_rows - 1) // sw_block_rows, K // GROUP),
+             dev)
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (M, N), dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_w8a16_gemm(_ptr(a), lda, _ptr(qw), _ptr(sw), sw_block_rows, _ptr(out),
+                                    code, M, N, K, _stream(stream)), "w8a8_w8a16_gemm")
+    return out
+
+
+def w8a16_grouped_gemm(a: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor,
+                       sw: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
+                       out: Optional[torch.Tensor] = None, sw_block_rows: int = 1,
+                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The grouped (MoE expert) weight-only GEMM over rows sorted by expert."""
+    lda = _require_act(a)
+    dev = a.device
+    R, K = a.shape
+    _require(qw, torch.int8, "qw", 3, device=dev)
+    E, N, K2 = qw.shape
+    if K2 != K:
+        raise ValueError(f"qw: expected K = {K} columns, got {K2}")
+    _require(sw, torch.float32, "sw", 3,
+             (E, (N + sw_block_rows - 1) // sw_block_rows, K // GROUP), dev)
+    _require(offsets, torch.int32, "offsets", 1, (E + 1,), dev)
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((R, N), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (R, N), dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_w8a16_grouped_gemm(_ptr(a), lda, _ptr(offsets), _ptr(qw), _ptr(sw),
+                                            sw_block_rows, _ptr(out), code, R, E, N, K,
+                                            _stream(stream)), "w8a8_w8a16_grouped_gemm")
     return out
 
 

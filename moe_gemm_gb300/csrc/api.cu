@@ -512,6 +512,62 @@ w8a8_status w8a8_linear_ex(const void *a_bf16, int64_t lda, w8a8_scale_mode act_
                       workspace_bytes, stream, sw_block_rows, act_mode == W8A8_SCALE_POW2);
 }
 
+// Weight-only INT8 with BF16 activations (no activation quantizer, no
+// workspace): the tensor-core kernels read the activations directly.
+static w8a8_status run_w8a16(const void *a_bf16, int64_t lda, const int32_t *offsets,
+                             const int8_t *qw, const float *sw, int32_t sw_block_rows, void *y,
+                             w8a8_dtype y_dtype, int64_t R, int64_t E, int64_t N, int64_t K,
+                             w8a8_stream_t stream) {
+    const bool grouped = offsets != nullptr;
+    if (y_dtype != W8A8_BF16 && y_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    if (sw_block_rows != 1 && sw_block_rows != 128) return W8A8_ERR_INVALID_ARG;
+    if (R < 0 || N <= 0 || K <= 0 || E <= 0 || K % W8A8_GROUP != 0 || lda < K || lda % 8 != 0)
+        return W8A8_ERR_INVALID_ARG;
+    if (grouped && E > w8a8::kMaxExperts) return W8A8_ERR_INVALID_ARG;
+    if (R > kMaxElems / lda || E * N > kMaxElems / K || R > kMaxElems / N)
+        return W8A8_ERR_INVALID_ARG;
+    if (R == 0) return W8A8_OK;
+    if (!a_bf16 || !qw || !sw || !y || (grouped && !offsets)) return W8A8_ERR_INVALID_ARG;
+    if (!aligned(a_bf16, 16) || !aligned(qw, 16) || !aligned(sw, 4) || !aligned(y, 4) ||
+        (offsets && !aligned(offsets, 4)))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    w8a8::GemmProblem p;
+    p.qa = nullptr;
+    p.sa = nullptr;
+    p.sw = sw;
+    p.qw = qw;
+    p.x16 = a_bf16;
+    p.offsets = offsets;
+    p.y = y;
+    p.debug_partials = nullptr;
+    p.R = R;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.out_fp32 = (y_dtype == W8A8_FP32);
+    p.sw_block_rows = sw_block_rows;
+    p.a16 = true;
+    p.ldx = lda;
+    return from_cuda(w8a8::launch_gemm(p, info.num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_w8a16_gemm(const void *a_bf16, int64_t lda, const int8_t *qw, const float *sw,
+                            int32_t sw_block_rows, void *y, w8a8_dtype y_dtype, int64_t M,
+                            int64_t N, int64_t K, w8a8_stream_t stream) {
+    return run_w8a16(a_bf16, lda, nullptr, qw, sw, sw_block_rows, y, y_dtype, M, 1, N, K, stream);
+}
+
+w8a8_status w8a8_w8a16_grouped_gemm(const void *a_bf16, int64_t lda, const int32_t *offsets,
+                                    const int8_t *qw, const float *sw, int32_t sw_block_rows,
+                                    void *y, w8a8_dtype y_dtype, int64_t R, int64_t E, int64_t N,
+                                    int64_t K, w8a8_stream_t stream) {
+    if (!offsets && R > 0) return W8A8_ERR_INVALID_ARG;
+    return run_w8a16(a_bf16, lda, offsets, qw, sw, sw_block_rows, y, y_dtype, R, E, N, K, stream);
+}
+
 w8a8_status w8a8_moe_route(const int32_t *topk_ids, int64_t T, int64_t k, int64_t E,
                            int32_t *offsets, int32_t *row_of, int32_t *token_of_row,
                            int32_t *pair_of_row, w8a8_stream_t stream) {

@@ -307,6 +307,15 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
            | ((M >> 4) << 24);      // M / 16
 }
 
+// Same for bf16 A and B operands (the weight-only path, BF16 activations).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4)                // D format: f32
+           | (1u << 7)              // A format: bf16
+           | (1u << 10)             // B format: bf16
+           | ((N >> 3) << 17)       // N / 8
+           | ((M >> 4) << 24);      // M / 16
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy accesses (TMA, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -373,6 +382,25 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(u), "r"(0x64646464u));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+// int8 x4 -> two bf16x2 words holding the exact integers (|x| <= 127): the
+// magnitude goes into the low mantissa bits of the bf16 number 128
+// (0x4300 | |x| = 128 + |x|, exact since bf16 has 7 mantissa bits), 128 is
+// subtracted (exact), and each byte's sign bit is copied to its half's sign
+// bit. (x = -128 never occurs: codes are clamped to [-127, 127].)
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t mag = __vabsss4(w);
+    const uint32_t sgn = w & 0x80808080u;
+    uint32_t a, b, sl, sh;
+    asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(mag), "r"(0x43434343u));
+    asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(mag), "r"(0x43434343u));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x43004300u));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x43004300u));
+    asm("prmt.b32 %0, %1, %2, 0x1404;" : "=r"(sl) : "r"(sgn), "r"(0u));
+    asm("prmt.b32 %0, %1, %2, 0x3424;" : "=r"(sh) : "r"(sgn), "r"(0u));
+    lo |= sl;
+    hi |= sh;
 }
 
 }  // namespace w8a8

@@ -133,6 +133,21 @@ struct KParams {
     int sk_ld;          // token columns per partial slot
 };
 
+// The token scale of row m: 1 when the call has none (weight-only path with
+// BF16 activations).
+__device__ __forceinline__ float load_sa(const KParams &p, int m) {
+    return p.sa != nullptr ? load_sa(p, m) : 1.0f;
+}
+
+// int8 x4 -> the MMA's A-operand type: fp16 (kBf16 false) or bf16, exact.
+template <bool kBf16>
+__device__ __forceinline__ void i8x4_to_op(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    if constexpr (kBf16)
+        i8x4_to_bf16x4(w, lo, hi);
+    else
+        i8x4_to_f16x4(w, lo, hi);
+}
+
 struct TileInfo {
     int e, n0, m0, rows;
 };
@@ -410,7 +425,9 @@ static_assert(NBar::count <= 128, "barrier area");
 // for that drain. Each epilogue warpgroup owns two 32-column chunks; the tile
 // table lives in the fixed area so that the weight stages fit beside the two
 // token stages.
-template <bool kDebug, bool kWide>
+// kA16: weight-only form: BF16 activations are the token operand (no token
+// scale), weights are widened to bf16.
+template <bool kDebug, bool kWide, bool kA16 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
@@ -547,7 +564,8 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             for_each_piece(plan, [&](int t, int s0, int s1) -> bool {
                 const TileInfo ti = decode_tile(t, s_base, s_lo, s_cnt, p.E, tt, p.n_tiles, p.gw);
                 const int n_eff = (ti.rows + 15) & ~15;
-                const uint32_t idesc = idesc_f16_f32(kTileN, static_cast<uint32_t>(n_eff));
+                const uint32_t idesc = kA16 ? idesc_bf16_f32(kTileN, static_cast<uint32_t>(n_eff))
+                                            : idesc_f16_f32(kTileN, static_cast<uint32_t>(n_eff));
                 for (int sg = s0; sg < s1; ++sg) {
                     const int g0 = 2 * sg;
                     const int ng = min(2, G - g0);
@@ -737,10 +755,10 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             const int c = 2 * jj + cc;
                             const uint4 v =
                                 *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
-                            i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
-                            i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
-                            i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
-                            i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
+                            i8x4_to_op<kA16>(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
+                            i8x4_to_op<kA16>(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
+                            i8x4_to_op<kA16>(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
+                            i8x4_to_op<kA16>(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
                         }
                         tmem_st_16cols(taddr + jj * 16, r16);
                     }
@@ -765,7 +783,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
         auto store_out = [&](int m, int n_local, float v) {
-            const float out = v * __ldg(p.sa + m);
+            const float out = v * load_sa(p, m);
             const size_t idx = static_cast<size_t>(m) * p.N + n_local;
             if (p.out_fp32)
                 static_cast<float *>(p.y)[idx] = out;
@@ -822,7 +840,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 for (int j = 0; j < 32; ++j) {
                     if (j < ti.rows) {
                         const size_t idx = static_cast<size_t>(ti.m0 + j) * p.N + n_local;
-                        const float out = sum[j] * __ldg(p.sa + ti.m0 + j);
+                        const float out = sum[j] * load_sa(p, ti.m0 + j);
                         if (p.out_fp32)
                             static_cast<float *>(p.y)[idx] = out;
                         else
@@ -1037,7 +1055,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     float sa_r[32], sum[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        sa_r[j] = kDebug ? 0.0f : __ldg(p.sa + ti.m0 + min(col0 + j, ti.rows - 1));
+                        sa_r[j] = kDebug ? 0.0f : load_sa(p, ti.m0 + min(col0 + j, ti.rows - 1));
                         sum[j] = 0.0f;
                     }
                     for (int c = c_first; c <= c_final; ++c) {   // K order
@@ -1060,7 +1078,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             const size_t idx =
                                 static_cast<size_t>(ti.m0 + col0 + j) * p.N + n_local;
                             const float out =
-                                sum[j] * (kDebug ? __ldg(p.sa + ti.m0 + col0 + j) : sa_r[j]);
+                                sum[j] * (kDebug ? load_sa(p, ti.m0 + col0 + j) : sa_r[j]);
                             if (p.out_fp32)
                                 static_cast<float *>(p.y)[idx] = out;
                             else
@@ -1133,7 +1151,7 @@ struct W2Bar {
 };
 static_assert(W2Bar::count <= 128, "barrier area");
 
-template <bool kDebug>
+template <bool kDebug, bool kA16 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                       const __grid_constant__ CUtensorMap tmap_x, const KParams p) {
@@ -1224,7 +1242,8 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             Ring b, sl;
             uint32_t dph = 0;
             bool ok = true;
-            const uint32_t idesc = idesc_f16_f32(kTileN, kW2Tokens);
+            const uint32_t idesc =
+                kA16 ? idesc_bf16_f32(kTileN, kW2Tokens) : idesc_f16_f32(kTileN, kW2Tokens);
             for (int t = blockIdx.x; t < total && ok; t += grid) {
                 for (int g = 0; g < G; ++g) {
                     if (!mbar_wait(bar(W2Bar::a_ready + sl.idx), sl.phase, s_abort, p.err,
@@ -1307,10 +1326,10 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     for (int cc = 0; cc < 2; ++cc) {
                         const int c = 2 * jj + cc;
                         const uint4 v = *reinterpret_cast<const uint4 *>(rowp + ((c ^ (row & 7)) << 4));
-                        i8x4_to_f16x4(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
-                        i8x4_to_f16x4(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
-                        i8x4_to_f16x4(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
-                        i8x4_to_f16x4(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
+                        i8x4_to_op<kA16>(v.x, r16[cc * 8 + 0], r16[cc * 8 + 1]);
+                        i8x4_to_op<kA16>(v.y, r16[cc * 8 + 2], r16[cc * 8 + 3]);
+                        i8x4_to_op<kA16>(v.z, r16[cc * 8 + 4], r16[cc * 8 + 5]);
+                        i8x4_to_op<kA16>(v.w, r16[cc * 8 + 6], r16[cc * 8 + 7]);
                     }
                     tmem_st_16cols(taddr + jj * 16, r16);
                 }
@@ -1384,13 +1403,13 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 // the token-scale loads are not all hoisted ahead of the
                 // stores (registers).
                 const int rows_here = ti.rows - col0;
-                const float *sap = p.sa + ti.m0 + col0;
+                const float *sap = p.sa != nullptr ? p.sa + ti.m0 + col0 : nullptr;
                 const size_t first = static_cast<size_t>(ti.m0 + col0) * p.N + n_local;
                 if (p.out_fp32) {
                     float *yp = static_cast<float *>(p.y) + first;
 #pragma unroll
                     for (int j = 0; j < 128; ++j) {
-                        if (j < rows_here) *yp = acc[j] * __ldg(sap + j);
+                        if (j < rows_here) *yp = acc[j] * (sap != nullptr ? __ldg(sap + j) : 1.0f);
                         yp += p.N;
                         if ((j & 15) == 15) asm volatile("" ::: "memory");
                     }
@@ -1398,7 +1417,8 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     __nv_bfloat16 *yp = static_cast<__nv_bfloat16 *>(p.y) + first;
 #pragma unroll
                     for (int j = 0; j < 128; ++j) {
-                        if (j < rows_here) *yp = __float2bfloat16_rn(acc[j] * __ldg(sap + j));
+                        if (j < rows_here)
+                            *yp = __float2bfloat16_rn(acc[j] * (sap != nullptr ? __ldg(sap + j) : 1.0f));
                         yp += p.N;
                         if ((j & 15) == 15) asm volatile("" ::: "memory");
                     }
@@ -1787,7 +1807,7 @@ w8a8_gemv_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
             auto store_out = [&](int i, int u, float v) {
                 const int m = tb * RM + u;
-                const float out = v * (kFuseQ ? s_tok[u] : __ldg(p.sa + ti.m0 + m));
+                const float out = v * (kFuseQ ? s_tok[u] : load_sa(p, ti.m0 + m));
                 const size_t idx = static_cast<size_t>(ti.m0 + m) * p.N + n_row[i];
                 if (p.out_fp32)
                     static_cast<float *>(p.y)[idx] = out;
@@ -1847,6 +1867,23 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, size_t elem_bytes, c
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The token operand: fp16 codes [R, K] (dense rows) or, for the weight-only
+// path, the caller's BF16 activations [R, ldx] (rows ldx elements apart).
+bool encode_tokens(CUtensorMap *map, const GemmProblem &pr, uint32_t box_rows) {
+    auto fn = get_encode_fn();
+    if (fn == nullptr) return false;
+    const uint64_t pitch = static_cast<uint64_t>(pr.ldx > 0 ? pr.ldx : pr.K);
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(pr.K), static_cast<cuuint64_t>(pr.R)};
+    cuuint64_t strides[1] = {pitch * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, pr.a16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          2, const_cast<void *>(pr.x16), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1919,8 +1956,7 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     CUtensorMap tw, tx;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
                    (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
-        !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x16, (uint64_t)pr.K,
-                   (uint64_t)pr.R, 64, kBoxRows))
+        !encode_tokens(&tx, pr, kBoxRows))
         return cudaErrorInvalidValue;
 
     static int attr_done[64] = {0};   // per device, per kernel instance
@@ -2006,8 +2042,7 @@ cudaError_t launch_wide(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     CUtensorMap tw, tx;
     if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, pr.qw, (uint64_t)pr.K,
                    (uint64_t)(pr.E * pr.N), kGroupK, kTileN) ||
-        !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.x16, (uint64_t)pr.K,
-                   (uint64_t)pr.R, 64, kW2Tokens))
+        !encode_tokens(&tx, pr, kW2Tokens))
         return cudaErrorInvalidValue;
     static int attr_done[64] = {0};   // per device, per kernel instance
     int dev = 0;
@@ -2157,6 +2192,20 @@ cudaError_t launch_gemv_mr(const GemmProblem &pr, int num_sms, cudaStream_t stre
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem &pr, int num_sms, cudaStream_t stream) {
+    if (pr.a16) {
+        // weight-only path: tensor-core kernels only, no debug partials, no K split
+        if (pr.debug_partials != nullptr || pr.sk_cnt != nullptr)
+            return cudaErrorInvalidValue;
+        if (uses_wide256(pr.R, pr.offsets != nullptr))
+            return launch_wide<w8a8_gemm_wide_kernel<false, true>>(pr, num_sms, stream);
+        const PipeShape ps = choose_pipe(pr);
+        if (ps.wide) {
+            if (pr.E > kWideMaxExperts) return cudaErrorInvalidConfiguration;
+            return launch_kernel<w8a8_gemm_narrow_kernel<false, true, true>>(pr, ps, num_sms,
+                                                                              stream);
+        }
+        return launch_kernel<w8a8_gemm_narrow_kernel<false, false, true>>(pr, ps, num_sms, stream);
+    }
     if (uses_gemv(pr.R, pr.offsets != nullptr)) {
         if (pr.R <= 1) return launch_gemv_mr<1, 1, 8>(pr, num_sms, stream);
         if (pr.R <= 2) return launch_gemv_mr<1, 2, 8>(pr, num_sms, stream);

@@ -78,6 +78,10 @@ struct GemmProblem {
     // Stream-K split of dense calls; null sk_cnt: whole tiles only.
     // Weight scales per [sw_block_rows x 128] block: 1 (per row) or 128.
     int sw_block_rows = 1;
+    // Weight-only path: x16 holds the caller's BF16 activations (row stride
+    // ldx elements), sa is null (no token scale).
+    bool a16 = false;
+    int64_t ldx = 0;
     int *sk_cnt = nullptr;        // [2 * kSkMaxCtas] counters, zeroed before the GEMM
     float *sk_part = nullptr;     // [kSkMaxCtas][2][sk_ld][128] FP32 partials
     int sk_ld = 0;
