@@ -136,7 +136,7 @@ struct KParams {
 // The token scale of row m: 1 when the call has none (weight-only path with
 // BF16 activations).
 __device__ __forceinline__ float load_sa(const KParams &p, int m) {
-    return p.sa != nullptr ? load_sa(p, m) : 1.0f;
+    return p.sa != nullptr ? __ldg(p.sa + m) : 1.0f;
 }
 
 // int8 x4 -> the MMA's A-operand type: fp16 (kBf16 false) or bf16, exact.

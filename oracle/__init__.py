@@ -78,6 +78,9 @@ def _load():
         lib.oracle_quant_weight_blocks.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
         lib.oracle_gemm_blocks.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p]
         lib.oracle_w8a16_gemm.argtypes = [p, p, p, i64, i64, i64, i64, p, p]
+        lib.oracle_kv_dequant.argtypes = [p, p, i64, i64, p]
+        lib.oracle_attention_decode.argtypes = [p, p, p, p, i64, i64, i64, i64, i64,
+                                                ctypes.c_double, p, p]
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_group_size.restype = ctypes.c_int
@@ -346,3 +349,43 @@ def w8a16_gemm(a_bf16: np.ndarray, qw: np.ndarray, sw: np.ndarray,
     T = np.empty((M, N), dtype=np.float64)
     _load().oracle_w8a16_gemm(_ptr(a), _ptr(qw), _ptr(sw), M, N, K, block_rows, _ptr(y), _ptr(T))
     return y, T
+
+
+# ------------------------------------------------- INT8 KV cache + attention
+def kv_quant(x_bf16: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-vector quantization of K or V vectors [..., D] (BF16 bit patterns):
+    one scale per vector, exactly the per-token activation quantizer."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    D = x.shape[-1]
+    q, s = quant_act(x.reshape(-1, D))
+    return q.reshape(x.shape), s.reshape(x.shape[:-1])
+
+
+def kv_dequant(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """q * s per vector (FP64, exact)."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    D = q.shape[-1]
+    n = q.size // D
+    out = np.empty(q.shape, dtype=np.float64)
+    _load().oracle_kv_dequant(_ptr(q), _ptr(s), n, D, _ptr(out))
+    return out
+
+
+def attention_decode(q_bf16: np.ndarray, K: np.ndarray, V: np.ndarray, lens: np.ndarray,
+                     scale: float) -> Tuple[np.ndarray, np.ndarray]:
+    """Decode attention (one query per sequence, grouped-query heads) in FP64:
+    q [B, Hq, D] BF16 bits, K and V [B, Hkv, S_max, D] (FP64 values), lens [B].
+    Returns (out [B, Hq, D], T [B, Hq, D])."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    K = np.ascontiguousarray(K, dtype=np.float64)
+    V = np.ascontiguousarray(V, dtype=np.float64)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    _, Hkv, S_max, D2 = K.shape
+    assert D2 == D and Hq % Hkv == 0 and V.shape == K.shape and lens.shape == (B,)
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    T = np.empty((B, Hq, D), dtype=np.float64)
+    _load().oracle_attention_decode(_ptr(q), _ptr(K), _ptr(V), _ptr(lens), B, Hq, Hkv, S_max, D,
+                                    float(scale), _ptr(out), _ptr(T))
+    return out, T

@@ -474,3 +474,66 @@ void oracle_w8a16_gemm(const uint16_t *a, const int8_t *qw, const float *sw, int
         }
     }
 }
+
+/* ======================================================================
+ * INT8 KV cache with per-token dynamic scales, dequantized inside attention
+ * ("Deploying Hunyuan 770B in INT8 on domestic accelerators", §3.4: one
+ * scale per key/value vector, computed when the vector is written; the
+ * attention kernel reads the INT8 data and applies the scales itself; §2.2:
+ * the cache is 2 x layers x kv_heads x head_dim x seq_len x batch elements).
+ * The quantization of one K or V vector is oracle_quant_act on a row of
+ * head_dim values.
+ * ====================================================================== */
+
+/* Dequantized vectors: out[i, d] = q[i, d] * s[i] (exact in FP64). */
+void oracle_kv_dequant(const int8_t *q, const float *s, int64_t n, int64_t D, double *out) {
+    for (int64_t i = 0; i < n; i++)
+        for (int64_t d = 0; d < D; d++) out[i * D + d] = (double)q[i * D + d] * (double)s[i];
+}
+
+/* Decode attention of one query token per sequence, grouped-query: query
+ * head hq reads kv head hq / (Hq / Hkv). K, V [B, Hkv, S_max, D] (FP64
+ * values), lens [B] valid positions, q [B, Hq, D] BF16 bit patterns:
+ *   s_j = scale * sum_d q_d k_{j,d},  p_j = exp(s_j - max_j s_j),
+ *   out_d = sum_j p_j v_{j,d} / sum_j p_j   over j < lens[b]   (FP64),
+ * and T_d = sum_j p_j |v_{j,d}| / sum_j p_j (the magnitude the error of an
+ * implementation is measured against). lens[b] == 0 gives 0. */
+void oracle_attention_decode(const uint16_t *q, const double *K, const double *V,
+                             const int32_t *lens, int64_t B, int64_t Hq, int64_t Hkv,
+                             int64_t S_max, int64_t D, double scale, double *out, double *T) {
+    const int64_t G = Hq / Hkv;
+#pragma omp parallel for schedule(static)
+    for (int64_t bh = 0; bh < B * Hq; bh++) {
+        const int64_t b = bh / Hq, hq = bh % Hq, h = hq / G;
+        const int64_t L = lens[b] < 0 ? 0 : (lens[b] > S_max ? S_max : lens[b]);
+        const uint16_t *qv = q + bh * D;
+        const double *Kb = K + (b * Hkv + h) * S_max * D;
+        const double *Vb = V + (b * Hkv + h) * S_max * D;
+        double *o = out + bh * D;
+        double *t = T + bh * D;
+        for (int64_t d = 0; d < D; d++) o[d] = t[d] = 0.0;
+        if (L == 0) continue;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < L; j++) {
+            double sj = 0.0;
+            for (int64_t d = 0; d < D; d++) sj += (double)bf16_bits_to_float(qv[d]) * Kb[j * D + d];
+            sj *= scale;
+            if (sj > m) m = sj;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < L; j++) {
+            double sj = 0.0;
+            for (int64_t d = 0; d < D; d++) sj += (double)bf16_bits_to_float(qv[d]) * Kb[j * D + d];
+            const double pj = exp(sj * scale - m);
+            l += pj;
+            for (int64_t d = 0; d < D; d++) {
+                o[d] += pj * Vb[j * D + d];
+                t[d] += pj * fabs(Vb[j * D + d]);
+            }
+        }
+        for (int64_t d = 0; d < D; d++) {
+            o[d] /= l;
+            t[d] /= l;
+        }
+    }
+}
