@@ -385,6 +385,62 @@ w8a8_status w8a8_moe_ffn(const void *x_bf16, int64_t ldx, const int32_t *topk_id
                          const int8_t *qw_down, const float *sw_down, void *y, w8a8_dtype y_dtype,
                          void *workspace, size_t workspace_bytes, w8a8_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * INT8 KV cache ("Deploying Hunyuan 770B in INT8 on domestic accelerators",
+ * §3.4: the KV cache is quantized to INT8 with a dynamic scale per key/value
+ * vector, and the attention kernel dequantizes while it reads the cache
+ * instead of running a separate dequantization pass; §2.2: the cache holds
+ * 2 x layers x kv_heads x head_dim x seq_len x batch elements). One layer's
+ * cache here: K and V [B, Hkv, S_max, head_dim] (row-major; one row per
+ * vector), and for the INT8 form the scales [B, Hkv, S_max]. head_dim = 128.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Writes n K or V vectors into an INT8 cache: vector i (x_bf16 [n, head_dim]
+ * BF16) gets scale amax / 127 and codes clamp(round-half-even(x / scale)),
+ * exactly as w8a8_quant_act, stored in row dst_rows[i] of cache [rows,
+ * head_dim] int8 and scales [rows] (dst_rows NULL: row i; a negative entry:
+ * not written). The caller maps (sequence, kv head, position) to a row, e.g.
+ * (b * Hkv + h) * S_max + pos.
+ */
+w8a8_status w8a8_kv_quant(const void *x_bf16, int64_t n, int64_t head_dim,
+                          const int32_t *dst_rows, int8_t *cache, float *scales,
+                          w8a8_stream_t stream);
+
+/* Bytes of workspace the decode attention calls need: per (sequence, query
+ * head, chunk of 128 positions) a partial output and two statistics (FP32). */
+size_t w8a8_attention_decode_workspace_size(int64_t B, int64_t Hq, int64_t S_max,
+                                            int64_t head_dim);
+
+/*
+ * Decode attention of one query token per sequence over the INT8 cache,
+ * grouped-query heads (query head hq reads kv head hq / (Hq / Hkv), Hq / Hkv
+ * in {1, 2, 4, 8, 16}):
+ *   s_j = softmax_scale * k_scale[j] * sum_d q[d] * k_code[j, d],
+ *   out[d] = sum_j softmax(s)_j * v_scale[j] * v_code[j, d],  j < lens[b].
+ * q [B, Hq, head_dim] BF16; lens [B] int32 on the device (clamped to
+ * [0, S_max]; 0 gives zeros); out [B, Hq, head_dim] BF16 or FP32. Every
+ * product and sum is FP32; a CTA handles 128 positions and the partial
+ * softmax results are merged with max/sum rescaling (exact in real
+ * arithmetic). Asynchronous, no host read of device data.
+ */
+w8a8_status w8a8_attention_decode_int8kv(const void *q_bf16, const int8_t *k_cache,
+                                         const float *k_scale, const int8_t *v_cache,
+                                         const float *v_scale, const int32_t *lens, int64_t B,
+                                         int64_t Hq, int64_t Hkv, int64_t S_max,
+                                         int64_t head_dim, float softmax_scale, void *out,
+                                         w8a8_dtype out_dtype, void *workspace,
+                                         size_t workspace_bytes, w8a8_stream_t stream);
+
+/* The same attention over a BF16 cache (the unquantized baseline the fused
+ * dequantization is measured against). */
+w8a8_status w8a8_attention_decode_bf16kv(const void *q_bf16, const void *k_cache,
+                                         const void *v_cache, const int32_t *lens, int64_t B,
+                                         int64_t Hq, int64_t Hkv, int64_t S_max,
+                                         int64_t head_dim, float softmax_scale, void *out,
+                                         w8a8_dtype out_dtype, void *workspace,
+                                         size_t workspace_bytes, w8a8_stream_t stream);
+
 /*
  * Size of the scratch array built into the library for w8a8_gemm_noalloc:
  * 8 MiB, enough for M * K <= 4,194,304 activation codes (e.g. M <= 512 at

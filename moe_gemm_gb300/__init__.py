@@ -75,6 +75,13 @@ def _load() -> ctypes.CDLL:
     lib.w8a8_w8a16_gemm.argtypes = [vp, i64, vp, vp, i32, vp, i32, i64, i64, i64, vp]
     lib.w8a8_w8a16_grouped_gemm.argtypes = [vp, i64, vp, vp, vp, i32, vp, i32, i64, i64, i64, i64,
                                             vp]
+    lib.w8a8_kv_quant.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+    lib.w8a8_attention_decode_workspace_size.argtypes = [i64, i64, i64, i64]
+    lib.w8a8_attention_decode_workspace_size.restype = ctypes.c_size_t
+    lib.w8a8_attention_decode_int8kv.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                 ctypes.c_float, vp, i32, vp, ctypes.c_size_t, vp]
+    lib.w8a8_attention_decode_bf16kv.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                 ctypes.c_float, vp, i32, vp, ctypes.c_size_t, vp]
     lib.w8a8_moe_route.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
     lib.w8a8_quant_act_rows.argtypes = [vp, i64, vp, i64, i64, vp, vp, vp]
     lib.w8a8_swiglu_quant.argtypes = [vp, i64, i64, vp, i64, vp, vp, vp]
@@ -92,7 +99,8 @@ def _load() -> ctypes.CDLL:
                  "w8a8_swiglu_quant", "w8a8_swiglu", "w8a8_moe_unpermute", "w8a8_moe_ffn",
                  "w8a8_quant_act_ex", "w8a8_quant_weight_ex", "w8a8_gemm_ex",
                  "w8a8_grouped_gemm_ex", "w8a8_linear_ex", "w8a8_w8a16_gemm",
-                 "w8a8_w8a16_grouped_gemm"):
+                 "w8a8_w8a16_grouped_gemm", "w8a8_kv_quant", "w8a8_attention_decode_int8kv",
+                 "w8a8_attention_decode_bf16kv"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -475,6 +483,86 @@ def w8a16_grouped_gemm(a: torch.Tensor, offsets: torch.Tensor, qw: torch.Tensor,
         _check(_lib.w8a8_w8a16_grouped_gemm(_ptr(a), lda, _ptr(offsets), _ptr(qw), _ptr(sw),
                                             sw_block_rows, _ptr(out), code, R, E, N, K,
                                             _stream(stream)), "w8a8_w8a16_grouped_gemm")
+    return out
+
+
+# ------------------------------------------------- INT8 KV cache + attention
+HEAD_DIM = 128
+
+
+def kv_quant(x: torch.Tensor, cache: torch.Tensor, scales: torch.Tensor,
+             dst_rows: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Quantizes K or V vectors x [n, 128] (BF16) into rows dst_rows (or 0..n-1)
+    of cache (int8, last dim 128) with one scale per row in scales."""
+    _require(x, torch.bfloat16, "x", 2)
+    dev = x.device
+    n, D = x.shape
+    if not cache.is_cuda or cache.dtype != torch.int8 or not cache.is_contiguous() \
+            or cache.shape[-1] != D or cache.device != dev:
+        raise ValueError("cache: expected a contiguous int8 CUDA tensor with last dim 128")
+    rows = cache.numel() // D
+    if not scales.is_cuda or scales.dtype != torch.float32 or not scales.is_contiguous() \
+            or scales.numel() != rows or scales.device != dev:
+        raise ValueError("scales: expected one float32 per cache row")
+    if dst_rows is not None:
+        _require(dst_rows, torch.int32, "dst_rows", 1, (n,), dev)
+    elif n > rows:
+        raise ValueError("more vectors than cache rows")
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_kv_quant(_ptr(x), n, D, _ptr(dst_rows), _ptr(cache), _ptr(scales),
+                                  _stream(stream)), "w8a8_kv_quant")
+
+
+def attention_decode_workspace_size(B: int, Hq: int, S_max: int) -> int:
+    return int(_lib.w8a8_attention_decode_workspace_size(B, Hq, S_max, HEAD_DIM))
+
+
+def attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     lens: torch.Tensor, softmax_scale: float,
+                     k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                     out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode attention of q [B, Hq, 128] over a KV cache [B, Hkv, S_max, 128]:
+    INT8 codes with per-vector scales k_scale / v_scale [B, Hkv, S_max], or a
+    BF16 cache (no scales); lens [B] int32 on the device."""
+    _require(q, torch.bfloat16, "q", 3)
+    dev = q.device
+    B, Hq, D = q.shape
+    int8 = k_cache.dtype == torch.int8
+    dt = torch.int8 if int8 else torch.bfloat16
+    _require(k_cache, dt, "k_cache", 4, device=dev)
+    _, Hkv, S_max, D2 = k_cache.shape
+    if D2 != D or k_cache.shape[0] != B:
+        raise ValueError("k_cache must be [B, Hkv, S_max, 128]")
+    _require(v_cache, dt, "v_cache", 4, tuple(k_cache.shape), dev)
+    if int8:
+        _require(k_scale, torch.float32, "k_scale", 3, (B, Hkv, S_max), dev)
+        _require(v_scale, torch.float32, "v_scale", 3, (B, Hkv, S_max), dev)
+    _require(lens, torch.int32, "lens", 1, (B,), dev)
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=dev)
+    elif (not out.is_cuda or out.dtype != out_dtype or tuple(out.shape) != (B, Hq, D)
+          or not out.is_contiguous() or out.device != dev):
+        raise ValueError(f"out: expected a contiguous {out_dtype} tensor of shape {(B, Hq, D)}")
+    if workspace is None:
+        workspace = torch.empty(max(attention_decode_workspace_size(B, Hq, S_max), 1),
+                                dtype=torch.uint8, device=dev)
+    else:
+        _require_workspace(workspace, dev)
+    with _on_device(dev, stream):
+        if int8:
+            _check(_lib.w8a8_attention_decode_int8kv(
+                _ptr(q), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale), _ptr(lens),
+                B, Hq, Hkv, S_max, D, float(softmax_scale), _ptr(out), code, _ptr(workspace),
+                workspace.numel(), _stream(stream)), "w8a8_attention_decode_int8kv")
+        else:
+            _check(_lib.w8a8_attention_decode_bf16kv(
+                _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), B, Hq, Hkv, S_max, D,
+                float(softmax_scale), _ptr(out), code, _ptr(workspace), workspace.numel(),
+                _stream(stream)), "w8a8_attention_decode_bf16kv")
     return out
 
 

@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libw8a8.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "probe.cu", "moe.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "probe.cu", "moe.cu", "attention.cu"]
 HEADERS = ["common.cuh", "quant_math.cuh", "internal.h"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 NVCC_FLAGS = [GENCODE, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",

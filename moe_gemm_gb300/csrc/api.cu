@@ -568,6 +568,98 @@ w8a8_status w8a8_w8a16_grouped_gemm(const void *a_bf16, int64_t lda, const int32
     return run_w8a16(a_bf16, lda, offsets, qw, sw, sw_block_rows, y, y_dtype, R, E, N, K, stream);
 }
 
+w8a8_status w8a8_kv_quant(const void *x_bf16, int64_t n, int64_t head_dim,
+                          const int32_t *dst_rows, int8_t *cache, float *scales,
+                          w8a8_stream_t stream) {
+    if (n < 0 || head_dim != w8a8::kAttnHeadDim || n > kMaxElems / head_dim)
+        return W8A8_ERR_INVALID_ARG;
+    if (n == 0) return W8A8_OK;
+    if (!x_bf16 || !cache || !scales || !aligned(x_bf16, 8) || !aligned(cache, 4) ||
+        !aligned(scales, 4) || !aligned(dst_rows, 4))
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_kv_quant(static_cast<const uint16_t *>(x_bf16), n, dst_rows,
+                                           cache, scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t w8a8_attention_decode_workspace_size(int64_t B, int64_t Hq, int64_t S_max,
+                                            int64_t head_dim) {
+    if (B <= 0 || Hq <= 0 || S_max <= 0 || head_dim != w8a8::kAttnHeadDim) return 0;
+    return w8a8::attn_workspace_bytes(B, Hq, S_max);
+}
+
+static w8a8_status run_attention(const void *q_bf16, const void *kc, const float *ks,
+                                 const void *vc, const float *vs, const int32_t *lens, int64_t B,
+                                 int64_t Hq, int64_t Hkv, int64_t S_max, int64_t head_dim,
+                                 float softmax_scale, void *out, w8a8_dtype out_dtype,
+                                 void *workspace, size_t workspace_bytes, bool int8,
+                                 w8a8_stream_t stream) {
+    if (out_dtype != W8A8_BF16 && out_dtype != W8A8_FP32) return W8A8_ERR_INVALID_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || S_max <= 0 ||
+        head_dim != w8a8::kAttnHeadDim)
+        return W8A8_ERR_INVALID_ARG;
+    const int64_t G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return W8A8_ERR_INVALID_ARG;
+    if (B > 65535 || Hkv > 65535 || S_max > (int64_t(1) << 24) ||
+        B * Hkv > kMaxElems / (S_max * head_dim) || !(softmax_scale > 0.0f))
+        return W8A8_ERR_INVALID_ARG;
+    if (B == 0) return W8A8_OK;
+    if (!q_bf16 || !kc || !vc || !lens || !out || (int8 && (!ks || !vs)))
+        return W8A8_ERR_INVALID_ARG;
+    if (!aligned(q_bf16, 2) || !aligned(kc, 16) || !aligned(vc, 16) || !aligned(ks, 4) ||
+        !aligned(vs, 4) || !aligned(lens, 4) || !aligned(out, 4))
+        return W8A8_ERR_INVALID_ARG;
+    const size_t need = w8a8::attn_workspace_bytes(B, Hq, S_max);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return W8A8_ERR_WORKSPACE;
+    w8a8::DeviceInfo info;
+    w8a8_status st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    w8a8::AttnProblem p;
+    p.q = static_cast<const uint16_t *>(q_bf16);
+    p.kc = kc;
+    p.vc = vc;
+    p.ks = ks;
+    p.vs = vs;
+    p.lens = lens;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.S_max = S_max;
+    p.scale = softmax_scale;
+    p.int8 = int8;
+    p.out = out;
+    p.out_fp32 = (out_dtype == W8A8_FP32);
+    const int64_t nch = (S_max + 127) / 128;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_ml = p.part_o + B * Hq * nch * head_dim;
+    return from_cuda(w8a8::launch_attention_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_attention_decode_int8kv(const void *q_bf16, const int8_t *k_cache,
+                                         const float *k_scale, const int8_t *v_cache,
+                                         const float *v_scale, const int32_t *lens, int64_t B,
+                                         int64_t Hq, int64_t Hkv, int64_t S_max,
+                                         int64_t head_dim, float softmax_scale, void *out,
+                                         w8a8_dtype out_dtype, void *workspace,
+                                         size_t workspace_bytes, w8a8_stream_t stream) {
+    return run_attention(q_bf16, k_cache, k_scale, v_cache, v_scale, lens, B, Hq, Hkv, S_max,
+                         head_dim, softmax_scale, out, out_dtype, workspace, workspace_bytes, true,
+                         stream);
+}
+
+w8a8_status w8a8_attention_decode_bf16kv(const void *q_bf16, const void *k_cache,
+                                         const void *v_cache, const int32_t *lens, int64_t B,
+                                         int64_t Hq, int64_t Hkv, int64_t S_max,
+                                         int64_t head_dim, float softmax_scale, void *out,
+                                         w8a8_dtype out_dtype, void *workspace,
+                                         size_t workspace_bytes, w8a8_stream_t stream) {
+    return run_attention(q_bf16, k_cache, nullptr, v_cache, nullptr, lens, B, Hq, Hkv, S_max,
+                         head_dim, softmax_scale, out, out_dtype, workspace, workspace_bytes,
+                         false, stream);
+}
+
 w8a8_status w8a8_moe_route(const int32_t *topk_ids, int64_t T, int64_t k, int64_t E,
                            int32_t *offsets, int32_t *row_of, int32_t *token_of_row,
                            int32_t *pair_of_row, w8a8_stream_t stream) {

@@ -124,6 +124,28 @@ inline size_t sk_area_bytes(int64_t R, bool grouped) {
 constexpr int kWide256MinRows = 256;
 inline bool uses_wide256(int64_t R, bool grouped) { return !grouped && R >= kWide256MinRows; }
 
+// Decode attention over a KV cache [B, Hkv, S_max, 128] (attention.cu): INT8
+// codes with one scale per vector (ks, vs [B, Hkv, S_max]), or BF16 values.
+struct AttnProblem {
+    const uint16_t *q;      // [B, Hq, 128] BF16
+    const void *kc, *vc;    // caches
+    const float *ks, *vs;   // INT8 caches: per-vector scales
+    const int32_t *lens;    // [B] device
+    int64_t B, Hq, Hkv, S_max;
+    float scale;
+    bool int8;
+    void *out;              // [B, Hq, 128]
+    bool out_fp32;
+    float *part_o, *part_ml;   // workspace: per-chunk partial outputs and statistics
+};
+constexpr int kAttnHeadDim = 128;
+size_t attn_workspace_bytes(int64_t B, int64_t Hq, int64_t S_max);
+cudaError_t launch_attention_decode(const AttnProblem &p, cudaStream_t stream);
+// Quantizes n vectors of 128 BF16 values into rows dst_rows[i] (or i) of an
+// INT8 cache [rows, 128] with one scale per row.
+cudaError_t launch_kv_quant(const uint16_t *x, int64_t n, const int32_t *dst_rows, int8_t *cache,
+                            float *scales, cudaStream_t stream);
+
 // Maximum number of experts a grouped call may have.
 constexpr int kMaxExperts = 1024;
 

@@ -306,3 +306,46 @@ def moe_gate_weights(spec: MoESpec, seed: int = DEFAULT_SEED) -> np.ndarray:
     rng = _rng(seed, spec.tag, "gate_weight", 0)
     w = rng.uniform(0.05, 1.0, size=(spec.T, spec.topk))
     return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+# ---------------------------------------------------- INT8 KV cache decode
+@dataclass(frozen=True)
+class AttnSpec:
+    """Decode attention over one layer's KV cache: B sequences of S positions
+    each (all full), Hq query heads sharing Hkv kv heads, head dim D. The
+    page's common configuration is a batch of 32 at a 4096-token context
+    ("Deploying Hunyuan 770B in INT8 on domestic accelerators", §2.2); the
+    head counts are a grouped-query shape of that model class."""
+    name: str
+    tag: int
+    B: int
+    Hq: int
+    Hkv: int
+    S: int
+    D: int = 128
+    k_outlier_frac: float = 0.02        # K channels scaled (keys carry channel outliers)
+    k_outlier_scale: float = 8.0
+
+
+ATTN: Dict[str, AttnSpec] = {
+    "decode": AttnSpec("decode", 60, B=32, Hq=64, Hkv=8, S=4096),
+}
+
+
+def attn_inputs(spec: AttnSpec, seed: int = DEFAULT_SEED):
+    """q [B, Hq, D], k and v [B, Hkv, S, D] as BF16 bit patterns: N(0,1) draws,
+    a fixed round(k_outlier_frac * D) K channels scaled by k_outlier_scale."""
+    rng = _rng(seed, spec.tag, "act", 0)
+    q = f32_to_bf16_bits(rng.standard_normal((spec.B, spec.Hq, spec.D), dtype=np.float32))
+    ch = np.sort(_rng(seed, spec.tag, "outlier_channels").choice(
+        spec.D, size=int(round(spec.k_outlier_frac * spec.D)), replace=False))
+    k = np.empty((spec.B, spec.Hkv, spec.S, spec.D), dtype=np.uint16)
+    v = np.empty_like(k)
+    for b in range(spec.B):
+        kb = _rng(seed, spec.tag, "weight", b).standard_normal(
+            (spec.Hkv, spec.S, spec.D), dtype=np.float32)
+        kb[..., ch] *= np.float32(spec.k_outlier_scale)
+        k[b] = f32_to_bf16_bits(kb)
+        v[b] = f32_to_bf16_bits(_rng(seed, spec.tag, "weight_down", b).standard_normal(
+            (spec.Hkv, spec.S, spec.D), dtype=np.float32))
+    return q, k, v
