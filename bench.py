@@ -12,7 +12,9 @@ A default run measures every workload and prints one JSON line:
     16x1024x1024, decode M in {1, 8, 32} x 8192 x 28672, prefill
     4096x8192x8192, MoE grouped (64 experts, top-8 of 512 tokens; gate_up
     3072x4096 and down 4096x1536), the whole MoE expert FFN of those 512
-    tokens (routing, both grouped GEMMs, SwiGLU, un-permute) and stress, each
+    tokens (routing, both grouped GEMMs, SwiGLU, un-permute), decode attention
+    over an INT8 KV cache (32 sequences x 4096 positions, 64 query heads on 8
+    kv heads, head dim 128; the step's cache write included) and stress, each
     with its throughput, the
     roofline of its dominant kernel, the quantizer's time, the end-to-end
     number through the public API with host buffers, and the CPU oracle timed
@@ -23,7 +25,7 @@ activations, then the group-scaled GEMM; w8a8_linear / w8a8_grouped_linear),
 the step's calls replayed as one CUDA graph.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --workload tiny|decode|prefill|moe|moe_ffn|stress   (one workload)
+  python bench.py --workload tiny|decode|prefill|moe|moe_ffn|attn_int8kv|stress   (one workload)
 """
 from __future__ import annotations
 
@@ -46,7 +48,7 @@ import workloads  # noqa: E402
 
 METRIC = "INT8 TOPS & % of roofline (tensor peak or HBM GB/s) per GEMM shape, 1xGB300"
 GROUP = 128
-WORKLOADS = ("tiny", "decode", "prefill", "moe", "moe_ffn", "stress")
+WORKLOADS = ("tiny", "decode", "prefill", "moe", "moe_ffn", "attn_int8kv", "stress")
 HEADLINE = "stress"
 # Workloads whose inputs fit in L2 (129 MB) get an L2 flush (a 256 MB write,
 # outside the timed events) before every timed step; the others read more
@@ -59,6 +61,8 @@ L2_FLUSH_BYTES = 256 << 20
 ORACLE_COLS = {"tiny": 1024, "decode": 2048, "prefill": 512, "moe": 256, "stress": 512}
 # The MoE expert FFN's oracle sample: its first FFN_ORACLE_TOKENS tokens, whole.
 FFN_ORACLE_TOKENS = 64
+# The decode attention's oracle sample: its first ATTN_ORACLE_SEQS sequences.
+ATTN_ORACLE_SEQS = 2
 KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM (one library call) replayed back to back "
                     "K times, events around the K launches, median of 3 such batches; the "
                     "GEMM overlaps the quantizer, so this includes any part of the quantizer "
@@ -147,8 +151,38 @@ class FfnShape:
         return w + sc + 2 * s.T * s.K_up * 2 + s.T * s.topk * 8
 
 
+class AttnShape:
+    """Decode attention over one layer's INT8 KV cache plus the cache write of
+    the step's new token: ops of the score and output products; algorithmic
+    bytes = the cache (codes and per-vector scales), the new K/V vectors
+    (read as BF16, written as codes + scales), q and the output."""
+
+    def __init__(self, spec):
+        self.spec = spec
+        self.M, self.N, self.K = spec.B * spec.Hq, spec.S, spec.D
+        self.out = "bf16"
+        self.E = 1
+
+    @property
+    def ops(self):
+        s = self.spec
+        return 4 * s.B * s.Hq * s.S * s.D
+
+    def alg_bytes(self, active_experts=None):
+        s = self.spec
+        cache = 2 * s.B * s.Hkv * s.S * (s.D + 4)
+        new = 2 * s.B * s.Hkv * (2 * s.D + s.D + 4)
+        return cache + new + 2 * s.B * s.Hq * s.D * 2
+
+
 def build_workload(name):
     """Returns (description, [Shape], weight spec, roofline bound)."""
+    if name == "attn_int8kv":
+        spec = workloads.ATTN["decode"]
+        desc = ("decode attention over an INT8 KV cache with per-vector scales: B=32 sequences "
+                "at 4096 positions, 64 query heads on 8 kv heads, head dim 128 (the step's "
+                "new K/V written into the cache, then attention), BF16 out")
+        return desc, [Shape(spec.B * spec.Hq, spec.S, spec.D, "bf16", None)], spec, "hbm"
     if name == "moe_ffn":
         spec = workloads.MOE["moe"]
         desc = ("MoE expert FFN: 64 experts, top-8 of T=512 tokens, H=4096, I=1536 (routing, "
@@ -189,6 +223,9 @@ def workload_config(name):
 
 
 def oracle_sample_desc(name, shapes):
+    if name == "attn_int8kv":
+        return (f"the first {ATTN_ORACLE_SEQS} sequences: their K/V cache quantized, "
+                "dequantized and attended by every query head")
     if name == "moe_ffn":
         return (f"the whole FFN of the first {FFN_ORACLE_TOKENS} tokens (all their routed rows, "
                 "every column of both GEMMs)")
@@ -364,6 +401,33 @@ def setup_workload(ctx, name):
     torch, w8, dev = ctx.torch, ctx.w8, ctx.dev
     desc, shapes, wspec, bound = build_workload(name)
     per = []
+    if name == "attn_int8kv":
+        spec = wspec
+        q_h, k_h, v_h = workloads.attn_inputs(spec)
+        B, Hkv, S, D = spec.B, spec.Hkv, spec.S, spec.D
+        d = dict(shape=AttnShape(spec), attn=True, off=None, a_host=q_h,
+                 a=upload_bf16(torch, dev, q_h), qw=torch.empty(0, dtype=torch.int8))
+        d["kc"] = torch.empty((B, Hkv, S, D), dtype=torch.int8, device=dev)
+        d["vc"] = torch.empty_like(d["kc"])
+        d["ks"] = torch.empty((B, Hkv, S), dtype=torch.float32, device=dev)
+        d["vs"] = torch.empty_like(d["ks"])
+        kb = upload_bf16(torch, dev, k_h)
+        vb = upload_bf16(torch, dev, v_h)
+        w8.kv_quant(kb.view(-1, D), d["kc"], d["ks"])
+        w8.kv_quant(vb.view(-1, D), d["vc"], d["vs"])
+        d["kb"], d["vb"] = kb, vb                   # the BF16 cache (baseline)
+        # the step's new token: position S - 1 of every (sequence, kv head)
+        d["k_new"] = kb[:, :, S - 1].contiguous().view(-1, D)
+        d["v_new"] = vb[:, :, S - 1].contiguous().view(-1, D)
+        d["rows_new"] = (torch.arange(B * Hkv, device=dev, dtype=torch.int32) * S + (S - 1))
+        d["lens"] = torch.full((B,), S, dtype=torch.int32, device=dev)
+        d["scale"] = 1.0 / float(np.sqrt(D))
+        d["y"] = torch.empty((B, spec.Hq, D), dtype=torch.bfloat16, device=dev)
+        d["ws"] = torch.empty(max(w8.attention_decode_workspace_size(B, spec.Hq, S), 1),
+                              dtype=torch.uint8, device=dev)
+        d["launches"] = 4
+        torch.cuda.synchronize()
+        return desc, shapes, wspec, bound, [d]
     if name == "moe_ffn":
         spec = wspec
         route = workloads.routing(spec)
@@ -422,7 +486,12 @@ def setup_workload(ctx, name):
 
 def linear_call(ctx, d, s):
     w8 = ctx.w8
-    if d.get("ffn"):
+    if d.get("attn"):
+        w8.kv_quant(d["k_new"], d["kc"], d["ks"], dst_rows=d["rows_new"], stream=s)
+        w8.kv_quant(d["v_new"], d["vc"], d["vs"], dst_rows=d["rows_new"], stream=s)
+        w8.attention_decode(d["a"], d["kc"], d["vc"], d["lens"], d["scale"], k_scale=d["ks"],
+                            v_scale=d["vs"], out=d["y"], workspace=d["ws"], stream=s)
+    elif d.get("ffn"):
         w8.moe_ffn(d["a"], d["ids"], d["w"], d["qw"], d["sw"], d["qw_dn"], d["sw_dn"], out=d["y"],
                    out_dtype=d["y"].dtype, workspace=d["ws"], stream=s)
     elif d["off"] is not None:
@@ -504,6 +573,11 @@ def measure_workload(ctx, name, headline):
               torch.empty((d["shape"].M,), dtype=torch.float32, device=ctx.dev)) for d in per]
 
     def quant_call(i):
+        if per[i].get("attn"):   # the step's quantizer is its cache write
+            d = per[i]
+            w8.kv_quant(d["k_new"], d["kc"], d["ks"], dst_rows=d["rows_new"], stream=stream)
+            w8.kv_quant(d["v_new"], d["vc"], d["vs"], dst_rows=d["rows_new"], stream=stream)
+            return
         w8.quant_act(per[i]["a"], qa=qbufs[i][0], sa=qbufs[i][1], stream=stream)
 
     run_quant = ([ctx.capture(lambda i=i: quant_call(i)).replay for i in range(len(per))]
@@ -585,6 +659,18 @@ def measure_workload(ctx, name, headline):
                 "ops_per_launch": flops,
                 "peak_source": (f"{peaks['source']} dense bf16 burst (the integer-exact path "
                                 "runs on the fp16 tensor cores, whose dense rate equals bf16's)")}
+    if name == "attn_int8kv":
+        # the same attention over the BF16 cache: the cost of not quantizing
+        d = per[0]
+
+        def bf16_call():
+            w8.attention_decode(d["a"], d["kb"], d["vb"], d["lens"], d["scale"], out=d["y"],
+                                workspace=d["ws"], stream=stream)
+
+        run_b = ctx.capture(bf16_call).replay if graphs else bf16_call
+        bms = ctx.batch_ms(run_b, args.steps)
+        roof["bf16_cache_attention_ms"] = round(bms, 5)
+        roof["int8_cache_step_over_bf16_attention"] = round(gemm_ms[0] / bms, 4)
     roof["kernel_ms_per_launch"] = [round(x, 5) for x in gemm_ms]
     roof["kernel_time"] = KERNEL_TIME_NOTE
     roof["quantizer_ms_per_launch"] = [round(x, 5) for x in quant_ms]
@@ -596,9 +682,11 @@ def measure_workload(ctx, name, headline):
         "ms_per_step": round(elapsed_ms / args.steps, 5),
         "l2": ("flushed before every timed step (256 MB write outside the events); inputs "
                "fit in L2" if flush else
-               "inputs larger than L2: each step streams "
-               f"{sum(d['qw'].numel() + d.get('qw_dn', d['qw'][:0]).numel() for d in per) / 1e6:.0f} MB of weights"
-               + (" (a weight copy per GEMM)" if len(per) > 1 and name != "moe" else "")),
+               (f"inputs larger than L2: each step streams the "
+                f"{per[0]['shape'].alg_bytes() / 1e6:.0f} MB KV cache" if name == "attn_int8kv" else
+                "inputs larger than L2: each step streams "
+                f"{sum(d['qw'].numel() + d.get('qw_dn', d['qw'][:0]).numel() for d in per) / 1e6:.0f} MB of weights"
+                + (" (a weight copy per GEMM)" if len(per) > 1 and name != "moe" else ""))),
         "roofline": roof,
         "gpu_launches_per_step": sum(d["launches"] for d in per),
     }
@@ -693,6 +781,13 @@ def oracle_items(name):
     """Inputs of the oracle's sample of a workload (ORACLE_COLS)."""
     import oracle
     _, shapes, wspec, _ = build_workload(name)
+    if name == "attn_int8kv":
+        spec = wspec
+        q_h, k_h, v_h = workloads.attn_inputs(spec)
+        ns = ATTN_ORACLE_SEQS
+        item = ("attn", q_h[:ns], k_h[:ns], v_h[:ns], np.full(ns, spec.S, np.int32),
+                1.0 / np.sqrt(spec.D))
+        return [item], 4 * ns * spec.Hq * spec.S * spec.D
     if name == "moe_ffn":
         # the whole FFN of the first FFN_ORACLE_TOKENS tokens, with the
         # weights of the experts they use (ids renumbered over those experts)
@@ -733,6 +828,13 @@ def oracle_items(name):
 def oracle_step(items):
     import oracle
     for it in items:
+        if isinstance(it[0], str) and it[0] == "attn":
+            _, q, k, v, lens, scale = it
+            qk, sk = oracle.kv_quant(k)
+            qv, sv = oracle.kv_quant(v)
+            oracle.attention_decode(q, oracle.kv_dequant(qk, sk), oracle.kv_dequant(qv, sv), lens,
+                                    scale)
+            continue
         if isinstance(it[0], str) and it[0] == "ffn":
             _, x, ids, w, W = it
             oracle.moe_ffn(x, ids, w, *W)
