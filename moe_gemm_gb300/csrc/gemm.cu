@@ -86,10 +86,6 @@ constexpr int kSmemLimit = 232448;
 // Dense problems with wide token tiles walk their tiles in bands of this many
 // weight tiles (see decode_tile).
 constexpr int kRasterBand = 8;
-// Narrow tiles of at most this many token rows issue the MMAs of a step's two
-// K groups alternately (two independent accumulators in flight: decode M=8
-// and M=32 ~1 us faster per GEMM; 64-row tiles were not, measured).
-constexpr int kInterleaveMaxRows = 32;
 
 // Shared memory: a fixed area (barriers, flags, tile table), then the weight
 // stages, then the token stages (offsets from a 1024-byte aligned base).
@@ -575,33 +571,6 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         return false;
                     }
                     tc_fence_after();
-                    if (!kWide && b_rows <= kInterleaveMaxRows) {
-                        // the two groups' accumulators are independent: their
-                        // MMAs take turns (descriptors formed once per step)
-                        const uint32_t d0 = tmem_base + pbuf_col(pr.idx, 0);
-                        const uint32_t d1 = tmem_base + pbuf_col(pr.idx, 1);
-                        const uint32_t a0 = tmem_base + kTmemA0 + st.idx * 128u;
-                        const uint64_t b0 = smem_desc_sw128(sB + bs.idx * b_stage_bytes);
-                        const uint64_t b1 = b0 + static_cast<uint64_t>((2u * b_atom_bytes) >> 4);
-                        const uint64_t atom_step = b_atom_bytes >> 4;
-                        if (ng == 2) {
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t bd =
-                                    (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
-                                mma_f16_tmemA(d0, a0 + kk * 8, b0 + bd, idesc, kk > 0 ? 1u : 0u);
-                                mma_f16_tmemA(d1, a0 + 64u + kk * 8, b1 + bd, idesc,
-                                              kk > 0 ? 1u : 0u);
-                            }
-                        } else {
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t bd =
-                                    (kk >> 2) * atom_step + static_cast<uint64_t>((kk & 3) * 2);
-                                mma_f16_tmemA(d0, a0 + kk * 8, b0 + bd, idesc, kk > 0 ? 1u : 0u);
-                            }
-                        }
-                    } else
                     for (int j = 0; j < ng; ++j) {
                         if constexpr (kWide) {
                             // group j's partial buffer drained by the epilogue;
