@@ -48,9 +48,10 @@ import workloads  # noqa: E402
 
 METRIC = "INT8 TOPS & % of roofline (tensor peak or HBM GB/s) per GEMM shape, 1xGB300"
 GROUP = 128
-WORKLOADS = ("tiny", "decode", "prefill", "moe", "moe_ffn", "attn_int8kv", "stress")
+WORKLOADS = ("tiny", "decode", "prefill", "moe", "moe_ffn", "attn_int8kv", "norm_quant",
+             "stress")
 HEADLINE = "stress"
-# Workloads whose inputs fit in L2 (129 MB) get an L2 flush (a 256 MB write,
+# Workloads whose inputs fit in L2 (129 MB) get an L2 flush (a 256 MB write and a 256 MB read,
 # outside the timed events) before every timed step; the others read more
 # than L2 holds every step.
 FLUSH_L2 = ("tiny", "prefill")
@@ -63,6 +64,15 @@ ORACLE_COLS = {"tiny": 1024, "decode": 2048, "prefill": 512, "moe": 256, "stress
 FFN_ORACLE_TOKENS = 64
 # The decode attention's oracle sample: its first ATTN_ORACLE_SEQS sequences.
 ATTN_ORACLE_SEQS = 2
+# The RMSNorm + quantizer's oracle sample: its first NORM_ORACLE_ROWS rows.
+NORM_ORACLE_ROWS = 256
+NORM_EPS = 1e-6
+
+
+def unit_of(name):
+    """Unit of a workload's value and its scale: GEMM-bearing workloads in
+    TOPS, the HBM-bound RMSNorm + quantizer in GB/s of algorithmic bytes."""
+    return ("GB/s", 1e9) if name == "norm_quant" else ("TOPS", 1e12)
 KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM (one library call) replayed back to back "
                     "K times, events around the K launches, median of 3 such batches; the "
                     "GEMM overlaps the quantizer, so this includes any part of the quantizer "
@@ -175,8 +185,31 @@ class AttnShape:
         return cache + new + 2 * s.B * s.Hq * s.D * 2
 
 
+class NormShape:
+    """RMSNorm fused with the per-token quantizer over M rows of K: its
+    algorithmic bytes (BF16 rows and weight read, int8 codes and FP32 scales
+    written); `ops` counts those bytes, the unit of this workload's value."""
+
+    def __init__(self, M, K):
+        self.M, self.N, self.K = M, K, K
+        self.out = "int8"
+        self.E = 1
+
+    def alg_bytes(self, active_experts=None):
+        return 2 * self.M * self.K + 2 * self.K + self.M * self.K + 4 * self.M
+
+    @property
+    def ops(self):
+        return self.alg_bytes()
+
+
 def build_workload(name):
     """Returns (description, [Shape], weight spec, roofline bound)."""
+    if name == "norm_quant":
+        spec = workloads.DENSE["prefill"]
+        desc = ("RMSNorm fused with per-token INT8 quantization: M=4096 rows of K=8192 (the "
+                "prefill activations), BF16 in, int8 codes + FP32 scales out")
+        return desc, [NormShape(spec.M, spec.K)], spec, "hbm"
     if name == "attn_int8kv":
         spec = workloads.ATTN["decode"]
         desc = ("decode attention over an INT8 KV cache with per-vector scales: B=32 sequences "
@@ -223,6 +256,9 @@ def workload_config(name):
 
 
 def oracle_sample_desc(name, shapes):
+    if name == "norm_quant":
+        return (f"the first {NORM_ORACLE_ROWS} rows: FP64 RMSNorm, BF16 rounding, per-token "
+                "quantization")
     if name == "attn_int8kv":
         return (f"the first {ATTN_ORACLE_SEQS} sequences: their K/V cache quantized, "
                 "dequantized and attended by every query head")
@@ -353,11 +389,18 @@ class GpuContext:
         return self._moe_w
 
     def flush_l2(self):
+        """Write a buffer larger than L2, then read another one: the write
+        evicts the step's inputs, the read evicts the write's dirty lines
+        (their write-back then happens here, outside the timed events, not
+        inside the next timed kernel)."""
         torch = self.torch
         if self.flush_buf is None:
             self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=self.dev)
+            self.flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=self.dev)
+            self.flush_sink = torch.empty((), dtype=torch.int64, device=self.dev)
         with torch.cuda.stream(self.stream):
             self.flush_buf.fill_(1)
+            torch.sum(self.flush_read, out=self.flush_sink)
 
     def capture(self, fn):
         torch = self.torch
@@ -680,8 +723,8 @@ def measure_workload(ctx, name, headline):
         "shapes": [[sh.M, sh.N, sh.K] for sh in shapes],
         "value": round(value, 3), "unit": "TOPS",
         "ms_per_step": round(elapsed_ms / args.steps, 5),
-        "l2": ("flushed before every timed step (256 MB write outside the events); inputs "
-               "fit in L2" if flush else
+        "l2": ("flushed before every timed step (256 MB write, then 256 MB read, outside "
+               "the events); inputs fit in L2" if flush else
                (f"inputs larger than L2: each step streams the "
                 f"{per[0]['shape'].alg_bytes() / 1e6:.0f} MB KV cache" if name == "attn_int8kv" else
                 "inputs larger than L2: each step streams "
@@ -697,6 +740,150 @@ def measure_workload(ctx, name, headline):
     if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
         entry["cpu_baseline"] = cpu_baseline(name, 8.0 if headline else 3.0)
     del per
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def measure_norm(ctx, headline):
+    """The RMSNorm + quantizer workload: the fused kernel over the prefill
+    activations (inputs fit in L2: flushed before every timed step), the
+    unfused pair (rmsnorm, then quant_act) timed the same way, and the fused
+    RMSNorm + linear call against rmsnorm followed by linear."""
+    torch, w8, args = ctx.torch, ctx.w8, ctx.args
+    stream = ctx.stream
+    desc, shapes, spec, _ = build_workload("norm_quant")
+    shp = shapes[0]
+    M, K = shp.M, shp.K
+    x_host = workloads.activations(spec)
+    g_host = workloads.norm_weight(spec)
+    x = upload_bf16(torch, ctx.dev, x_host)
+    g = upload_bf16(torch, ctx.dev, g_host)
+    qa = torch.empty((M, K), dtype=torch.int8, device=ctx.dev)
+    sa = torch.empty((M,), dtype=torch.float32, device=ctx.dev)
+    ybuf = torch.empty((M, K), dtype=torch.bfloat16, device=ctx.dev)
+    graphs = not args.no_graph
+
+    def fused():
+        w8.rmsnorm_quant(x, g, NORM_EPS, qa=qa, sa=sa, stream=stream)
+
+    def unfused():
+        w8.rmsnorm(x, g, NORM_EPS, out=ybuf, stream=stream)
+        w8.quant_act(ybuf, qa=qa, sa=sa, stream=stream)
+
+    def flushed_ms(run, steps):
+        out = []
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                ctx.flush_l2()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                run()
+                e1.record(stream)
+                e1.synchronize()
+                out.append(e0.elapsed_time(e1))
+        return out
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            fused()
+            unfused()
+    torch.cuda.synchronize()
+    run_f = ctx.capture(fused).replay if graphs else fused
+    run_u = ctx.capture(unfused).replay if graphs else unfused
+    ctx.barrier()
+    torch.cuda.synchronize()
+    step_ms = flushed_ms(run_f, args.steps)
+    elapsed_ms = slowest_rank_ms(sum(step_ms), ctx.world, ctx.dev)
+    ctx.barrier()
+    unf_ms = statistics.median(flushed_ms(run_u, args.steps))
+    fused_ms = statistics.median(step_ms)
+    alg = shp.alg_bytes()
+    value = alg * args.steps * ctx.world / (elapsed_ms * 1e-3) / 1e9
+    achieved = alg / (fused_ms * 1e-3) / 1e9
+    peaks = ctx.peaks
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": recorded_traffic("norm_quant"), "alg_bytes_per_launch": [alg],
+            "peak_source": f"{peaks['source']} HBM copy bandwidth",
+            "kernel_ms_per_launch": [round(fused_ms, 5)],
+            "kernel_time": "median over the timed steps, L2 flushed before each",
+            "unfused_ms": round(unf_ms, 5),
+            "unfused": "rmsnorm (BF16 rows to HBM) then quant_act, L2 flushed before each pair",
+            "fused_over_unfused": round(fused_ms / unf_ms, 4)}
+
+    # RMSNorm + linear on the prefill GEMM: fused call against the two calls
+    N = spec.N
+    qw = torch.empty((N, K), dtype=torch.int8, device=ctx.dev)
+    sw = torch.empty((N, K // GROUP), dtype=torch.float32, device=ctx.dev)
+    for r0, wb in workloads.weight_blocks(spec, block_rows=4096):
+        q, sc = w8.quant_weight(torch.from_numpy(wb).to(ctx.dev))
+        qw[r0:r0 + wb.shape[0]].copy_(q)
+        sw[r0:r0 + wb.shape[0]].copy_(sc)
+        del q, sc
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=ctx.dev)
+    ws = torch.empty(w8.linear_workspace_size(M, N, K), dtype=torch.uint8, device=ctx.dev)
+
+    def norm_linear():
+        w8.rmsnorm_linear(x, g, NORM_EPS, qw, sw, out=y, workspace=ws, stream=stream)
+
+    def norm_then_linear():
+        w8.rmsnorm(x, g, NORM_EPS, out=ybuf, stream=stream)
+        w8.linear(ybuf, qw, sw, out=y, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            norm_linear()
+            norm_then_linear()
+    torch.cuda.synchronize()
+    run_nl = ctx.capture(norm_linear).replay if graphs else norm_linear
+    run_ntl = ctx.capture(norm_then_linear).replay if graphs else norm_then_linear
+    nsteps = max(3, min(args.steps, 10))
+    roof["rmsnorm_linear_ms"] = round(statistics.median(flushed_ms(run_nl, nsteps)), 5)
+    roof["rmsnorm_then_linear_ms"] = round(statistics.median(flushed_ms(run_ntl, nsteps)), 5)
+    del qw, sw, y, ws
+
+    entry = {"workload": desc, "shapes": [[M, K]], "value": round(value, 1), "unit": "GB/s",
+             "ms_per_step": round(elapsed_ms / args.steps, 5),
+             "l2": "flushed before every timed step (256 MB write, then 256 MB read, outside "
+                   "the events); inputs fit in L2",
+             "roofline": roof, "gpu_launches_per_step": 1}
+    if not args.no_e2e:
+        host_in = torch.from_numpy(np.ascontiguousarray(x_host).view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+        host_q = torch.empty((M, K), dtype=torch.int8).pin_memory()
+        host_s = torch.empty((M,), dtype=torch.float32).pin_memory()
+        cur = torch.cuda.current_stream()
+
+        def e2e_step():
+            x.copy_(host_in, non_blocking=True)
+            w8.rmsnorm_quant(x, g, NORM_EPS, qa=qa, sa=sa, stream=cur)
+            host_q.copy_(qa, non_blocking=True)
+            host_s.copy_(sa, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        ctx.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        ems = slowest_rank_ms(e0.elapsed_time(e1), ctx.world, ctx.dev)
+        entry["e2e"] = {"value": round(alg * args.steps * ctx.world / (ems * 1e-3) / 1e9, 1),
+                        "unit": "GB/s", "h2d_bytes_per_step": int(2 * M * K),
+                        "d2h_bytes_per_step": int(M * K + 4 * M),
+                        "ms_per_step": round(ems / args.steps, 5),
+                        "how": "pinned host rows -> device, the fused call, codes and scales "
+                               "-> pinned host; stream launches"}
+        del host_in, host_q, host_s
+    if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
+        entry["cpu_baseline"] = cpu_baseline("norm_quant", 8.0 if headline else 3.0)
+    del x, g, qa, sa, ybuf
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return entry
@@ -743,7 +930,8 @@ def run_ours(args):
         int_peak = measure_int_path_peak(ctx)
     entries = {}
     for name in names:
-        entries[name] = measure_workload(ctx, name, name == head)
+        entries[name] = (measure_norm(ctx, name == head) if name == "norm_quant"
+                         else measure_workload(ctx, name, name == head))
     h = entries[head]
     roof = dict(h["roofline"])
     if int_peak and roof["bound"] == "tensor":
@@ -781,6 +969,10 @@ def oracle_items(name):
     """Inputs of the oracle's sample of a workload (ORACLE_COLS)."""
     import oracle
     _, shapes, wspec, _ = build_workload(name)
+    if name == "norm_quant":
+        rows = np.arange(NORM_ORACLE_ROWS)
+        item = ("norm", workloads.activations(wspec, rows=rows), workloads.norm_weight(wspec))
+        return [item], NormShape(NORM_ORACLE_ROWS, wspec.K).alg_bytes()
     if name == "attn_int8kv":
         spec = wspec
         q_h, k_h, v_h = workloads.attn_inputs(spec)
@@ -828,6 +1020,10 @@ def oracle_items(name):
 def oracle_step(items):
     import oracle
     for it in items:
+        if isinstance(it[0], str) and it[0] == "norm":
+            _, x, g = it
+            oracle.quant_act(oracle.bf16_round(oracle.rmsnorm(x, g, float(np.float32(NORM_EPS)))))
+            continue
         if isinstance(it[0], str) and it[0] == "attn":
             _, q, k, v, lens, scale = it
             qk, sk = oracle.kv_quant(k)
@@ -859,7 +1055,8 @@ def cpu_baseline(name, target_s):
         oracle_step(items)
         reps += 1
         dt = time.perf_counter() - t
-    return {"value": round(ops * reps / dt / 1e12, 6), "unit": "TOPS",
+    unit, scale = unit_of(name)
+    return {"value": round(ops * reps / dt / scale, 6), "unit": unit,
             "cores": oracle.max_threads(), "kind": "oracle",
             "sample": oracle_sample_desc(name, shapes), "passes": reps, "seconds": round(dt, 2)}
 
@@ -880,18 +1077,19 @@ def run_reference(args):
     for _ in range(args.steps):
         oracle_step(items)
     dt = time.perf_counter() - t
-    value = ops * args.steps / dt / 1e12
+    unit, scale = unit_of(name)
+    value = ops * args.steps / dt / scale
     cores = oracle.max_threads()
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS",
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": workload_config(name),
         "timing": {"parallelism": "the CPU oracle on the host cores (rank 0)"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": cores,
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores,
                          "kind": "oracle", "sample": oracle_sample_desc(name, shapes)},
-        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
 

@@ -259,6 +259,50 @@ w8a8_status w8a8_linear_ex(const void *a_bf16, int64_t lda, w8a8_scale_mode act_
                            size_t workspace_bytes, w8a8_stream_t stream);
 
 /*
+ * RMSNorm in front of the per-token quantizer, in one kernel (the quantizer
+ * fused into the preceding normalisation: "Deploying Hunyuan 770B in INT8 on
+ * domestic accelerators", §4.1 operator table, RMSNorm kept in high precision
+ * next to the INT8 GEMMs, and §3.1, dynamic per-token INT8 activations).
+ * Row m of x is normalised as
+ *   y[m, k] = bf16_rn((x[m, k] * inv) * gamma[k]),
+ *   inv = 1 / sqrt(sum_k x[m, k]^2 / K + eps),
+ * with IEEE fp32 operations (every product rounded; the sum of squares in
+ * fp32 in a fixed order, so results are run-to-run identical). y is the BF16
+ * activation an unfused RMSNorm would write; its codes and scale are then
+ * exactly what w8a8_quant_act / w8a8_quant_act_ex give for the rows y.
+ *   x_bf16 [M, K] BF16, row stride ldx (multiple of 8, >= K), 16-byte aligned
+ *   gamma_bf16 [K] BF16, 16-byte aligned
+ *   eps > 0 and finite; K a multiple of 8, at most 32768
+ * Accuracy of y against the exact value (real arithmetic on the same inputs):
+ * the fp32 value before the BF16 rounding is within 2^-19 relative of it (at
+ * most 32 sequential fma terms per thread and 10 tree levels in the sum of
+ * squares, then five rounded operations), so y is within half a BF16 ulp plus
+ * 2^-19 relative (tested).
+ * Non-finite inputs give unspecified codes and scales.
+ */
+/* The normalised rows themselves: y_bf16 [M, K], row stride ldy (multiple of
+ * 8, >= K), 16-byte aligned. */
+w8a8_status w8a8_rmsnorm(const void *x_bf16, int64_t ldx, const void *gamma_bf16, float eps,
+                         int64_t M, int64_t K, void *y_bf16, int64_t ldy, w8a8_stream_t stream);
+/* Normalised and quantized: qa [M, ldq] int8 (ldq multiple of 8, >= K,
+ * 8-byte aligned), sa [M] float; mode as for w8a8_quant_act_ex. */
+w8a8_status w8a8_rmsnorm_quant(const void *x_bf16, int64_t ldx, const void *gamma_bf16, float eps,
+                               w8a8_scale_mode mode, int64_t M, int64_t K, int8_t *qa,
+                               int64_t ldq, float *sa, w8a8_stream_t stream);
+/*
+ * RMSNorm, quantization and the group-scaled GEMM: w8a8_linear applied to the
+ * normalised rows y, with the normalisation done inside the quantizer kernel
+ * (the BF16 rows y never reach HBM). Workspace and all GEMM arguments as for
+ * w8a8_linear (w8a8_linear_workspace_size(M, N, K) bytes); x, gamma and eps as
+ * above, K a multiple of 128. The result is identical to w8a8_rmsnorm
+ * followed by w8a8_linear.
+ */
+w8a8_status w8a8_rmsnorm_linear(const void *x_bf16, int64_t ldx, const void *gamma_bf16, float eps,
+                                const int8_t *qw, const float *sw, void *y, w8a8_dtype y_dtype,
+                                int64_t M, int64_t N, int64_t K, void *workspace,
+                                size_t workspace_bytes, w8a8_stream_t stream);
+
+/*
  * Weight-only INT8 GEMM with BF16 activations (the "WNA16" reading of the
  * MoE runner on "Running DeepSeek-V4-Flash-Vision on 4xA800", §二: INT8
  * weights with one scale per group of 128 K, 16-bit activations that are not

@@ -91,6 +91,10 @@ def _load() -> ctypes.CDLL:
     lib.w8a8_moe_ffn_workspace_size.restype = ctypes.c_size_t
     lib.w8a8_moe_ffn.argtypes = [vp, i64, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
                                  i32, vp, ctypes.c_size_t, vp]
+    lib.w8a8_rmsnorm.argtypes = [vp, i64, vp, ctypes.c_float, i64, i64, vp, i64, vp]
+    lib.w8a8_rmsnorm_quant.argtypes = [vp, i64, vp, ctypes.c_float, i32, i64, i64, vp, i64, vp, vp]
+    lib.w8a8_rmsnorm_linear.argtypes = [vp, i64, vp, ctypes.c_float, vp, vp, vp, i32, i64, i64,
+                                        i64, vp, ctypes.c_size_t, vp]
     lib.w8a8_version.restype = i32
     for name in ("w8a8_quant_act", "w8a8_quant_weight", "w8a8_gemm", "w8a8_grouped_gemm",
                  "w8a8_gemm_noalloc", "w8a8_device_error", "w8a8_selftest_wait_timeout",
@@ -100,7 +104,8 @@ def _load() -> ctypes.CDLL:
                  "w8a8_quant_act_ex", "w8a8_quant_weight_ex", "w8a8_gemm_ex",
                  "w8a8_grouped_gemm_ex", "w8a8_linear_ex", "w8a8_w8a16_gemm",
                  "w8a8_w8a16_grouped_gemm", "w8a8_kv_quant", "w8a8_attention_decode_int8kv",
-                 "w8a8_attention_decode_bf16kv"):
+                 "w8a8_attention_decode_bf16kv", "w8a8_rmsnorm", "w8a8_rmsnorm_quant",
+                 "w8a8_rmsnorm_linear"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -397,6 +402,88 @@ def linear(a: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor,
             _check(_lib.w8a8_linear_ex(_ptr(a), lda, act_scale_mode, _ptr(qw), _ptr(sw),
                                        sw_block_rows, _ptr(out), code, M, N, K, _ptr(workspace),
                                        workspace.numel(), _stream(stream)), "w8a8_linear_ex")
+    return out
+
+
+def _require_norm_input(x: torch.Tensor, gamma: torch.Tensor) -> int:
+    ldx = _require_act(x)
+    K = x.shape[1]
+    _require(gamma, torch.bfloat16, "gamma", 1, (K,), x.device)
+    return ldx
+
+
+def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, out: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """RMSNorm of BF16 rows x [M, K] with BF16 weights gamma [K]:
+    bf16((x / sqrt(mean(x^2) + eps)) * gamma), fp32 arithmetic."""
+    ldx = _require_norm_input(x, gamma)
+    M, K = x.shape
+    dev = x.device
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    elif (not out.is_cuda or out.dtype != torch.bfloat16 or out.dim() != 2
+          or tuple(out.shape) != (M, K) or out.stride(1) != 1 or out.device != dev):
+        raise ValueError(f"out: expected a bf16 [{M}, {K}] tensor with unit column stride on {dev}")
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_rmsnorm(_ptr(x), ldx, _ptr(gamma), eps, M, K, _ptr(out), out.stride(0),
+                                 _stream(stream)), "w8a8_rmsnorm")
+    return out
+
+
+def rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float,
+                  qa: Optional[torch.Tensor] = None, sa: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None,
+                  scale_mode: int = SCALE_AMAX) -> Tuple[torch.Tensor, torch.Tensor]:
+    """RMSNorm and per-token INT8 quantization in one kernel: the codes and
+    scales quant_act gives for rmsnorm(x, gamma, eps)."""
+    ldx = _require_norm_input(x, gamma)
+    M, K = x.shape
+    dev = x.device
+    if qa is None:
+        qa = torch.empty((M, K), dtype=torch.int8, device=dev)
+    elif (not qa.is_cuda or qa.dtype != torch.int8 or qa.dim() != 2 or tuple(qa.shape) != (M, K)
+          or qa.stride(1) != 1 or qa.device != dev):
+        raise ValueError(f"qa: expected an int8 [{M}, {K}] tensor with unit column stride on {dev}")
+    if sa is None:
+        sa = torch.empty((M,), dtype=torch.float32, device=dev)
+    else:
+        _require(sa, torch.float32, "sa", 1, (M,), dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_rmsnorm_quant(_ptr(x), ldx, _ptr(gamma), eps, scale_mode, M, K, _ptr(qa),
+                                       qa.stride(0), _ptr(sa), _stream(stream)),
+               "w8a8_rmsnorm_quant")
+    return qa, sa
+
+
+def rmsnorm_linear(x: torch.Tensor, gamma: torch.Tensor, eps: float, qw: torch.Tensor,
+                   sw: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
+                   out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """linear(rmsnorm(x, gamma, eps), qw, sw) with the normalisation inside
+    the quantizer kernel (the normalised rows never reach HBM)."""
+    ldx = _require_norm_input(x, gamma)
+    dev = x.device
+    M, K = x.shape
+    _require(qw, torch.int8, "qw", 2, device=dev)
+    N = qw.shape[0]
+    if qw.shape[1] != K:
+        raise ValueError(f"qw: expected K = {K} columns, got {qw.shape[1]}")
+    _require(sw, torch.float32, "sw", 2, (N, K // GROUP), dev)
+    code = _dtype_code(out_dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    else:
+        _require_out(out, out_dtype, (M, N), dev)
+    if workspace is None:
+        workspace = torch.empty(max(linear_workspace_size(M, N, K), 1), dtype=torch.uint8,
+                                device=dev)
+    else:
+        _require_workspace(workspace, dev)
+    with _on_device(dev, stream):
+        _check(_lib.w8a8_rmsnorm_linear(_ptr(x), ldx, _ptr(gamma), eps, _ptr(qw), _ptr(sw),
+                                        _ptr(out), code, M, N, K, _ptr(workspace),
+                                        workspace.numel(), _stream(stream)),
+               "w8a8_rmsnorm_linear")
     return out
 
 

@@ -3,6 +3,7 @@
 // No call allocates device memory, synchronises the host or reads device data.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -169,10 +170,17 @@ w8a8_status check_linear(const void *a, int64_t lda, const void *offsets, const 
     return W8A8_OK;
 }
 
+// RMSNorm in front of the quantizer of a linear call (null: none).
+struct NormArg {
+    const uint16_t *gamma;
+    float eps;
+};
+
 w8a8_status run_linear(const void *a, int64_t lda, const int32_t *offsets, const int8_t *qw,
                        const float *sw, void *y, w8a8_dtype y_dtype, int64_t R, int64_t E,
                        int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
-                       w8a8_stream_t stream, int sw_block_rows = 1, bool pow2 = false) {
+                       w8a8_stream_t stream, int sw_block_rows = 1, bool pow2 = false,
+                       const NormArg *norm = nullptr) {
     w8a8::DeviceInfo info;
     w8a8_status st = check_device(&info);
     if (st != W8A8_OK) return st;
@@ -190,7 +198,15 @@ w8a8_status run_linear(const void *a, int64_t lda, const int32_t *offsets, const
     }
     const uint16_t *a16 = static_cast<const uint16_t *>(a);
     cudaError_t e = cudaSuccess;
-    if (w8a8::uses_gemv(R, grouped) && !pow2 && w8a8::gemv_can_fuse_quant(R, K, lda, a)) {
+    if (norm != nullptr) {
+        // RMSNorm and quantization in one kernel, then the GEMM
+        const bool gemv = w8a8::uses_gemv(R, grouped);
+        e = w8a8::launch_rmsnorm_quant(a16, R, K, lda, norm->gamma, norm->eps, gemv ? 0 : 1, ws, K,
+                                       sa, gemv ? nullptr : p.sk_cnt,
+                                       p.sk_cnt != nullptr ? 2 * w8a8::kSkMaxCtas : 0, pow2, s);
+        p.qa = gemv ? reinterpret_cast<const int8_t *>(ws) : nullptr;
+    } else if (w8a8::uses_gemv(R, grouped) && !pow2 &&
+               w8a8::gemv_can_fuse_quant(R, K, lda, a)) {
         // one kernel: the GEMV quantizes its token rows itself
         p.act = a16;
         p.lda = lda;
@@ -658,6 +674,66 @@ w8a8_status w8a8_attention_decode_bf16kv(const void *q_bf16, const void *k_cache
     return run_attention(q_bf16, k_cache, nullptr, v_cache, nullptr, lens, B, Hq, Hkv, S_max,
                          head_dim, softmax_scale, out, out_dtype, workspace, workspace_bytes,
                          false, stream);
+}
+
+namespace {
+// Arguments shared by the RMSNorm entry points.
+w8a8_status check_rmsnorm(const void *x, int64_t ldx, const void *gamma, float eps, int64_t M,
+                          int64_t K) {
+    if (M < 0 || K <= 0 || K % 8 != 0 || K > w8a8::kRmsNormMaxK || ldx < K || ldx % 8 != 0)
+        return W8A8_ERR_INVALID_ARG;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return W8A8_ERR_INVALID_ARG;
+    if (M > kMaxElems / ldx || M > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
+    if (M == 0) return W8A8_OK;
+    if (!x || !gamma || !aligned(x, 16) || !aligned(gamma, 16)) return W8A8_ERR_INVALID_ARG;
+    return W8A8_OK;
+}
+}  // namespace
+
+w8a8_status w8a8_rmsnorm(const void *x_bf16, int64_t ldx, const void *gamma_bf16, float eps,
+                         int64_t M, int64_t K, void *y_bf16, int64_t ldy, w8a8_stream_t stream) {
+    w8a8_status st = check_rmsnorm(x_bf16, ldx, gamma_bf16, eps, M, K);
+    if (st != W8A8_OK || M == 0) return st;
+    if (!y_bf16 || !aligned(y_bf16, 16) || ldy < K || ldy % 8 != 0 || M > kMaxElems / ldy)
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_rmsnorm_quant(
+        static_cast<const uint16_t *>(x_bf16), M, K, ldx, static_cast<const uint16_t *>(gamma_bf16),
+        eps, 2, y_bf16, ldy, nullptr, nullptr, 0, false, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_rmsnorm_quant(const void *x_bf16, int64_t ldx, const void *gamma_bf16, float eps,
+                               w8a8_scale_mode mode, int64_t M, int64_t K, int8_t *qa,
+                               int64_t ldq, float *sa, w8a8_stream_t stream) {
+    if (mode != W8A8_SCALE_AMAX && mode != W8A8_SCALE_POW2) return W8A8_ERR_INVALID_ARG;
+    w8a8_status st = check_rmsnorm(x_bf16, ldx, gamma_bf16, eps, M, K);
+    if (st != W8A8_OK || M == 0) return st;
+    if (!qa || !sa || !aligned(qa, 8) || !aligned(sa, 4) || ldq < K || ldq % 8 != 0 ||
+        M > kMaxElems / ldq)
+        return W8A8_ERR_INVALID_ARG;
+    w8a8::DeviceInfo info;
+    st = check_device(&info);
+    if (st != W8A8_OK) return st;
+    return from_cuda(w8a8::launch_rmsnorm_quant(
+        static_cast<const uint16_t *>(x_bf16), M, K, ldx, static_cast<const uint16_t *>(gamma_bf16),
+        eps, 0, qa, ldq, sa, nullptr, 0, mode == W8A8_SCALE_POW2,
+        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w8a8_status w8a8_rmsnorm_linear(const void *x_bf16, int64_t ldx, const void *gamma_bf16, float eps,
+                                const int8_t *qw, const float *sw, void *y, w8a8_dtype y_dtype,
+                                int64_t M, int64_t N, int64_t K, void *workspace,
+                                size_t workspace_bytes, w8a8_stream_t stream) {
+    w8a8_status st = check_rmsnorm(x_bf16, ldx, gamma_bf16, eps, M, K);
+    if (st != W8A8_OK) return st;
+    st = check_linear(x_bf16, ldx, nullptr, qw, sw, y, y_dtype, M, 1, N, K, false, workspace,
+                      workspace_bytes);
+    if (st != W8A8_OK || M == 0) return st;
+    const NormArg norm = {static_cast<const uint16_t *>(gamma_bf16), eps};
+    return run_linear(x_bf16, ldx, nullptr, qw, sw, y, y_dtype, M, 1, N, K, workspace,
+                      workspace_bytes, stream, 1, false, &norm);
 }
 
 w8a8_status w8a8_moe_route(const int32_t *topk_ids, int64_t T, int64_t k, int64_t E,

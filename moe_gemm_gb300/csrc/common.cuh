@@ -361,6 +361,34 @@ __device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthre
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also ORs a predicate over its participants: every thread
+// gets true when any participant passed true. Warp-uniform use only.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool c) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pc, pr;\n\t"
+        "setp.ne.u32 pc, %1, 0;\n\t"
+        "bar.red.or.pred pr, %2, %3, pc;\n\t"
+        "selp.u32 %0, 1, 0, pr;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(c)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// 4-byte asynchronous copy global -> shared; src_bytes 0 writes zero (the
+// source is then not read, but must still be a valid address).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Waits for this thread's cp.async copies.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 template <uint32_t RegCount>
 __device__ __forceinline__ void setmaxnreg_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(RegCount));

@@ -752,7 +752,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
         auto store_out = [&](int m, int n_local, float v) {
-            const float out = v * load_sa(p, m);
+            const float out = v;
             const size_t idx = static_cast<size_t>(m) * p.N + n_local;
             if (p.out_fp32)
                 static_cast<float *>(p.y)[idx] = out;
@@ -838,6 +838,19 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const bool n_ok = n_local < p.N;
             const float *swp =
                 p.sw + (static_cast<size_t>(ti.e) * p.sw_rows + ((n_ok ? n_local : 0) >> p.sw_shift)) * G;
+            // Token scales of a whole tile's columns, one per lane (lane l
+            // holds column 32 c + l of chunk c), loaded now and broadcast at
+            // the store: their latency hides behind the tile's steps instead
+            // of lengthening its epilogue.
+            const bool whole = s0 == 0 && s1 == plan.S;
+            float sa_l[NCH];
+#pragma unroll
+            for (int h = 0; h < NCH; ++h) {
+                const int col = 32 * (ewg + 2 * h) + lane;
+                sa_l[h] = !(whole && col < ti.rows) ? 0.0f
+                          : p.sa != nullptr        ? ldg_nc_f32_now(p.sa + ti.m0 + col)
+                                                   : 1.0f;
+            }
             // Scales of this row a quad of groups (two steps) ahead; loads are
             // issued in place and only read after the next quad boundary.
             auto load_quad = [&](int g) -> float4 {
@@ -870,8 +883,9 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     // One group at a time: wait for its MMAs, drain its buffer,
                     // release it (group 0 drains while group 1's MMAs issue).
                     for (int j = 0; j < ng; ++j) {
-                        if (!mbar_wait(bar(NBar::p_full + j), gph[j], s_abort, p.err,
-                                       ROLE_EPILOGUE, 2)) {
+                        const bool ok = mbar_wait(bar(NBar::p_full + j), gph[j], s_abort, p.err,
+                                                  ROLE_EPILOGUE, 2);
+                        if (__any_sync(0xFFFFFFFFu, !ok)) {   // the warp fails as one
                             failed = true;
                             break;
                         }
@@ -912,8 +926,9 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     }
                     continue;
                 }
-                if (!mbar_wait(bar(NBar::done + st.idx), st.phase, s_abort, p.err, ROLE_EPILOGUE,
-                               1)) {
+                const bool ok =
+                    mbar_wait(bar(NBar::done + st.idx), st.phase, s_abort, p.err, ROLE_EPILOGUE, 1);
+                if (__any_sync(0xFFFFFFFFu, !ok)) {   // the warp fails as one
                     failed = true;
                     continue;
                 }
@@ -959,14 +974,16 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 st.advance(kNarrowSlots);
                 pr.advance(NP);
             }
-            if (s0 == 0 && s1 == plan.S) {
-                if (n_ok && !failed) {
+            if (whole) {
+                // every lane takes the shuffles (the column bound is warp-uniform)
 #pragma unroll
-                    for (int h = 0; h < NCH; ++h) {
+                for (int h = 0; h < NCH; ++h) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int col = 32 * (ewg + 2 * h) + j;
-                            if (col < ti.rows) store_out(ti.m0 + col, n_local, acc[h][j]);
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = 32 * (ewg + 2 * h) + j;
+                        if (col < ti.rows) {
+                            const float sa = __shfl_sync(0xFFFFFFFFu, sa_l[h], j);
+                            if (n_ok && !failed) store_out(ti.m0 + col, n_local, acc[h][j] * sa);
                         }
                     }
                 }
@@ -1105,6 +1122,10 @@ constexpr int kW2SmemBytes =
     kW2OffStages + kW2TokStages * kW2TokStageBytes + kW2WStages * kAStageBytes + 1024;
 static_assert(kW2SmemBytes <= kSmemLimit, "wide-tile shared memory");
 constexpr uint32_t kW2TmemA0 = 256;
+// Token scales of the current tile, 128 per epilogue warpgroup, in the fixed
+// area: after the barriers, and after the tile table of a dense call.
+constexpr int kW2OffSa0 = 256;
+constexpr int kW2OffSa1 = 1536;
 
 struct W2Bar {
     static constexpr int a_full = 0;                       // [kW2WStages] weight TMA -> converter
@@ -1119,6 +1140,9 @@ struct W2Bar {
     static constexpr int count = drain + 1;
 };
 static_assert(W2Bar::count <= 128, "barrier area");
+static_assert(W2Bar::count * 8 <= kW2OffSa0 && kW2OffSa0 + 512 <= kOffMisc, "token-scale area 0");
+static_assert(kWideOffTab + 3 * 2 * 4 <= kW2OffSa1 && kW2OffSa1 + 512 <= kW2OffStages,
+              "token-scale area 1 (dense calls: one expert)");
 
 template <bool kDebug, bool kA16 = false>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1319,6 +1343,7 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        float *s_sa = reinterpret_cast<float *>(smem + (h == 0 ? kW2OffSa0 : kW2OffSa1));
         float acc[128];
 #pragma unroll
         for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
@@ -1334,11 +1359,25 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             float sc0 = n_ok ? ldg_nc_f32_now(swp) : 0.0f;
             float sc1 = (n_ok && G > 1) ? ldg_nc_f32_now(swp + 1) : 0.0f;
             const int col0 = 128 * h;
+            // The tile's token scales, copied into shared memory now (one per
+            // thread, asynchronously) and read at the store: the copies land
+            // while the tile's groups run. The barrier first lets every
+            // thread of the warpgroup finish reading the previous tile's.
+            named_barrier_sync(1 + h, 128);
+            {
+                const int col = col0 + lrow;
+                if (p.sa != nullptr)
+                    cp_async_4(smem_u32(s_sa + lrow), p.sa + ti.m0 + min(col, ti.rows - 1),
+                               col < ti.rows ? 4u : 0u);
+                else
+                    s_sa[lrow] = 1.0f;
+            }
             for (int g = 0; g < G; ++g) {
                 const float sc = sc0;
                 sc0 = sc1;
                 sc1 = (n_ok && g + 2 < G) ? ldg_nc_f32_now(swp + g + 2) : 0.0f;
-                if (!mbar_wait(bar(W2Bar::d_full), dph, s_abort, p.err, ROLE_EPILOGUE, 11)) {
+                const bool ok = mbar_wait(bar(W2Bar::d_full), dph, s_abort, p.err, ROLE_EPILOGUE, 11);
+                if (__any_sync(0xFFFFFFFFu, !ok)) {   // the warp fails as one
                     failed = true;
                     break;
                 }
@@ -1365,31 +1404,28 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 __syncwarp();
                 if (lane == 0) mbar_arrive_relaxed(bar(W2Bar::d_empty));
             }
-            if (failed) break;
+            // The warpgroup's copies have landed once all its threads pass the
+            // barrier, which also makes a failure of any of its warps theirs.
+            cp_async_wait_all();
+            if (named_barrier_or(1 + h, 128, failed)) break;
             if (n_ok) {
                 // Token rows [m0 + col0, m0 + col0 + 128) of output column
-                // n_local: one running pointer, and chunks of 16 rows so that
-                // the token-scale loads are not all hoisted ahead of the
-                // stores (registers).
+                // n_local through one running pointer.
                 const int rows_here = ti.rows - col0;
-                const float *sap = p.sa != nullptr ? p.sa + ti.m0 + col0 : nullptr;
                 const size_t first = static_cast<size_t>(ti.m0 + col0) * p.N + n_local;
                 if (p.out_fp32) {
                     float *yp = static_cast<float *>(p.y) + first;
 #pragma unroll
                     for (int j = 0; j < 128; ++j) {
-                        if (j < rows_here) *yp = acc[j] * (sap != nullptr ? __ldg(sap + j) : 1.0f);
+                        if (j < rows_here) *yp = acc[j] * s_sa[j];
                         yp += p.N;
-                        if ((j & 15) == 15) asm volatile("" ::: "memory");
                     }
                 } else {
                     __nv_bfloat16 *yp = static_cast<__nv_bfloat16 *>(p.y) + first;
 #pragma unroll
                     for (int j = 0; j < 128; ++j) {
-                        if (j < rows_here)
-                            *yp = __float2bfloat16_rn(acc[j] * (sap != nullptr ? __ldg(sap + j) : 1.0f));
+                        if (j < rows_here) *yp = __float2bfloat16_rn(acc[j] * s_sa[j]);
                         yp += p.N;
-                        if ((j & 15) == 15) asm volatile("" ::: "memory");
                     }
                 }
             }

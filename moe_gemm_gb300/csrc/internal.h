@@ -122,6 +122,16 @@ inline size_t sk_area_bytes(int64_t R, bool grouped) {
 // Dense calls of at least this many token rows run tiles of 128 weight rows x
 // 256 token rows (one 256-column MMA per 16 K).
 constexpr int kWide256MinRows = 256;
+// RMSNorm + per-token quantization (quant.cu): out_kind 0 int8 codes, 1 fp16
+// codes (dense rows of K; zeroes n_cnt split counters), 2 the BF16 rows.
+// K a multiple of 8, at most kRmsNormMaxK; x, gamma 16-byte aligned, out 16
+// (8 for int8 codes); row strides multiples of 8 elements.
+constexpr int64_t kRmsNormMaxK = 32768;
+cudaError_t launch_rmsnorm_quant(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                                 const uint16_t *gamma, float eps, int out_kind, void *out,
+                                 int64_t ldo, float *sa, int *cnt, int n_cnt, bool pow2,
+                                 cudaStream_t stream);
+
 inline bool uses_wide256(int64_t R, bool grouped) { return !grouped && R >= kWide256MinRows; }
 
 // Decode attention over a KV cache [B, Hkv, S_max, 128] (attention.cu): INT8

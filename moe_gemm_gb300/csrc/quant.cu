@@ -96,6 +96,136 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
     }
 }
 
+// Block-wide sum of floats in a fixed order (all threads get the same result):
+// a butterfly over each warp's 32 values, then one over the NT / 32 warp sums.
+template <int NT>
+__device__ __forceinline__ float block_sum_f32(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = lane < (NT / 32) ? red[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Block-wide max of non-negative 32-bit integers over NT threads.
+template <int NT>
+__device__ __forceinline__ uint32_t block_max_u32_n(uint32_t v, uint32_t *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = lane < (NT / 32) ? red[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// RMSNorm of 8 BF16 values (one 16-byte vector) with their 8 BF16 weights:
+// bf16_rn((x * inv) * gamma), two IEEE fp32 products.
+__device__ __forceinline__ uint4 rmsnorm8(const uint4 v, const uint4 g, float inv) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[i] & 0xFFFFu), inv),
+                                   bf16_bits_to_f32(gw[i] & 0xFFFFu));
+        const float hi = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[i] >> 16), inv),
+                                   bf16_bits_to_f32(gw[i] >> 16));
+        o[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// RMSNorm of each token row followed by its per-token quantization, one CTA
+// of NT threads per row with the row in registers (at most 4 vectors of 8
+// values per thread): y = bf16_rn((x * inv) * gamma) with
+// inv = 1 / sqrt(sum(x^2) / K + eps) in IEEE fp32 (the sum of squares: one
+// fma per element in K order within a thread, then block_sum_f32). The codes
+// and scale are those quant_act_vec_kernel gives for the BF16 rows y, so the
+// fused kernel equals a BF16 RMSNorm followed by the quantizer, with one HBM
+// pass fewer. kOut: 0 int8 codes, 1 fp16 codes (the tensor-core GEMM's
+// operand; block 0 also zeroes the n_cnt split counters, as quant_act does),
+// 2 the BF16 rows y themselves (no quantization; sa unused).
+template <int NT, int kOut>
+__global__ void __launch_bounds__(NT) rmsnorm_quant_kernel(
+    const uint16_t *__restrict__ x, int K, int64_t ldx, const uint16_t *__restrict__ gamma,
+    float eps, void *__restrict__ out, int64_t ldo, float *__restrict__ sa, int *__restrict__ cnt,
+    int n_cnt, int pow2) {
+    griddep_launch_dependents();   // as in quant_act_vec_kernel
+    griddep_wait();
+    if (kOut == 1 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
+    constexpr int VPT = 4;
+    __shared__ float redf[NT / 32];
+    __shared__ uint32_t red[NT / 32];
+    const int64_t row = blockIdx.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + row * ldx);
+    const int nvec = K >> 3;
+    uint4 v[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * NT;
+        v[i] = idx < nvec ? __ldcs(src + idx) : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = bf16_bits_to_f32(w[j] & 0xFFFFu);
+            const float hi = bf16_bits_to_f32(w[j] >> 16);
+            ss = __fmaf_rn(lo, lo, ss);
+            ss = __fmaf_rn(hi, hi, ss);
+        }
+    }
+    ss = block_sum_f32<NT>(ss, redf);
+    const float inv =
+        __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps)));
+    const uint4 *gv = reinterpret_cast<const uint4 *>(gamma);
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * NT;
+        if (idx < nvec) v[i] = rmsnorm8(v[i], __ldg(gv + idx), inv);
+        m = max(m, amax_bits8(v[i]));
+    }
+    if constexpr (kOut == 2) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int idx = threadIdx.x + i * NT;
+            if (idx < nvec)
+                __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + row * ldo) + idx,
+                       v[i]);
+        }
+        return;
+    }
+    m = block_max_u32_n<NT>(m, red);
+    const float amax = bf16_bits_to_f32(m);
+    const float s = pow2 ? pow2_scale(amax) : __fdiv_rn(amax, 127.0f);
+    const bool fast = s >= 1.17549435e-38f;  // normal scale: 1/s is finite
+    const float r = fast ? __frcp_rn(s) : 0.0f;
+    if (threadIdx.x == 0) sa[row] = s;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * NT;
+        if (idx >= nvec) continue;
+        const uint2 q = quantize8(v[i], s, r, fast);
+        if constexpr (kOut == 1) {
+            uint4 h;
+            i8x4_to_f16x4(q.x, h.x, h.y);
+            i8x4_to_f16x4(q.y, h.z, h.w);
+            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldo)[idx] = h;
+        } else {
+            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldo) + idx, q);
+        }
+    }
+}
+
 // Any K / stride / alignment: scalar two-pass version (re-reads the row).
 template <bool kF16>
 __global__ void __launch_bounds__(kQuantThreads) quant_act_generic_kernel(
@@ -266,7 +396,45 @@ cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, v
                       out, ldq, sa, cnt, n_cnt, pow2);
 }
 
+template <int kOut>
+cudaError_t launch_rmsnorm_k(const uint16_t *x, int64_t M, int K, int64_t ldx,
+                             const uint16_t *gamma, float eps, void *out, int64_t ldo, float *sa,
+                             int *cnt, int n_cnt, int pow2, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(M));
+    if (K <= 128 * 32)
+        return launch_pdl(rmsnorm_quant_kernel<128, kOut>, grid, dim3(128), stream, x, K, ldx,
+                          gamma, eps, out, ldo, sa, cnt, n_cnt, pow2);
+    if (K <= 256 * 32)
+        return launch_pdl(rmsnorm_quant_kernel<256, kOut>, grid, dim3(256), stream, x, K, ldx,
+                          gamma, eps, out, ldo, sa, cnt, n_cnt, pow2);
+    if (K <= 512 * 32)
+        return launch_pdl(rmsnorm_quant_kernel<512, kOut>, grid, dim3(512), stream, x, K, ldx,
+                          gamma, eps, out, ldo, sa, cnt, n_cnt, pow2);
+    return launch_pdl(rmsnorm_quant_kernel<1024, kOut>, grid, dim3(1024), stream, x, K, ldx,
+                      gamma, eps, out, ldo, sa, cnt, n_cnt, pow2);
+}
+
 }  // namespace
+
+cudaError_t launch_rmsnorm_quant(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                                 const uint16_t *gamma, float eps, int out_kind, void *out,
+                                 int64_t ldo, float *sa, int *cnt, int n_cnt, bool pow2,
+                                 cudaStream_t stream) {
+    const uintptr_t out_align = out_kind == 0 ? 8 : 16;   // one 8-value vector per store
+    if (K <= 0 || K % 8 != 0 || K > kRmsNormMaxK || ldx % 8 != 0 || ldo % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(gamma) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(out) % out_align != 0)
+        return cudaErrorInvalidValue;
+    if (cnt == nullptr) n_cnt = 0;
+    const int k = static_cast<int>(K);
+    const int p2 = pow2 ? 1 : 0;
+    switch (out_kind) {
+    case 0: return launch_rmsnorm_k<0>(x, M, k, ldx, gamma, eps, out, ldo, sa, cnt, n_cnt, p2, stream);
+    case 1: return launch_rmsnorm_k<1>(x, M, k, ldx, gamma, eps, out, ldo, sa, cnt, n_cnt, p2, stream);
+    case 2: return launch_rmsnorm_k<2>(x, M, k, ldx, gamma, eps, out, ldo, sa, cnt, n_cnt, p2, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_quant_act(const uint16_t *a, int64_t M, int64_t K, int64_t lda, int8_t *qa,
                              int64_t ldq, float *sa, cudaStream_t stream) {

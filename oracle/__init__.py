@@ -78,6 +78,7 @@ def _load():
         lib.oracle_quant_weight_blocks.argtypes = [p, i64, i64, i64, ctypes.c_int, p, p]
         lib.oracle_gemm_blocks.argtypes = [p, p, p, p, i64, i64, i64, i64, p, p]
         lib.oracle_w8a16_gemm.argtypes = [p, p, p, i64, i64, i64, i64, p, p]
+        lib.oracle_rmsnorm.argtypes = [p, i64, i64, i64, p, ctypes.c_double, p]
         lib.oracle_kv_dequant.argtypes = [p, p, i64, i64, p]
         lib.oracle_attention_decode.argtypes = [p, p, p, p, i64, i64, i64, i64, i64,
                                                 ctypes.c_double, p, p]
@@ -389,3 +390,20 @@ def attention_decode(q_bf16: np.ndarray, K: np.ndarray, V: np.ndarray, lens: np.
     _load().oracle_attention_decode(_ptr(q), _ptr(K), _ptr(V), _ptr(lens), B, Hq, Hkv, S_max, D,
                                     float(scale), _ptr(out), _ptr(T))
     return out, T
+
+
+def rmsnorm(x_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of BF16 rows [M, K] (uint16 bit patterns) with BF16 weights
+    gamma [K], in FP64: x / sqrt(mean(x^2) + eps) * gamma ("Deploying Hunyuan
+    770B in INT8 on domestic accelerators", §4.1, RMSNorm in high precision
+    before the INT8 GEMM). eps is taken as given (pass the FP32 value the
+    kernel uses)."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma_bf16, dtype=np.uint16)
+    M, K = x.shape
+    if g.shape != (K,):
+        raise ValueError("gamma must have K entries")
+    y = np.empty((M, K), np.float64)
+    lib.oracle_rmsnorm(_ptr(x), M, K, K, _ptr(g), float(eps), _ptr(y))
+    return y

@@ -537,3 +537,28 @@ void oracle_attention_decode(const uint16_t *q, const double *K, const double *V
         }
     }
 }
+
+/* ------------------------------------------------------------------------
+ * RMSNorm in front of the per-token quantizer ("Deploying Hunyuan 770B in
+ * INT8 on domestic accelerators", §4.1 operator table: RMSNorm runs in high
+ * precision beside the INT8 GEMMs, whose activations §3.1 quantizes per
+ * token). The definition, in FP64 from the BF16 inputs:
+ *   y[m, k] = x[m, k] / sqrt(mean_k(x[m, k]^2) + eps) * gamma[k].
+ * The BF16 rounding of y and the quantization of the rounded rows are the
+ * existing oracle functions (oracle_bf16_round, oracle_quant_act). */
+void oracle_rmsnorm(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, const uint16_t *gamma,
+                    double eps, double *y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *row = x + m * ldx;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double v = (double)bf16_bits_to_float(row[k]);
+            ss += v * v;   /* exact: a BF16 square has at most 16 significant bits */
+        }
+        const double r = sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k)
+            y[m * K + k] = (double)bf16_bits_to_float(row[k]) / r *
+                           (double)bf16_bits_to_float(gamma[k]);
+    }
+}

@@ -189,3 +189,37 @@ def test_linear_host_validation(lib):
     assert gcall(E=1025) == INVALID
     assert gcall(wsb=100) == WORKSPACE
     assert gcall(R=0) == OK
+
+
+def test_rmsnorm_host_validation(lib):
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.w8a8_rmsnorm.argtypes = [vp, i64, vp, f32, i64, i64, vp, i64, vp]
+    lib.w8a8_rmsnorm_quant.argtypes = [vp, i64, vp, f32, i32, i64, i64, vp, i64, vp, vp]
+    lib.w8a8_rmsnorm_linear.argtypes = [vp, i64, vp, f32, vp, vp, vp, i32, i64, i64, i64, vp,
+                                        ctypes.c_size_t, vp]
+
+    def norm(x=FAKE, ldx=64, g=FAKE, eps=1e-5, M=4, K=64, y=FAKE, ldy=64):
+        return lib.w8a8_rmsnorm(x, ldx, g, eps, M, K, y, ldy, None)
+    assert norm(eps=0.0) == INVALID
+    assert norm(eps=-1.0) == INVALID
+    assert norm(eps=float("inf")) == INVALID
+    assert norm(eps=float("nan")) == INVALID
+    assert norm(K=12, ldx=16, ldy=16) == INVALID        # K % 8 != 0
+    assert norm(K=32776, ldx=32776, ldy=32776) == INVALID   # K above 32768
+    assert norm(ldx=68) == INVALID                      # row stride not a multiple of 8
+    assert norm(ldx=56) == INVALID                      # ldx < K
+    assert norm(x=FAKE + 8) == INVALID                  # x not 16-byte aligned
+    assert norm(g=FAKE + 8) == INVALID
+    assert norm(y=None) == INVALID
+    assert norm(M=0, x=None, g=None, y=None) == OK
+    assert lib.w8a8_rmsnorm_quant(FAKE, 64, FAKE, 1e-5, 7, 4, 64, FAKE, 64, FAKE, None) == INVALID
+    assert lib.w8a8_rmsnorm_quant(FAKE, 64, FAKE, 1e-5, 0, 4, 64, FAKE + 4, 64, FAKE,
+                                  None) == INVALID      # codes not 8-byte aligned
+    # linear: K % 128 and the workspace as for w8a8_linear
+    assert lib.w8a8_rmsnorm_linear(FAKE, 64, FAKE, 1e-5, FAKE, FAKE, FAKE, 0, 4, 128, 64, FAKE,
+                                   1 << 30, None) == INVALID
+    assert lib.w8a8_rmsnorm_linear(FAKE, 256, FAKE, 1e-5, FAKE, FAKE, FAKE, 0, 4, 128, 256, None,
+                                   0, None) == WORKSPACE
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert norm() in (CUDA_ERR, UNSUPPORTED)

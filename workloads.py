@@ -41,7 +41,7 @@ DEFAULT_SEED = 0
 
 # Stable integer tags for the seed spawn keys.
 _TENSOR_TAGS = {"act": 1, "weight": 2, "outlier_channels": 3, "routing": 4,
-                "act_down": 5, "weight_down": 6, "gate_weight": 7}
+                "act_down": 5, "weight_down": 6, "gate_weight": 7, "norm_weight": 8}
 
 
 @dataclass(frozen=True)
@@ -174,6 +174,14 @@ def _weight_block(tag: int, tensor: str, block: int, K: int, std: float,
                   seed: int) -> np.ndarray:
     rng = _rng(seed, tag, tensor, block)
     return (rng.standard_normal((ROW_BLOCK, K), dtype=np.float32) * np.float32(std))
+
+
+def norm_weight(spec: DenseSpec, seed: int = DEFAULT_SEED) -> np.ndarray:
+    """BF16 bit patterns [K] of an RMSNorm weight for the spec's activation
+    rows: gamma ~ N(1, 0.25) (trained norm weights sit around 1; a few are
+    small or negative)."""
+    g = _rng(seed, spec.tag, "norm_weight").normal(1.0, 0.25, spec.K).astype(np.float32)
+    return f32_to_bf16_bits(g)
 
 
 def weights(spec: DenseSpec, rows: Optional[Sequence[int]] = None,
