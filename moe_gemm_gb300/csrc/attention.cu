@@ -9,14 +9,16 @@
 //    arithmetic), written to its row of the cache.
 //  * attn_decode_kernel: one query token per sequence, grouped-query heads
 //    (G query heads per kv head). A CTA takes 128 positions of one (sequence,
-//    kv head): it stages the chunk's K and V in shared memory, forms the G x
-//    128 scores (K codes widened exactly, the vector's scale applied to the
-//    dot product), the chunk's softmax statistics and its unnormalised
-//    output; attn_combine_kernel merges the chunks (max / sum rescaling).
+//    kv head): its lanes load their K and V pieces straight into tensor-core
+//    fragments, form the 128 x G scores (K codes widened exactly, the
+//    vector's scale applied to the dot product), the chunk's softmax
+//    statistics and its unnormalised output; attn_combine_kernel merges the
+//    chunks (max / sum rescaling).
 // Both kernels are HBM-bound streams of the cache; the BF16-cache form of the
 // same kernel (kInt8 = false) is the baseline the fused dequantization is
 // measured against.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -58,45 +60,110 @@ kv_quant_kernel(const uint16_t *__restrict__ x, int64_t n, const int32_t *__rest
     if (lane == 0) scales[row] = s;
 }
 
-// int8 x4 (one word) -> 4 floats, exact: each byte biased to unsigned is put
-// in the low mantissa bits of 2^23 and 2^23 + 128 subtracted.
-__device__ __forceinline__ void i8x4_to_f32x4(uint32_t w, float (&f)[4]) {
-    const uint32_t u = w ^ 0x80808080u;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        f[c] = __uint_as_float(0x4B000000u | ((u >> (8 * c)) & 0xFFu)) - 8388736.0f;
+// ------------------------------------------------------- tensor-core helpers
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Shared memory of one CTA (kInt8: codes; else BF16 values).
-template <int G, bool kInt8>
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8 x 8 matrix of 16-bit values held one 32-bit pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t x) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&x));
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t x) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Shared memory of one CTA: per-warp softmax statistics and unnormalised
+// outputs, merged across the 4 warps at the end.
+template <int G>
 struct AttnSmem {
-    static constexpr int kRowWords = kInt8 ? kHeadDim / 4 + 1 : kHeadDim / 2 + 1;  // padded
-    float q[G][kHeadDim];
-    uint32_t k[kChunk][kRowWords];
-    uint32_t v[kChunk][kInt8 ? kHeadDim / 4 : kHeadDim / 2];
-    float p[kChunk][G];              // scores, then probabilities times the V scale
-    float ks[kChunk], vs[kChunk];
-    float red[kAttnThreads / 32][G];
-    float stat[2][G];                // max, sum
+    static constexpr int kHeads = ((G + 7) / 8) * 8;
+    float red_m[kAttnThreads / 32][kHeads];
+    float red_l[kAttnThreads / 32][kHeads];
+    float red_o[kAttnThreads / 32][G][kHeadDim];
 };
 
-// grid (chunks, Hkv, B). Writes, per query head, the chunk's max score,
-// sum of exp(score - max) and unnormalised output sum_j exp(s_j - max) v_j.
-// Chunks at or past the sequence's length write nothing (the combine reads
-// only the first ceil(len / 128)).
-template <int G, bool kInt8>
+// grid (chunks, Hkv, B), 4 warps; warp w takes positions [32 w, 32 w + 32) of
+// the CTA's 128. Writes, per query head, the chunk's max score, sum of
+// exp(score - max) and unnormalised output sum_j exp(s_j - max) v_j. Chunks
+// at or past the sequence's length write nothing (the combine reads only the
+// first ceil(len / 128)).
+//
+// Both products run on the tensor cores (mma.sync m16n8k16, FP32
+// accumulation), each operand read from HBM straight into its fragment:
+//  * scores S^T[p, g] = sum_d K[p, d] q[g, d]: A = the K rows (int8 codes
+//    widened exactly to bf16, or the BF16 values), B = q (BF16). The
+//    reduction index d is permuted identically in A and B (a lane reads 32
+//    contiguous dimensions of its rows), which leaves every sum unchanged.
+//    Then s = S^T * (k_scale * softmax scale), as before;
+//  * output O^T[d, g] = sum_p V[p, d] P'[p, g] with P' = exp(s - m) * v_scale:
+//    A = V^T (codes widened exactly to fp16, or BF16 values; output rows d
+//    permuted so that a lane reads 16 contiguous dimensions), B = P' moved
+//    from the score fragments by an in-register transpose (movmatrix). P' is
+//    split into fp16 hi + lo (bf16 hi + mid + lo for the BF16 cache), so the
+//    products keep 22 (24) significant bits of P': the same accuracy class as
+//    FP32 products. For the INT8 cache, P' is first scaled by the power of two
+//    2^(14 - e) (e the exponent of the warp's largest v_scale), keeping it in
+//    fp16's normal range; the sums are scaled back exactly.
+template <int G, bool kInt8, bool kQVec>
 __global__ void __launch_bounds__(kAttnThreads)
 attn_decode_kernel(const uint16_t *__restrict__ q, const void *__restrict__ kc,
                    const float *__restrict__ ksc, const void *__restrict__ vc,
                    const float *__restrict__ vsc, const int32_t *__restrict__ lens, int Hkv,
                    int S_max, float scale, float *__restrict__ part_o,
                    float *__restrict__ part_ml) {
+    constexpr int NT = (G + 7) / 8;                 // n-tiles of 8 query heads
+    constexpr int kRowBytes = kInt8 ? kHeadDim : 2 * kHeadDim;
+    constexpr int KV = kRowBytes / 4 / 16;          // 16-byte vectors of a lane's K dims (32)
+    constexpr int VV = kRowBytes / 8 / 16;          // 16-byte vectors of a lane's V dims (16)
     griddep_launch_dependents();
     griddep_wait();   // the cache may have been written by the kernel before
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    AttnSmem<G, kInt8> &sm = *reinterpret_cast<AttnSmem<G, kInt8> *>(smem_raw);
+    AttnSmem<G> &sm = *reinterpret_cast<AttnSmem<G> *>(smem_raw);
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gid = lane >> 2, t = lane & 3;
     const int Hq = Hkv * G;
     const int nch = gridDim.x;
     const int L = min(max(lens[b], 0), S_max);
@@ -104,152 +171,274 @@ attn_decode_kernel(const uint16_t *__restrict__ q, const void *__restrict__ kc,
     if (j0 >= L) return;
     const int n = min(kChunk, L - j0);
     const int64_t vec0 = (static_cast<int64_t>(b) * Hkv + h) * S_max + j0;   // first cache row
+    const int pw = warp * 32;
+    const uint8_t *kbase = static_cast<const uint8_t *>(kc) + vec0 * kRowBytes;
+    const uint8_t *vbase = static_cast<const uint8_t *>(vc) + vec0 * kRowBytes;
+    const uint4 zero4 = make_uint4(0, 0, 0, 0);
 
-    // ---- stage q (FP32), the chunk's K and V rows and their scales
+    // ---- every load first: K rows pw + 16 mt + gid (+ 8), dims [32 t, 32 t + 32);
+    // V rows pw + 16 mt + 2 t + {0, 1, 8, 9}, dims [16 gid, 16 gid + 16); the
+    // scales of the K rows; q rows 8 nt + gid, dims [32 t, 32 t + 32)
+    uint4 kr[2][2][KV];
+    uint4 vr[2][4][VV];
+    float ksr[2][2], vsr[2][2];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-        sm.q[g][tid] = bf16_bits_to_f32(q[(static_cast<int64_t>(b) * Hq + h * G + g) * kHeadDim + tid]);
-    constexpr int kWords = kInt8 ? kHeadDim / 4 : kHeadDim / 2;   // 32-bit words per row
-    const uint4 *kg = reinterpret_cast<const uint4 *>(
-        static_cast<const uint8_t *>(kc) + vec0 * kWords * 4);
-    const uint4 *vg = reinterpret_cast<const uint4 *>(
-        static_cast<const uint8_t *>(vc) + vec0 * kWords * 4);
-    for (int idx = tid; idx < n * (kWords / 4); idx += kAttnThreads) {
-        const int r = idx / (kWords / 4), w4 = idx % (kWords / 4);
-        const uint4 kv = __ldcs(kg + idx);
-        const uint4 vv = __ldcs(vg + idx);
-        sm.k[r][4 * w4 + 0] = kv.x;
-        sm.k[r][4 * w4 + 1] = kv.y;
-        sm.k[r][4 * w4 + 2] = kv.z;
-        sm.k[r][4 * w4 + 3] = kv.w;
-        *reinterpret_cast<uint4 *>(&sm.v[r][4 * w4]) = vv;
-    }
-    if (kInt8 && tid < n) {
-        sm.ks[tid] = ksc[vec0 + tid];
-        sm.vs[tid] = vsc[vec0 + tid];
-    }
-    __syncthreads();
-
-    // ---- scores: thread = position
-    float acc[G];
+    for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.0f;
-    if (tid < n) {
-#pragma unroll 4
-        for (int w = 0; w < kWords; ++w) {
-            const uint32_t kw = sm.k[tid][w];
+        for (int hf = 0; hf < 2; ++hf) {
+            const int row = pw + 16 * mt + gid + 8 * hf;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                kbase + static_cast<int64_t>(row) * kRowBytes + t * (kRowBytes / 4));
+#pragma unroll
+            for (int v = 0; v < KV; ++v) kr[mt][hf][v] = row < n ? __ldcs(src + v) : zero4;
             if constexpr (kInt8) {
-                float f[4];
-                i8x4_to_f32x4(kw, f);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float4 qv = *reinterpret_cast<const float4 *>(&sm.q[g][4 * w]);
-                    acc[g] = fmaf(qv.x, f[0], fmaf(qv.y, f[1], fmaf(qv.z, f[2], fmaf(qv.w, f[3], acc[g]))));
-                }
+                ksr[mt][hf] = row < n ? __ldcs(ksc + vec0 + row) : 0.0f;
+                vsr[mt][hf] = row < n ? __ldcs(vsc + vec0 + row) : 0.0f;
             } else {
-                const float f0 = __uint_as_float(kw << 16), f1 = __uint_as_float(kw & 0xFFFF0000u);
+                ksr[mt][hf] = 1.0f;
+                vsr[mt][hf] = row < n ? 1.0f : 0.0f;
+            }
+        }
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float2 qv = *reinterpret_cast<const float2 *>(&sm.q[g][2 * w]);
-                    acc[g] = fmaf(qv.x, f0, fmaf(qv.y, f1, acc[g]));
+        for (int j = 0; j < 4; ++j) {
+            const int row = pw + 16 * mt + 2 * t + (j < 2 ? j : j + 6);
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                vbase + static_cast<int64_t>(row) * kRowBytes + gid * (kRowBytes / 8));
+#pragma unroll
+            for (int v = 0; v < VV; ++v) vr[mt][j][v] = row < n ? __ldcs(src + v) : zero4;
+        }
+    }
+    uint32_t qf[NT][16];   // q[8 nt + gid][32 t + 2 w .. + 1] as bf16 pairs
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int g = 8 * nt + gid;
+        const uint16_t *qrow =
+            q + (static_cast<int64_t>(b) * Hq + h * G + (g < G ? g : 0)) * kHeadDim + 32 * t;
+        if constexpr (kQVec) {   // q 16-byte aligned, else 2-byte loads
+            const uint4 *src = reinterpret_cast<const uint4 *>(qrow);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 x = g < G ? __ldg(src + v) : zero4;
+                qf[nt][4 * v + 0] = x.x;
+                qf[nt][4 * v + 1] = x.y;
+                qf[nt][4 * v + 2] = x.z;
+                qf[nt][4 * v + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int w = 0; w < 16; ++w)
+                qf[nt][w] = g < G ? (static_cast<uint32_t>(__ldg(qrow + 2 * w)) |
+                                     (static_cast<uint32_t>(__ldg(qrow + 2 * w + 1)) << 16))
+                                  : 0u;
+        }
+    }
+
+    // ---- scores: k-step kb covers dims 32 t + 4 kb + {0..3} of each lane
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sacc[mt][nt][i] = 0.0f;
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            uint32_t a[4];
+            if constexpr (kInt8) {
+                i8x4_to_bf16x4(word_of(kr[mt][0][kb >> 2], kb & 3), a[0], a[2]);
+                i8x4_to_bf16x4(word_of(kr[mt][1][kb >> 2], kb & 3), a[1], a[3]);
+            } else {
+                a[0] = word_of(kr[mt][0][kb >> 1], (2 * kb) & 3);
+                a[2] = word_of(kr[mt][0][kb >> 1], (2 * kb + 1) & 3);
+                a[1] = word_of(kr[mt][1][kb >> 1], (2 * kb) & 3);
+                a[3] = word_of(kr[mt][1][kb >> 1], (2 * kb + 1) & 3);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_bf16(sacc[mt][nt], a, qf[nt][2 * kb], qf[nt][2 * kb + 1]);
+        }
+    }
+    // scaled scores; fragment i: row gid + 8 (i >> 1), head 8 nt + 2 t + (i & 1)
+    float m_loc[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) m_loc[nt][0] = m_loc[nt][1] = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int hf = i >> 1;
+                const int row = pw + 16 * mt + gid + 8 * hf;
+                const float sv = row < n ? sacc[mt][nt][i] * (ksr[mt][hf] * scale) : -INFINITY;
+                sacc[mt][nt][i] = sv;
+                m_loc[nt][i & 1] = fmaxf(m_loc[nt][i & 1], sv);
+            }
+    // ---- softmax statistics: max over the lanes of a head, then the warps
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float m = m_loc[nt][j];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (gid == 0) sm.red_m[warp][8 * nt + 2 * t + j] = m;
+        }
+    __syncthreads();
+    float mx[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float m = sm.red_m[0][8 * nt + 2 * t + j];
+#pragma unroll
+            for (int w = 1; w < kAttnThreads / 32; ++w)
+                m = fmaxf(m, sm.red_m[w][8 * nt + 2 * t + j]);
+            mx[nt][j] = m;
+        }
+    // the warp's largest V scale sets the power of two that keeps P' in
+    // fp16's normal range (INT8 cache); rows of other lanes t are the same
+    float pscale = 1.0f, pinv = 1.0f;
+    if constexpr (kInt8) {
+        float vmax = fmaxf(fmaxf(vsr[0][0], vsr[0][1]), fmaxf(vsr[1][0], vsr[1][1]));
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
+        const int bexp = static_cast<int>((__float_as_uint(vmax) >> 23) & 0xFFu);
+        if (bexp != 0) {
+            const int se = max(-100, min(100, 14 - (bexp - 127)));
+            pscale = __uint_as_float(static_cast<uint32_t>(se + 127) << 23);
+            pinv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);
+        }
+    }
+    // probabilities, their sums, and the B fragments of the output product
+    float l_loc[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) l_loc[nt][0] = l_loc[nt][1] = 0.0f;
+    constexpr int NS = kInt8 ? 2 : 3;   // hi, lo (fp16) or hi, mid, lo (bf16)
+    uint32_t bp[2][NT][NS][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float pp[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float pr = expf(sacc[mt][nt][i] - mx[nt][i & 1]);
+                l_loc[nt][i & 1] += pr;
+                pp[i] = (pr * vsr[mt][i >> 1]) * pscale;
+            }
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float x0 = pp[2 * hf], x1 = pp[2 * hf + 1];
+                if constexpr (kInt8) {
+                    const uint32_t hi = pack_f16x2(x0, x1);
+                    const float2 hv = unpack_f16x2(hi);
+                    const uint32_t lo = pack_f16x2(x0 - hv.x, x1 - hv.y);
+                    bp[mt][nt][0][hf] = movmatrix_trans(hi);
+                    bp[mt][nt][1][hf] = movmatrix_trans(lo);
+                } else {
+                    const uint32_t hi = pack_bf16x2(x0, x1);
+                    const float2 hv = unpack_bf16x2(hi);
+                    const float r0 = x0 - hv.x, r1 = x1 - hv.y;
+                    const uint32_t mid = pack_bf16x2(r0, r1);
+                    const float2 mv = unpack_bf16x2(mid);
+                    const uint32_t lo = pack_bf16x2(r0 - mv.x, r1 - mv.y);
+                    bp[mt][nt][0][hf] = movmatrix_trans(hi);
+                    bp[mt][nt][1][hf] = movmatrix_trans(mid);
+                    bp[mt][nt][2][hf] = movmatrix_trans(lo);
                 }
             }
         }
-    }
-    const float kscale = (kInt8 && tid < n) ? sm.ks[tid] * scale : scale;
-    float s[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) s[g] = tid < n ? acc[g] * kscale : -INFINITY;
-    // ---- softmax statistics of the chunk, per head
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float m = s[g];
+        for (int j = 0; j < 2; ++j) {
+            float l = l_loc[nt][j];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0) sm.red[warp][g] = m;
-    }
-    __syncthreads();
-    if (tid < G) {
-        float m = sm.red[0][tid];
-        for (int w = 1; w < kAttnThreads / 32; ++w) m = fmaxf(m, sm.red[w][tid]);
-        sm.stat[0][tid] = m;
-    }
-    __syncthreads();
-    float pr[G];
+            for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+            if (gid == 0) sm.red_l[warp][8 * nt + 2 * t + j] = l;
+        }
+
+    // ---- unnormalised output: m-tile i holds dims 16 gid + 2 i (row gid) and
+    // 16 gid + 2 i + 1 (row gid + 8)
+    float oacc[8][NT][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        pr[g] = tid < n ? expf(s[g] - sm.stat[0][g]) : 0.0f;
-        float l = pr[g];
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-        if (lane == 0) sm.red[warp][g] = l;
-        // probability times the V vector's scale (applied to the PV products)
-        sm.p[tid][g] = pr[g] * ((kInt8 && tid < n) ? sm.vs[tid] : 1.0f);
-    }
-    __syncthreads();
-    if (tid < G) {
-        float l = 0.0f;
-        for (int w = 0; w < kAttnThreads / 32; ++w) l += sm.red[w][tid];
-        sm.stat[1][tid] = l;
-    }
-    // ---- unnormalised output: warp = a quarter of the positions, lane = a
-    // word of V (4 int8 or 2 BF16 dimensions); then a sum over the warps
-    constexpr int kDimsPerLane = kInt8 ? 4 : 2;
-    constexpr int kLaneGroups = kHeadDim / (32 * kDimsPerLane);   // 1 (int8) or 2 (bf16)
-    float o[kLaneGroups][G][kDimsPerLane];
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int a = 0; a < kLaneGroups; ++a)
+            for (int r = 0; r < 4; ++r) oacc[i][nt][r] = 0.0f;
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+    for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-            for (int d = 0; d < kDimsPerLane; ++d) o[a][g][d] = 0.0f;
-    const int r0 = warp * (kChunk / 4), r1 = min(r0 + kChunk / 4, n);
-    for (int r = r0; r < r1; ++r) {
-#pragma unroll
-        for (int a = 0; a < kLaneGroups; ++a) {
-            const uint32_t vw = sm.v[r][lane + 32 * a];
-            float f[kDimsPerLane];
+        for (int i = 0; i < 8; ++i) {
+            uint32_t a[4];
             if constexpr (kInt8) {
-                float t[4];
-                i8x4_to_f32x4(vw, t);
+                // bytes 2i, 2i + 1 of the four positions' 16-byte vectors, as
+                // fp16 pairs over positions (1024 + biased byte, minus 1152)
+                const int w = i >> 1;
+                const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                const uint32_t g01 = prmt(word_of(vr[mt][0][0], w) ^ 0x80808080u,
+                                          word_of(vr[mt][1][0], w) ^ 0x80808080u, sel);
+                const uint32_t g23 = prmt(word_of(vr[mt][2][0], w) ^ 0x80808080u,
+                                          word_of(vr[mt][3][0], w) ^ 0x80808080u, sel);
+                uint32_t r[4] = {prmt(g01, 0x64646464u, 0x4140u), prmt(g01, 0x64646464u, 0x4342u),
+                                 prmt(g23, 0x64646464u, 0x4140u), prmt(g23, 0x64646464u, 0x4342u)};
 #pragma unroll
-                for (int d = 0; d < 4; ++d) f[d] = t[d];
+                for (int k = 0; k < 4; ++k)
+                    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(a[k]) : "r"(r[k]), "r"(0x64806480u));
             } else {
-                f[0] = __uint_as_float(vw << 16);
-                f[1] = __uint_as_float(vw & 0xFFFF0000u);
+                const uint32_t w0 = word_of(vr[mt][0][i >> 2], i & 3);
+                const uint32_t w1 = word_of(vr[mt][1][i >> 2], i & 3);
+                const uint32_t w2 = word_of(vr[mt][2][i >> 2], i & 3);
+                const uint32_t w3 = word_of(vr[mt][3][i >> 2], i & 3);
+                a[0] = prmt(w0, w1, 0x5410u);
+                a[1] = prmt(w0, w1, 0x7632u);
+                a[2] = prmt(w2, w3, 0x5410u);
+                a[3] = prmt(w2, w3, 0x7632u);
             }
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float pg = sm.p[r][g];
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int d = 0; d < kDimsPerLane; ++d) o[a][g][d] = fmaf(pg, f[d], o[a][g][d]);
-            }
+                for (int sp = 0; sp < NS; ++sp) {
+                    if constexpr (kInt8)
+                        mma_f16(oacc[i][nt], a, bp[mt][nt][sp][0], bp[mt][nt][sp][1]);
+                    else
+                        mma_bf16(oacc[i][nt], a, bp[mt][nt][sp][0], bp[mt][nt][sp][1]);
+                }
         }
     }
-    __syncthreads();   // sm.k and sm.v (contiguous) hold the cross-warp sum below
-    float *red_o = reinterpret_cast<float *>(&sm.k[0][0]);   // [4 warps][G][128]
-    static_assert(sizeof(AttnSmem<G, kInt8>::k) + sizeof(AttnSmem<G, kInt8>::v) >=
-                      4 * G * kHeadDim * sizeof(float),
-                  "cross-warp sum area");
+    // the warp's sums, scaled back exactly, to shared memory
 #pragma unroll
-    for (int a = 0; a < kLaneGroups; ++a)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int d = 0; d < kDimsPerLane; ++d)
-                red_o[(warp * G + g) * kHeadDim + (lane + 32 * a) * kDimsPerLane + d] = o[a][g][d];
+            for (int r = 0; r < 4; ++r) {
+                const int g = 8 * nt + 2 * t + (r & 1);
+                const int d = 16 * gid + 2 * i + (r >> 1);
+                if (g < G) sm.red_o[warp][g][d] = oacc[i][nt][r] * pinv;
+            }
     __syncthreads();
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         float sum = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kAttnThreads / 32; ++w) sum += red_o[(w * G + g) * kHeadDim + tid];
+        for (int w = 0; w < kAttnThreads / 32; ++w) sum += sm.red_o[w][g][tid];
         const int64_t hq = static_cast<int64_t>(b) * Hq + h * G + g;
         part_o[(hq * nch + c) * kHeadDim + tid] = sum;
-        if (tid == 0) {
-            part_ml[(hq * nch + c) * 2 + 0] = sm.stat[0][g];
-            part_ml[(hq * nch + c) * 2 + 1] = sm.stat[1][g];
-        }
+    }
+    if (tid < G) {
+        float m = sm.red_m[0][tid], l = 0.0f;
+#pragma unroll
+        for (int w = 1; w < kAttnThreads / 32; ++w) m = fmaxf(m, sm.red_m[w][tid]);
+#pragma unroll
+        for (int w = 0; w < kAttnThreads / 32; ++w) l += sm.red_l[w][tid];
+        const int64_t hq = static_cast<int64_t>(b) * Hq + h * G + tid;
+        part_ml[(hq * nch + c) * 2 + 0] = m;
+        part_ml[(hq * nch + c) * 2 + 1] = l;
     }
 }
 
@@ -298,10 +487,10 @@ cudaError_t launch_pdl_attn(void (*kernel)(Params...), dim3 grid, dim3 block, si
     return cudaGetLastError();
 }
 
-template <int G, bool kInt8>
-cudaError_t launch_attn_g(const AttnProblem &p, cudaStream_t stream) {
-    auto kernel = attn_decode_kernel<G, kInt8>;
-    const size_t smem = sizeof(AttnSmem<G, kInt8>);
+template <int G, bool kInt8, bool kQVec>
+cudaError_t launch_attn_q(const AttnProblem &p, cudaStream_t stream) {
+    auto kernel = attn_decode_kernel<G, kInt8, kQVec>;
+    const size_t smem = sizeof(AttnSmem<G>);
     static int attr_done[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -322,6 +511,12 @@ cudaError_t launch_attn_g(const AttnProblem &p, cudaStream_t stream) {
                            dim3(kAttnThreads), 0, stream, p.part_o, p.part_ml, p.lens,
                            static_cast<int>(p.Hkv * G), static_cast<int>(p.S_max), nch, p.out,
                            p.out_fp32 ? 1 : 0);
+}
+
+template <int G, bool kInt8>
+cudaError_t launch_attn_g(const AttnProblem &p, cudaStream_t stream) {
+    return (reinterpret_cast<uintptr_t>(p.q) & 15u) == 0 ? launch_attn_q<G, kInt8, true>(p, stream)
+                                                        : launch_attn_q<G, kInt8, false>(p, stream);
 }
 
 template <bool kInt8>
