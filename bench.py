@@ -400,7 +400,7 @@ class GpuContext:
             self.flush_sink = torch.empty((), dtype=torch.int64, device=self.dev)
         with torch.cuda.stream(self.stream):
             self.flush_buf.fill_(1)
-            torch.sum(self.flush_read, out=self.flush_sink)
+            torch.sum(self.flush_read, dim=0, out=self.flush_sink)
 
     def capture(self, fn):
         torch = self.torch
