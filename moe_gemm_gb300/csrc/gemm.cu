@@ -412,6 +412,11 @@ struct NBar {
     static constexpr int count = drain + 1;
 };
 static_assert(NBar::count <= 128, "barrier area");
+// Token scales of the current whole tile, 64 per epilogue warpgroup, in the
+// barrier area past the barriers.
+constexpr int kOffTokScales = 512;
+static_assert(NBar::count * 8 <= kOffTokScales && kOffTokScales + 2 * 64 * 4 <= kOffMisc,
+              "token-scale area");
 
 // kWide: 96- or 128-row token tiles. The two steps' partial buffers (2 x 2 x
 // 128 columns) would not fit next to the operand slots in TMEM, so one pair
@@ -750,6 +755,7 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        float *s_sa = reinterpret_cast<float *>(smem + kOffTokScales) + 32 * NCH * ewg;
         const bool vec_sw = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.sw) & 15u) == 0);
         auto store_out = [&](int m, int n_local, float v) {
             const float out = v;
@@ -838,18 +844,23 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const bool n_ok = n_local < p.N;
             const float *swp =
                 p.sw + (static_cast<size_t>(ti.e) * p.sw_rows + ((n_ok ? n_local : 0) >> p.sw_shift)) * G;
-            // Token scales of a whole tile's columns, one per lane (lane l
-            // holds column 32 c + l of chunk c), loaded now and broadcast at
-            // the store: their latency hides behind the tile's steps instead
-            // of lengthening its epilogue.
+            // Token scales of a whole tile's columns (this warpgroup's chunks),
+            // copied into shared memory now, one per thread, and read at the
+            // store: the copies land while the tile's steps run. (Loaded into
+            // registers instead, they were waited for at the store, ~1.5 us
+            // per tile under the weight stream.) The barrier first lets the
+            // warpgroup finish reading the previous tile's.
             const bool whole = s0 == 0 && s1 == plan.S;
-            float sa_l[NCH];
-#pragma unroll
-            for (int h = 0; h < NCH; ++h) {
-                const int col = 32 * (ewg + 2 * h) + lane;
-                sa_l[h] = !(whole && col < ti.rows) ? 0.0f
-                          : p.sa != nullptr        ? ldg_nc_f32_now(p.sa + ti.m0 + col)
-                                                   : 1.0f;
+            if (whole) {
+                named_barrier_sync(4 + ewg, 128);
+                if (lrow < 32 * NCH) {
+                    const int col = 32 * (ewg + 2 * (lrow >> 5)) + (lrow & 31);
+                    if (p.sa != nullptr)
+                        cp_async_4(smem_u32(s_sa + lrow), p.sa + ti.m0 + min(col, ti.rows - 1),
+                                   col < ti.rows ? 4u : 0u);
+                    else
+                        s_sa[lrow] = 1.0f;
+                }
             }
             // Scales of this row a quad of groups (two steps) ahead; loads are
             // issued in place and only read after the next quad boundary.
@@ -975,15 +986,17 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 pr.advance(NP);
             }
             if (whole) {
-                // every lane takes the shuffles (the column bound is warp-uniform)
+                // the warpgroup's copies have landed once all its threads pass
+                cp_async_wait_all();
+                named_barrier_sync(4 + ewg, 128);
+                if (n_ok && !failed) {
 #pragma unroll
-                for (int h = 0; h < NCH; ++h) {
+                    for (int h = 0; h < NCH; ++h) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = 32 * (ewg + 2 * h) + j;
-                        if (col < ti.rows) {
-                            const float sa = __shfl_sync(0xFFFFFFFFu, sa_l[h], j);
-                            if (n_ok && !failed) store_out(ti.m0 + col, n_local, acc[h][j] * sa);
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = 32 * (ewg + 2 * h) + j;
+                            if (col < ti.rows)
+                                store_out(ti.m0 + col, n_local, acc[h][j] * s_sa[32 * h + j]);
                         }
                     }
                 }

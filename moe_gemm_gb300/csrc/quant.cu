@@ -84,14 +84,12 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
     for (int i = 0; i < VPT; ++i) {
         const int idx = threadIdx.x + i * kQuantThreads;
         if (idx >= nvec) continue;
-        const uint2 q = quantize8(v[i], s, r, fast);
         if constexpr (kF16) {
-            uint4 h;
-            i8x4_to_f16x4(q.x, h.x, h.y);
-            i8x4_to_f16x4(q.y, h.z, h.w);
-            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldq)[idx] = h;
+            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldq)[idx] =
+                quantize8_f16(v[i], s, r, fast);
         } else {
-            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldq) + idx, q);
+            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldq) + idx,
+                   quantize8(v[i], s, r, fast));
         }
     }
 }
@@ -214,14 +212,12 @@ __global__ void __launch_bounds__(NT) rmsnorm_quant_kernel(
     for (int i = 0; i < VPT; ++i) {
         const int idx = threadIdx.x + i * NT;
         if (idx >= nvec) continue;
-        const uint2 q = quantize8(v[i], s, r, fast);
         if constexpr (kOut == 1) {
-            uint4 h;
-            i8x4_to_f16x4(q.x, h.x, h.y);
-            i8x4_to_f16x4(q.y, h.z, h.w);
-            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldo)[idx] = h;
+            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldo)[idx] =
+                quantize8_f16(v[i], s, r, fast);
         } else {
-            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldo) + idx, q);
+            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldo) + idx,
+                   quantize8(v[i], s, r, fast));
         }
     }
 }

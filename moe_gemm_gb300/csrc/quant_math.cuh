@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace w8a8 {
@@ -37,44 +38,84 @@ __device__ __forceinline__ int quantize_fast(float x, float s, float r) {
     return max(-127, min(127, q));
 }
 
+// The exact quotient's rounding, kept out of line: it runs for about one
+// value in 16000, and inlining it at every use made the quantizer's loop large
+// enough to stall on instruction fetch.
+static __device__ __noinline__ float code_by_division(float x, float s) {
+    return fminf(fmaxf(rintf(__fdiv_rn(x, s)), -127.0f), 127.0f);
+}
+
+// Adding 1.5 * 2^23 to a float of magnitude below 2^22 rounds it to an
+// integer (round-half-even, the FP32 adder's mode) and leaves that integer,
+// plus 2^22, in the low mantissa bits: the low byte is then the integer's
+// two's-complement byte, and subtracting the constant back is exact.
+constexpr float kRoundAdd = 12582912.0f;
+
+// The code of x, as the float code + kRoundAdd: the same code quantize_fast /
+// quantize_exact give. For finite x with |x| <= amax, s = fl(amax / 127) a
+// normal number and r = fl(1 / s): |x * r| and |x / s| are at most
+// 127 (1 + 2^-24)^3 < 127.5, so no clamp is needed on the fast path. A zero
+// code is +0 (y + c - c is +0 for |y| < 1/2).
+__device__ __forceinline__ float code_plus_round(float x, float s, float r, bool fast) {
+    if (!fast) return __fadd_rn(s == 0.0f ? 0.0f : code_by_division(x, s), kRoundAdd);
+    const float y = __fmul_rn(x, r);
+    const float f = __fadd_rn(y, kRoundAdd);
+    const float yi = __fsub_rn(f, kRoundAdd);
+    return fabsf(__fsub_rn(y, yi)) >= 0.5f - 3.0e-5f ? __fadd_rn(code_by_division(x, s), kRoundAdd)
+                                                      : f;
+}
+
 __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
     return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
            ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
 }
 
-// Quantize 8 BF16 values (one 16-byte vector) into 8 int8 codes.
-__device__ __forceinline__ uint2 quantize8(const uint4 v, float s, float r, bool fast) {
+// The codes of 8 BF16 values (one 16-byte vector), each as code + kRoundAdd.
+__device__ __forceinline__ void codes8(const uint4 v, float s, float r, bool fast, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    int q[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float lo = bf16_bits_to_f32(w[i] & 0xFFFFu);
-        const float hi = bf16_bits_to_f32(w[i] >> 16);
-        if (s == 0.0f) {
-            q[2 * i] = 0;
-            q[2 * i + 1] = 0;
-        } else if (fast) {
-            q[2 * i] = quantize_fast(lo, s, r);
-            q[2 * i + 1] = quantize_fast(hi, s, r);
-        } else {
-            q[2 * i] = quantize_exact(lo, s);
-            q[2 * i + 1] = quantize_exact(hi, s);
-        }
+        f[2 * i] = code_plus_round(bf16_bits_to_f32(w[i] & 0xFFFFu), s, r, fast);
+        f[2 * i + 1] = code_plus_round(bf16_bits_to_f32(w[i] >> 16), s, r, fast);
     }
-    return make_uint2(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]));
+}
+
+// The low bytes of four code + kRoundAdd floats, packed in order.
+__device__ __forceinline__ uint32_t pack_code_bytes(float a, float b, float c, float d) {
+    uint32_t lo, hi, w;
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(lo) : "r"(__float_as_uint(a)), "r"(__float_as_uint(b)));
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(hi) : "r"(__float_as_uint(c)), "r"(__float_as_uint(d)));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(lo), "r"(hi));
+    return w;
+}
+
+// Quantize 8 BF16 values (one 16-byte vector) into 8 int8 codes.
+__device__ __forceinline__ uint2 quantize8(const uint4 v, float s, float r, bool fast) {
+    float f[8];
+    codes8(v, s, r, fast, f);
+    return make_uint2(pack_code_bytes(f[0], f[1], f[2], f[3]), pack_code_bytes(f[4], f[5], f[6], f[7]));
+}
+
+// The same 8 codes as fp16 (exact integers; the tensor-core GEMM's operand).
+__device__ __forceinline__ uint4 quantize8_f16(const uint4 v, float s, float r, bool fast) {
+    float f[8];
+    codes8(v, s, r, fast, f);
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 p = __floats2half2_rn(__fsub_rn(f[2 * i], kRoundAdd),
+                                            __fsub_rn(f[2 * i + 1], kRoundAdd));
+        h[i] = *reinterpret_cast<const uint32_t *>(&p);
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 // Max of |bf16| over a 16-byte vector, as the BF16 magnitude bit pattern:
 // for finite values, ordering of |x| equals the unsigned ordering of (bits & 0x7FFF).
 __device__ __forceinline__ uint32_t amax_bits8(const uint4 v) {
-    uint32_t m = 0;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        m = max(m, w[i] & 0x7FFFu);
-        m = max(m, (w[i] >> 16) & 0x7FFFu);
-    }
-    return m;
+    uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                          __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
 }
 
 // Power-of-two (UE8M0) scale of a group whose largest magnitude is amax: the
