@@ -91,26 +91,33 @@ def load_peaks():
             "source": "fallback"}
 
 
-def gemm_source_hash() -> str:
+def kernel_source_hash() -> str:
+    """Hash of every CUDA source of the library (a recorded ncu traffic figure
+    is used only while the kernels it was taken on are unchanged)."""
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh", "quant_math.cuh"):
-        with open(os.path.join(ROOT, "moe_gemm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "moe_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per GEMM launch from an ncu capture, if it was taken on the
-    current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    """DRAM bytes per launch of the workload's dominant kernel from an ncu
+    capture, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     rec = d.get(workload)
-    if not rec or rec.get("kernel_source_hash") != gemm_source_hash():
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch")
+    # the step's launches of the dominant kernel, summed (one launch for most
+    # workloads); the per-launch figures beside it
+    return rec.get("dram_bytes_per_step"), rec.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------ workloads
@@ -690,7 +697,8 @@ def measure_workload(ctx, name, headline):
         achieved = sum(alg) / (sum(gemm_ms) * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": recorded_traffic(name),
+                "traffic": (recorded_traffic(name) or (None, None))[0],
+                "traffic_per_launch": (recorded_traffic(name) or (None, None))[1],
                 "alg_bytes_per_launch": alg,
                 "peak_source": f"{peaks['source']} HBM copy bandwidth"}
     else:
@@ -698,7 +706,8 @@ def measure_workload(ctx, name, headline):
         achieved = sum(flops) / (sum(gemm_ms) * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": recorded_traffic(name),
+                "traffic": (recorded_traffic(name) or (None, None))[0],
+                "traffic_per_launch": (recorded_traffic(name) or (None, None))[1],
                 "ops_per_launch": flops,
                 "peak_source": (f"{peaks['source']} dense bf16 burst (the integer-exact path "
                                 "runs on the fp16 tensor cores, whose dense rate equals bf16's)")}
@@ -805,7 +814,9 @@ def measure_norm(ctx, headline):
     peaks = ctx.peaks
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": recorded_traffic("norm_quant"), "alg_bytes_per_launch": [alg],
+            "traffic": (recorded_traffic("norm_quant") or (None, None))[0],
+            "traffic_per_launch": (recorded_traffic("norm_quant") or (None, None))[1],
+            "alg_bytes_per_launch": [alg],
             "peak_source": f"{peaks['source']} HBM copy bandwidth",
             "kernel_ms_per_launch": [round(fused_ms, 5)],
             "kernel_time": "median over the timed steps, L2 flushed before each",
