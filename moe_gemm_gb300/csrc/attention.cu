@@ -252,7 +252,7 @@ struct WarpState {
 template <int G, bool kInt8>
 __device__ __forceinline__ void attend_chunk(WarpState<(G + 7) / 8> &st, const ChunkRegs<kInt8> &r,
                                              const uint32_t (&qf)[(G + 7) / 8][16], int n,
-                                             float scale, int pw, int gid, int t) {
+                                             float scale, float qinv, int pw, int gid, int t) {
     constexpr int NT = (G + 7) / 8;
     // ---- scores: k-step kb covers dims 32 t + 4 kb + {0..3} of each lane
     float sacc[2][NT][4];
@@ -268,17 +268,21 @@ __device__ __forceinline__ void attend_chunk(WarpState<(G + 7) / 8> &st, const C
         for (int mt = 0; mt < 2; ++mt) {
             uint32_t a[4];
             if constexpr (kInt8) {
-                i8x4_to_bf16x4(word_of(r.k[mt][0][kb >> 2], kb & 3), a[0], a[2]);
-                i8x4_to_bf16x4(word_of(r.k[mt][1][kb >> 2], kb & 3), a[1], a[3]);
+                // codes widened exactly to fp16; q is in fp16 too (scaled)
+                i8x4_to_f16x4(word_of(r.k[mt][0][kb >> 2], kb & 3), a[0], a[2]);
+                i8x4_to_f16x4(word_of(r.k[mt][1][kb >> 2], kb & 3), a[1], a[3]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16(sacc[mt][nt], a, qf[nt][2 * kb], qf[nt][2 * kb + 1]);
             } else {
                 a[0] = word_of(r.k[mt][0][kb >> 1], (2 * kb) & 3);
                 a[2] = word_of(r.k[mt][0][kb >> 1], (2 * kb + 1) & 3);
                 a[1] = word_of(r.k[mt][1][kb >> 1], (2 * kb) & 3);
                 a[3] = word_of(r.k[mt][1][kb >> 1], (2 * kb + 1) & 3);
-            }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma_bf16(sacc[mt][nt], a, qf[nt][2 * kb], qf[nt][2 * kb + 1]);
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_bf16(sacc[mt][nt], a, qf[nt][2 * kb], qf[nt][2 * kb + 1]);
+            }
         }
     }
     // scaled scores (fragment i: row gid + 8 (i >> 1), head 8 nt + 2 t + (i & 1))
@@ -294,7 +298,9 @@ __device__ __forceinline__ void attend_chunk(WarpState<(G + 7) / 8> &st, const C
             for (int i = 0; i < 4; ++i) {
                 const int hf = i >> 1;
                 const int row = pw + 16 * mt + gid + 8 * hf;
-                const float sv = row < n ? sacc[mt][nt][i] * (r.ks[mt][hf] * scale) : -INFINITY;
+                // (the fp16 q carries the power of two 1/qinv: scaling back is exact)
+                const float sv =
+                    row < n ? (sacc[mt][nt][i] * (r.ks[mt][hf] * scale)) * qinv : -INFINITY;
                 sacc[mt][nt][i] = sv;
                 mc[nt][i & 1] = fmaxf(mc[nt][i & 1], sv);
             }
@@ -501,6 +507,35 @@ attn_decode_kernel(const uint16_t *__restrict__ q, const void *__restrict__ kc,
                                   : 0u;
         }
     }
+    // INT8 cache: the score product runs in fp16 (the codes widen to fp16 in
+    // half the instructions bf16 takes). q goes to fp16 scaled by the power of
+    // two 2^(14 - e), e the exponent of the largest |q| of the CTA's heads (the
+    // warp holds all of them), so the largest value sits in [2^14, 2^15) and
+    // every value of at least 2^-14 of the scaled range converts exactly; the
+    // scores are scaled back by qinv exactly.
+    float qinv = 1.0f;
+    if constexpr (kInt8) {
+        uint32_t mq = 0;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int w = 0; w < 16; ++w) mq = __vmaxu2(mq, qf[nt][w] & 0x7FFF7FFFu);
+        mq = max(mq & 0xFFFFu, mq >> 16);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) mq = max(mq, __shfl_xor_sync(0xFFFFFFFFu, mq, o));
+        const int bexp = static_cast<int>((mq >> 7) & 0xFFu);   // bf16 exponent field
+        const int se = bexp == 0 ? 0 : max(-100, min(100, 14 - (bexp - 127)));
+        const float qs = __uint_as_float(static_cast<uint32_t>(se + 127) << 23);
+        qinv = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+                const __half2 hq = __floats2half2_rn(__uint_as_float(qf[nt][w] << 16) * qs,
+                                                     __uint_as_float(qf[nt][w] & 0xFFFF0000u) * qs);
+                qf[nt][w] = *reinterpret_cast<const uint32_t *>(&hq);
+            }
+    }
     WarpState<NT> st;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -525,7 +560,7 @@ attn_decode_kernel(const uint16_t *__restrict__ q, const void *__restrict__ kc,
         __syncthreads();            // every warp has its fragments: the stage is free
         if (cc + 2 < c_end) issue(cc + 2);
         cp_async_commit();
-        attend_chunk<G, kInt8>(st, r, qf, rows_of(cc), scale, pw, gid, t);
+        attend_chunk<G, kInt8>(st, r, qf, rows_of(cc), scale, qinv, pw, gid, t);
     }
     cp_async_wait_group<0>();
     __syncthreads();   // the stages are free for the merge below

@@ -25,85 +25,112 @@ namespace w8a8 {
 namespace {
 
 // ------------------------------------------------------------------ routing
-constexpr int kRouteThreads = 512;
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
 
-// One CTA. Shared memory: cnt[E + 1] (counts, then offsets) and fill[E].
-// Entries whose id is outside [0, E) are not routed (row_of = -1).
+// One CTA of 32 warps. Warp w owns the entries [w C, (w + 1) C), C = ceil(n /
+// 32), and walks them 32 at a time in entry order. Shared memory: cntw[w][e]
+// (the warp's count of expert e, then the first row of its expert-e entries)
+// and tot[e + 1]. Entries whose id is outside [0, E) are not routed (row_of =
+// -1). The rows of an expert keep the entries' order (warps in order, lanes
+// in order within a warp), so the permutation is the stable sort by expert.
 __global__ void __launch_bounds__(kRouteThreads)
 moe_route_kernel(const int32_t *__restrict__ ids, int n, int k, int E, int32_t *__restrict__ offsets,
                  int32_t *__restrict__ row_of, int32_t *__restrict__ token_of_row,
                  int32_t *__restrict__ pair_of_row) {
     extern __shared__ int s_route[];
-    int *cnt = s_route;           // [E + 1]
-    int *fill = s_route + E + 1;  // [E]
+    int *cntw = s_route;                       // [kRouteWarps][E]
+    int *tot = s_route + kRouteWarps * E;      // [E + 1]
+    __shared__ int s_part[kRouteWarps];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const unsigned lt_mask = (1u << lane) - 1u;
     griddep_wait();   // the ids may come from the kernel launched before
-    for (int e = tid; e <= E; e += kRouteThreads) cnt[e] = 0;
+    for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) cntw[i] = 0;
     for (int r = tid; r < n; r += kRouteThreads) {
         token_of_row[r] = -1;
         pair_of_row[r] = -1;
     }
     __syncthreads();
-    // histogram
-    for (int i = tid; i < n; i += kRouteThreads) {
-        const int e = ids[i];
-        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    }
-    __syncthreads();
-    // exclusive prefix sum over the experts (warp 0: contiguous chunks per lane)
-    if (warp == 0) {
-        const int per = (E + 31) / 32;
-        const int e0 = min(lane * per, E), e1 = min(e0 + per, E);
-        int local = 0;
-        for (int e = e0; e < e1; ++e) local += cnt[e];
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - local;
-        for (int e = e0; e < e1; ++e) {
-            const int c = cnt[e];
-            cnt[e] = run;
-            fill[e] = run;
-            offsets[e] = run;
-            run += c;
-        }
-        if (lane == 31) {
-            cnt[E] = incl;
-            offsets[E] = incl;
-        }
-    }
-    __syncthreads();
-    // Stable scatter, 512 entries at a time: within a warp the entries of one
-    // expert are ranked by lane (match + popc), and the warps take their
-    // expert counters in warp order, one warp per barrier interval.
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = 0; base < n; base += kRouteThreads) {
-        const int i = base + tid;
-        const int e = i < n ? ids[i] : -1;
+    const int C = (n + kRouteWarps - 1) / kRouteWarps;
+    const int i0 = warp * C, i1 = min(i0 + C, n);
+    int *mine = cntw + warp * E;
+    // counts per (warp, expert): one leader per group of equal ids
+    for (int b = i0; b < i1; b += 32) {
+        const int i = b + lane;
+        const int e = i < i1 ? ids[i] : -1;
         const bool valid = e >= 0 && e < E;
         const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
-        const int rank = __popc(peers & lt_mask);
-        for (int w = 0; w < kRouteThreads / 32; ++w) {
-            if (warp == w && valid) {
-                const int leader = __ffs(peers) - 1;
-                int start = 0;
-                if (lane == leader) {
-                    start = fill[e];
-                    fill[e] = start + __popc(peers);
-                }
-                start = __shfl_sync(peers, start, leader);
-                const int r = start + rank;
-                row_of[i] = r;
-                token_of_row[r] = i / k;
-                pair_of_row[r] = i;
-            }
-            __syncthreads();
+        if (valid && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // per expert: exclusive prefix over the warps, and the expert's total
+    for (int e = tid; e < E; e += kRouteThreads) {
+        int run = 0;
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int c = cntw[w * E + e];
+            cntw[w * E + e] = run;
+            run += c;
         }
-        if (i < n && !valid) row_of[i] = -1;
+        tot[e] = run;
+    }
+    __syncthreads();
+    // exclusive prefix over the experts: each warp scans a contiguous range
+    // of experts, then the warps' sums are scanned
+    const int per = (E + kRouteThreads - 1) / kRouteThreads;   // experts per thread
+    const int e0 = min(tid * per, E), e1 = min(e0 + per, E);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += tot[e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_part[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += s_part[w];
+    int run = wbase + incl - local;
+    __syncthreads();   // every thread has read tot[e0, e1) before it is overwritten
+    for (int e = e0; e < e1; ++e) {
+        const int c = tot[e];
+        tot[e] = run;
+        offsets[e] = run;
+        run += c;
+    }
+    if (tid == kRouteThreads - 1) {
+        int all = 0;
+        for (int w = 0; w < kRouteWarps; ++w) all += s_part[w];
+        offsets[E] = all;
+    }
+    __syncthreads();
+    for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) cntw[i] += tot[i % E];
+    __syncthreads();
+    // scatter: the same walk, each group of equal ids taking its rows from
+    // the warp's running start for that expert
+    for (int b = i0; b < i1; b += 32) {
+        const int i = b + lane;
+        const int e = i < i1 ? ids[i] : -1;
+        const bool valid = e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+        const int leader = __ffs(peers) - 1;
+        int start = 0;
+        if (valid && lane == leader) {
+            start = mine[e];
+            mine[e] = start + __popc(peers);
+        }
+        start = __shfl_sync(0xFFFFFFFFu, start, leader);
+        if (valid) {
+            const int r = start + __popc(peers & lt_mask);
+            row_of[i] = r;
+            token_of_row[r] = i / k;
+            pair_of_row[r] = i;
+        } else if (i < i1) {
+            row_of[i] = -1;
+        }
+        __syncwarp();
     }
 }
 
@@ -304,7 +331,18 @@ cudaError_t launch_swiglu(const float *U, int64_t rows, int64_t I, const int32_t
 cudaError_t launch_moe_route(const int32_t *ids, int64_t T, int64_t k, int64_t E, int32_t *offsets,
                              int32_t *row_of, int32_t *token_of_row, int32_t *pair_of_row,
                              cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(2 * E + 1) * sizeof(int);
+    const size_t smem = static_cast<size_t>(kRouteWarps * E + E + 1) * sizeof(int);
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>((kRouteWarps * kMaxExperts + kMaxExperts + 1) *
+                                                  sizeof(int)));
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = 1;
+    }
     return launch_pdl_moe(moe_route_kernel, dim3(1), dim3(kRouteThreads), smem, stream, ids,
                           static_cast<int>(T * k), static_cast<int>(k), static_cast<int>(E),
                           offsets, row_of, token_of_row, pair_of_row);

@@ -135,8 +135,8 @@ __device__ __forceinline__ uint4 rmsnorm8(const uint4 v, const uint4 g, float in
                                    bf16_bits_to_f32(gw[i] & 0xFFFFu));
         const float hi = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[i] >> 16), inv),
                                    bf16_bits_to_f32(gw[i] >> 16));
-        o[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-               (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);   // one conversion for both
+        o[i] = *reinterpret_cast<const uint32_t *>(&b);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }

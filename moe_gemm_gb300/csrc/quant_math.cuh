@@ -70,13 +70,32 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
            ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
 }
 
-// The codes of 8 BF16 values (one 16-byte vector), each as code + kRoundAdd.
+// The codes of 8 BF16 values (one 16-byte vector), each as code + kRoundAdd:
+// code_plus_round for each value, with the near-half check of all 8 folded
+// into one branch (taken for about one vector in 2000).
 __device__ __forceinline__ void codes8(const uint4 v, float s, float r, bool fast, float (&f)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float x[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        f[2 * i] = code_plus_round(bf16_bits_to_f32(w[i] & 0xFFFFu), s, r, fast);
-        f[2 * i + 1] = code_plus_round(bf16_bits_to_f32(w[i] >> 16), s, r, fast);
+        x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+    if (!fast) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = code_plus_round(x[j], s, r, false);
+        return;
+    }
+    bool near = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float y = __fmul_rn(x[j], r);
+        f[j] = __fadd_rn(y, kRoundAdd);
+        near |= fabsf(__fsub_rn(y, __fsub_rn(f[j], kRoundAdd))) >= 0.5f - 3.0e-5f;
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = code_plus_round(x[j], s, r, true);
     }
 }
 
