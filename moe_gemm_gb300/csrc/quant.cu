@@ -23,6 +23,7 @@ namespace w8a8 {
 namespace {
 
 constexpr int kQuantThreads = 256;
+constexpr int64_t kQuantFewRows = 64;   // up to this many rows: 1024 threads per row
 
 // Block-wide max of non-negative 32-bit integers (all threads get the result).
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
@@ -35,63 +36,6 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
-}
-
-// kF16: the codes are written as fp16 (exact integers; the tensor-core GEMM's
-// operand) instead of int8, and block 0 also zeroes n_cnt split counters of
-// the GEMM that follows (after the wait below, so the GEMM before it, which
-// may share them, has finished).
-// src_rows (nullable): output row r quantizes input row src_rows[r] (a
-// gather, e.g. tokens into expert-sorted order); rows whose entry is
-// negative are skipped.
-// pow2: power-of-two (UE8M0) scales instead of amax / 127.
-template <int VPT, bool kF16>
-__global__ void __launch_bounds__(kQuantThreads) quant_act_vec_kernel(
-    const uint16_t *__restrict__ a, int K, int64_t lda, const int32_t *__restrict__ src_rows,
-    void *__restrict__ out, int64_t ldq, float *__restrict__ sa, int *__restrict__ cnt,
-    int n_cnt, int pow2) {
-    // A GEMM launched after this kernel as a programmatic dependent may start
-    // its set-up and weight stream now; it waits for this grid (and so for qa
-    // and sa) before it reads the codes. This kernel is itself launched as a
-    // programmatic dependent of the kernel before it (which may have written
-    // the activations, or still read qa/sa): it waits for that grid before
-    // touching either.
-    griddep_launch_dependents();
-    griddep_wait();
-    if (kF16 && blockIdx.x == 0)
-        for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
-    __shared__ uint32_t red[kQuantThreads / 32];
-    const int64_t row = blockIdx.x;
-    const int64_t in_row = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
-    if (in_row < 0) return;
-    const uint4 *src = reinterpret_cast<const uint4 *>(a + in_row * lda);
-    const int nvec = K >> 3;
-    uint4 v[VPT];
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int idx = threadIdx.x + i * kQuantThreads;
-        v[i] = idx < nvec ? __ldcs(src + idx) : make_uint4(0, 0, 0, 0);
-        m = max(m, amax_bits8(v[i]));
-    }
-    m = block_max_u32(m, red);
-    const float amax = bf16_bits_to_f32(m);
-    const float s = pow2 ? pow2_scale(amax) : __fdiv_rn(amax, 127.0f);
-    const bool fast = s >= 1.17549435e-38f;  // normal scale: 1/s is finite
-    const float r = fast ? __frcp_rn(s) : 0.0f;
-    if (threadIdx.x == 0) sa[row] = s;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int idx = threadIdx.x + i * kQuantThreads;
-        if (idx >= nvec) continue;
-        if constexpr (kF16) {
-            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldq)[idx] =
-                quantize8_f16(v[i], s, r, fast);
-        } else {
-            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldq) + idx,
-                   quantize8(v[i], s, r, fast));
-        }
-    }
 }
 
 // Block-wide sum of floats in a fixed order (all threads get the same result):
@@ -121,6 +65,65 @@ __device__ __forceinline__ uint32_t block_max_u32_n(uint32_t v, uint32_t *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
+}
+
+// kF16: the codes are written as fp16 (exact integers; the tensor-core GEMM's
+// operand) instead of int8, and block 0 also zeroes n_cnt split counters of
+// the GEMM that follows (after the wait below, so the GEMM before it, which
+// may share them, has finished).
+// src_rows (nullable): output row r quantizes input row src_rows[r] (a
+// gather, e.g. tokens into expert-sorted order); rows whose entry is
+// negative are skipped.
+// pow2: power-of-two (UE8M0) scales instead of amax / 127.
+// NT threads per row (256; 1024 for a few rows, where the latency of each
+// thread's chain of work, not bandwidth, sets the time), VPT vectors each.
+template <int NT, int VPT, bool kF16>
+__global__ void __launch_bounds__(NT) quant_act_vec_kernel(
+    const uint16_t *__restrict__ a, int K, int64_t lda, const int32_t *__restrict__ src_rows,
+    void *__restrict__ out, int64_t ldq, float *__restrict__ sa, int *__restrict__ cnt,
+    int n_cnt, int pow2) {
+    // A GEMM launched after this kernel as a programmatic dependent may start
+    // its set-up and weight stream now; it waits for this grid (and so for qa
+    // and sa) before it reads the codes. This kernel is itself launched as a
+    // programmatic dependent of the kernel before it (which may have written
+    // the activations, or still read qa/sa): it waits for that grid before
+    // touching either.
+    griddep_launch_dependents();
+    griddep_wait();
+    if (kF16 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
+    __shared__ uint32_t red[NT / 32];
+    const int64_t row = blockIdx.x;
+    const int64_t in_row = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
+    if (in_row < 0) return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a + in_row * lda);
+    const int nvec = K >> 3;
+    uint4 v[VPT];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * NT;
+        v[i] = idx < nvec ? __ldcs(src + idx) : make_uint4(0, 0, 0, 0);
+        m = max(m, amax_bits8(v[i]));
+    }
+    m = block_max_u32_n<NT>(m, red);
+    const float amax = bf16_bits_to_f32(m);
+    const float s = pow2 ? pow2_scale(amax) : __fdiv_rn(amax, 127.0f);
+    const bool fast = s >= 1.17549435e-38f;  // normal scale: 1/s is finite
+    const float r = fast ? __frcp_rn(s) : 0.0f;
+    if (threadIdx.x == 0) sa[row] = s;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int idx = threadIdx.x + i * NT;
+        if (idx >= nvec) continue;
+        if constexpr (kF16) {
+            reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * ldq)[idx] =
+                quantize8_f16(v[i], s, r, fast);
+        } else {
+            __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + row * ldq) + idx,
+                   quantize8(v[i], s, r, fast));
+        }
+    }
 }
 
 // RMSNorm of 8 BF16 values (one 16-byte vector) with their 8 BF16 weights:
@@ -376,18 +379,25 @@ cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, v
     const dim3 grid(static_cast<unsigned>(M));
     const dim3 block(kQuantThreads);
     if (cnt == nullptr) n_cnt = 0;
+    // a few rows: 1024 threads per row (one or two vectors each)
+    if (vec_ok && M <= kQuantFewRows && K <= 1024 * 8 * 1)
+        return launch_pdl(quant_act_vec_kernel<1024, 1, kF16>, grid, dim3(1024), stream, a, k, lda,
+                          src_rows, out, ldq, sa, cnt, n_cnt, pow2);
+    if (vec_ok && M <= kQuantFewRows && K <= 1024 * 8 * 2)
+        return launch_pdl(quant_act_vec_kernel<1024, 2, kF16>, grid, dim3(1024), stream, a, k, lda,
+                          src_rows, out, ldq, sa, cnt, n_cnt, pow2);
     if (vec_ok && K <= 256 * 8 * 1)
-        return launch_pdl(quant_act_vec_kernel<1, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt, pow2);
+        return launch_pdl(quant_act_vec_kernel<256, 1, kF16>, grid, block, stream, a, k, lda,
+                          src_rows, out, ldq, sa, cnt, n_cnt, pow2);
     if (vec_ok && K <= 256 * 8 * 2)
-        return launch_pdl(quant_act_vec_kernel<2, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt, pow2);
+        return launch_pdl(quant_act_vec_kernel<256, 2, kF16>, grid, block, stream, a, k, lda,
+                          src_rows, out, ldq, sa, cnt, n_cnt, pow2);
     if (vec_ok && K <= 256 * 8 * 4)
-        return launch_pdl(quant_act_vec_kernel<4, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt, pow2);
+        return launch_pdl(quant_act_vec_kernel<256, 4, kF16>, grid, block, stream, a, k, lda,
+                          src_rows, out, ldq, sa, cnt, n_cnt, pow2);
     if (vec_ok && K <= 256 * 8 * 8)
-        return launch_pdl(quant_act_vec_kernel<8, kF16>, grid, block, stream, a, k, lda, src_rows,
-                          out, ldq, sa, cnt, n_cnt, pow2);
+        return launch_pdl(quant_act_vec_kernel<256, 8, kF16>, grid, block, stream, a, k, lda,
+                          src_rows, out, ldq, sa, cnt, n_cnt, pow2);
     return launch_pdl(quant_act_generic_kernel<kF16>, grid, block, stream, a, k, lda, src_rows,
                       out, ldq, sa, cnt, n_cnt, pow2);
 }
