@@ -73,10 +73,14 @@ def unit_of(name):
     """Unit of a workload's value and its scale: GEMM-bearing workloads in
     TOPS, the HBM-bound RMSNorm + quantizer in GB/s of algorithmic bytes."""
     return ("GB/s", 1e9) if name == "norm_quant" else ("TOPS", 1e12)
-KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM (one library call) replayed back to back "
-                    "K times, events around the K launches, median of 3 such batches; the "
-                    "GEMM overlaps the quantizer, so this includes any part of the quantizer "
-                    "it does not hide")
+# Calls of one shape captured back to back in one graph for its per-launch
+# time (one graph launch per call would add the host's graph-launch gaps).
+SHAPE_CHAIN = 8
+KERNEL_TIME_NOTE = ("per shape: its quantizer + GEMM (one library call), %d calls back to back "
+                    "in one graph replayed K times, events around the K replays, median of 3 "
+                    "such batches, divided by %d K; the GEMM overlaps the quantizer, so this "
+                    "includes any part of the quantizer it does not hide"
+                    % (SHAPE_CHAIN, SHAPE_CHAIN))
 
 
 def load_peaks():
@@ -571,10 +575,12 @@ def measure_workload(ctx, name, headline):
     torch.cuda.synchronize()
     if graphs:
         run_step = ctx.capture(step).replay
-        run_shape = [ctx.capture(lambda d=d: linear_call(ctx, d, stream)).replay for d in per]
+        run_shape = [ctx.capture(lambda d=d: [linear_call(ctx, d, stream)
+                                              for _ in range(SHAPE_CHAIN)]).replay for d in per]
     else:
         run_step = step
-        run_shape = [lambda d=d: linear_call(ctx, d, stream) for d in per]
+        run_shape = [lambda d=d: [linear_call(ctx, d, stream) for _ in range(SHAPE_CHAIN)]
+                     for d in per]
     with torch.cuda.stream(stream):
         for _ in range(3):
             run_step()
@@ -616,7 +622,7 @@ def measure_workload(ctx, name, headline):
     ctx.barrier()
 
     # ---- per-shape time of the fused call (the GEMM dominates it)
-    gemm_ms = [ctx.batch_ms(r, args.steps) for r in run_shape]
+    gemm_ms = [ctx.batch_ms(r, args.steps) / SHAPE_CHAIN for r in run_shape]
     # ---- the quantizer alone (step a1; HBM-bound: 2 B read + 1 B written
     # per element + 4 B per row), per shape
     qbufs = [(torch.empty((d["shape"].M, d["shape"].K), dtype=torch.int8, device=ctx.dev),
@@ -630,9 +636,11 @@ def measure_workload(ctx, name, headline):
             return
         w8.quant_act(per[i]["a"], qa=qbufs[i][0], sa=qbufs[i][1], stream=stream)
 
-    run_quant = ([ctx.capture(lambda i=i: quant_call(i)).replay for i in range(len(per))]
-                 if graphs else [lambda i=i: quant_call(i) for i in range(len(per))])
-    quant_ms = [ctx.batch_ms(r, args.steps) for r in run_quant]
+    run_quant = ([ctx.capture(lambda i=i: [quant_call(i) for _ in range(SHAPE_CHAIN)]).replay
+                  for i in range(len(per))]
+                 if graphs else [lambda i=i: [quant_call(i) for _ in range(SHAPE_CHAIN)]
+                                 for i in range(len(per))])
+    quant_ms = [ctx.batch_ms(r, args.steps) / SHAPE_CHAIN for r in run_quant]
     del qbufs
 
     clocks = None
@@ -719,8 +727,9 @@ def measure_workload(ctx, name, headline):
             w8.attention_decode(d["a"], d["kb"], d["vb"], d["lens"], d["scale"], out=d["y"],
                                 workspace=d["ws"], stream=stream)
 
-        run_b = ctx.capture(bf16_call).replay if graphs else bf16_call
-        bms = ctx.batch_ms(run_b, args.steps)
+        run_b = (ctx.capture(lambda: [bf16_call() for _ in range(SHAPE_CHAIN)]).replay if graphs
+                 else lambda: [bf16_call() for _ in range(SHAPE_CHAIN)])
+        bms = ctx.batch_ms(run_b, args.steps) / SHAPE_CHAIN
         roof["bf16_cache_attention_ms"] = round(bms, 5)
         roof["int8_cache_step_over_bf16_attention"] = round(gemm_ms[0] / bms, 4)
     roof["kernel_ms_per_launch"] = [round(x, 5) for x in gemm_ms]

@@ -13,7 +13,7 @@ namespace w8a8 {
 // error word (first writer wins). Layout of the 64-bit code:
 //   bits 56..63 kernel id, 48..55 role, 32..47 wait site, 0..31 CTA index.
 
-enum KernelId : unsigned { KID_GEMM = 1, KID_SELFTEST = 2 };
+enum KernelId : unsigned { KID_GEMM = 1, KID_SELFTEST = 2, KID_QUANT = 3 };
 enum Role : unsigned {
     ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_CONVERT = 3, ROLE_EPILOGUE = 4, ROLE_SELFTEST = 5
 };
@@ -162,6 +162,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (both addresses 16-byte aligned,
+// bytes a multiple of 16), completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 

@@ -25,9 +25,9 @@
 //    kernel by the fused quantizer or by a staging kernel) is loaded by TMA
 //    with the 128-byte swizzle, through a ring of token stages that runs
 //    ahead of the MMAs. This kernel is launched as a programmatic dependent
-//    of that kernel: only the token producer waits for it
-//    (griddepcontrol.wait); the weight stream, the conversion and all set-up
-//    start at once.
+//    of that kernel: the token producer waits for it (griddepcontrol.wait)
+//    before loading codes, the epilogue before reading token scales; the
+//    weight stream, the conversion and all set-up start at once.
 //  * Two K groups move through the pipeline per step (one barrier hand-off,
 //    one commit and one epilogue wait per 32 KB of weights); see the kernel.
 //  * Epilogue warpgroups drain the partial buffers (tcgen05.ld), fma each
@@ -751,6 +751,9 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
     } else {
         // -------------------------------------------------------- epilogue
         setmaxnreg_inc<kEpiR>();
+        // The token scales come from the kernel launched before (which lets
+        // this grid start early): no read of them before that grid is done.
+        griddep_wait();
         const int ewg = wg - 2;   // owns token columns [32 c, 32 c + 32) for chunks c = ewg + 2 h
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
@@ -1390,6 +1393,7 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
     } else {
         // -------------------------------------------------------- epilogue
         setmaxnreg_inc<kEpiRegs>();
+        griddep_wait();   // the token scales come from the kernel launched before
         const int h = wg - 2;   // token columns [128 h, 128 h + 128)
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
@@ -2075,8 +2079,8 @@ cudaError_t launch_kernel(const GemmProblem &pr, const PipeShape &ps, int num_sm
     kp.sk_ld = split ? pr.sk_ld : 0;
 
     // Programmatic dependent launch: the kernel may start while the staging
-    // kernel before it in the stream is still running; only its token
-    // producer waits for that kernel (griddepcontrol.wait).
+    // kernel before it in the stream is still running; its token producer and
+    // its epilogue wait for that kernel (griddepcontrol.wait).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
@@ -2137,8 +2141,8 @@ cudaError_t launch_wide(const GemmProblem &pr, int num_sms, cudaStream_t stream)
     const int64_t tiles = (pr.R + kW2Tokens - 1) / kW2Tokens * kp.n_tiles;
     const int64_t grid = tiles < num_sms ? tiles : num_sms;
     if (grid <= 0) return cudaSuccess;
-    // Programmatic dependent launch: only the token producer waits for the
-    // kernel before it (which writes the fp16 codes).
+    // Programmatic dependent launch: the token producer and the epilogue wait
+    // for the kernel before it (which writes the fp16 codes and the scales).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
