@@ -132,12 +132,16 @@ __device__ __forceinline__ uint4 rmsnorm8(const uint4 v, const uint4 g, float in
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
     uint32_t o[4];
+    const unsigned long long inv2 = f2_bits(inv, inv);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float lo = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[i] & 0xFFFFu), inv),
-                                   bf16_bits_to_f32(gw[i] & 0xFFFFu));
-        const float hi = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[i] >> 16), inv),
-                                   bf16_bits_to_f32(gw[i] >> 16));
+        // (x * inv) * gamma for both halves, two IEEE products each (f32x2)
+        float lo, hi;
+        f2_split(f2_mul(f2_mul(f2_bits(bf16_bits_to_f32(w[i] & 0xFFFFu),
+                                       bf16_bits_to_f32(w[i] >> 16)),
+                               inv2),
+                        f2_bits(bf16_bits_to_f32(gw[i] & 0xFFFFu), bf16_bits_to_f32(gw[i] >> 16))),
+                 lo, hi);
         const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);   // one conversion for both
         o[i] = *reinterpret_cast<const uint32_t *>(&b);
     }

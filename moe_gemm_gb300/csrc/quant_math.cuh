@@ -70,6 +70,33 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
            ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
 }
 
+// Two IEEE binary32 operations in one instruction (the f32x2 forms of
+// sm_100-family GPUs): each half is rounded to nearest even exactly as the
+// scalar __fmul_rn / __fadd_rn / __fsub_rn of that half would be.
+__device__ __forceinline__ unsigned long long f2_bits(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(unsigned long long v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // The codes of 8 BF16 values (one 16-byte vector), each as code + kRoundAdd:
 // code_plus_round for each value, with the near-half check of all 8 folded
 // into one branch (taken for about one vector in 2000).
@@ -87,11 +114,16 @@ __device__ __forceinline__ void codes8(const uint4 v, float s, float r, bool fas
         return;
     }
     bool near = false;
+    const unsigned long long r2 = f2_bits(r, r), c2 = f2_bits(kRoundAdd, kRoundAdd);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float y = __fmul_rn(x[j], r);
-        f[j] = __fadd_rn(y, kRoundAdd);
-        near |= fabsf(__fsub_rn(y, __fsub_rn(f[j], kRoundAdd))) >= 0.5f - 3.0e-5f;
+    for (int i = 0; i < 4; ++i) {   // pairs: y = x*r, f = y + c, d = y - (f - c)
+        const unsigned long long y2 = f2_mul(f2_bits(x[2 * i], x[2 * i + 1]), r2);
+        const unsigned long long f2 = f2_add(y2, c2);
+        float d0, d1;
+        f2_split(f2_sub(y2, f2_sub(f2, c2)), d0, d1);
+        f2_split(f2, f[2 * i], f[2 * i + 1]);
+        near |= fabsf(d0) >= 0.5f - 3.0e-5f;
+        near |= fabsf(d1) >= 0.5f - 3.0e-5f;
     }
     if (near) {
 #pragma unroll
@@ -120,10 +152,12 @@ __device__ __forceinline__ uint4 quantize8_f16(const uint4 v, float s, float r, 
     float f[8];
     codes8(v, s, r, fast, f);
     uint32_t h[4];
+    const unsigned long long c2 = f2_bits(kRoundAdd, kRoundAdd);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const __half2 p = __floats2half2_rn(__fsub_rn(f[2 * i], kRoundAdd),
-                                            __fsub_rn(f[2 * i + 1], kRoundAdd));
+        float lo, hi;
+        f2_split(f2_sub(f2_bits(f[2 * i], f[2 * i + 1]), c2), lo, hi);
+        const __half2 p = __floats2half2_rn(lo, hi);
         h[i] = *reinterpret_cast<const uint32_t *>(&p);
     }
     return make_uint4(h[0], h[1], h[2], h[3]);
