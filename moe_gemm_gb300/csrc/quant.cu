@@ -250,7 +250,7 @@ constexpr int64_t kRowStreamMaxK = 16384;
 
 // kOut: 0 int8 codes, 1 fp16 codes (block 0 zeroes n_cnt split counters).
 template <int NT, int VPT, int kOut>
-__global__ void __launch_bounds__(NT) rows_stream_kernel(
+__global__ void __launch_bounds__(NT) quant_act_stream_kernel(
     const uint16_t *__restrict__ x, int64_t M, int K, int64_t ldx, void *__restrict__ out,
     int64_t ldo, float *__restrict__ sa, int *__restrict__ cnt, int n_cnt, int pow2,
     unsigned long long *__restrict__ err) {
@@ -479,10 +479,10 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStr
 // Row stream: a persistent grid of as many CTAs as fit on the device (by
 // shared memory), at most one per row; launched as a programmatic dependent.
 template <int NT, int VPT, int kOut>
-cudaError_t launch_rows_stream(const uint16_t *x, int64_t M, int K, int64_t ldx, void *out,
+cudaError_t launch_quant_stream(const uint16_t *x, int64_t M, int K, int64_t ldx, void *out,
                                int64_t ldo, float *sa, int *cnt, int n_cnt, int pow2,
                                cudaStream_t stream) {
-    auto kernel = rows_stream_kernel<NT, VPT, kOut>;
+    auto kernel = quant_act_stream_kernel<NT, VPT, kOut>;
     const int smem = kRowRing * K * 2;
     DeviceInfo info;
     cudaError_t e = current_device_info(&info);
@@ -518,16 +518,16 @@ cudaError_t launch_rows_stream(const uint16_t *x, int64_t M, int K, int64_t ldx,
 }
 
 template <int kOut>
-cudaError_t launch_rows_stream_k(const uint16_t *x, int64_t M, int K, int64_t ldx, void *out,
+cudaError_t launch_quant_stream_k(const uint16_t *x, int64_t M, int K, int64_t ldx, void *out,
                                  int64_t ldo, float *sa, int *cnt, int n_cnt, int pow2,
                                  cudaStream_t stream) {
     if (K <= 2048)
-        return launch_rows_stream<256, 1, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
+        return launch_quant_stream<256, 1, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
     if (K <= 4096)
-        return launch_rows_stream<256, 2, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
+        return launch_quant_stream<256, 2, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
     if (K <= 8192)
-        return launch_rows_stream<256, 4, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
-    return launch_rows_stream<512, 4, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
+        return launch_quant_stream<256, 4, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
+    return launch_quant_stream<512, 4, kOut>(x, M, K, ldx, out, ldo, sa, cnt, n_cnt, pow2, stream);
 }
 
 template <bool kF16>
@@ -544,7 +544,7 @@ cudaError_t launch_quant(const uint16_t *a, int64_t M, int64_t K, int64_t lda, v
     if (cnt == nullptr) n_cnt = 0;
     // many rows: the persistent row stream
     if (vec_ok && src_rows == nullptr && M > kRowStreamMinRows && K <= kRowStreamMaxK)
-        return launch_rows_stream_k<kF16 ? 1 : 0>(a, M, k, lda, out, ldq, sa, cnt, n_cnt, pow2,
+        return launch_quant_stream_k<kF16 ? 1 : 0>(a, M, k, lda, out, ldq, sa, cnt, n_cnt, pow2,
                                                   stream);
     // a few rows: 1024 threads per row (one or two vectors each)
     if (vec_ok && M <= kQuantFewRows && K <= 1024 * 8 * 1)
