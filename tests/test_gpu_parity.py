@@ -105,6 +105,52 @@ def test_quant_act_bitexact(M, K):
     np.testing.assert_array_equal(sa.cpu().numpy().view(np.uint32), sa_o.view(np.uint32))
 
 
+@pytest.mark.parametrize("M,K,pad,pow2", [
+    (65, 1024, 0, False), (300, 4104, 8, False), (1000, 16384, 0, False), (129, 24, 8, True),
+    (2000, 8192, 16, True), (70, 24576, 0, False),
+])
+def test_quant_act_many_rows_bitexact(M, K, pad, pow2):
+    """More than 64 rows (K <= 16384, aligned) take the persistent row stream;
+    K = 24576 takes the one-CTA-per-row kernel. Rows of every kind (zero,
+    subnormal scale, halves, large) land in different CTAs and ring buffers,
+    and the input rows may be padded (lda > K)."""
+    rng = np.random.default_rng(M + K + pad)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= rng.uniform(0.01, 30.0, (M, 1)).astype(np.float32)
+    x[0, : min(K, 64)] *= 50
+    x[1] = 0.0                                       # amax = 0 row
+    x[2] *= 2.0 ** -130                              # subnormal scale row
+    x[M - 1, : min(K, 8)] = [127.0, 2.5, 3.5, -2.5, 0.5, 1.5, 126.5, -126.5][: min(K, 8)]
+    x[M - 1, 8:] = 0.0                               # ties at amax 127
+    bits = workloads.f32_to_bf16_bits(x)
+    big = np.zeros((M, K + pad), np.uint16)
+    big[:, :K] = bits
+    a = to_dev_bf16(big)[:, :K]
+    mode = w8.SCALE_POW2 if pow2 else w8.SCALE_AMAX
+    qa, sa = w8.quant_act(a, scale_mode=mode)
+    qa_o, sa_o = (oracle.quant_act_pow2 if pow2 else oracle.quant_act)(bits)
+    np.testing.assert_array_equal(qa.cpu().numpy(), qa_o)
+    np.testing.assert_array_equal(sa.cpu().numpy().view(np.uint32), sa_o.view(np.uint32))
+    assert w8.device_error() == 0
+
+
+@pytest.mark.parametrize("M", [65, 300])
+def test_linear_fp16_codes_equal_int8_codes_path(M):
+    """The fused linear writes fp16 codes with the row stream (> 64 rows); the
+    GEMM on the int8 codes of quant_act must give the same output, bit for bit."""
+    K, N = 2048, 384
+    rng = np.random.default_rng(M)
+    bits = workloads.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    a = to_dev_bf16(bits)
+    qw, sw = w8.quant_weight((torch.randn(N, K, device=DEV) * 0.02).float())
+    qa, sa = w8.quant_act(a)
+    y0 = run_gemm(qa, sa, qw, sw, torch.bfloat16)
+    y1 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    w8.linear(a, qw, sw, out_dtype=torch.bfloat16, out=y1)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+
+
 def test_quant_act_ties_and_strided_rows():
     rows = np.zeros((4, 256), np.float32)
     rows[0, :10] = [127.0, 2.5, 3.5, -2.5, 0.5, 1.5, 126.5, -126.5, -0.5, 5.5]
