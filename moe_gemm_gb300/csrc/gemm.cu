@@ -1147,36 +1147,41 @@ w8a8_gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
 // =============================================================================
 // Large dense problems (at least 256 token rows): tiles of 128 weight rows x
-// 256 token rows, one K group per pipeline step, and one tcgen05.mma of
-// N = 256 per 16 K. On this part an MMA instruction costs about the same
-// whether it covers 128 or 256 token columns (~130 vs ~137 cycles at M = 128,
-// K = 16, measured with w8a8_probe_tc_rate), so the 256-column form does
-// nearly twice the work per instruction.
-// Tensor memory: the group's exact partial sums in columns [0, 256) (one
-// buffer; the epilogue drains it before the next group's MMAs), the fp16 A
-// operand (weights) of four groups in columns [256, 512), 64 each, so the
-// converter runs up to four groups ahead of the MMAs.
-// Shared memory: three 64 KB token stages (256 rows x 128 K fp16, two
-// 128-byte swizzle atom columns) and two 16 KB weight stages.
+// 192 token rows, one K group per pipeline step, and one tcgen05.mma of
+// N = 192 per 16 K. On this part an MMA instruction costs about the same
+// whatever its token columns (~130-155 cycles at M = 128, K = 16 for N up to
+// 256, measured with w8a8_probe_tc_rate), so wide instructions pay.
+// Tensor memory: two buffers of a group's exact partial sums in columns
+// [0, 192) and [192, 384), so the MMAs of group g + 1 run while the epilogue
+// drains group g (with one 256-column buffer every group's MMAs waited for
+// the previous group's drain), and the fp16 A operand (weights) of two groups
+// in columns [384, 512), 64 each, so the converter runs a group ahead.
+// Shared memory (exactly the 227 KB limit): four 48 KB token stages (192 rows
+// x 128 K fp16, two 128-byte swizzle atom columns) and two 16 KB weight
+// stages.
 // Warp roles: 0 weight TMA producer; 1 MMA issuer and TMEM allocation; 2
 // token TMA producer (waits for the kernel that wrote the codes); 4-7
 // converter (int8 -> fp16 A operand in TMEM); 8-15 epilogue: warpgroup h
-// drains token columns [128 h, 128 h + 128) of every lane (weight row),
-// fma with sw[n, g] into 128 register accumulators per thread, and at the end
-// of the tile multiplies by sa[m] and stores.
+// drains token columns [96 h, 96 h + 96) of every lane (weight row), fma
+// with sw[n, g] into 96 register accumulators per thread, and at the end of
+// the tile multiplies by sa[m] and stores.
 // =============================================================================
-constexpr int kW2Tokens = 256;
-constexpr int kW2TokStages = 3;
+constexpr int kW2Tokens = 192;
+constexpr int kW2TokStages = 4;
 constexpr int kW2WStages = 2;
-constexpr int kW2ASlots = 4;
+constexpr int kW2ASlots = 2;
+constexpr int kW2Bufs = 2;                                  // partial-sum buffers in TMEM
+constexpr int kW2Half = kW2Tokens / 2;                      // token columns per epilogue warpgroup
 constexpr int kW2OffStages = 2048;
-constexpr int kW2AtomBytes = kW2Tokens * 128;              // one 128-byte atom column, 32 KB
-constexpr int kW2TokStageBytes = 2 * kW2AtomBytes;          // one K group of tokens, 64 KB
+constexpr int kW2AtomBytes = kW2Tokens * 128;              // one 128-byte atom column, 24 KB
+constexpr int kW2TokStageBytes = 2 * kW2AtomBytes;          // one K group of tokens, 48 KB
 constexpr int kW2SmemBytes =
     kW2OffStages + kW2TokStages * kW2TokStageBytes + kW2WStages * kAStageBytes + 1024;
 static_assert(kW2SmemBytes <= kSmemLimit, "wide-tile shared memory");
-constexpr uint32_t kW2TmemA0 = 256;
-// Token scales of the current tile, 128 per epilogue warpgroup, in the fixed
+static_assert(kW2Half % 32 == 0, "32-column chunks per epilogue warpgroup");
+constexpr uint32_t kW2TmemA0 = kW2Bufs * kW2Tokens;
+static_assert(kW2TmemA0 + 64 * kW2ASlots <= kTmemCols, "wide-tile tensor memory");
+// Token scales of the current tile, 96 per epilogue warpgroup, in the fixed
 // area: after the barriers, and after the tile table of a dense call.
 constexpr int kW2OffSa0 = 256;
 constexpr int kW2OffSa1 = 1536;
@@ -1188,9 +1193,9 @@ struct W2Bar {
     static constexpr int b_empty = b_full + kW2TokStages;  // [kW2TokStages] MMA commit -> token TMA
     static constexpr int a_ready = b_empty + kW2TokStages; // [kW2ASlots] converter (4) -> MMA
     static constexpr int a_free = a_ready + kW2ASlots;     // [kW2ASlots] MMA commit -> converter
-    static constexpr int d_full = a_free + kW2ASlots;      // MMA commit -> epilogue
-    static constexpr int d_empty = d_full + 1;             // epilogue (8 warps) -> MMA
-    static constexpr int drain = d_empty + 1;
+    static constexpr int d_full = a_free + kW2ASlots;      // [kW2Bufs] MMA commit -> epilogue
+    static constexpr int d_empty = d_full + kW2Bufs;       // [kW2Bufs] epilogue (8 warps) -> MMA
+    static constexpr int drain = d_empty + kW2Bufs;
     static constexpr int count = drain + 1;
 };
 static_assert(W2Bar::count <= 128, "barrier area");
@@ -1232,8 +1237,10 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(bar(W2Bar::a_ready + i), 4);
             mbar_init(bar(W2Bar::a_free + i), 1);
         }
-        mbar_init(bar(W2Bar::d_full), 1);
-        mbar_init(bar(W2Bar::d_empty), 8);
+        for (int i = 0; i < kW2Bufs; ++i) {
+            mbar_init(bar(W2Bar::d_full + i), 1);
+            mbar_init(bar(W2Bar::d_empty + i), 8);
+        }
         mbar_init(bar(W2Bar::drain), 1);
         *s_abort = 0;
         fence_mbarrier_init();
@@ -1286,8 +1293,7 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             if (!ok) drain_ring(bar(W2Bar::a_full), issued, kW2WStages);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------- MMA issuer
-            Ring b, sl;
-            uint32_t dph = 0;
+            Ring b, sl, d;   // token stage, A slot, partial buffer
             bool ok = true;
             const uint32_t idesc =
                 kA16 ? idesc_bf16_f32(kTileN, kW2Tokens) : idesc_f16_f32(kTileN, kW2Tokens);
@@ -1297,11 +1303,11 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                    ROLE_MMA, 11) ||
                         !mbar_wait(bar(W2Bar::b_full + b.idx), b.phase, s_abort, p.err, ROLE_MMA,
                                    12) ||
-                        !mbar_wait(bar(W2Bar::d_empty), dph ^ 1u, s_abort, p.err, ROLE_MMA, 13)) {
+                        !mbar_wait(bar(W2Bar::d_empty + d.idx), d.phase ^ 1u, s_abort, p.err,
+                                   ROLE_MMA, 13)) {
                         ok = false;
                         break;
                     }
-                    dph ^= 1u;
                     tc_fence_after();
                     const uint32_t stage = sTok + b.idx * kW2TokStageBytes;
                     const uint32_t a_tmem = tmem_base + kW2TmemA0 + sl.idx * 64u;
@@ -1309,13 +1315,15 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t bdesc = smem_desc_sw128(stage + (kk >> 2) * kW2AtomBytes) +
                                                static_cast<uint64_t>((kk & 3) * 2);
-                        mma_f16_tmemA(tmem_base, a_tmem + kk * 8, bdesc, idesc, kk > 0 ? 1u : 0u);
+                        mma_f16_tmemA(tmem_base + d.idx * kW2Tokens, a_tmem + kk * 8, bdesc, idesc,
+                                      kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(W2Bar::d_full));
+                    mma_commit(bar(W2Bar::d_full + d.idx));
                     mma_commit(bar(W2Bar::a_free + sl.idx));
                     mma_commit(bar(W2Bar::b_empty + b.idx));
                     sl.advance(kW2ASlots);
                     b.advance(kW2TokStages);
+                    d.advance(kW2Bufs);
                 }
             }
             mma_commit(bar(W2Bar::drain));
@@ -1394,15 +1402,15 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
         // -------------------------------------------------------- epilogue
         setmaxnreg_inc<kEpiRegs>();
         griddep_wait();   // the token scales come from the kernel launched before
-        const int h = wg - 2;   // token columns [128 h, 128 h + 128)
+        const int h = wg - 2;   // token columns [kW2Half h, kW2Half (h + 1))
         const int q = warp & 3;
         const int lrow = q * 32 + lane;
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         float *s_sa = reinterpret_cast<float *>(smem + (h == 0 ? kW2OffSa0 : kW2OffSa1));
-        float acc[128];
+        float acc[kW2Half];
 #pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-        uint32_t dph = 0;
+        for (int j = 0; j < kW2Half; ++j) acc[j] = 0.0f;
+        Ring d;   // partial buffer
         bool failed = false;
         for (int t = blockIdx.x; t < total && !failed; t += grid) {
             const TileInfo ti = tile_of(t);
@@ -1413,13 +1421,13 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
             // this row's weight scales two groups ahead (loads issued in place)
             float sc0 = n_ok ? ldg_nc_f32_now(swp) : 0.0f;
             float sc1 = (n_ok && G > 1) ? ldg_nc_f32_now(swp + 1) : 0.0f;
-            const int col0 = 128 * h;
+            const int col0 = kW2Half * h;
             // The tile's token scales, copied into shared memory now (one per
             // thread, asynchronously) and read at the store: the copies land
             // while the tile's groups run. The barrier first lets every
             // thread of the warpgroup finish reading the previous tile's.
             named_barrier_sync(1 + h, 128);
-            {
+            if (lrow < kW2Half) {
                 const int col = col0 + lrow;
                 if (p.sa != nullptr)
                     cp_async_4(smem_u32(s_sa + lrow), p.sa + ti.m0 + min(col, ti.rows - 1),
@@ -1431,17 +1439,18 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 const float sc = sc0;
                 sc0 = sc1;
                 sc1 = (n_ok && g + 2 < G) ? ldg_nc_f32_now(swp + g + 2) : 0.0f;
-                const bool ok = mbar_wait(bar(W2Bar::d_full), dph, s_abort, p.err, ROLE_EPILOGUE, 11);
+                const bool ok = mbar_wait(bar(W2Bar::d_full + d.idx), d.phase, s_abort, p.err,
+                                          ROLE_EPILOGUE, 11);
                 if (__any_sync(0xFFFFFFFFu, !ok)) {   // the warp fails as one
                     failed = true;
                     break;
                 }
-                dph ^= 1u;
                 tc_fence_after();
+                const uint32_t dcol = d.idx * kW2Tokens;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kW2Half / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld_32cols_sync(lane_base + col0 + 32u * c, v);
+                    tmem_ld_32cols_sync(lane_base + dcol + col0 + 32u * c, v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         acc[32 * c + j] = fmaf(__uint_as_float(v[j]), sc, acc[32 * c + j]);
@@ -1457,35 +1466,36 @@ w8a8_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_relaxed(bar(W2Bar::d_empty));
+                if (lane == 0) mbar_arrive_relaxed(bar(W2Bar::d_empty + d.idx));
+                d.advance(kW2Bufs);
             }
             // The warpgroup's copies have landed once all its threads pass the
             // barrier, which also makes a failure of any of its warps theirs.
             cp_async_wait_all();
             if (named_barrier_or(1 + h, 128, failed)) break;
             if (n_ok) {
-                // Token rows [m0 + col0, m0 + col0 + 128) of output column
+                // Token rows [m0 + col0, m0 + col0 + kW2Half) of output column
                 // n_local through one running pointer.
                 const int rows_here = ti.rows - col0;
                 const size_t first = static_cast<size_t>(ti.m0 + col0) * p.N + n_local;
                 if (p.out_fp32) {
                     float *yp = static_cast<float *>(p.y) + first;
 #pragma unroll
-                    for (int j = 0; j < 128; ++j) {
+                    for (int j = 0; j < kW2Half; ++j) {
                         if (j < rows_here) *yp = acc[j] * s_sa[j];
                         yp += p.N;
                     }
                 } else {
                     __nv_bfloat16 *yp = static_cast<__nv_bfloat16 *>(p.y) + first;
 #pragma unroll
-                    for (int j = 0; j < 128; ++j) {
+                    for (int j = 0; j < kW2Half; ++j) {
                         if (j < rows_here) *yp = __float2bfloat16_rn(acc[j] * s_sa[j]);
                         yp += p.N;
                     }
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < kW2Half; ++j) acc[j] = 0.0f;
         }
     }
 

@@ -120,7 +120,7 @@ inline size_t sk_area_bytes(int64_t R, bool grouped) {
 }
 
 // Dense calls of at least this many token rows run tiles of 128 weight rows x
-// 256 token rows (one 256-column MMA per 16 K).
+// 192 token rows (one 192-column MMA per 16 K, two partial buffers in TMEM).
 constexpr int kWide256MinRows = 256;
 // RMSNorm + per-token quantization (quant.cu): out_kind 0 int8 codes, 1 fp16
 // codes (dense rows of K; zeroes n_cnt split counters), 2 the BF16 rows.
